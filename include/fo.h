@@ -1,0 +1,196 @@
+/*
+ * fo.h -- C ABI of the GB300 Flash-Overlap library.
+ *
+ * The method (FlashOverlap: Minimizing Tail Latency in Communication Overlap
+ * for Distributed LLM Training, technical summary section 2 "Methodology")
+ * replaces a tensor-parallel collective by ring point-to-point steps and
+ * schedules the compute around them:
+ *   - Flash-AG   all-gather -> column-parallel GEMM, local slice computed first;
+ *   - Flash-RS   row-parallel GEMM -> reduce-scatter, the slice the rank keeps
+ *                computed last (rank-adaptive scheduling);
+ *   - query-split attention, whose K/V slices travel the ring like Flash-AG.
+ *
+ * Here all P "ranks" live on ONE GPU: rank r is a set of caller buffers plus a
+ * disjoint arena of the context's workspace, and a ring hop is a device-local
+ * copy (copy engine) or an epilogue store into the successor's arena, signalled
+ * through per-slice / per-tile flags in device memory.
+ *
+ * Conventions for every entry point
+ *   - Matrices are row-major fo_mat views: element (i, j) at ptr + (i*ld + j)*size.
+ *     Pointers are DEVICE pointers unless an entry point says otherwise, must be
+ *     16-byte aligned, and ld*element_size must be a multiple of 16 bytes.
+ *   - The caller owns every input and output buffer.  The context owns its
+ *     workspace (ring receive slots, flags, intermediates) and grows it on demand.
+ *   - Calls enqueue work on `stream` (a cudaStream_t, 0 = legacy default) and
+ *     return without synchronising.  Argument errors are reported synchronously
+ *     and nothing is enqueued.  Device-side failures (a wait that ran past its
+ *     time limit) are reported by fo_ctx_poll after the stream has completed.
+ *   - A context is not thread-safe; use one per host thread.  Calls on one
+ *     context must be ordered (same stream, or streams the caller orders).
+ *   - Weights use the nn.Linear layout [out_features, in_features].
+ *   - Arithmetic: bf16 operands, fp32 accumulation (tensor cores), fp32 ring
+ *     partials for reduce-scatter, outputs rounded once to bf16
+ *     (round-to-nearest-even).
+ */
+#ifndef FO_H_
+#define FO_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define FO_API __attribute__((visibility("default")))
+#else
+#define FO_API
+#endif
+
+typedef struct fo_ctx fo_ctx;
+
+typedef enum {
+  FO_OK = 0,
+  FO_ERR_INVALID_ARG = 1,   /* null pointer, bad enum, P out of range           */
+  FO_ERR_SHAPE = 2,         /* shapes inconsistent across ranks or operands     */
+  FO_ERR_UNSUPPORTED = 3,   /* valid but outside what the kernels handle        */
+  FO_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed                */
+  FO_ERR_TIMEOUT = 5,       /* a device wait ran past opts.timeout_us           */
+  FO_ERR_OOM = 6            /* workspace growth failed                          */
+} fo_status;
+
+typedef enum { FO_BF16 = 0, FO_F32 = 1 } fo_dtype;
+
+typedef struct {
+  void* ptr;       /* first element                                   */
+  int32_t dtype;   /* fo_dtype                                        */
+  int32_t reserved;
+  int64_t rows;
+  int64_t cols;
+  int64_t ld;      /* elements between consecutive rows, >= cols      */
+} fo_mat;
+
+typedef enum {
+  FO_ORDER_FLASH = 0,    /* the method: local-first AG, kept-slice-last RS, one fused launch    */
+  FO_ORDER_NAIVE = 1,    /* RS only: every rank computes chunks in ascending index order         */
+  FO_ORDER_SLICING = 2,  /* baseline: equal data slices, collective per slice, launch per slice  */
+  FO_ORDER_SERIAL = 3    /* baseline: whole collective, then whole GEMM (or GEMM then collective) */
+} fo_order;
+
+typedef enum {
+  FO_LINK_DEFAULT = 0, /* all-gather: FO_LINK_CE; fused reduce-scatter: FO_LINK_PUSH      */
+  FO_LINK_CE = 1,      /* hop = copy-engine copy on a per-rank link stream               */
+  FO_LINK_PUSH = 2     /* RS only: the epilogue stores the partial sum straight into the
+                          successor's receive slot and releases a per-tile flag          */
+} fo_link;
+
+typedef enum {
+  FO_FAULT_NONE = 0,
+  FO_FAULT_SKIP_HOP = 1  /* fault injection (host side): the last ring hop is not enqueued,
+                            so a device wait runs out; the call must end with
+                            FO_ERR_TIMEOUT from fo_ctx_poll and the context stays usable */
+} fo_fault;
+
+typedef struct {
+  int32_t order;        /* fo_order                                                   */
+  int32_t link;         /* fo_link; all-gather hops are always copy-engine copies      */
+  int32_t n_slices;     /* FO_ORDER_SLICING: number of slices (0 = P)                 */
+  uint32_t timeout_us;  /* limit of every device-side wait (0 = 1 second)             */
+  int32_t causal_prune; /* attention: forward a K/V slice only to ranks that use it   */
+  int32_t num_sms;      /* persistent grid size cap (0 = every SM)                    */
+  int32_t fault;        /* fo_fault                                                   */
+  int32_t reserved;
+} fo_opts;
+
+/* Version of this ABI (major*100 + minor). */
+FO_API int fo_version(void);
+
+/* Text of the last error raised on this host thread ("" if none).  Valid until
+ * the next call on this thread. */
+FO_API const char* fo_last_error_string(void);
+
+/* Creates a context on CUDA device `device` (made current for the call).
+ * Allocates the link streams, events and a small device control block; the
+ * ring workspace is allocated on first use.  *out receives the context. */
+FO_API fo_status fo_ctx_create(int device, fo_ctx** out);
+
+/* Synchronises the context's streams, frees its workspace.  NULL is a no-op. */
+FO_API fo_status fo_ctx_destroy(fo_ctx* ctx);
+
+/* Reads the device error word after the caller has synchronised the stream of
+ * the previous calls, and clears it.  FO_OK, or FO_ERR_TIMEOUT when a device
+ * wait gave up (the work of that call is then incomplete). */
+FO_API fo_status fo_ctx_poll(fo_ctx* ctx);
+
+/* Device milliseconds of the two phases of the last FO_ORDER_SERIAL call on
+ * this context: the ring collective alone and the GEMM alone (valid once that
+ * call's stream has completed). */
+FO_API fo_status fo_ctx_phase_ms(fo_ctx* ctx, float* collective_ms, float* gemm_ms);
+
+/* Plain GEMM on the tensor cores, C = A * B^T (no ring):
+ * A [M, K] bf16, B [N, K] bf16, C [M, N] bf16 or fp32.  K % 8 == 0. */
+FO_API fo_status fo_gemm(fo_ctx* ctx, const fo_mat* A, const fo_mat* B, const fo_mat* C,
+                  const fo_opts* opts, void* stream);
+
+/* Flash-AG (technical summary section 2, "Flash-All-Gather"): all-gather of the
+ * sequence-sharded activations followed by the column-parallel GEMM.
+ *   X_shards[r]  [m, K]  bf16   rank r's token slice (m = M/P rows)
+ *   W_col[r]     [N, K]  bf16   rank r's column block of the weight
+ *   Y[r]         [M, N]  bf16   rank r's output over all M = P*m tokens
+ * Ring: at hop t (1..P-1) rank r forwards slice (r-t+1) mod P to rank r+1.
+ * Rank r computes slice (r-t) mod P at step t, so step 0 is its own slice. */
+FO_API fo_status fo_ag_gemm(fo_ctx* ctx, const fo_mat* X_shards, const fo_mat* W_col, int P,
+                     const fo_mat* Y, const fo_opts* opts, void* stream);
+
+/* Flash-RS (technical summary section 2, "Flash-Reduce-Scatter"): row-parallel
+ * GEMM followed by the reduce-scatter of the partial sums.
+ *   X[r]      [M, Kr] bf16   rank r's in-feature shard of the activations
+ *   W_row[r]  [N, Kr] bf16   rank r's in-feature shard of the weight
+ *   Y[r]      [m, N]  bf16   rank r's token slice of sum_r X[r] W_row[r]^T
+ * At step t rank r computes chunk c = (r-t-1) mod P, adds the fp32 partial sum
+ * received from rank r-1 and passes it to rank r+1; at t = P-1, c = r (the kept
+ * slice) and the sum is rounded into Y[r].  FO_ORDER_NAIVE keeps the ring but
+ * makes every rank compute chunk t at step t. */
+FO_API fo_status fo_gemm_rs(fo_ctx* ctx, const fo_mat* X, const fo_mat* W_row, int P,
+                     const fo_mat* Y, const fo_opts* opts, void* stream);
+
+/* MLP activation glue: H = SiLU(G) * U elementwise, with G = columns [0, F) and
+ * U = columns [F, 2F) of GU[r] ([M, 2F] bf16); H[r] [M, F] bf16.  Computed in
+ * fp32 from the bf16 inputs, rounded once. */
+FO_API fo_status fo_silu_mul(fo_ctx* ctx, const fo_mat* GU, int P, const fo_mat* H, void* stream);
+
+/* One MLP layer (technical summary section 2, "Row/Column Parallel Projection"):
+ * Flash-AG with W_col (gate rows then up rows when gated), SiLU(gate)*up when
+ * gated (identity otherwise), then Flash-RS with W_row.
+ *   X_shards[r] [m, Hd] bf16; W_col[r] [Nc, Hd]; W_row[r] [Hd, F_r] bf16 with
+ *   F_r = Nc/2 (gated) or Nc; Z[r] [m, Hd] bf16 (rank r's token slice).
+ * Intermediates live in the context's workspace. */
+FO_API fo_status fo_mlp_layer(fo_ctx* ctx, const fo_mat* X_shards, const fo_mat* W_col,
+                       const fo_mat* W_row, int P, int gated, const fo_mat* Z,
+                       const fo_opts* opts, void* stream);
+
+/* fo_mlp_layer with HOST activations: X_shards[r].ptr and Z[r].ptr point to host
+ * memory (page-locked for asynchronous copies); weights are device pointers.
+ * The call enqueues the host->device copies of X, the layer and the
+ * device->host copies of Z on `stream`. */
+FO_API fo_status fo_mlp_layer_host(fo_ctx* ctx, const fo_mat* X_shards, const fo_mat* W_col,
+                            const fo_mat* W_row, int P, int gated, const fo_mat* Z,
+                            const fo_opts* opts, void* stream);
+
+/* Query-split attention (technical summary section 2, "Query Split Attention"):
+ * rank r keeps its query slice; K/V slices travel the ring local-first.
+ *   Q[r], K_shards[r], V_shards[r], O[r]: [m, heads*head_dim] bf16, token-major,
+ *   head_dim contiguous.  head_dim == 128.  Scale 1/sqrt(head_dim).
+ *   causal != 0: key j attends query i only if j <= i (global token indices);
+ *   slices wholly above the diagonal are skipped.
+ * Softmax statistics and the output accumulator are fp32 (online softmax). */
+FO_API fo_status fo_qsplit_attn(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K_shards,
+                         const fo_mat* V_shards, int P, int heads, int head_dim, int causal,
+                         const fo_mat* O, const fo_opts* opts, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FO_H_ */

@@ -1,0 +1,1008 @@
+// Host side of the Flash-Overlap library: context and workspace, argument
+// validation, the ring step engine (per-rank link streams, copy-engine hops,
+// stream memory operations that publish per-slice flags), the step schedules
+// of Flash-AG / Flash-RS and of the two baselines, and the C ABI of fo.h.
+//
+// Method: FlashOverlap (technical summary, section 2): collectives decomposed
+// into ring P2P steps; Flash-AG computes the local slice first, Flash-RS
+// defers the kept slice to the last step; section 1: data slicing leaves the
+// last chunk's communication exposed (reproduced here as a baseline).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <string>
+#include <vector>
+
+#include "fo_internal.h"
+
+namespace fo {
+fo_status attn_run(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K, const fo_mat* V, int P, int heads,
+                   int head_dim, int causal, const fo_mat* O, const fo_opts* opts, cudaStream_t stream);
+}
+
+using namespace fo;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+fo_status fail(fo_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+#define FO_CUDA(expr)                                                                      \
+  do {                                                                                     \
+    cudaError_t e_ = (expr);                                                               \
+    if (e_ != cudaSuccess) return fail(FO_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(e_)); \
+  } while (0)
+
+// Driver entry points, resolved through the runtime so that the library has no
+// link-time dependency on libcuda (it loads on hosts without a GPU driver).
+typedef CUresult (*PfnEncodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+typedef CUresult (*PfnWriteValue32)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+typedef CUresult (*PfnGetErrorString)(CUresult, const char**);
+
+struct DriverFns {
+  PfnEncodeTiled encode_tiled = nullptr;
+  PfnWriteValue32 write_value32 = nullptr;
+  PfnGetErrorString get_error_string = nullptr;
+};
+
+const DriverFns* driver() {
+  static DriverFns fns;
+  static bool loaded = false;
+  if (!loaded) {
+    cudaDriverEntryPointQueryResult q;
+    cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", reinterpret_cast<void**>(&fns.encode_tiled), 12000,
+                                     cudaEnableDefault, &q);
+    cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", reinterpret_cast<void**>(&fns.write_value32), 12000,
+                                     cudaEnableDefault, &q);
+    cudaGetDriverEntryPointByVersion("cuGetErrorString", reinterpret_cast<void**>(&fns.get_error_string), 12000,
+                                     cudaEnableDefault, &q);
+    loaded = fns.encode_tiled && fns.write_value32 && fns.get_error_string;
+  }
+  return loaded ? &fns : nullptr;
+}
+
+#define FO_CU(expr)                                                       \
+  do {                                                                    \
+    CUresult r_ = (expr);                                                 \
+    if (r_ != CUDA_SUCCESS) {                                             \
+      const char* s_ = nullptr;                                           \
+      driver()->get_error_string(r_, &s_);                                \
+      return fail(FO_ERR_CUDA, "%s: %s", #expr, s_ ? s_ : "unknown");     \
+    }                                                                     \
+  } while (0)
+
+#define FO_TRY(expr)                \
+  do {                              \
+    fo_status st_ = (expr);         \
+    if (st_ != FO_OK) return st_;   \
+  } while (0)
+
+enum BufId : int {
+  kBufFlags = 0,
+  kBufAgRecv,
+  kBufRsRecv,
+  kBufPart,
+  kBufMlpY,
+  kBufMlpH,
+  kBufHostX,
+  kBufHostZ,
+  kBufAttnRecv,
+};
+
+// Flag layout (uint32 words, epoch-valued):
+//   [0, kMaxP*kMaxP)                AG / attention arrival: rank r holds slice s
+//   [kRsFlagBase, ...)             RS per-(rank, hop, tile, quadrant) partial-sum flags
+constexpr int64_t kAgFlagBase = 0;
+constexpr int64_t kRsFlagBase = 256;
+
+constexpr int kMaxSlices = 16;
+
+struct Buffer {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+
+}  // namespace
+
+struct fo_ctx {
+  int device = 0;
+  int num_sms = 0;
+  cudaStream_t link[kMaxP] = {};
+  cudaStream_t aux = nullptr;
+  cudaEvent_t ev_fork = nullptr;
+  cudaEvent_t ev_join[kMaxP] = {};
+  cudaEvent_t ev_hop[kMaxP][kMaxP] = {};
+  cudaEvent_t ev_slice[kMaxSlices][kMaxP] = {};
+  cudaEvent_t ev_aux = nullptr;
+  cudaEvent_t ev_phase[3] = {};
+  bool phase_valid = false;
+  bool phase_gemm_first = false;  // RS serial: GEMM phase precedes the collective
+  uint32_t* ctrl = nullptr;
+  uint32_t epoch = 0;
+  std::map<int, Buffer> bufs;
+};
+
+namespace {
+
+size_t elem_size(int32_t dtype) { return dtype == FO_F32 ? 4 : 2; }
+
+fo_status ensure_buf(fo_ctx* ctx, int id, size_t bytes, void** out) {
+  Buffer& b = ctx->bufs[id];
+  if (b.bytes < bytes) {
+    if (b.ptr) {
+      FO_CUDA(cudaDeviceSynchronize());  // in-flight work may still use the old buffer
+      FO_CUDA(cudaFree(b.ptr));
+      b.ptr = nullptr;
+      b.bytes = 0;
+    }
+    const size_t rounded = (bytes + (2u << 20) - 1) & ~static_cast<size_t>((2u << 20) - 1);
+    if (cudaMalloc(&b.ptr, rounded) != cudaSuccess) {
+      cudaGetLastError();
+      b.ptr = nullptr;
+      return fail(FO_ERR_OOM, "workspace growth to %zu bytes failed", rounded);
+    }
+    b.bytes = rounded;
+    if (id == kBufFlags) FO_CUDA(cudaMemset(b.ptr, 0, rounded));  // epochs start at 1
+  }
+  *out = b.ptr;
+  return FO_OK;
+}
+
+// --------------------------------------------------------------------------
+// validation
+// --------------------------------------------------------------------------
+
+fo_status check_mat(const fo_mat& a, int32_t dtype, const char* what, int r) {
+  if (!a.ptr) return fail(FO_ERR_INVALID_ARG, "%s[%d]: null pointer", what, r);
+  if (a.dtype != dtype)
+    return fail(FO_ERR_INVALID_ARG, "%s[%d]: dtype %d, expected %d", what, r, a.dtype, dtype);
+  if (a.rows < 0 || a.cols < 0 || a.ld < a.cols)
+    return fail(FO_ERR_SHAPE, "%s[%d]: bad shape rows=%lld cols=%lld ld=%lld", what, r, (long long)a.rows,
+                (long long)a.cols, (long long)a.ld);
+  if (reinterpret_cast<uintptr_t>(a.ptr) % 16 != 0)
+    return fail(FO_ERR_UNSUPPORTED, "%s[%d]: pointer not 16-byte aligned", what, r);
+  if ((a.ld * static_cast<int64_t>(elem_size(dtype))) % 16 != 0)
+    return fail(FO_ERR_UNSUPPORTED, "%s[%d]: row pitch ld*size=%lld not a multiple of 16 bytes", what, r,
+                (long long)(a.ld * elem_size(dtype)));
+  if (a.rows > (1ll << 30) || a.cols > (1ll << 30))
+    return fail(FO_ERR_UNSUPPORTED, "%s[%d]: dimension above 2^30", what, r);
+  return FO_OK;
+}
+
+fo_status check_common(fo_ctx* ctx, int P, const fo_opts* opts) {
+  if (!ctx) return fail(FO_ERR_INVALID_ARG, "null context");
+  if (P < 1 || P > kMaxP) return fail(FO_ERR_INVALID_ARG, "P=%d outside [1, %d]", P, kMaxP);
+  if (opts) {
+    if (opts->order < FO_ORDER_FLASH || opts->order > FO_ORDER_SERIAL)
+      return fail(FO_ERR_INVALID_ARG, "unknown order %d", opts->order);
+    if (opts->link < FO_LINK_DEFAULT || opts->link > FO_LINK_PUSH)
+      return fail(FO_ERR_INVALID_ARG, "unknown link %d", opts->link);
+    if (opts->n_slices < 0 || opts->n_slices > kMaxSlices)
+      return fail(FO_ERR_INVALID_ARG, "n_slices=%d outside [0, %d]", opts->n_slices, kMaxSlices);
+    if (opts->fault < FO_FAULT_NONE || opts->fault > FO_FAULT_SKIP_HOP)
+      return fail(FO_ERR_INVALID_ARG, "unknown fault %d", opts->fault);
+    if (opts->num_sms < 0) return fail(FO_ERR_INVALID_ARG, "num_sms < 0");
+  }
+  return FO_OK;
+}
+
+fo_opts default_opts() {
+  fo_opts o;
+  std::memset(&o, 0, sizeof(o));
+  o.order = FO_ORDER_FLASH;
+  o.link = FO_LINK_DEFAULT;
+  return o;
+}
+
+uint64_t timeout_ns(const fo_opts& o) {
+  return (o.timeout_us ? static_cast<uint64_t>(o.timeout_us) : 1000000ull) * 1000ull;
+}
+
+int grid_size(const fo_ctx* ctx, const fo_opts& o, int tiles) {
+  int g = ctx->num_sms;
+  if (o.num_sms > 0 && o.num_sms < g) g = o.num_sms;
+  if (tiles < g) g = tiles;
+  return g < 1 ? 1 : g;
+}
+
+// --------------------------------------------------------------------------
+// TMA maps
+// --------------------------------------------------------------------------
+
+fo_status encode_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  FO_CU(driver()->encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
+  return FO_OK;
+}
+
+struct Launch {
+  GemmParams p;
+  int num_units = 0;
+  int num_groups = 0;
+  int num_maps = 0;
+  Launch() { std::memset(&p, 0, sizeof(p)); }
+
+  int add_map(fo_status* st, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+    if (num_maps >= kMaxMaps) {
+      *st = fail(FO_ERR_UNSUPPORTED, "too many operand maps");
+      return -1;
+    }
+    *st = encode_map(&p.maps[num_maps], ptr, rows, cols, ld, box_rows);
+    return num_maps++;
+  }
+  void begin_group() {
+    p.group_unit_begin[num_groups] = num_units;
+    ++num_groups;
+  }
+  GemmUnit& add_unit() { return p.units[num_units++]; }
+
+  // Finalises group boundaries and tile counts.  All units of a group share one tile grid.
+  fo_status finish(uint32_t epoch, uint64_t tmo, uint32_t* flags, uint32_t* ctrl, int mblock_major) {
+    if (num_units > kMaxUnits || num_groups > kMaxGroups)
+      return fail(FO_ERR_UNSUPPORTED, "too many units (%d) or groups (%d)", num_units, num_groups);
+    p.group_unit_begin[num_groups] = num_units;
+    int64_t tiles = 0;
+    for (int g = 0; g < num_groups; ++g) {
+      p.group_tile_begin[g] = static_cast<int32_t>(tiles);
+      const int u0 = p.group_unit_begin[g], u1 = p.group_unit_begin[g + 1];
+      for (int u = u0; u < u1; ++u) {
+        GemmUnit& x = p.units[u];
+        x.tiles_m = (x.m_rows + kBM - 1) / kBM;
+        x.tiles_n = (x.n_cols + kBN - 1) / kBN;
+        if (x.tiles_m != p.units[u0].tiles_m || x.tiles_n != p.units[u0].tiles_n)
+          return fail(FO_ERR_SHAPE, "units of one step must share a tile grid");
+        tiles += static_cast<int64_t>(x.tiles_m) * x.tiles_n;
+      }
+    }
+    if (tiles > (1ll << 30)) return fail(FO_ERR_UNSUPPORTED, "too many tiles");
+    p.group_tile_begin[num_groups] = static_cast<int32_t>(tiles);
+    p.num_groups = num_groups;
+    p.num_maps = num_maps;
+    p.total_tiles = static_cast<int32_t>(tiles);
+    p.mblock_major = mblock_major;
+    p.epoch = epoch;
+    p.timeout_ns = tmo;
+    p.flags = flags;
+    p.ctrl = ctrl;
+    return FO_OK;
+  }
+};
+
+GemmUnit blank_unit() {
+  GemmUnit u;
+  std::memset(&u, 0, sizeof(u));
+  u.wait_flag = -1;
+  u.in_flag_base = -1;
+  u.out_flag_base = -1;
+  return u;
+}
+
+fo_status launch_gemm(fo_ctx* ctx, Launch& L, const fo_opts& o, cudaStream_t stream) {
+  if (L.p.total_tiles == 0) return FO_OK;
+  FO_CUDA(gemm_launch(L.p, grid_size(ctx, o, L.p.total_tiles), stream));
+  return FO_OK;
+}
+
+int mod(int a, int P) { return ((a % P) + P) % P; }
+
+char* bptr(const fo_mat& a, int64_t row) {
+  return static_cast<char*>(a.ptr) + row * a.ld * static_cast<int64_t>(elem_size(a.dtype));
+}
+
+// Copy `rows` rows of `cols` bf16 elements (a rank's slice) on a link stream.
+fo_status copy_rows(void* dst, int64_t dld, const void* src, int64_t sld, int64_t rows, int64_t cols,
+                    size_t esz, cudaStream_t s) {
+  if (rows == 0 || cols == 0) return FO_OK;
+  if (dld == cols && sld == cols) {
+    FO_CUDA(cudaMemcpyAsync(dst, src, rows * cols * esz, cudaMemcpyDeviceToDevice, s));
+  } else {
+    FO_CUDA(cudaMemcpy2DAsync(dst, dld * esz, src, sld * esz, cols * esz, rows, cudaMemcpyDeviceToDevice, s));
+  }
+  return FO_OK;
+}
+
+fo_status write_flag(cudaStream_t s, uint32_t* flag, uint32_t value) {
+  // default flags: the write is ordered after (and made visible after) the prior copy on the stream
+  FO_CU(driver()->write_value32(reinterpret_cast<CUstream>(s), reinterpret_cast<CUdeviceptr>(flag), value,
+                             CU_STREAM_WRITE_VALUE_DEFAULT));
+  return FO_OK;
+}
+
+fo_status fork_links(fo_ctx* ctx, int P, cudaStream_t stream) {
+  FO_CUDA(cudaEventRecord(ctx->ev_fork, stream));
+  for (int r = 0; r < P; ++r) FO_CUDA(cudaStreamWaitEvent(ctx->link[r], ctx->ev_fork, 0));
+  return FO_OK;
+}
+
+fo_status join_links(fo_ctx* ctx, int P, cudaStream_t stream) {
+  for (int r = 0; r < P; ++r) {
+    FO_CUDA(cudaEventRecord(ctx->ev_join[r], ctx->link[r]));
+    FO_CUDA(cudaStreamWaitEvent(stream, ctx->ev_join[r], 0));
+  }
+  return FO_OK;
+}
+
+// --------------------------------------------------------------------------
+// Flash-AG and its baselines
+// --------------------------------------------------------------------------
+
+struct AgArgs {
+  const fo_mat* X;
+  const fo_mat* W;
+  const fo_mat* Y;
+  int P;
+  int64_t m, K, N;
+  char* recv;  // rank r's gathered copy: recv + r*M*K*2, slice s at row s*m
+};
+
+char* ag_slot(const AgArgs& a, int r, int s, int64_t row_in_slice) {
+  return a.recv + ((static_cast<int64_t>(r) * a.P + s) * a.m + row_in_slice) * a.K * 2;
+}
+
+// The ring all-gather of rows [row0, row0 + rows) of every slice, on the link
+// streams.  Hop t: rank r forwards slice (r - t + 1) mod P (its own at t = 1)
+// to rank r+1 and, with `flags`, publishes arrival of that slice at r+1.
+fo_status enqueue_ag_ring(fo_ctx* ctx, const AgArgs& a, int64_t row0, int64_t rows, bool flags, uint32_t epoch,
+                          int fault, uint32_t* flag_base) {
+  const int P = a.P;
+  for (int t = 1; t < P; ++t) {
+    for (int r = 0; r < P; ++r) {
+      const int d = mod(r + 1, P);
+      const int s = mod(r - t + 1, P);
+      if (fault == FO_FAULT_SKIP_HOP && t == P - 1 && r == 0) continue;
+      cudaStream_t ls = ctx->link[r];
+      if (t >= 2) FO_CUDA(cudaStreamWaitEvent(ls, ctx->ev_hop[mod(r - 1, P)][t - 1], 0));
+      if (t == 1) {
+        FO_TRY(copy_rows(ag_slot(a, d, s, row0), a.K, bptr(a.X[r], row0), a.X[r].ld, rows, a.K, 2, ls));
+      } else {
+        FO_TRY(copy_rows(ag_slot(a, d, s, row0), a.K, ag_slot(a, r, s, row0), a.K, rows, a.K, 2, ls));
+      }
+      if (flags) FO_TRY(write_flag(ls, flag_base + kAgFlagBase + d * P + s, epoch));
+      FO_CUDA(cudaEventRecord(ctx->ev_hop[r][t], ls));
+    }
+  }
+  return FO_OK;
+}
+
+// Adds the P*P (rank, slice) GEMM units over rows [row0, row0 + rows) of every slice.
+fo_status add_ag_units(Launch& L, const AgArgs& a, const int* xmap, const int* rmap, const int* wmap, int64_t row0,
+                       int64_t rows, bool flash, uint32_t* flags) {
+  const int P = a.P;
+  for (int t = 0; t < P; ++t) {
+    if (flash || t == 0) L.begin_group();
+    for (int r = 0; r < P; ++r) {
+      const int s = mod(r - t, P);  // local slice first
+      GemmUnit& u = L.add_unit();
+      u = blank_unit();
+      if (t == 0) {
+        u.a_map = xmap[r];
+        u.a_row0 = static_cast<int32_t>(row0);
+      } else {
+        u.a_map = rmap[r];
+        u.a_row0 = static_cast<int32_t>(s * a.m + row0);
+        if (flash) u.wait_flag = static_cast<int32_t>(kAgFlagBase + r * P + s);
+      }
+      u.b_map = wmap[r];
+      u.m_rows = static_cast<int32_t>(rows);
+      u.n_cols = static_cast<int32_t>(a.N);
+      u.k = static_cast<int32_t>(a.K);
+      u.epi = kEpiBF16;
+      u.c = bptr(a.Y[r], s * a.m + row0);
+      u.ldc = a.Y[r].ld;
+    }
+  }
+  (void)flags;
+  return FO_OK;
+}
+
+fo_status ag_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_mat* Y, const fo_opts& o,
+                 cudaStream_t stream) {
+  const int64_t m = X[0].rows, K = X[0].cols, N = W[0].rows, M = m * P;
+  for (int r = 0; r < P; ++r) {
+    FO_TRY(check_mat(X[r], FO_BF16, "X_shards", r));
+    FO_TRY(check_mat(W[r], FO_BF16, "W_col", r));
+    FO_TRY(check_mat(Y[r], FO_BF16, "Y", r));
+    if (X[r].rows != m || X[r].cols != K) return fail(FO_ERR_SHAPE, "X_shards[%d] shape differs from rank 0", r);
+    if (W[r].rows != N || W[r].cols != K) return fail(FO_ERR_SHAPE, "W_col[%d] must be [N, K] like rank 0", r);
+    if (Y[r].rows != M || Y[r].cols != N) return fail(FO_ERR_SHAPE, "Y[%d] must be [P*m, N]", r);
+  }
+  if (K % 8 != 0) return fail(FO_ERR_UNSUPPORTED, "K=%lld must be a multiple of 8", (long long)K);
+  if (m == 0 || N == 0) return FO_OK;
+  if (K == 0) return fail(FO_ERR_UNSUPPORTED, "K == 0");
+  void* flags_v = nullptr;
+  void* recv_v = nullptr;
+  FO_TRY(ensure_buf(ctx, kBufFlags, 1 << 20, &flags_v));
+  FO_TRY(ensure_buf(ctx, kBufAgRecv, static_cast<size_t>(P) * M * K * 2, &recv_v));
+  uint32_t* flags = static_cast<uint32_t*>(flags_v);
+  AgArgs a{X, W, Y, P, m, K, N, static_cast<char*>(recv_v)};
+  const uint32_t epoch = ++ctx->epoch;
+  const uint64_t tmo = timeout_ns(o);
+
+  fo_status st = FO_OK;
+  auto build = [&](Launch& L, int64_t row0, int64_t rows, bool flash, int* xmap, int* rmap, int* wmap) -> fo_status {
+    for (int r = 0; r < P; ++r) {
+      xmap[r] = L.add_map(&st, X[r].ptr, m, K, X[r].ld, kBM);
+      if (st != FO_OK) return st;
+      rmap[r] = L.add_map(&st, ag_slot(a, r, 0, 0), M, K, K, kBM);
+      if (st != FO_OK) return st;
+      wmap[r] = L.add_map(&st, W[r].ptr, N, K, W[r].ld, kBN);
+      if (st != FO_OK) return st;
+    }
+    FO_TRY(add_ag_units(L, a, xmap, rmap, wmap, row0, rows, flash, flags));
+    return L.finish(epoch, tmo, flags, ctx->ctrl, 0);
+  };
+  int xmap[kMaxP], rmap[kMaxP], wmap[kMaxP];
+
+  if (o.order == FO_ORDER_FLASH || o.order == FO_ORDER_NAIVE) {
+    Launch L;
+    FO_TRY(build(L, 0, m, true, xmap, rmap, wmap));
+    FO_CUDA(cudaEventRecord(ctx->ev_fork, stream));
+    FO_TRY(launch_gemm(ctx, L, o, stream));  // runs concurrently with the ring below
+    for (int r = 0; r < P; ++r) FO_CUDA(cudaStreamWaitEvent(ctx->link[r], ctx->ev_fork, 0));
+    FO_TRY(enqueue_ag_ring(ctx, a, 0, m, true, epoch, o.fault, flags));
+    return join_links(ctx, P, stream);
+  }
+  if (o.order == FO_ORDER_SERIAL) {
+    Launch L;
+    FO_TRY(build(L, 0, m, false, xmap, rmap, wmap));
+    FO_CUDA(cudaEventRecord(ctx->ev_phase[0], stream));
+    FO_TRY(fork_links(ctx, P, stream));
+    FO_TRY(enqueue_ag_ring(ctx, a, 0, m, false, epoch, FO_FAULT_NONE, flags));
+    FO_TRY(join_links(ctx, P, stream));
+    FO_CUDA(cudaEventRecord(ctx->ev_phase[1], stream));
+    FO_TRY(launch_gemm(ctx, L, o, stream));
+    FO_CUDA(cudaEventRecord(ctx->ev_phase[2], stream));
+    ctx->phase_valid = true;
+    ctx->phase_gemm_first = false;
+    return FO_OK;
+  }
+  // FO_ORDER_SLICING: all-gather of sub-slice i, then one GEMM launch over sub-slice i
+  const int n = o.n_slices ? o.n_slices : P;
+  if (m % n != 0) return fail(FO_ERR_SHAPE, "slice rows m=%lld not divisible by n_slices=%d", (long long)m, n);
+  const int64_t sub = m / n;
+  FO_TRY(fork_links(ctx, P, stream));
+  for (int i = 0; i < n; ++i) {
+    FO_TRY(enqueue_ag_ring(ctx, a, i * sub, sub, false, epoch, FO_FAULT_NONE, flags));
+    for (int r = 0; r < P; ++r) FO_CUDA(cudaEventRecord(ctx->ev_slice[i][r], ctx->link[r]));
+  }
+  for (int i = 0; i < n; ++i) {
+    Launch L;
+    FO_TRY(build(L, i * sub, sub, false, xmap, rmap, wmap));
+    for (int r = 0; r < P; ++r) FO_CUDA(cudaStreamWaitEvent(stream, ctx->ev_slice[i][r], 0));
+    FO_TRY(launch_gemm(ctx, L, o, stream));
+  }
+  return join_links(ctx, P, stream);
+}
+
+// --------------------------------------------------------------------------
+// Flash-RS and its baselines
+// --------------------------------------------------------------------------
+
+struct RsArgs {
+  const fo_mat* X;
+  const fo_mat* W;
+  const fo_mat* Y;
+  int P;
+  int64_t M, m, Kr, N;
+  float* recv;  // rank r's receive slot for hop h: recv + ((r*P + h)*m)*N
+  float* part;  // baselines: partial of rank r for chunk c: part + ((r*P + c)*m)*N
+};
+
+float* rs_slot(const RsArgs& a, float* base, int r, int h) {
+  return base + (static_cast<int64_t>(r) * a.P + h) * a.m * a.N;
+}
+
+fo_status rs_flash(fo_ctx* ctx, const RsArgs& a, const fo_opts& o, cudaStream_t stream, uint32_t* flags,
+                   uint32_t epoch) {
+  const int P = a.P;
+  Launch L;
+  fo_status st = FO_OK;
+  int xmap[kMaxP], wmap[kMaxP];
+  for (int r = 0; r < P; ++r) {
+    xmap[r] = L.add_map(&st, a.X[r].ptr, a.M, a.Kr, a.X[r].ld, kBM);
+    if (st != FO_OK) return st;
+    wmap[r] = L.add_map(&st, a.W[r].ptr, a.N, a.Kr, a.W[r].ld, kBN);
+    if (st != FO_OK) return st;
+  }
+  const int64_t tm = (a.m + kBM - 1) / kBM, tn = (a.N + kBN - 1) / kBN;
+  auto fbase = [&](int r, int h) { return kRsFlagBase + (static_cast<int64_t>(r) * P + h) * tm * tn * 4; };
+  if (fbase(P - 1, P) > (1 << 18)) return fail(FO_ERR_UNSUPPORTED, "too many reduce-scatter tiles for the flag area");
+  auto add = [&](int r, int c) {
+    const int h = mod(r - c - 1, P);  // position of rank r on chunk c's reduction chain
+    GemmUnit& u = L.add_unit();
+    u = blank_unit();
+    u.a_map = xmap[r];
+    u.a_row0 = static_cast<int32_t>(c * a.m);
+    u.b_map = wmap[r];
+    u.m_rows = static_cast<int32_t>(a.m);
+    u.n_cols = static_cast<int32_t>(a.N);
+    u.k = static_cast<int32_t>(a.Kr);
+    if (h > 0) {
+      u.acc_in = rs_slot(a, a.recv, r, h);
+      u.ld_acc = a.N;
+      u.in_flag_base = static_cast<int32_t>(fbase(r, h));
+    }
+    if (h < P - 1) {
+      const int d = mod(r + 1, P);
+      u.c = rs_slot(a, a.recv, d, h + 1);
+      u.ldc = a.N;
+      u.out_flag_base = static_cast<int32_t>(fbase(d, h + 1));
+      u.epi = h == 0 ? kEpiF32 : kEpiAddF32;
+    } else {
+      u.c = a.Y[r].ptr;
+      u.ldc = a.Y[r].ld;
+      u.epi = h == 0 ? kEpiBF16 : kEpiAddBF16;
+    }
+  };
+  if (o.order == FO_ORDER_NAIVE) {
+    for (int c = 0; c < P; ++c) {  // every rank computes chunk c at step c (chain order inside the step)
+      L.begin_group();
+      for (int h = 0; h < P; ++h) add(mod(c + 1 + h, P), c);
+    }
+  } else {
+    for (int t = 0; t < P; ++t) {  // rank-adaptive: chunk (r - t - 1) mod P, kept chunk r last
+      L.begin_group();
+      for (int r = 0; r < P; ++r) add(r, mod(r - t - 1, P));
+    }
+  }
+  FO_TRY(L.finish(epoch, timeout_ns(o), flags, ctx->ctrl, 1));
+  return launch_gemm(ctx, L, o, stream);
+}
+
+// Baselines: partial GEMMs into `part`, then a ring reduce with copy-engine hops
+// and fp32 add kernels.  Rows [row0, row0 + rows) of every chunk.
+fo_status rs_partials(fo_ctx* ctx, const RsArgs& a, const fo_opts& o, cudaStream_t stream, int64_t row0,
+                      int64_t rows, uint32_t* flags, uint32_t epoch) {
+  const int P = a.P;
+  Launch L;
+  fo_status st = FO_OK;
+  int xmap[kMaxP], wmap[kMaxP];
+  for (int r = 0; r < P; ++r) {
+    xmap[r] = L.add_map(&st, a.X[r].ptr, a.M, a.Kr, a.X[r].ld, kBM);
+    if (st != FO_OK) return st;
+    wmap[r] = L.add_map(&st, a.W[r].ptr, a.N, a.Kr, a.W[r].ld, kBN);
+    if (st != FO_OK) return st;
+  }
+  L.begin_group();
+  for (int r = 0; r < P; ++r) {
+    for (int c = 0; c < P; ++c) {
+      GemmUnit& u = L.add_unit();
+      u = blank_unit();
+      u.a_map = xmap[r];
+      u.a_row0 = static_cast<int32_t>(c * a.m + row0);
+      u.b_map = wmap[r];
+      u.m_rows = static_cast<int32_t>(rows);
+      u.n_cols = static_cast<int32_t>(a.N);
+      u.k = static_cast<int32_t>(a.Kr);
+      u.epi = kEpiF32;
+      u.c = rs_slot(a, a.part, r, c) + row0 * a.N;
+      u.ldc = a.N;
+    }
+  }
+  FO_TRY(L.finish(epoch, timeout_ns(o), flags, ctx->ctrl, 0));
+  return launch_gemm(ctx, L, o, stream);
+}
+
+// Ring reduce of rows [row0, row0 + rows) of every chunk, issued on `rs` (adds)
+// and the link streams (hops).  Hop h: rank c+h sends its running sum of chunk c
+// to rank c+h+1, which adds its own partial (in place) or, at the owner, rounds
+// the final sum into Y[c].
+fo_status rs_ring_reduce(fo_ctx* ctx, const RsArgs& a, cudaStream_t rs, int64_t row0, int64_t rows) {
+  const int P = a.P;  // P >= 2 (a single rank takes the fused path)
+  for (int h = 1; h < P; ++h) {
+    FO_TRY(fork_links(ctx, P, rs));
+    for (int c = 0; c < P; ++c) {
+      const int s = mod(c + h, P), d = mod(c + h + 1, P);
+      FO_TRY(copy_rows(rs_slot(a, a.recv, d, h) + row0 * a.N, a.N, rs_slot(a, a.part, s, c) + row0 * a.N, a.N,
+                       rows, a.N, 4, ctx->link[s]));
+    }
+    FO_TRY(join_links(ctx, P, rs));
+    for (int c = 0; c < P; ++c) {
+      const int d = mod(c + h + 1, P);
+      float* mine = rs_slot(a, a.part, d, c) + row0 * a.N;
+      const float* in = rs_slot(a, a.recv, d, h) + row0 * a.N;
+      if (h < P - 1) {
+        FO_CUDA(launch_add_f32(mine, a.N, in, a.N, mine, nullptr, a.N, rows, a.N, rs));
+      } else {
+        FO_CUDA(launch_add_f32(mine, a.N, in, a.N, nullptr, reinterpret_cast<uint16_t*>(bptr(a.Y[d], row0)),
+                               a.Y[d].ld, rows, a.N, rs));
+      }
+    }
+  }
+  return FO_OK;
+}
+
+fo_status rs_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_mat* Y, const fo_opts& o,
+                 cudaStream_t stream) {
+  const int64_t M = X[0].rows, Kr = X[0].cols, N = W[0].rows;
+  for (int r = 0; r < P; ++r) {
+    FO_TRY(check_mat(X[r], FO_BF16, "X", r));
+    FO_TRY(check_mat(W[r], FO_BF16, "W_row", r));
+    FO_TRY(check_mat(Y[r], FO_BF16, "Y", r));
+    if (X[r].rows != M || X[r].cols != Kr) return fail(FO_ERR_SHAPE, "X[%d] shape differs from rank 0", r);
+    if (W[r].rows != N || W[r].cols != Kr) return fail(FO_ERR_SHAPE, "W_row[%d] must be [N, Kr] like rank 0", r);
+  }
+  if (M % P != 0) return fail(FO_ERR_SHAPE, "M=%lld not divisible by P=%d", (long long)M, P);
+  const int64_t m = M / P;
+  for (int r = 0; r < P; ++r)
+    if (Y[r].rows != m || Y[r].cols != N) return fail(FO_ERR_SHAPE, "Y[%d] must be [M/P, N]", r);
+  if (Kr % 8 != 0) return fail(FO_ERR_UNSUPPORTED, "Kr=%lld must be a multiple of 8", (long long)Kr);
+  if (N % 4 != 0) return fail(FO_ERR_UNSUPPORTED, "N=%lld must be a multiple of 4", (long long)N);
+  if (m == 0 || N == 0) return FO_OK;
+  if (Kr == 0) return fail(FO_ERR_UNSUPPORTED, "Kr == 0");
+  void *flags_v = nullptr, *recv_v = nullptr;
+  FO_TRY(ensure_buf(ctx, kBufFlags, 1 << 20, &flags_v));
+  FO_TRY(ensure_buf(ctx, kBufRsRecv, static_cast<size_t>(P) * P * m * N * 4, &recv_v));
+  RsArgs a{X, W, Y, P, M, m, Kr, N, static_cast<float*>(recv_v), nullptr};
+  uint32_t* flags = static_cast<uint32_t*>(flags_v);
+  const uint32_t epoch = ++ctx->epoch;
+  if (o.order == FO_ORDER_FLASH || o.order == FO_ORDER_NAIVE || P == 1) {
+    if (o.link == FO_LINK_CE)
+      return fail(FO_ERR_UNSUPPORTED, "fused reduce-scatter hops are epilogue pushes (FO_LINK_PUSH)");
+    return rs_flash(ctx, a, o, stream, flags, epoch);
+  }
+  void* part_v = nullptr;
+  FO_TRY(ensure_buf(ctx, kBufPart, static_cast<size_t>(P) * P * m * N * 4, &part_v));
+  a.part = static_cast<float*>(part_v);
+  if (o.order == FO_ORDER_SERIAL) {
+    FO_CUDA(cudaEventRecord(ctx->ev_phase[0], stream));
+    FO_TRY(rs_partials(ctx, a, o, stream, 0, m, flags, epoch));
+    FO_CUDA(cudaEventRecord(ctx->ev_phase[1], stream));
+    FO_TRY(rs_ring_reduce(ctx, a, stream, 0, m));
+    FO_CUDA(cudaEventRecord(ctx->ev_phase[2], stream));
+    ctx->phase_valid = true;
+    ctx->phase_gemm_first = true;
+    return FO_OK;
+  }
+  // FO_ORDER_SLICING: partial GEMM of sub-slice i (main stream), its ring reduce on the aux stream
+  const int n = o.n_slices ? o.n_slices : P;
+  if (m % n != 0) return fail(FO_ERR_SHAPE, "slice rows m=%lld not divisible by n_slices=%d", (long long)m, n);
+  const int64_t sub = m / n;
+  for (int i = 0; i < n; ++i) {
+    FO_TRY(rs_partials(ctx, a, o, stream, i * sub, sub, flags, epoch));
+    FO_CUDA(cudaEventRecord(ctx->ev_aux, stream));
+    FO_CUDA(cudaStreamWaitEvent(ctx->aux, ctx->ev_aux, 0));
+    FO_TRY(rs_ring_reduce(ctx, a, ctx->aux, i * sub, sub));
+  }
+  FO_CUDA(cudaEventRecord(ctx->ev_aux, ctx->aux));
+  FO_CUDA(cudaStreamWaitEvent(stream, ctx->ev_aux, 0));
+  return FO_OK;
+}
+
+// --------------------------------------------------------------------------
+// MLP layer
+// --------------------------------------------------------------------------
+
+fo_status mlp_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* Wc, const fo_mat* Wr, int P, int gated,
+                  const fo_mat* Z, const fo_opts& o, cudaStream_t stream) {
+  const int64_t m = X[0].rows, M = m * P, Nc = Wc[0].rows;
+  if (gated && Nc % 16 != 0) return fail(FO_ERR_UNSUPPORTED, "gated layer needs 2F with F % 8 == 0");
+  const int64_t F = gated ? Nc / 2 : Nc;
+  void* y_v = nullptr;
+  FO_TRY(ensure_buf(ctx, kBufMlpY, static_cast<size_t>(P) * M * Nc * 2 + 16, &y_v));
+  fo_mat Y[kMaxP], H[kMaxP];
+  for (int r = 0; r < P; ++r) {
+    Y[r] = fo_mat{static_cast<char*>(y_v) + static_cast<int64_t>(r) * M * Nc * 2, FO_BF16, 0, M, Nc, Nc};
+  }
+  fo_opts oa = o;
+  if (oa.order == FO_ORDER_NAIVE) oa.order = FO_ORDER_FLASH;  // the naive order concerns the RS step
+  FO_TRY(ag_run(ctx, X, Wc, P, Y, oa, stream));
+  if (gated) {
+    void* h_v = nullptr;
+    FO_TRY(ensure_buf(ctx, kBufMlpH, static_cast<size_t>(P) * M * F * 2 + 16, &h_v));
+    SiluMulArgs sa;
+    std::memset(&sa, 0, sizeof(sa));
+    for (int r = 0; r < P; ++r) {
+      H[r] = fo_mat{static_cast<char*>(h_v) + static_cast<int64_t>(r) * M * F * 2, FO_BF16, 0, M, F, F};
+      sa.gu[r] = static_cast<const uint16_t*>(Y[r].ptr);
+      sa.h[r] = static_cast<uint16_t*>(H[r].ptr);
+      sa.ld_gu[r] = Nc;
+      sa.ld_h[r] = F;
+    }
+    sa.rows = M;
+    sa.f = F;
+    sa.P = P;
+    FO_CUDA(launch_silu_mul(sa, stream));
+  } else {
+    for (int r = 0; r < P; ++r) H[r] = Y[r];
+  }
+  return rs_run(ctx, H, Wr, P, Z, o, stream);
+}
+
+}  // namespace
+
+// ============================================================================
+// C ABI
+// ============================================================================
+
+extern "C" {
+
+int fo_version(void) { return 100; }
+
+const char* fo_last_error_string(void) { return g_last_error.c_str(); }
+
+fo_status fo_ctx_create(int device, fo_ctx** out) {
+  if (!out) return fail(FO_ERR_INVALID_ARG, "null out pointer");
+  *out = nullptr;
+  int ndev = 0;
+  FO_CUDA(cudaGetDeviceCount(&ndev));
+  if (device < 0 || device >= ndev) return fail(FO_ERR_INVALID_ARG, "device %d of %d", device, ndev);
+  FO_CUDA(cudaSetDevice(device));
+  cudaDeviceProp prop;
+  FO_CUDA(cudaGetDeviceProperties(&prop, device));
+  if (prop.major != 10 || prop.minor != 3)
+    return fail(FO_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a", device, prop.major,
+                prop.minor);
+  if (!driver()) return fail(FO_ERR_CUDA, "driver entry points (tensor maps, stream memory operations) unavailable");
+  fo_ctx* c = new fo_ctx();
+  c->device = device;
+  c->num_sms = prop.multiProcessorCount;
+  auto cleanup = [&](fo_status st) {
+    fo_ctx_destroy(c);
+    return st;
+  };
+  if (gemm_configure() != cudaSuccess) return cleanup(fail(FO_ERR_CUDA, "gemm kernel configuration failed"));
+  for (int r = 0; r < kMaxP; ++r) {
+    if (cudaStreamCreateWithFlags(&c->link[r], cudaStreamNonBlocking) != cudaSuccess)
+      return cleanup(fail(FO_ERR_CUDA, "stream creation failed"));
+    if (cudaEventCreateWithFlags(&c->ev_join[r], cudaEventDisableTiming) != cudaSuccess)
+      return cleanup(fail(FO_ERR_CUDA, "event creation failed"));
+    for (int t = 0; t < kMaxP; ++t)
+      if (cudaEventCreateWithFlags(&c->ev_hop[r][t], cudaEventDisableTiming) != cudaSuccess)
+        return cleanup(fail(FO_ERR_CUDA, "event creation failed"));
+    for (int i = 0; i < kMaxSlices; ++i)
+      if (cudaEventCreateWithFlags(&c->ev_slice[i][r], cudaEventDisableTiming) != cudaSuccess)
+        return cleanup(fail(FO_ERR_CUDA, "event creation failed"));
+  }
+  if (cudaStreamCreateWithFlags(&c->aux, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->ev_aux, cudaEventDisableTiming) != cudaSuccess)
+    return cleanup(fail(FO_ERR_CUDA, "stream/event creation failed"));
+  for (int i = 0; i < 3; ++i)
+    if (cudaEventCreate(&c->ev_phase[i]) != cudaSuccess) return cleanup(fail(FO_ERR_CUDA, "event creation failed"));
+  if (cudaMalloc(&c->ctrl, kCtrlWords * sizeof(uint32_t)) != cudaSuccess)
+    return cleanup(fail(FO_ERR_OOM, "control block allocation failed"));
+  if (cudaMemset(c->ctrl, 0, kCtrlWords * sizeof(uint32_t)) != cudaSuccess)
+    return cleanup(fail(FO_ERR_CUDA, "control block init failed"));
+  *out = c;
+  return FO_OK;
+}
+
+fo_status fo_ctx_destroy(fo_ctx* ctx) {
+  if (!ctx) return FO_OK;
+  cudaSetDevice(ctx->device);
+  cudaDeviceSynchronize();
+  for (auto& kv : ctx->bufs)
+    if (kv.second.ptr) cudaFree(kv.second.ptr);
+  if (ctx->ctrl) cudaFree(ctx->ctrl);
+  for (int r = 0; r < kMaxP; ++r) {
+    if (ctx->link[r]) cudaStreamDestroy(ctx->link[r]);
+    if (ctx->ev_join[r]) cudaEventDestroy(ctx->ev_join[r]);
+    for (int t = 0; t < kMaxP; ++t)
+      if (ctx->ev_hop[r][t]) cudaEventDestroy(ctx->ev_hop[r][t]);
+    for (int i = 0; i < kMaxSlices; ++i)
+      if (ctx->ev_slice[i][r]) cudaEventDestroy(ctx->ev_slice[i][r]);
+  }
+  if (ctx->aux) cudaStreamDestroy(ctx->aux);
+  if (ctx->ev_fork) cudaEventDestroy(ctx->ev_fork);
+  if (ctx->ev_aux) cudaEventDestroy(ctx->ev_aux);
+  for (int i = 0; i < 3; ++i)
+    if (ctx->ev_phase[i]) cudaEventDestroy(ctx->ev_phase[i]);
+  delete ctx;
+  return FO_OK;
+}
+
+fo_status fo_ctx_poll(fo_ctx* ctx) {
+  if (!ctx) return fail(FO_ERR_INVALID_ARG, "null context");
+  uint32_t w[kCtrlWords];
+  FO_CUDA(cudaMemcpy(w, ctx->ctrl, sizeof(w), cudaMemcpyDeviceToHost));
+  if (w[kCtrlError] == 0) return FO_OK;
+  FO_CUDA(cudaMemset(ctx->ctrl, 0, sizeof(w)));
+  return fail(static_cast<fo_status>(w[kCtrlError]), "device wait gave up (site %u, index %u)", w[kCtrlWhere],
+              w[kCtrlDetail]);
+}
+
+fo_status fo_ctx_phase_ms(fo_ctx* ctx, float* collective_ms, float* gemm_ms) {
+  if (!ctx || !collective_ms || !gemm_ms) return fail(FO_ERR_INVALID_ARG, "null argument");
+  if (!ctx->phase_valid) return fail(FO_ERR_INVALID_ARG, "no FO_ORDER_SERIAL call on this context yet");
+  float a = 0.f, b = 0.f;
+  FO_CUDA(cudaEventElapsedTime(&a, ctx->ev_phase[0], ctx->ev_phase[1]));
+  FO_CUDA(cudaEventElapsedTime(&b, ctx->ev_phase[1], ctx->ev_phase[2]));
+  // AG: phase 0->1 is the ring, 1->2 the GEMM; RS: 0->1 the GEMM, 1->2 the ring
+  *collective_ms = ctx->phase_gemm_first ? b : a;
+  *gemm_ms = ctx->phase_gemm_first ? a : b;
+  return FO_OK;
+}
+
+fo_status fo_gemm(fo_ctx* ctx, const fo_mat* A, const fo_mat* B, const fo_mat* C, const fo_opts* opts,
+                  void* stream) {
+  FO_TRY(check_common(ctx, 1, opts));
+  if (!A || !B || !C) return fail(FO_ERR_INVALID_ARG, "null matrix");
+  FO_TRY(check_mat(*A, FO_BF16, "A", 0));
+  FO_TRY(check_mat(*B, FO_BF16, "B", 0));
+  FO_TRY(check_mat(*C, C->dtype == FO_F32 ? FO_F32 : FO_BF16, "C", 0));
+  if (A->cols != B->cols) return fail(FO_ERR_SHAPE, "A and B must share K");
+  if (C->rows != A->rows || C->cols != B->rows) return fail(FO_ERR_SHAPE, "C must be [M, N]");
+  if (A->cols % 8 != 0) return fail(FO_ERR_UNSUPPORTED, "K must be a multiple of 8");
+  if (A->rows == 0 || B->rows == 0) return FO_OK;
+  if (A->cols == 0) return fail(FO_ERR_UNSUPPORTED, "K == 0");
+  FO_CUDA(cudaSetDevice(ctx->device));
+  fo_opts o = opts ? *opts : default_opts();
+  Launch L;
+  fo_status st = FO_OK;
+  const int am = L.add_map(&st, A->ptr, A->rows, A->cols, A->ld, kBM);
+  FO_TRY(st);
+  const int bm = L.add_map(&st, B->ptr, B->rows, B->cols, B->ld, kBN);
+  FO_TRY(st);
+  L.begin_group();
+  GemmUnit& u = L.add_unit();
+  u = blank_unit();
+  u.a_map = am;
+  u.b_map = bm;
+  u.m_rows = static_cast<int32_t>(A->rows);
+  u.n_cols = static_cast<int32_t>(B->rows);
+  u.k = static_cast<int32_t>(A->cols);
+  u.epi = C->dtype == FO_F32 ? kEpiF32 : kEpiBF16;
+  u.c = C->ptr;
+  u.ldc = C->ld;
+  if (A->rows > (1 << 30)) return fail(FO_ERR_UNSUPPORTED, "M too large");
+  void* flags_v = nullptr;
+  FO_TRY(ensure_buf(ctx, kBufFlags, 1 << 20, &flags_v));
+  FO_TRY(L.finish(++ctx->epoch, timeout_ns(o), static_cast<uint32_t*>(flags_v), ctx->ctrl, 0));
+  return launch_gemm(ctx, L, o, static_cast<cudaStream_t>(stream));
+}
+
+fo_status fo_ag_gemm(fo_ctx* ctx, const fo_mat* X_shards, const fo_mat* W_col, int P, const fo_mat* Y,
+                     const fo_opts* opts, void* stream) {
+  FO_TRY(check_common(ctx, P, opts));
+  if (!X_shards || !W_col || !Y) return fail(FO_ERR_INVALID_ARG, "null matrix array");
+  FO_CUDA(cudaSetDevice(ctx->device));
+  const fo_opts o = opts ? *opts : default_opts();
+  if (o.order == FO_ORDER_NAIVE) return fail(FO_ERR_INVALID_ARG, "FO_ORDER_NAIVE applies to reduce-scatter only");
+  return ag_run(ctx, X_shards, W_col, P, Y, o, static_cast<cudaStream_t>(stream));
+}
+
+fo_status fo_gemm_rs(fo_ctx* ctx, const fo_mat* X, const fo_mat* W_row, int P, const fo_mat* Y,
+                     const fo_opts* opts, void* stream) {
+  FO_TRY(check_common(ctx, P, opts));
+  if (!X || !W_row || !Y) return fail(FO_ERR_INVALID_ARG, "null matrix array");
+  FO_CUDA(cudaSetDevice(ctx->device));
+  const fo_opts o = opts ? *opts : default_opts();
+  return rs_run(ctx, X, W_row, P, Y, o, static_cast<cudaStream_t>(stream));
+}
+
+fo_status fo_silu_mul(fo_ctx* ctx, const fo_mat* GU, int P, const fo_mat* H, void* stream) {
+  FO_TRY(check_common(ctx, P, nullptr));
+  if (!GU || !H) return fail(FO_ERR_INVALID_ARG, "null matrix array");
+  FO_CUDA(cudaSetDevice(ctx->device));
+  SiluMulArgs sa;
+  std::memset(&sa, 0, sizeof(sa));
+  const int64_t rows = GU[0].rows, F = GU[0].cols / 2;
+  for (int r = 0; r < P; ++r) {
+    FO_TRY(check_mat(GU[r], FO_BF16, "GU", r));
+    FO_TRY(check_mat(H[r], FO_BF16, "H", r));
+    if (GU[r].rows != rows || GU[r].cols != 2 * F || H[r].rows != rows || H[r].cols != F)
+      return fail(FO_ERR_SHAPE, "GU[%d] must be [rows, 2F] and H[%d] [rows, F]", r, r);
+    sa.gu[r] = static_cast<const uint16_t*>(GU[r].ptr);
+    sa.h[r] = static_cast<uint16_t*>(H[r].ptr);
+    sa.ld_gu[r] = GU[r].ld;
+    sa.ld_h[r] = H[r].ld;
+  }
+  if (F % 8 != 0) return fail(FO_ERR_UNSUPPORTED, "F must be a multiple of 8");
+  sa.rows = rows;
+  sa.f = F;
+  sa.P = P;
+  FO_CUDA(launch_silu_mul(sa, static_cast<cudaStream_t>(stream)));
+  return FO_OK;
+}
+
+fo_status fo_mlp_layer(fo_ctx* ctx, const fo_mat* X_shards, const fo_mat* W_col, const fo_mat* W_row, int P,
+                       int gated, const fo_mat* Z, const fo_opts* opts, void* stream) {
+  FO_TRY(check_common(ctx, P, opts));
+  if (!X_shards || !W_col || !W_row || !Z) return fail(FO_ERR_INVALID_ARG, "null matrix array");
+  FO_CUDA(cudaSetDevice(ctx->device));
+  const fo_opts o = opts ? *opts : default_opts();
+  for (int r = 0; r < P; ++r) {
+    FO_TRY(check_mat(W_col[r], FO_BF16, "W_col", r));
+    FO_TRY(check_mat(W_row[r], FO_BF16, "W_row", r));
+    const int64_t F = gated ? W_col[r].rows / 2 : W_col[r].rows;
+    if (W_row[r].cols != F) return fail(FO_ERR_SHAPE, "W_row[%d] must have F=%lld columns", r, (long long)F);
+  }
+  return mlp_run(ctx, X_shards, W_col, W_row, P, gated, Z, o, static_cast<cudaStream_t>(stream));
+}
+
+fo_status fo_mlp_layer_host(fo_ctx* ctx, const fo_mat* X_shards, const fo_mat* W_col, const fo_mat* W_row, int P,
+                            int gated, const fo_mat* Z, const fo_opts* opts, void* stream) {
+  FO_TRY(check_common(ctx, P, opts));
+  if (!X_shards || !W_col || !W_row || !Z) return fail(FO_ERR_INVALID_ARG, "null matrix array");
+  FO_CUDA(cudaSetDevice(ctx->device));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t m = X_shards[0].rows, Hd = X_shards[0].cols;
+  for (int r = 0; r < P; ++r) {
+    if (!X_shards[r].ptr || !Z[r].ptr) return fail(FO_ERR_INVALID_ARG, "null host pointer");
+    if (X_shards[r].dtype != FO_BF16 || Z[r].dtype != FO_BF16) return fail(FO_ERR_INVALID_ARG, "bf16 expected");
+    if (X_shards[r].rows != m || X_shards[r].cols != Hd || Z[r].rows != m || Z[r].cols != Hd ||
+        X_shards[r].ld < Hd || Z[r].ld < Hd)
+      return fail(FO_ERR_SHAPE, "host X_shards[%d] / Z[%d] must be [m, hidden]", r, r);
+  }
+  void *xv = nullptr, *zv = nullptr;
+  const size_t bytes = static_cast<size_t>(P) * m * Hd * 2 + 16;
+  FO_TRY(ensure_buf(ctx, kBufHostX, bytes, &xv));
+  FO_TRY(ensure_buf(ctx, kBufHostZ, bytes, &zv));
+  fo_mat Xd[kMaxP], Zd[kMaxP];
+  for (int r = 0; r < P; ++r) {
+    Xd[r] = fo_mat{static_cast<char*>(xv) + static_cast<int64_t>(r) * m * Hd * 2, FO_BF16, 0, m, Hd, Hd};
+    Zd[r] = fo_mat{static_cast<char*>(zv) + static_cast<int64_t>(r) * m * Hd * 2, FO_BF16, 0, m, Hd, Hd};
+    FO_CUDA(cudaMemcpy2DAsync(Xd[r].ptr, Hd * 2, X_shards[r].ptr, X_shards[r].ld * 2, Hd * 2, m,
+                              cudaMemcpyHostToDevice, s));
+  }
+  FO_TRY(fo_mlp_layer(ctx, Xd, W_col, W_row, P, gated, Zd, opts, stream));
+  for (int r = 0; r < P; ++r)
+    FO_CUDA(cudaMemcpy2DAsync(Z[r].ptr, Z[r].ld * 2, Zd[r].ptr, Hd * 2, Hd * 2, m, cudaMemcpyDeviceToHost, s));
+  return FO_OK;
+}
+
+fo_status fo_qsplit_attn(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K_shards, const fo_mat* V_shards, int P,
+                         int heads, int head_dim, int causal, const fo_mat* O, const fo_opts* opts, void* stream) {
+  FO_TRY(check_common(ctx, P, opts));
+  if (!Q || !K_shards || !V_shards || !O) return fail(FO_ERR_INVALID_ARG, "null matrix array");
+  FO_CUDA(cudaSetDevice(ctx->device));
+  return attn_run(ctx, Q, K_shards, V_shards, P, heads, head_dim, causal, O, opts,
+                  static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
+// Host services for the attention module (fo_attn.cu), declared in fo_host.h.
+namespace fo {
+fo_status host_buffer(fo_ctx* ctx, int slot, size_t bytes, void** out) {
+  return ensure_buf(ctx, kBufAttnRecv + slot, bytes, out);
+}
+fo_status host_flags(fo_ctx* ctx, uint32_t** out) {
+  void* v = nullptr;
+  FO_TRY(ensure_buf(ctx, kBufFlags, 1 << 20, &v));
+  *out = static_cast<uint32_t*>(v) + kAgFlagBase;
+  return FO_OK;
+}
+uint32_t host_next_epoch(fo_ctx* ctx) { return ++ctx->epoch; }
+uint32_t* host_ctrl(fo_ctx* ctx) { return ctx->ctrl; }
+int host_num_sms(fo_ctx* ctx) { return ctx->num_sms; }
+cudaStream_t host_link(fo_ctx* ctx, int r) { return ctx->link[r]; }
+cudaEvent_t host_ev_hop(fo_ctx* ctx, int r, int t) { return ctx->ev_hop[r][t]; }
+fo_status host_fork(fo_ctx* ctx, int P, cudaStream_t s) { return fork_links(ctx, P, s); }
+fo_status host_join(fo_ctx* ctx, int P, cudaStream_t s) { return join_links(ctx, P, s); }
+fo_status host_copy_rows(void* dst, int64_t dld, const void* src, int64_t sld, int64_t rows, int64_t cols,
+                         size_t esz, cudaStream_t s) {
+  return copy_rows(dst, dld, src, sld, rows, cols, esz, s);
+}
+fo_status host_write_flag(cudaStream_t s, uint32_t* flag, uint32_t value) { return write_flag(s, flag, value); }
+fo_status host_encode_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+  return encode_map(map, ptr, rows, cols, ld, box_rows);
+}
+fo_status host_check_mat(const fo_mat& a, int32_t dtype, const char* what, int r) {
+  return check_mat(a, dtype, what, r);
+}
+fo_status host_fail(fo_status st, const char* msg) { return fail(st, "%s", msg); }
+uint64_t host_timeout_ns(const fo_opts& o) { return timeout_ns(o); }
+int host_grid(fo_ctx* ctx, const fo_opts& o, int work) { return grid_size(ctx, o, work); }
+}  // namespace fo

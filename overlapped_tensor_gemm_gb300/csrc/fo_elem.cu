@@ -1,0 +1,102 @@
+// Elementwise kernels of the MLP layer glue and of the baselines.  Both are
+// bound by HBM bandwidth: 16-byte vector accesses, grid sized in multiples of
+// the SM count by the caller's launch helper.
+#include <cuda_bf16.h>
+
+#include "fo_internal.h"
+
+namespace fo {
+namespace {
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+// H = SiLU(G) * U, 8 columns per thread; G = GU[:, 0:f], U = GU[:, f:2f].
+__global__ void silu_mul_kernel(const __grid_constant__ SiluMulArgs a) {
+  const int64_t vec_per_row = a.f / 8;
+  const int64_t per_rank = a.rows * vec_per_row;
+  const int64_t total = per_rank * a.P;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(i / per_rank);
+    const int64_t j = i - r * per_rank;
+    const int64_t row = j / vec_per_row;
+    const int64_t col = (j - row * vec_per_row) * 8;
+    const uint16_t* gp = a.gu[r] + row * a.ld_gu[r] + col;
+    const uint4 g = *reinterpret_cast<const uint4*>(gp);
+    const uint4 u = *reinterpret_cast<const uint4*>(gp + a.f);
+    uint4 o;
+    o.x = pack2(silu(bf16_lo(g.x)) * bf16_lo(u.x), silu(bf16_hi(g.x)) * bf16_hi(u.x));
+    o.y = pack2(silu(bf16_lo(g.y)) * bf16_lo(u.y), silu(bf16_hi(g.y)) * bf16_hi(u.y));
+    o.z = pack2(silu(bf16_lo(g.z)) * bf16_lo(u.z), silu(bf16_hi(g.z)) * bf16_hi(u.z));
+    o.w = pack2(silu(bf16_lo(g.w)) * bf16_lo(u.w), silu(bf16_hi(g.w)) * bf16_hi(u.w));
+    *reinterpret_cast<uint4*>(a.h[r] + row * a.ld_h[r] + col) = o;
+  }
+}
+
+// c = a + b over a [rows, cols] fp32 block, 4 columns per thread.
+__global__ void add_f32_kernel(const float* __restrict__ a, int64_t lda, const float* __restrict__ b, int64_t ldb,
+                               float* c32, uint16_t* c16, int64_t ldc, int64_t rows, int64_t cols) {
+  const int64_t vec_per_row = cols / 4;
+  const int64_t total = rows * vec_per_row;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row = i / vec_per_row;
+    const int64_t col = (i - row * vec_per_row) * 4;
+    const float4 x = *reinterpret_cast<const float4*>(a + row * lda + col);
+    const float4 y = *reinterpret_cast<const float4*>(b + row * ldb + col);
+    const float4 z = make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w);
+    if (c32) {
+      *reinterpret_cast<float4*>(c32 + row * ldc + col) = z;
+    } else {
+      uint2 o;
+      o.x = pack2(z.x, z.y);
+      o.y = pack2(z.z, z.w);
+      *reinterpret_cast<uint2*>(c16 + row * ldc + col) = o;
+    }
+  }
+}
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+int grid_for(int64_t work, int threads) {
+  const int64_t blocks = (work + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;  // 8 resident 256-thread blocks per SM
+  return static_cast<int>(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_silu_mul(const SiluMulArgs& a, cudaStream_t s) {
+  const int64_t work = a.rows * (a.f / 8) * a.P;
+  if (work == 0) return cudaSuccess;
+  silu_mul_kernel<<<grid_for(work, 256), 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_add_f32(const float* a, int64_t lda, const float* b, int64_t ldb, float* c_f32, uint16_t* c_bf16,
+                           int64_t ldc, int64_t rows, int64_t cols, cudaStream_t s) {
+  const int64_t work = rows * (cols / 4);
+  if (work == 0) return cudaSuccess;
+  add_f32_kernel<<<grid_for(work, 256), 256, 0, s>>>(a, lda, b, ldb, c_f32, c_bf16, ldc, rows, cols);
+  return cudaGetLastError();
+}
+
+}  // namespace fo

@@ -1,0 +1,348 @@
+// Persistent tcgen05 GEMM with ring-aware tile schedule and epilogues.
+//
+// One launch computes every (rank, step) unit of a decomposed collective:
+// Flash-AG (FlashOverlap technical summary, section 2 "Flash-All-Gather") and
+// Flash-RS (section 2 "Flash-Reduce-Scatter").  The host lays the units out in
+// the method's step order; the kernel walks the tiles in that order, so the
+// slices that need no transfer (AG: local slice; RS: first hop) are computed
+// while the ring moves the others, and the RS kept slice comes last.
+//
+// CTA layout (192 threads, one CTA per SM, persistent):
+//   warp 0      TMA producer: waits for a slice's arrival flag (AG), then streams
+//               128x64 A and 256x64 B bf16 tiles (128-byte swizzle) into a
+//               4-stage shared-memory ring.
+//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators) and
+//               issues tcgen05.mma (M=128, N=256, K=16) from one thread.
+//   warps 2-5   epilogue: tcgen05.ld of its 32-lane quadrant, optional fp32
+//               partial-sum add (RS, after acquiring the per-tile flag), store,
+//               then release of the per-tile flag read by the next rank.
+// Accumulators are double-buffered so the epilogue of tile i overlaps the
+// main loop of tile i+1.
+#include <cuda_bf16.h>
+
+#include "fo_internal.h"
+#include "fo_ptx.cuh"
+
+namespace fo {
+namespace {
+
+constexpr uint32_t kABytes = kBM * kBK * 2;  // 16 KiB
+constexpr uint32_t kBBytes = kBN * kBK * 2;  // 32 KiB
+constexpr uint32_t kStageBytes = kABytes + kBBytes;
+constexpr uint32_t kTmemCols = 2 * kBN;      // two accumulators
+constexpr uint32_t kIdesc = umma_idesc_bf16(kBM, kBN);
+constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;  // 200 ms for in-flight async work on abort
+
+struct alignas(8) SmemCtl {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  uint32_t pad;
+};
+
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 + static_cast<int>(sizeof(SmemCtl));
+
+__device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int tile) {
+  int g = 0;
+  while (g + 1 < p.num_groups && tile >= p.group_tile_begin[g + 1]) ++g;
+  const int j = tile - p.group_tile_begin[g];
+  const int u0 = p.group_unit_begin[g];
+  const int nu = p.group_unit_begin[g + 1] - u0;
+  const int tm = p.units[u0].tiles_m;
+  const int tn = p.units[u0].tiles_n;
+  TileCoord c;
+  if (p.mblock_major) {
+    c.mb = j / (nu * tn);
+    const int rem = j - c.mb * nu * tn;
+    c.unit = u0 + rem / tn;
+    c.nb = rem % tn;
+  } else {
+    const int u = j / (tm * tn);
+    const int rem = j - u * tm * tn;
+    c.unit = u0 + u;
+    c.mb = rem / tn;
+    c.nb = rem % tn;
+  }
+  return c;
+}
+
+// ---------------------------------------------------------------------------
+// warp roles
+// ---------------------------------------------------------------------------
+
+__device__ void producer_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl) {
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t armed = 0;        // bit s: stage s has been armed at least once
+  uint32_t armed_phase = 0;  // bit s: phase parity of the last arming of stage s
+  int waited_unit = -1;
+  bool ok = true;
+  for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
+    const TileCoord tc = decode_tile(p, tile);
+    const GemmUnit& u = p.units[tc.unit];
+    if (u.wait_flag >= 0 && tc.unit != waited_unit) {
+      ok = flag_wait(p.flags + u.wait_flag, p.epoch, p.ctrl, p.timeout_ns, kSiteAgFlag,
+                     static_cast<uint32_t>(u.wait_flag));
+      if (!ok) break;
+      // the slice was written by the copy engine; order the TMA reads after the acquire
+      fence_proxy_async_global();
+      waited_unit = tc.unit;
+    }
+    const int nk = (u.k + kBK - 1) / kBK;
+    const int a_row = u.a_row0 + tc.mb * kBM;
+    const int b_row = u.b_row0 + tc.nb * kBN;
+    for (int kb = 0; kb < nk; ++kb) {
+      if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty,
+                     static_cast<uint32_t>(tile))) {
+        ok = false;
+        break;
+      }
+      uint8_t* a = tiles + stage * kStageBytes;
+      uint8_t* b = a + kABytes;
+      mbar_arrive_expect_tx(&ctl->full[stage], kStageBytes);
+      tma_load_2d(&p.maps[u.a_map], a, &ctl->full[stage], kb * kBK, a_row);
+      tma_load_2d(&p.maps[u.b_map], b, &ctl->full[stage], kb * kBK, b_row);
+      armed |= 1u << stage;
+      armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+  if (!ok) {
+    // leave no TMA write in flight into this CTA's shared memory
+    for (int s = 0; s < kStages; ++s)
+      if ((armed >> s) & 1u) mbar_wait_drain(&ctl->full[s], (armed_phase >> s) & 1u, kDrainNs);
+  }
+}
+
+__device__ void mma_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl, uint32_t tmem_base) {
+  int stage = 0;
+  uint32_t phase = 0;
+  int acc = 0;
+  uint32_t acc_phase = 0;
+  bool issued = false;
+  bool ok = true;
+  const uint32_t tiles_addr = smem_u32(tiles);
+  for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
+    const TileCoord tc = decode_tile(p, tile);
+    const GemmUnit& u = p.units[tc.unit];
+    if (!mbar_wait(&ctl->tmem_empty[acc], acc_phase ^ 1u, p.ctrl, p.timeout_ns, kSiteTmemEmpty,
+                   static_cast<uint32_t>(tile))) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+    const int nk = (u.k + kBK - 1) / kBK;
+    for (int kb = 0; kb < nk; ++kb) {
+      if (!mbar_wait(&ctl->full[stage], phase, p.ctrl, p.timeout_ns, kSiteFull, static_cast<uint32_t>(tile))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t a_addr = tiles_addr + stage * kStageBytes;
+      const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+      for (int k = 0; k < kBK / 16; ++k) {
+        // K advance inside the 128-byte swizzle atom: +32 bytes per UMMA_K=16
+        umma_bf16_ss(d_tmem, umma_sdesc_sw128(a_addr + k * 32), umma_sdesc_sw128(b_addr + k * 32), kIdesc,
+                     (kb | k) != 0 ? 1u : 0u);
+      }
+      issued = true;
+      umma_commit(&ctl->empty[stage]);  // frees the stage once these MMAs have read it
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok) break;
+    umma_commit(&ctl->tmem_full[acc]);  // accumulator complete
+    acc ^= 1;
+    if (acc == 0) acc_phase ^= 1u;
+  }
+  if (!ok && issued) {
+    // wait for every issued MMA before TMEM is released
+    umma_commit(&ctl->drain);
+    mbar_wait_drain(&ctl->drain, 0, kDrainNs);
+  }
+}
+
+// One 32-column chunk of one row: optional fp32 partial add, then store.
+__device__ __forceinline__ void store_chunk(const GemmUnit& u, int row, int col, const uint32_t (&v)[32]) {
+  float f[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+  const bool full = col + 32 <= u.n_cols;
+  const int ncol = full ? 32 : u.n_cols - col;
+  if (u.epi == kEpiAddF32 || u.epi == kEpiAddBF16) {
+    const float* src = u.acc_in + static_cast<int64_t>(row) * u.ld_acc + col;
+    if (full) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 a = ld_cg_f4(src + 4 * i);
+        f[4 * i + 0] += a.x;
+        f[4 * i + 1] += a.y;
+        f[4 * i + 2] += a.z;
+        f[4 * i + 3] += a.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < ncol) f[i] += __ldcg(src + i);
+    }
+  }
+  if (u.epi == kEpiBF16 || u.epi == kEpiAddBF16) {
+    uint16_t* dst = static_cast<uint16_t*>(u.c) + static_cast<int64_t>(row) * u.ldc + col;
+    if (full) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        st_v4_u32(dst + 8 * i, pack_bf16x2(f[8 * i + 0], f[8 * i + 1]), pack_bf16x2(f[8 * i + 2], f[8 * i + 3]),
+                  pack_bf16x2(f[8 * i + 4], f[8 * i + 5]), pack_bf16x2(f[8 * i + 6], f[8 * i + 7]));
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < ncol) dst[i] = __bfloat16_as_ushort(__float2bfloat16_rn(f[i]));
+    }
+  } else {
+    float* dst = static_cast<float*>(u.c) + static_cast<int64_t>(row) * u.ldc + col;
+    if (full) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        st_v4_u32(dst + 4 * i, __float_as_uint(f[4 * i + 0]), __float_as_uint(f[4 * i + 1]),
+                  __float_as_uint(f[4 * i + 2]), __float_as_uint(f[4 * i + 3]));
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < ncol) dst[i] = f[i];
+    }
+  }
+}
+
+// Lane 0 waits; the outcome is broadcast so the whole warp takes one path.
+__device__ __forceinline__ bool warp_mbar_wait(uint64_t* bar, uint32_t parity, const GemmParams& p,
+                                               uint32_t site, uint32_t detail, int lane) {
+  uint32_t ok = 0;
+  if (lane == 0) ok = mbar_wait(bar, parity, p.ctrl, p.timeout_ns, site, detail) ? 1u : 0u;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ bool warp_flag_wait(const uint32_t* flag, const GemmParams& p, uint32_t site,
+                                               uint32_t detail, int lane) {
+  uint32_t ok = 0;
+  if (lane == 0) ok = flag_wait(flag, p.epoch, p.ctrl, p.timeout_ns, site, detail) ? 1u : 0u;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) (void)ld_acquire_gpu(flag);  // every lane orders its own partial-sum reads after the flag
+  return ok != 0;
+}
+
+__device__ void epilogue_loop(const GemmParams& p, SmemCtl* ctl, uint32_t tmem_base, int warp, int lane) {
+  const int q = warp & 3;  // TMEM lanes [32q, 32q+32) are the only ones this warp may access
+  int acc = 0;
+  uint32_t acc_phase = 0;
+  for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
+    const TileCoord tc = decode_tile(p, tile);
+    const GemmUnit& u = p.units[tc.unit];
+    if (!warp_mbar_wait(&ctl->tmem_full[acc], acc_phase, p, kSiteTmemFull, static_cast<uint32_t>(tile), lane))
+      return;
+    tc_fence_after();
+    const int tile_in_unit = tc.mb * u.tiles_n + tc.nb;
+    if (u.in_flag_base >= 0) {
+      const int f = u.in_flag_base + tile_in_unit * 4 + q;
+      if (!warp_flag_wait(p.flags + f, p, kSiteAccInFlag, static_cast<uint32_t>(f), lane)) return;
+    }
+    const int row = tc.mb * kBM + q * 32 + lane;
+    const bool row_ok = row < u.m_rows;
+    const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      uint32_t v[32];
+      tmem_ld32(tbase + c * 32, v);
+      tmem_wait_ld();
+      const int col = tc.nb * kBN + c * 32;
+      if (row_ok && col < u.n_cols) store_chunk(u, row, col, v);
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl->tmem_empty[acc]);
+    if (u.out_flag_base >= 0) {
+      // rows of this quadrant are stored: publish them to the next rank
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) st_release_gpu(p.flags + u.out_flag_base + tile_in_unit * 4 + q, p.epoch);
+    }
+    acc ^= 1;
+    if (acc == 0) acc_phase ^= 1u;
+  }
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t base = smem_u32(smem_raw);
+  uint8_t* tiles = smem_raw + ((1024u - (base & 1023u)) & 1023u);
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(tiles + kStages * kStageBytes);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&ctl->tmem_full[b], 1);
+      mbar_init(&ctl->tmem_empty[b], 4);
+    }
+    mbar_init(&ctl->drain, 1);
+    fence_barrier_init();
+    fence_proxy_async_shared();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < p.num_maps; ++i) tma_prefetch_desc(&p.maps[i]);
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) producer_loop(p, tiles, ctl);
+  } else if (warp == 1) {
+    if (lane == 0) mma_loop(p, tiles, ctl, tmem_base);
+    __syncwarp();
+  } else {
+    epilogue_loop(p, ctl, tmem_base, warp, lane);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace
+
+int gemm_smem_bytes() { return kSmemBytes; }
+
+cudaError_t gemm_configure() {
+  return cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+}
+
+cudaError_t gemm_launch(const GemmParams& p, int grid, cudaStream_t s) {
+  gemm_kernel<<<grid, kGemmThreads, kSmemBytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace fo

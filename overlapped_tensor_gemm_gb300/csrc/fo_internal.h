@@ -1,0 +1,111 @@
+// Internal definitions shared by the host side and the kernels of the
+// Flash-Overlap library (not part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fo.h"
+
+namespace fo {
+
+constexpr int kMaxP = 8;
+
+// ---------------------------------------------------------------------------
+// Persistent tcgen05 GEMM: problem description
+// ---------------------------------------------------------------------------
+//
+// A launch computes a list of "units".  A unit is one rank's GEMM on one ring
+// step: rows [a_row0, a_row0 + m_rows) of its A operand (via a TMA map)
+// times the rows [b_row0, b_row0 + n_cols) of its B operand (nn.Linear
+// layout, K contiguous), written through a per-unit epilogue.  Units are
+// grouped (one group per ring step); the tiles of a launch are enumerated group
+// by group, and inside a group either unit-major or m-block-major.  Every CTA
+// walks the global tile sequence with stride gridDim.x, so a tile only ever
+// waits on tiles with a smaller index (deadlock freedom of the in-kernel ring).
+
+constexpr int kBM = 128;            // UMMA M
+constexpr int kBN = 256;            // UMMA N
+constexpr int kBK = 64;             // one 128-byte swizzle atom of bf16
+constexpr int kStages = 4;
+constexpr int kGemmThreads = 192;   // warp 0: TMA, warp 1: MMA, warps 2-5: epilogue
+constexpr int kMaxMaps = 24;
+constexpr int kMaxUnits = 64;
+constexpr int kMaxGroups = 16;
+
+enum EpiMode : int32_t {
+  kEpiBF16 = 0,        // C (bf16) = acc
+  kEpiF32 = 1,         // C (fp32) = acc
+  kEpiAddF32 = 2,      // C (fp32) = acc + acc_in
+  kEpiAddBF16 = 3,     // C (bf16) = acc + acc_in
+};
+
+struct GemmUnit {
+  int32_t a_map, b_map;        // indices into GemmParams::maps
+  int32_t a_row0, b_row0;      // row offsets into the A / B tensors
+  int32_t m_rows, n_cols, k;   // valid extent of this unit
+  int32_t tiles_m, tiles_n;
+  int32_t wait_flag;           // AG: flag index that must reach `epoch` before A is read (-1: none)
+  int32_t in_flag_base;        // RS: per-tile flags guarding acc_in (-1: none)
+  int32_t out_flag_base;       // RS: per-tile flags released after C is written (-1: none)
+  int32_t epi;                 // EpiMode
+  int32_t pad0;
+  void* c;                     // output
+  const float* acc_in;         // fp32 partial sum to add (kEpiAdd*)
+  int64_t ldc, ld_acc;         // leading dimensions in elements
+};
+
+struct GemmParams {
+  CUtensorMap maps[kMaxMaps];
+  GemmUnit units[kMaxUnits];
+  int32_t group_unit_begin[kMaxGroups + 1];
+  int32_t group_tile_begin[kMaxGroups + 1];
+  int32_t num_groups;
+  int32_t num_maps;            // maps[0, num_maps) are valid
+  int32_t mblock_major;        // 1: tiles of a group ordered (m-block, unit, n-block)
+  int32_t total_tiles;
+  uint32_t epoch;
+  uint64_t timeout_ns;
+  uint32_t* flags;             // ring flags (epoch-valued)
+  uint32_t* ctrl;              // device control block (error word, abort flag)
+};
+// A tile's position: unit index, m-block and n-block inside the unit.
+struct TileCoord {
+  int unit, mb, nb;
+};
+
+// Device control block layout (uint32 words).
+enum CtrlWord : int {
+  kCtrlError = 0,     // first error code (FO_ERR_*), 0 = none
+  kCtrlAbort = 1,     // non-zero: every CTA leaves its loops
+  kCtrlWhere = 2,     // where the first timeout happened (see WaitSite)
+  kCtrlDetail = 3,    // flag index / tile index of the first timeout
+  kCtrlWords = 8
+};
+
+enum WaitSite : uint32_t {
+  kSiteAgFlag = 1, kSiteFull = 2, kSiteEmpty = 3, kSiteTmemFull = 4,
+  kSiteTmemEmpty = 5, kSiteAccInFlag = 6, kSiteDrain = 7, kSiteAttnFlag = 8,
+  kSiteAttnBar = 9
+};
+
+// host launchers (fo_gemm.cu)
+cudaError_t gemm_configure();
+cudaError_t gemm_launch(const GemmParams& p, int grid, cudaStream_t s);
+int gemm_smem_bytes();
+
+// elementwise kernels (fo_elem.cu); bf16 data is passed as raw uint16_t
+struct SiluMulArgs {
+  const uint16_t* gu[kMaxP];
+  uint16_t* h[kMaxP];
+  int64_t ld_gu[kMaxP], ld_h[kMaxP];
+  int64_t rows, f;
+  int32_t P;
+};
+cudaError_t launch_silu_mul(const SiluMulArgs& a, cudaStream_t s);
+// c = a + b (fp32 inputs); c is fp32 (c_f32) or bf16 (c_bf16), exactly one non-null
+cudaError_t launch_add_f32(const float* a, int64_t lda, const float* b, int64_t ldb, float* c_f32,
+                           uint16_t* c_bf16, int64_t ldc, int64_t rows, int64_t cols, cudaStream_t s);
+
+}  // namespace fo

@@ -1,0 +1,50 @@
+"""Shared helpers of the GPU parity tests (CPU side: bf16 bit transfers, tolerances)."""
+import numpy as np
+import torch
+
+from oracle import bf16
+
+# Tolerance for Gaussian bf16 inputs with fp32 accumulation (relative L2 and
+# max-abs relative to the largest reference magnitude).
+REL_L2 = 2e-3
+MAX_ABS_FRAC = 1e-2
+
+
+def to_dev(bits: np.ndarray, device="cuda") -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16).copy()).view(torch.bfloat16)
+    return t.to(device)
+
+
+def to_bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def f64(bits) -> np.ndarray:
+    return bf16.to_f64(bits)
+
+
+def assert_bits_equal(got_bits: np.ndarray, ref_f64: np.ndarray, what: str = ""):
+    ref_bits = bf16.from_f64(ref_f64)
+    diff = np.nonzero(got_bits != ref_bits)
+    if diff[0].size:
+        i = tuple(d[0] for d in diff)
+        raise AssertionError(f"{what}: {diff[0].size} of {got_bits.size} elements differ; first at {i}: "
+                             f"got {bf16.to_f64(got_bits[i])} want {ref_f64[i]}")
+
+
+def assert_close(got: np.ndarray, ref: np.ndarray, what: str = "", round_ref: bool = True):
+    """Tolerance check of a bf16 result; the reference is rounded to bf16 (the
+    operation's output type) unless round_ref is False."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    if round_ref:
+        ref = bf16.round_f64(ref)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    num = np.linalg.norm(got - ref)
+    den = np.linalg.norm(ref) or 1.0
+    rel = num / den
+    mx = np.abs(got - ref).max() if got.size else 0.0
+    lim = MAX_ABS_FRAC * (np.abs(ref).max() if ref.size else 0.0)
+    assert rel <= REL_L2, f"{what}: rel-L2 {rel:.3e} > {REL_L2}"
+    assert mx <= lim, f"{what}: max-abs {mx:.3e} > {lim:.3e}"

@@ -1,0 +1,56 @@
+"""The C-ABI library loads on a host without a GPU, exports every entry point that
+include/fo.h declares, and rejects bad arguments synchronously (no compute calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import overlapped_tensor_gemm_gb300 as fo
+
+
+@pytest.fixture(scope="module")
+def lib(repo_root):
+    if not os.path.exists(fo.LIB_PATH):
+        from overlapped_tensor_gemm_gb300 import _build
+        _build.build()
+    return fo.load()
+
+
+def _declared(repo_root):
+    with open(os.path.join(repo_root, "include", "fo.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"FO_API\s+[\w\s\*]*?\b(fo_\w+)\s*\(", text)))
+
+
+def test_header_and_binding_agree(repo_root):
+    assert _declared(repo_root) == sorted(fo.ABI_SYMBOLS)
+
+
+def test_every_declared_symbol_is_exported(lib, repo_root):
+    for name in _declared(repo_root):
+        assert hasattr(lib, name), name
+    assert lib.fo_version() == 100
+
+
+def test_null_arguments_are_rejected(lib):
+    null = ctypes.c_void_p()
+    mats = (fo.FoMat * 2)()
+    o = fo.opts()
+    assert lib.fo_ag_gemm(null, mats, mats, 2, mats, ctypes.byref(o), null) == fo.FO_ERR_INVALID_ARG
+    assert b"context" in lib.fo_last_error_string()
+    assert lib.fo_gemm_rs(null, mats, mats, 2, mats, ctypes.byref(o), null) == fo.FO_ERR_INVALID_ARG
+    assert lib.fo_ctx_poll(null) == fo.FO_ERR_INVALID_ARG
+    assert lib.fo_ctx_create(0, None) == fo.FO_ERR_INVALID_ARG
+    assert lib.fo_ctx_destroy(null) == fo.FO_OK
+
+
+def test_context_creation_without_gpu_fails_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = ctypes.c_void_p()
+    st = lib.fo_ctx_create(0, ctypes.byref(h))
+    assert st in (fo.FO_ERR_CUDA, fo.FO_ERR_INVALID_ARG)
+    assert not h.value
+    assert lib.fo_last_error_string()

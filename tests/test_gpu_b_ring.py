@@ -1,0 +1,118 @@
+"""Parity of Flash-AG / Flash-RS / the MLP layer (and their baselines) against the
+oracle's simulated ring, through the C ABI (FlashOverlap technical summary, section 2)."""
+import numpy as np
+import pytest
+import torch
+
+import fo_workloads as wl
+from helpers import assert_bits_equal, assert_close, f64, to_bits, to_dev
+from oracle import bf16, ops
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    import overlapped_tensor_gemm_gb300 as fo
+    c = fo.Context(0)
+    yield c
+    c.close()
+
+
+def _ag(ctx, P, m, K, N, integer, seed, **kw):
+    inp = wl.ag_inputs(P, m, K, N, seed, integer)
+    X = [to_dev(x) for x in inp["X_shards"]]
+    W = [to_dev(w) for w in inp["W_col"]]
+    Y = [torch.full((P * m, N), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    ctx.ag_gemm(X, W, Y, **kw)
+    torch.cuda.synchronize()
+    ctx.poll()
+    ref, _ = ops.ag_gemm_ring([f64(x) for x in inp["X_shards"]], [f64(w) for w in inp["W_col"]])
+    return Y, ref
+
+
+def _rs(ctx, P, m, Kr, N, integer, seed, **kw):
+    inp = wl.rs_inputs(P, P * m, N, Kr, seed, integer)
+    X = [to_dev(x) for x in inp["X"]]
+    W = [to_dev(w) for w in inp["W_row"]]
+    Y = [torch.full((m, N), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    ctx.gemm_rs(X, W, Y, **kw)
+    torch.cuda.synchronize()
+    ctx.poll()
+    chunks = [ops.split_chunks(f64(x), P) for x in inp["X"]]
+    ref, _ = ops.gemm_rs_ring(chunks, [f64(w) for w in inp["W_row"]])
+    return Y, ref
+
+
+@pytest.mark.parametrize("P,m,K,N", [(1, 128, 256, 256), (2, 128, 256, 512), (4, 256, 512, 768),
+                                     (3, 200, 136, 300), (8, 128, 128, 256)])
+def test_ag_flash_integer_bit_exact(ctx, P, m, K, N):
+    Y, ref = _ag(ctx, P, m, K, N, True, 100 + P)
+    for r in range(P):
+        assert_bits_equal(to_bits(Y[r]), ref[r], f"AG P={P} rank {r}")
+
+
+@pytest.mark.parametrize("order", ["serial", "slicing"])
+def test_ag_baselines_integer_bit_exact(ctx, order):
+    P, m, K, N = 4, 256, 512, 512
+    Y, ref = _ag(ctx, P, m, K, N, True, 7, order=order)
+    for r in range(P):
+        assert_bits_equal(to_bits(Y[r]), ref[r], f"AG {order} rank {r}")
+
+
+@pytest.mark.parametrize("P,m,Kr,N", [(1, 128, 256, 256), (2, 128, 256, 512), (4, 256, 384, 512),
+                                      (3, 72, 200, 264), (8, 64, 128, 1024)])
+@pytest.mark.parametrize("order", ["flash", "naive"])
+def test_rs_integer_bit_exact(ctx, P, m, Kr, N, order):
+    Y, ref = _rs(ctx, P, m, Kr, N, True, 200 + P, order=order)
+    for r in range(P):
+        assert_bits_equal(to_bits(Y[r]), ref[r], f"RS {order} P={P} rank {r}")
+
+
+@pytest.mark.parametrize("order", ["serial", "slicing"])
+def test_rs_baselines_integer_bit_exact(ctx, order):
+    P, m, Kr, N = 4, 256, 256, 512
+    Y, ref = _rs(ctx, P, m, Kr, N, True, 9, order=order)
+    for r in range(P):
+        assert_bits_equal(to_bits(Y[r]), ref[r], f"RS {order} rank {r}")
+
+
+def test_ag_rs_gaussian_tolerance(ctx):
+    Y, ref = _ag(ctx, 4, 256, 1024, 512, False, 11)
+    for r in range(4):
+        assert_close(f64(to_bits(Y[r])), ref[r], f"AG gaussian rank {r}")
+    Y, ref = _rs(ctx, 4, 256, 1024, 512, False, 12)
+    for r in range(4):
+        assert_close(f64(to_bits(Y[r])), ref[r], f"RS gaussian rank {r}")
+
+
+def test_tiny_mlp_layer_bit_exact(ctx):
+    cfg = wl.TINY
+    inp = wl.mlp_inputs(cfg)
+    X = [to_dev(x) for x in inp["X_shards"]]
+    Wc = [to_dev(w) for w in inp["W_col"]]
+    Wr = [to_dev(w) for w in inp["W_row"]]
+    Z = [torch.empty((cfg.m, cfg.hidden), dtype=torch.bfloat16, device="cuda") for _ in range(cfg.P)]
+    ctx.mlp_layer(X, Wc, Wr, Z, gated=False)
+    torch.cuda.synchronize()
+    ctx.poll()
+    _, _, ref = ops.mlp_layer([f64(x) for x in inp["X_shards"]], [f64(w) for w in inp["W_col"]],
+                              [f64(w) for w in inp["W_row"]], gated=False)
+    for r in range(cfg.P):
+        assert_bits_equal(to_bits(Z[r]), ref[r], f"tiny MLP rank {r}")
+
+
+def test_gated_mlp_layer_tolerance(ctx):
+    cfg = wl.MLPConfig("small-gated", 1, P=4, tokens=512, hidden=256, ffn=1024, gated=True, integer=False)
+    inp = wl.mlp_inputs(cfg)
+    X = [to_dev(x) for x in inp["X_shards"]]
+    Wc = [to_dev(w) for w in inp["W_col"]]
+    Wr = [to_dev(w) for w in inp["W_row"]]
+    Z = [torch.empty((cfg.m, cfg.hidden), dtype=torch.bfloat16, device="cuda") for _ in range(cfg.P)]
+    ctx.mlp_layer(X, Wc, Wr, Z, gated=True)
+    torch.cuda.synchronize()
+    ctx.poll()
+    _, _, ref = ops.mlp_layer([f64(x) for x in inp["X_shards"]], [f64(w) for w in inp["W_col"]],
+                              [f64(w) for w in inp["W_row"]], gated=True)
+    for r in range(cfg.P):
+        assert_close(f64(to_bits(Z[r])), ref[r], f"gated MLP rank {r}")

@@ -1,0 +1,78 @@
+"""Parity of query-split attention (fo_qsplit_attn) against the oracle's two-pass fp64
+definition and its ring simulation (FlashOverlap technical summary, section 2)."""
+import numpy as np
+import pytest
+import torch
+
+import fo_workloads as wl
+from helpers import assert_close, f64, to_bits, to_dev
+from oracle import bf16, ops
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    import overlapped_tensor_gemm_gb300 as fo
+    c = fo.Context(0)
+    yield c
+    c.close()
+
+
+def _attn(ctx, P, m, H, seed, causal=True, **kw):
+    inp = wl.attn_inputs(P, P * m, H, 128, seed)
+    Q = [to_dev(x).reshape(m, H * 128) for x in inp["Q"]]
+    K = [to_dev(x).reshape(m, H * 128) for x in inp["K"]]
+    V = [to_dev(x).reshape(m, H * 128) for x in inp["V"]]
+    O = [torch.full((m, H * 128), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    ctx.qsplit_attn(Q, K, V, O, heads=H, head_dim=128, causal=causal, **kw)
+    torch.cuda.synchronize()
+    ctx.poll()
+    got = [f64(to_bits(o)).reshape(m, H, 128) for o in O]
+    return inp, got
+
+
+@pytest.mark.parametrize("P,m,H", [(1, 128, 1), (2, 128, 2), (4, 256, 3), (3, 384, 2)])
+def test_attention_matches_definition(ctx, P, m, H):
+    inp, got = _attn(ctx, P, m, H, 300 + P)
+    ref = ops.attention_definition(np.concatenate([f64(x) for x in inp["Q"]]),
+                                   np.concatenate([f64(x) for x in inp["K"]]),
+                                   np.concatenate([f64(x) for x in inp["V"]]))
+    assert_close(np.concatenate(got), ref, f"attention P={P}")
+
+
+def test_attention_matches_ring_simulation_pruned(ctx):
+    P, m, H = 4, 128, 2
+    inp, got = _attn(ctx, P, m, H, 41, causal_prune=True)
+    ref, _ = ops.qsplit_attention_ring([f64(x) for x in inp["Q"]], [f64(x) for x in inp["K"]],
+                                       [f64(x) for x in inp["V"]], prune=True)
+    for r in range(P):
+        assert_close(got[r], ref[r], f"pruned ring rank {r}")
+
+
+def test_attention_non_causal(ctx):
+    P, m, H = 2, 256, 2
+    inp, got = _attn(ctx, P, m, H, 42, causal=False)
+    ref = ops.attention_definition(np.concatenate([f64(x) for x in inp["Q"]]),
+                                   np.concatenate([f64(x) for x in inp["K"]]),
+                                   np.concatenate([f64(x) for x in inp["V"]]), causal=False)
+    assert_close(np.concatenate(got), ref, "non-causal attention")
+
+
+def test_attention_constant_v_is_exact(ctx):
+    # closed form: a constant V gives that constant at every query
+    P, m, H = 2, 128, 1
+    inp = wl.attn_inputs(P, P * m, H, 128, 43)
+    c = wl.gaussian_bf16(torch.Generator().manual_seed(5), (1, H, 128))
+    V = [np.repeat(c, m, axis=0) for _ in range(P)]
+    Q = [to_dev(x).reshape(m, H * 128) for x in inp["Q"]]
+    K = [to_dev(x).reshape(m, H * 128) for x in inp["K"]]
+    Vd = [to_dev(x).reshape(m, H * 128) for x in V]
+    O = [torch.empty((m, H * 128), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    ctx.qsplit_attn(Q, K, Vd, O, heads=H, head_dim=128)
+    torch.cuda.synchronize()
+    want = np.repeat(c.reshape(1, -1), m, axis=0)
+    for r in range(P):
+        got = to_bits(O[r])
+        # one bf16 ulp allowed: the weights' sum and the P.V accumulation round differently
+        assert np.abs(f64(got) - f64(want)).max() <= np.abs(f64(want)).max() * 2 ** -7
