@@ -60,6 +60,13 @@ def peaks():
     return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
+def aggregate(flop_per_rank: float, ms_per_rank: float, world: int, reduce_max) -> tuple[float, float]:
+    """Whole-job throughput of `world` independent replicas: all ranks' FLOP over the
+    slowest rank's time.  Returns (TFLOP/s, max ms)."""
+    ms_max = reduce_max(ms_per_rank)
+    return world * flop_per_rank / (ms_max * 1e-3) / 1e12, ms_max
+
+
 def mlp_config(name: str):
     if name == "llama8b":
         return wl.LLAMA8B
@@ -226,8 +233,7 @@ def run_ours(args, rank: int, world: int, device: int):
     barrier()
     ctx.poll()
     ms = e0.elapsed_time(e1) / args.steps
-    ms_max = max_over_ranks(ms)
-    value = world * flops["total"] / (ms_max * 1e-3) / 1e12
+    value, ms_max = aggregate(flops["total"], ms, world, max_over_ranks)
     launches_per_step = 3 if cfg.gated else 2
 
     out = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,

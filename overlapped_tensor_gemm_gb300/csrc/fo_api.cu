@@ -224,12 +224,13 @@ int grid_size(const fo_ctx* ctx, const fo_opts& o, int tiles) {
 // TMA maps
 // --------------------------------------------------------------------------
 
-fo_status encode_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+fo_status encode_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows,
+                     CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
-  FO_CU(driver()->encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+  FO_CU(driver()->encode_tiled(map, dtype, 2, const_cast<void*>(ptr), dims, strides,
                                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
   return FO_OK;
@@ -560,12 +561,18 @@ fo_status rs_flash(fo_ctx* ctx, const RsArgs& a, const fo_opts& o, cudaStream_t 
       for (int h = 0; h < P; ++h) add(mod(c + 1 + h, P), c);
     }
   } else {
-    for (int t = 0; t < P; ++t) {  // rank-adaptive: chunk (r - t - 1) mod P, kept chunk r last
+    // rank-adaptive: chunk (r - t - 1) mod P, kept chunk r last.  Step t lists the
+    // ranks starting at t, so every unit sits at the same position as the unit of
+    // the previous step whose partial sum it consumes: a whole step apart.
+    for (int t = 0; t < P; ++t) {
       L.begin_group();
-      for (int r = 0; r < P; ++r) add(r, mod(r - t - 1, P));
+      for (int i = 0; i < P; ++i) {
+        const int r = mod(t + i, P);
+        add(r, mod(r - t - 1, P));
+      }
     }
   }
-  FO_TRY(L.finish(epoch, timeout_ns(o), flags, ctx->ctrl, 1));
+  FO_TRY(L.finish(epoch, timeout_ns(o), flags, ctx->ctrl, 0));
   return launch_gemm(ctx, L, o, stream);
 }
 
@@ -996,8 +1003,9 @@ fo_status host_copy_rows(void* dst, int64_t dld, const void* src, int64_t sld, i
   return copy_rows(dst, dld, src, sld, rows, cols, esz, s);
 }
 fo_status host_write_flag(cudaStream_t s, uint32_t* flag, uint32_t value) { return write_flag(s, flag, value); }
-fo_status host_encode_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
-  return encode_map(map, ptr, rows, cols, ld, box_rows);
+fo_status host_encode_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows,
+                          CUtensorMapDataType dtype) {
+  return encode_map(map, ptr, rows, cols, ld, box_rows, dtype);
 }
 fo_status host_check_mat(const fo_mat& a, int32_t dtype, const char* what, int r) {
   return check_mat(a, dtype, what, r);

@@ -63,8 +63,8 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int tile) 
     const int u = j / (tm * tn);
     const int rem = j - u * tm * tn;
     c.unit = u0 + u;
-    c.mb = rem / tn;
-    c.nb = rem % tn;
+    c.nb = rem / tm;
+    c.mb = rem % tm;
   }
   return c;
 }

@@ -16,7 +16,8 @@ fo_status host_join(fo_ctx* ctx, int P, cudaStream_t s);
 fo_status host_copy_rows(void* dst, int64_t dld, const void* src, int64_t sld, int64_t rows, int64_t cols,
                          size_t esz, cudaStream_t s);
 fo_status host_write_flag(cudaStream_t s, uint32_t* flag, uint32_t value);
-fo_status host_encode_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows);
+fo_status host_encode_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows,
+                          CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 fo_status host_check_mat(const fo_mat& a, int32_t dtype, const char* what, int r);
 fo_status host_fail(fo_status st, const char* msg);
 uint64_t host_timeout_ns(const fo_opts& o);

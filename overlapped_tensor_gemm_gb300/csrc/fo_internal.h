@@ -21,7 +21,9 @@ constexpr int kMaxP = 8;
 // times the rows [b_row0, b_row0 + n_cols) of its B operand (nn.Linear
 // layout, K contiguous), written through a per-unit epilogue.  Units are
 // grouped (one group per ring step); the tiles of a launch are enumerated group
-// by group, and inside a group either unit-major or m-block-major.  Every CTA
+// by group, and inside a group either unit by unit (n-block outer, m-block
+// inner: consecutive CTAs share the B tile, the whole A slice stays in L2) or
+// m-block-major across units.  Every CTA
 // walks the global tile sequence with stride gridDim.x, so a tile only ever
 // waits on tiles with a smaller index (deadlock freedom of the in-kernel ring).
 
@@ -63,7 +65,8 @@ struct GemmParams {
   int32_t group_tile_begin[kMaxGroups + 1];
   int32_t num_groups;
   int32_t num_maps;            // maps[0, num_maps) are valid
-  int32_t mblock_major;        // 1: tiles of a group ordered (m-block, unit, n-block)
+  int32_t mblock_major;        // 1: tiles of a group ordered (m-block, unit, n-block);
+                               // 0: unit by unit, n-block outer, m-block inner
   int32_t total_tiles;
   uint32_t epoch;
   uint64_t timeout_ns;

@@ -48,3 +48,12 @@ def assert_close(got: np.ndarray, ref: np.ndarray, what: str = "", round_ref: bo
     lim = MAX_ABS_FRAC * (np.abs(ref).max() if ref.size else 0.0)
     assert rel <= REL_L2, f"{what}: rel-L2 {rel:.3e} > {REL_L2}"
     assert mx <= lim, f"{what}: max-abs {mx:.3e} > {lim:.3e}"
+
+
+def padded(rows: int, cols: int, dtype, fill=float("nan"), device="cuda"):
+    """[rows, cols] view of a buffer whose row pitch is padded to 16 bytes."""
+    import torch
+    esz = torch.empty((), dtype=dtype).element_size()
+    per = 16 // esz
+    ld = (cols + per - 1) // per * per
+    return torch.full((rows, ld), fill, dtype=dtype, device=device)[:, :cols]

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import fo_workloads as wl
-from helpers import assert_bits_equal, assert_close, f64, to_bits, to_dev
+from helpers import assert_bits_equal, assert_close, f64, padded, to_bits, to_dev
 from oracle import ops
 
 pytestmark = pytest.mark.gpu
@@ -28,7 +28,7 @@ def _run_gemm(ctx, M, N, K, integer, out_dtype=torch.bfloat16, seed=0):
     else:
         A = wl.gaussian_bf16(g, (M, K))
         B = wl.gaussian_bf16(g, (N, K), 0.02)
-    C = torch.zeros((M, N), dtype=out_dtype, device="cuda")
+    C = padded(M, N, out_dtype)
     ctx.gemm(to_dev(A), to_dev(B), C)
     torch.cuda.synchronize()
     ctx.poll()

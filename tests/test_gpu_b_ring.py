@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import fo_workloads as wl
-from helpers import assert_bits_equal, assert_close, f64, to_bits, to_dev
+from helpers import assert_bits_equal, assert_close, f64, padded, to_bits, to_dev
 from oracle import bf16, ops
 
 pytestmark = pytest.mark.gpu
@@ -23,7 +23,7 @@ def _ag(ctx, P, m, K, N, integer, seed, **kw):
     inp = wl.ag_inputs(P, m, K, N, seed, integer)
     X = [to_dev(x) for x in inp["X_shards"]]
     W = [to_dev(w) for w in inp["W_col"]]
-    Y = [torch.full((P * m, N), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    Y = [padded(P * m, N, torch.bfloat16) for _ in range(P)]
     ctx.ag_gemm(X, W, Y, **kw)
     torch.cuda.synchronize()
     ctx.poll()
@@ -35,7 +35,7 @@ def _rs(ctx, P, m, Kr, N, integer, seed, **kw):
     inp = wl.rs_inputs(P, P * m, N, Kr, seed, integer)
     X = [to_dev(x) for x in inp["X"]]
     W = [to_dev(w) for w in inp["W_row"]]
-    Y = [torch.full((m, N), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    Y = [padded(m, N, torch.bfloat16) for _ in range(P)]
     ctx.gemm_rs(X, W, Y, **kw)
     torch.cuda.synchronize()
     ctx.poll()

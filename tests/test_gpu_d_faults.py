@@ -1,0 +1,58 @@
+"""Failure detection without a GPU fault: the host skips one ring hop (fault
+injection on the host), so a device wait runs past its short limit; the kernel
+returns, fo_ctx_poll reports FO_ERR_TIMEOUT, and the context stays usable."""
+import pytest
+import torch
+
+import fo_workloads as wl
+from helpers import assert_bits_equal, f64, to_bits, to_dev
+from oracle import ops
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(P, m, K, N):
+    inp = wl.ag_inputs(P, m, K, N, 77, True)
+    X = [to_dev(x) for x in inp["X_shards"]]
+    W = [to_dev(w) for w in inp["W_col"]]
+    Y = [torch.zeros((P * m, N), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    return inp, X, W, Y
+
+
+def test_skipped_hop_times_out_and_context_recovers():
+    import overlapped_tensor_gemm_gb300 as fo
+    P, m, K, N = 4, 128, 256, 256
+    inp, X, W, Y = _inputs(P, m, K, N)
+    with fo.Context(0) as ctx:
+        ctx.ag_gemm(X, W, Y, fault="skip_hop", timeout_us=20000)
+        torch.cuda.synchronize()
+        with pytest.raises(fo.FoError) as e:
+            ctx.poll()
+        assert e.value.status == fo.FO_ERR_TIMEOUT
+        ctx.poll()  # cleared
+        # the same context computes the right answer afterwards
+        ctx.ag_gemm(X, W, Y)
+        torch.cuda.synchronize()
+        ctx.poll()
+        ref, _ = ops.ag_gemm_ring([f64(x) for x in inp["X_shards"]], [f64(w) for w in inp["W_col"]])
+        for r in range(P):
+            assert_bits_equal(to_bits(Y[r]), ref[r], f"after recovery rank {r}")
+
+
+def test_skipped_kv_hop_times_out_in_attention():
+    import overlapped_tensor_gemm_gb300 as fo
+    P, m, H = 3, 128, 1
+    inp = wl.attn_inputs(P, P * m, H, 128, 78)
+    Q = [to_dev(x).reshape(m, 128) for x in inp["Q"]]
+    K = [to_dev(x).reshape(m, 128) for x in inp["K"]]
+    V = [to_dev(x).reshape(m, 128) for x in inp["V"]]
+    O = [torch.zeros((m, 128), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    with fo.Context(0) as ctx:
+        ctx.qsplit_attn(Q, K, V, O, heads=H, head_dim=128, fault="skip_hop", timeout_us=20000)
+        torch.cuda.synchronize()
+        with pytest.raises(fo.FoError) as e:
+            ctx.poll()
+        assert e.value.status == fo.FO_ERR_TIMEOUT
+        ctx.qsplit_attn(Q, K, V, O, heads=H, head_dim=128)
+        torch.cuda.synchronize()
+        ctx.poll()
