@@ -199,6 +199,8 @@ def run_ours(args, rank: int, world: int, device: int):
     pk = peaks()
     if args.workload == "attn":
         return run_attention_only(args, rank, world, device, pk, barrier, max_over_ranks)
+    if args.workload == "tail_rs":
+        return run_tail_rs(args, world, device, pk)
     cfg = mlp_config(args.workload)
     inp = wl.mlp_inputs(cfg)
 
@@ -367,6 +369,54 @@ def attention_bench(ctx, pk, iters: int):
                         f"{c.head_dim}", "ms": round(ms, 4), "tflops": round(tf, 2),
             "frac_of_bf16_peak": round(tf / pk["bf16_burst"], 4), "flop": c.flops(),
             "flop_counting": "causal triangle only (QK^T and PV)"}
+
+
+def run_tail_rs(args, world, device, pk):
+    """Small-batch tail-dominated GEMM-RS (P=8, tokens 512, in-features 28672, out 8192):
+    rank-adaptive kept-slice-last order against the naive ring order and the baselines."""
+    import torch
+    import overlapped_tensor_gemm_gb300 as fo
+    c = wl.TAIL_RS
+    inp = wl.rs_inputs(c.P, c.tokens, c.n_out, c.k_row, c.seed, integer=False)
+
+    def dev(bits):
+        return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).cuda()
+
+    X = [dev(x) for x in inp["X"]]
+    W = [dev(w) for w in inp["W_row"]]
+    Y = [torch.empty((c.m, c.n_out), dtype=torch.bfloat16, device="cuda") for _ in range(c.P)]
+    ctx = fo.Context(device)
+    stream = torch.cuda.current_stream()
+
+    def timed(order):
+        for _ in range(max(args.warmup, 3)):
+            ctx.gemm_rs(X, W, Y, order=order)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            ctx.gemm_rs(X, W, Y, order=order)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ctx.poll()
+        return a.elapsed_time(b) / args.steps
+
+    with ClockSampler(device) as clk:
+        t = {o: timed(o) for o in ("flash", "naive", "serial", "slicing")}
+    ctx.gemm_rs(X, W, Y, order="serial")
+    torch.cuda.synchronize()
+    ring_ms, gemm_ms = ctx.phase_ms()
+    ctx.close()
+    tf = c.flops() / (t["flash"] * 1e-3) / 1e12
+    return {"metric": METRIC, "value": round(tf, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(t["flash"], 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"tail-dominated GEMM-RS, P={c.P}, tokens {c.tokens}, in {c.k_total}, out "
+                                   f"{c.n_out}"},
+            "pct_of_peak": round(100 * tf / pk["bf16_burst"], 2), "clocks": clk.summary(),
+            "orders_ms": {k: round(v, 4) for k, v in t.items()},
+            "serial_phases_ms": {"gemm": round(gemm_ms, 4), "ring_reduce": round(ring_ms, 4)},
+            "exposed_ms": {k: round(v - gemm_ms, 4) for k, v in t.items()}}
 
 
 def run_attention_only(args, rank, world, device, pk, barrier, max_over_ranks):

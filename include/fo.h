@@ -87,8 +87,9 @@ typedef enum {
 
 typedef enum {
   FO_FAULT_NONE = 0,
-  FO_FAULT_SKIP_HOP = 1  /* fault injection (host side): the last ring hop is not enqueued,
-                            so a device wait runs out; the call must end with
+  FO_FAULT_SKIP_HOP = 1  /* fault injection (host side): one ring hop into rank 1 is not
+                            enqueued (all-gather: the last hop from rank 0; attention: the
+                            first), so a device wait runs out; the call must end with
                             FO_ERR_TIMEOUT from fo_ctx_poll and the context stays usable */
 } fo_fault;
 
@@ -127,6 +128,15 @@ FO_API fo_status fo_ctx_poll(fo_ctx* ctx);
  * this context: the ring collective alone and the GEMM alone (valid once that
  * call's stream has completed). */
 FO_API fo_status fo_ctx_phase_ms(fo_ctx* ctx, float* collective_ms, float* gemm_ms);
+
+/* Launch order of the fused ring launches, for inspection (host only, no GPU):
+ * op 0 = Flash-AG (order FO_ORDER_FLASH), op 1 = Flash-RS (FO_ORDER_FLASH or
+ * FO_ORDER_NAIVE).  Unit i of step t is written at index t*P + i: rank[] gets
+ * the rank, item[] the slice (AG) or chunk (RS) it computes.  Returns P*P, or
+ * -1 on a bad argument (capacity < P*P included).  Follows the technical
+ * summary's section 2: AG step 0 is the rank's own slice; RS step P-1 is the
+ * rank's kept chunk. */
+FO_API int fo_step_order(int op, int P, int order, int32_t* rank, int32_t* item, int capacity);
 
 /* Plain GEMM on the tensor cores, C = A * B^T (no ring):
  * A [M, K] bf16, B [N, K] bf16, C [M, N] bf16 or fp32.  K % 8 == 0. */

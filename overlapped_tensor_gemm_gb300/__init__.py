@@ -30,7 +30,7 @@ FAULTS = {"none": 0, "skip_hop": 1}
 # Every entry point declared in include/fo.h.
 ABI_SYMBOLS = ("fo_version", "fo_last_error_string", "fo_ctx_create", "fo_ctx_destroy", "fo_ctx_poll",
                "fo_ctx_phase_ms", "fo_gemm", "fo_ag_gemm", "fo_gemm_rs", "fo_silu_mul", "fo_mlp_layer",
-               "fo_mlp_layer_host", "fo_qsplit_attn")
+               "fo_mlp_layer_host", "fo_qsplit_attn", "fo_step_order")
 
 
 class FoMat(ctypes.Structure):
@@ -64,6 +64,7 @@ def load() -> ctypes.CDLL:
         P = ctypes.POINTER
         vp = ctypes.c_void_p
         lib.fo_version.restype = ctypes.c_int
+        lib.fo_step_order.restype = ctypes.c_int
         lib.fo_last_error_string.restype = ctypes.c_char_p
         lib.fo_ctx_create.argtypes = [ctypes.c_int, P(vp)]
         lib.fo_ctx_destroy.argtypes = [vp]
@@ -78,8 +79,10 @@ def load() -> ctypes.CDLL:
                                            P(FoMat), P(FoOpts), vp]
         lib.fo_qsplit_attn.argtypes = [vp, P(FoMat), P(FoMat), P(FoMat), ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_int, P(FoMat), P(FoOpts), vp]
+        lib.fo_step_order.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P(ctypes.c_int32),
+                                      P(ctypes.c_int32), ctypes.c_int]
         for name in ABI_SYMBOLS:
-            if name not in ("fo_version", "fo_last_error_string"):
+            if name not in ("fo_version", "fo_last_error_string", "fo_step_order"):
                 getattr(lib, name).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -203,3 +206,15 @@ class Context:
         o = opts(**kw)
         _check(self._lib.fo_qsplit_attn(self._h, _mats(Q), _mats(K), _mats(V), P, heads, head_dim, int(causal),
                                         _mats(O), ctypes.byref(o), _stream(stream)))
+
+
+def step_order(op: str, P: int, order: str = "flash") -> list[list[tuple[int, int]]]:
+    """The library's launch order: per step, (rank, slice or chunk) of each unit."""
+    lib = load()
+    n = P * P
+    rank = (ctypes.c_int32 * n)()
+    item = (ctypes.c_int32 * n)()
+    got = lib.fo_step_order({"ag": 0, "rs": 1}[op], P, ORDERS[order], rank, item, n)
+    if got != n:
+        raise FoError(FO_ERR_INVALID_ARG, "bad step-order request")
+    return [[(rank[t * P + i], item[t * P + i]) for i in range(P)] for t in range(P)]

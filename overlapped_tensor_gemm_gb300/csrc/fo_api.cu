@@ -268,8 +268,9 @@ struct Launch {
       const int u0 = p.group_unit_begin[g], u1 = p.group_unit_begin[g + 1];
       for (int u = u0; u < u1; ++u) {
         GemmUnit& x = p.units[u];
+        const int bn = x.gated ? kBN / 2 : kBN;  // output columns per tile
         x.tiles_m = (x.m_rows + kBM - 1) / kBM;
-        x.tiles_n = (x.n_cols + kBN - 1) / kBN;
+        x.tiles_n = (x.n_cols + bn - 1) / bn;
         if (x.tiles_m != p.units[u0].tiles_m || x.tiles_n != p.units[u0].tiles_n)
           return fail(FO_ERR_SHAPE, "units of one step must share a tile grid");
         tiles += static_cast<int64_t>(x.tiles_m) * x.tiles_n;
@@ -305,6 +306,28 @@ fo_status launch_gemm(fo_ctx* ctx, Launch& L, const fo_opts& o, cudaStream_t str
 }
 
 int mod(int a, int P) { return ((a % P) + P) % P; }
+
+// Step schedules (FlashOverlap technical summary, section 2).  Pure functions:
+// the launch builders below and fo_step_order use exactly these.
+//   Flash-AG: unit i of step t is rank i, computing slice (i - t) mod P (its own at t = 0).
+//   Flash-RS: unit i of step t is rank (t + i) mod P, computing chunk (r - t - 1) mod P,
+//             so the kept chunk r comes at t = P-1; the rotation places every unit at the
+//             position of the unit of step t-1 whose partial sum it consumes.
+//   naive RS: step c is chunk c on every rank, units in chain order r = c+1, c+2, ..., c.
+void ag_unit(int P, int t, int i, int* rank, int* slice) {
+  *rank = i;
+  *slice = mod(i - t, P);
+}
+
+void rs_unit(int P, int order, int t, int i, int* rank, int* chunk) {
+  if (order == FO_ORDER_NAIVE) {
+    *rank = mod(t + 1 + i, P);
+    *chunk = t;
+  } else {
+    *rank = mod(t + i, P);
+    *chunk = mod(*rank - t - 1, P);
+  }
+}
 
 char* bptr(const fo_mat& a, int64_t row) {
   return static_cast<char*>(a.ptr) + row * a.ld * static_cast<int64_t>(elem_size(a.dtype));
@@ -386,13 +409,16 @@ fo_status enqueue_ag_ring(fo_ctx* ctx, const AgArgs& a, int64_t row0, int64_t ro
 }
 
 // Adds the P*P (rank, slice) GEMM units over rows [row0, row0 + rows) of every slice.
+// gated_f > 0: W_col[r] is [2F, K] (gate rows then up rows) and Y[r] receives
+// H = SiLU(gate) * up, [M, F] (the MLP glue fused into the epilogue).
 fo_status add_ag_units(Launch& L, const AgArgs& a, const int* xmap, const int* rmap, const int* wmap, int64_t row0,
-                       int64_t rows, bool flash, uint32_t* flags) {
+                       int64_t rows, bool flash, int64_t gated_f) {
   const int P = a.P;
   for (int t = 0; t < P; ++t) {
     if (flash || t == 0) L.begin_group();
-    for (int r = 0; r < P; ++r) {
-      const int s = mod(r - t, P);  // local slice first
+    for (int i = 0; i < P; ++i) {
+      int r, s;
+      ag_unit(P, t, i, &r, &s);  // local slice first
       GemmUnit& u = L.add_unit();
       u = blank_unit();
       if (t == 0) {
@@ -405,27 +431,36 @@ fo_status add_ag_units(Launch& L, const AgArgs& a, const int* xmap, const int* r
       }
       u.b_map = wmap[r];
       u.m_rows = static_cast<int32_t>(rows);
-      u.n_cols = static_cast<int32_t>(a.N);
       u.k = static_cast<int32_t>(a.K);
-      u.epi = kEpiBF16;
+      if (gated_f > 0) {
+        u.gated = 1;
+        u.b_row1 = static_cast<int32_t>(gated_f);
+        u.n_cols = static_cast<int32_t>(gated_f);
+        u.epi = kEpiSiluMul;
+      } else {
+        u.n_cols = static_cast<int32_t>(a.N);
+        u.epi = kEpiBF16;
+      }
       u.c = bptr(a.Y[r], s * a.m + row0);
       u.ldc = a.Y[r].ld;
     }
   }
-  (void)flags;
   return FO_OK;
 }
 
 fo_status ag_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_mat* Y, const fo_opts& o,
-                 cudaStream_t stream) {
+                 cudaStream_t stream, bool gated = false) {
   const int64_t m = X[0].rows, K = X[0].cols, N = W[0].rows, M = m * P;
+  const int64_t gated_f = gated ? N / 2 : 0;
+  if (gated && N % 2 != 0) return fail(FO_ERR_SHAPE, "gated weight must have 2F rows");
   for (int r = 0; r < P; ++r) {
     FO_TRY(check_mat(X[r], FO_BF16, "X_shards", r));
     FO_TRY(check_mat(W[r], FO_BF16, "W_col", r));
     FO_TRY(check_mat(Y[r], FO_BF16, "Y", r));
     if (X[r].rows != m || X[r].cols != K) return fail(FO_ERR_SHAPE, "X_shards[%d] shape differs from rank 0", r);
     if (W[r].rows != N || W[r].cols != K) return fail(FO_ERR_SHAPE, "W_col[%d] must be [N, K] like rank 0", r);
-    if (Y[r].rows != M || Y[r].cols != N) return fail(FO_ERR_SHAPE, "Y[%d] must be [P*m, N]", r);
+    if (Y[r].rows != M || Y[r].cols != (gated ? gated_f : N))
+      return fail(FO_ERR_SHAPE, "Y[%d] must be [P*m, %s]", r, gated ? "F" : "N");
   }
   if (K % 8 != 0) return fail(FO_ERR_UNSUPPORTED, "K=%lld must be a multiple of 8", (long long)K);
   if (m == 0 || N == 0) return FO_OK;
@@ -446,10 +481,10 @@ fo_status ag_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_
       if (st != FO_OK) return st;
       rmap[r] = L.add_map(&st, ag_slot(a, r, 0, 0), M, K, K, kBM);
       if (st != FO_OK) return st;
-      wmap[r] = L.add_map(&st, W[r].ptr, N, K, W[r].ld, kBN);
+      wmap[r] = L.add_map(&st, W[r].ptr, N, K, W[r].ld, gated ? kBN / 2 : kBN);
       if (st != FO_OK) return st;
     }
-    FO_TRY(add_ag_units(L, a, xmap, rmap, wmap, row0, rows, flash, flags));
+    FO_TRY(add_ag_units(L, a, xmap, rmap, wmap, row0, rows, flash, gated_f));
     return L.finish(epoch, tmo, flags, ctx->ctrl, 0);
   };
   int xmap[kMaxP], rmap[kMaxP], wmap[kMaxP];
@@ -555,21 +590,12 @@ fo_status rs_flash(fo_ctx* ctx, const RsArgs& a, const fo_opts& o, cudaStream_t 
       u.epi = h == 0 ? kEpiBF16 : kEpiAddBF16;
     }
   };
-  if (o.order == FO_ORDER_NAIVE) {
-    for (int c = 0; c < P; ++c) {  // every rank computes chunk c at step c (chain order inside the step)
-      L.begin_group();
-      for (int h = 0; h < P; ++h) add(mod(c + 1 + h, P), c);
-    }
-  } else {
-    // rank-adaptive: chunk (r - t - 1) mod P, kept chunk r last.  Step t lists the
-    // ranks starting at t, so every unit sits at the same position as the unit of
-    // the previous step whose partial sum it consumes: a whole step apart.
-    for (int t = 0; t < P; ++t) {
-      L.begin_group();
-      for (int i = 0; i < P; ++i) {
-        const int r = mod(t + i, P);
-        add(r, mod(r - t - 1, P));
-      }
+  for (int t = 0; t < P; ++t) {
+    L.begin_group();
+    for (int i = 0; i < P; ++i) {
+      int r, c;
+      rs_unit(P, o.order, t, i, &r, &c);
+      add(r, c);
     }
   }
   FO_TRY(L.finish(epoch, timeout_ns(o), flags, ctx->ctrl, 0));
@@ -705,32 +731,24 @@ fo_status mlp_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* Wc, const fo_mat* 
   const int64_t m = X[0].rows, M = m * P, Nc = Wc[0].rows;
   if (gated && Nc % 16 != 0) return fail(FO_ERR_UNSUPPORTED, "gated layer needs 2F with F % 8 == 0");
   const int64_t F = gated ? Nc / 2 : Nc;
-  void* y_v = nullptr;
-  FO_TRY(ensure_buf(ctx, kBufMlpY, static_cast<size_t>(P) * M * Nc * 2 + 16, &y_v));
   fo_mat Y[kMaxP], H[kMaxP];
-  for (int r = 0; r < P; ++r) {
-    Y[r] = fo_mat{static_cast<char*>(y_v) + static_cast<int64_t>(r) * M * Nc * 2, FO_BF16, 0, M, Nc, Nc};
+  if (!gated) {
+    void* y_v = nullptr;
+    FO_TRY(ensure_buf(ctx, kBufMlpY, static_cast<size_t>(P) * M * Nc * 2 + 16, &y_v));
+    for (int r = 0; r < P; ++r)
+      Y[r] = fo_mat{static_cast<char*>(y_v) + static_cast<int64_t>(r) * M * Nc * 2, FO_BF16, 0, M, Nc, Nc};
   }
   fo_opts oa = o;
   if (oa.order == FO_ORDER_NAIVE) oa.order = FO_ORDER_FLASH;  // the naive order concerns the RS step
-  FO_TRY(ag_run(ctx, X, Wc, P, Y, oa, stream));
   if (gated) {
+    // SiLU(gate) * up is fused into the Flash-AG epilogue: H is written directly
     void* h_v = nullptr;
     FO_TRY(ensure_buf(ctx, kBufMlpH, static_cast<size_t>(P) * M * F * 2 + 16, &h_v));
-    SiluMulArgs sa;
-    std::memset(&sa, 0, sizeof(sa));
-    for (int r = 0; r < P; ++r) {
+    for (int r = 0; r < P; ++r)
       H[r] = fo_mat{static_cast<char*>(h_v) + static_cast<int64_t>(r) * M * F * 2, FO_BF16, 0, M, F, F};
-      sa.gu[r] = static_cast<const uint16_t*>(Y[r].ptr);
-      sa.h[r] = static_cast<uint16_t*>(H[r].ptr);
-      sa.ld_gu[r] = Nc;
-      sa.ld_h[r] = F;
-    }
-    sa.rows = M;
-    sa.f = F;
-    sa.P = P;
-    FO_CUDA(launch_silu_mul(sa, stream));
+    FO_TRY(ag_run(ctx, X, Wc, P, H, oa, stream, true));
   } else {
+    FO_TRY(ag_run(ctx, X, Wc, P, Y, oa, stream));
     for (int r = 0; r < P; ++r) H[r] = Y[r];
   }
   return rs_run(ctx, H, Wr, P, Z, o, stream);
@@ -827,6 +845,26 @@ fo_status fo_ctx_poll(fo_ctx* ctx) {
   FO_CUDA(cudaMemset(ctx->ctrl, 0, sizeof(w)));
   return fail(static_cast<fo_status>(w[kCtrlError]), "device wait gave up (site %u, index %u)", w[kCtrlWhere],
               w[kCtrlDetail]);
+}
+
+int fo_step_order(int op, int P, int order, int32_t* rank, int32_t* item, int capacity) {
+  if (P < 1 || P > kMaxP || (op != 0 && op != 1) || !rank || !item) return -1;
+  if (order != FO_ORDER_FLASH && order != FO_ORDER_NAIVE) return -1;
+  if (op == 0 && order != FO_ORDER_FLASH) return -1;
+  if (capacity < P * P) return -1;
+  for (int t = 0; t < P; ++t) {
+    for (int i = 0; i < P; ++i) {
+      int r, x;
+      if (op == 0) {
+        ag_unit(P, t, i, &r, &x);
+      } else {
+        rs_unit(P, order, t, i, &r, &x);
+      }
+      rank[t * P + i] = r;
+      item[t * P + i] = x;
+    }
+  }
+  return P * P;
 }
 
 fo_status fo_ctx_phase_ms(fo_ctx* ctx, float* collective_ms, float* gemm_ms) {

@@ -535,7 +535,8 @@ fo_status attn_run(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K, const fo_mat* 
       const int d = (r + 1) % P;
       const int s = ((r - t + 1) % P + P) % P;
       if (prune && (d == 0 || d - t < 0)) continue;  // slice s is only needed by ranks above it
-      if (o.fault == FO_FAULT_SKIP_HOP && t == P - 1 && r == 0) continue;
+      // fault injection: the first hop into rank 1 (slice 0, which rank 1 always uses) is dropped
+      if (o.fault == FO_FAULT_SKIP_HOP && t == 1 && r == 0) continue;
       cudaStream_t ls = host_link(ctx, r);
       if (t >= 2 && cudaStreamWaitEvent(ls, host_ev_hop(ctx, (r - 1 + P) % P, t - 1), 0) != cudaSuccess)
         return host_fail(FO_ERR_CUDA, "event wait failed");

@@ -93,7 +93,8 @@ __device__ void producer_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl)
     }
     const int nk = (u.k + kBK - 1) / kBK;
     const int a_row = u.a_row0 + tc.mb * kBM;
-    const int b_row = u.b_row0 + tc.nb * kBN;
+    const int b_row = u.b_row0 + tc.nb * (u.gated ? kBN / 2 : kBN);
+    const int b_row_up = u.b_row1 + tc.nb * (kBN / 2);
     for (int kb = 0; kb < nk; ++kb) {
       if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty,
                      static_cast<uint32_t>(tile))) {
@@ -104,7 +105,12 @@ __device__ void producer_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl)
       uint8_t* b = a + kABytes;
       mbar_arrive_expect_tx(&ctl->full[stage], kStageBytes);
       tma_load_2d(&p.maps[u.a_map], a, &ctl->full[stage], kb * kBK, a_row);
-      tma_load_2d(&p.maps[u.b_map], b, &ctl->full[stage], kb * kBK, b_row);
+      if (u.gated) {  // gate rows -> B rows [0,128), up rows -> B rows [128,256) (128-row boxes)
+        tma_load_2d(&p.maps[u.b_map], b, &ctl->full[stage], kb * kBK, b_row);
+        tma_load_2d(&p.maps[u.b_map], b + kBBytes / 2, &ctl->full[stage], kb * kBK, b_row_up);
+      } else {
+        tma_load_2d(&p.maps[u.b_map], b, &ctl->full[stage], kb * kBK, b_row);
+      }
       armed |= 1u << stage;
       armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
       if (++stage == kStages) {
@@ -225,6 +231,37 @@ __device__ __forceinline__ void store_chunk(const GemmUnit& u, int row, int col,
   }
 }
 
+__device__ __forceinline__ float round_bf16(float x) {
+  return __uint_as_float(static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x))) << 16);
+}
+
+// MLP glue fused into the gate/up epilogue: the gate and up accumulators are
+// rounded to bf16 first (as the unfused layer stores them), then
+// SiLU(g) * u = g / (1 + exp(-g)) * u in fp32, rounded once to bf16.
+__device__ __forceinline__ void store_silu_chunk(const GemmUnit& u, int row, int col, const uint32_t (&g)[32],
+                                                 const uint32_t (&v)[32]) {
+  float h[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float gi = round_bf16(__uint_as_float(g[i]));
+    const float ui = round_bf16(__uint_as_float(v[i]));
+    h[i] = gi / (1.0f + expf(-gi)) * ui;
+  }
+  uint16_t* dst = static_cast<uint16_t*>(u.c) + static_cast<int64_t>(row) * u.ldc + col;
+  if (col + 32 <= u.n_cols) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      st_v4_u32(dst + 8 * i, pack_bf16x2(h[8 * i + 0], h[8 * i + 1]), pack_bf16x2(h[8 * i + 2], h[8 * i + 3]),
+                pack_bf16x2(h[8 * i + 4], h[8 * i + 5]), pack_bf16x2(h[8 * i + 6], h[8 * i + 7]));
+    }
+  } else {
+    const int ncol = u.n_cols - col;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < ncol) dst[i] = __bfloat16_as_ushort(__float2bfloat16_rn(h[i]));
+  }
+}
+
 // Lane 0 waits; the outcome is broadcast so the whole warp takes one path.
 __device__ __forceinline__ bool warp_mbar_wait(uint64_t* bar, uint32_t parity, const GemmParams& p,
                                                uint32_t site, uint32_t detail, int lane) {
@@ -260,13 +297,25 @@ __device__ void epilogue_loop(const GemmParams& p, SmemCtl* ctl, uint32_t tmem_b
     const int row = tc.mb * kBM + q * 32 + lane;
     const bool row_ok = row < u.m_rows;
     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
+    if (u.epi == kEpiSiluMul) {
 #pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
-      uint32_t v[32];
-      tmem_ld32(tbase + c * 32, v);
-      tmem_wait_ld();
-      const int col = tc.nb * kBN + c * 32;
-      if (row_ok && col < u.n_cols) store_chunk(u, row, col, v);
+      for (int c = 0; c < kBN / 64; ++c) {
+        uint32_t g[32], v[32];
+        tmem_ld32(tbase + c * 32, g);
+        tmem_ld32(tbase + kBN / 2 + c * 32, v);
+        tmem_wait_ld();
+        const int col = tc.nb * (kBN / 2) + c * 32;
+        if (row_ok && col < u.n_cols) store_silu_chunk(u, row, col, g, v);
+      }
+    } else {
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tbase + c * 32, v);
+        tmem_wait_ld();
+        const int col = tc.nb * kBN + c * 32;
+        if (row_ok && col < u.n_cols) store_chunk(u, row, col, v);
+      }
     }
     tc_fence_before();
     __syncwarp();

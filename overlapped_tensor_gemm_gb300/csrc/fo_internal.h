@@ -41,6 +41,7 @@ enum EpiMode : int32_t {
   kEpiF32 = 1,         // C (fp32) = acc
   kEpiAddF32 = 2,      // C (fp32) = acc + acc_in
   kEpiAddBF16 = 3,     // C (bf16) = acc + acc_in
+  kEpiSiluMul = 4,     // gated tile: C (bf16) = SiLU(bf16(acc[:, :128])) * bf16(acc[:, 128:])
 };
 
 struct GemmUnit {
@@ -52,6 +53,8 @@ struct GemmUnit {
   int32_t in_flag_base;        // RS: per-tile flags guarding acc_in (-1: none)
   int32_t out_flag_base;       // RS: per-tile flags released after C is written (-1: none)
   int32_t epi;                 // EpiMode
+  int32_t gated;               // 1: B tile = 128 gate rows at b_row0 + 128 up rows at b_row1 (kEpiSiluMul)
+  int32_t b_row1;              // gated: row offset of the up half of B
   int32_t pad0;
   void* c;                     // output
   const float* acc_in;         // fp32 partial sum to add (kEpiAdd*)

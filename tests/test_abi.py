@@ -54,3 +54,29 @@ def test_context_creation_without_gpu_fails_cleanly(lib):
     assert st in (fo.FO_ERR_CUDA, fo.FO_ERR_INVALID_ARG)
     assert not h.value
     assert lib.fo_last_error_string()
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 8])
+def test_library_step_order_follows_the_oracle_schedule(lib, P):
+    """The fused launches' unit order (host logic, no GPU) against the oracle's step
+    formulas: AG step 0 is every rank's own slice, RS step P-1 its kept chunk, and
+    the naive order computes chunk t on every rank at step t."""
+    from oracle import schedule
+    ag = fo.step_order("ag", P)
+    rs = fo.step_order("rs", P)
+    nv = fo.step_order("rs", P, "naive")
+    for t in range(P):
+        assert sorted(r for r, _ in ag[t]) == list(range(P))
+        assert sorted(r for r, _ in rs[t]) == list(range(P))
+        for r, s in ag[t]:
+            assert s == schedule.ag_slice(r, t, P)
+        for r, c in rs[t]:
+            assert c == schedule.rs_chunk(r, t, P)
+        for h, (r, c) in enumerate(nv[t]):
+            assert c == schedule.rs_chunk_naive(r, t, P)
+            assert schedule.rs_hop(r, c, P) == h      # chain order inside the step
+    # every RS unit consumes a partial sum produced one whole step earlier, same position
+    for t in range(1, P):
+        for i, (r, c) in enumerate(rs[t]):
+            assert rs[t - 1][i] == ((r - 1) % P, c)
+    assert lib.fo_step_order(0, P, 1, (ctypes.c_int32 * 64)(), (ctypes.c_int32 * 64)(), 64) == -1

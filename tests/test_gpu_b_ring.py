@@ -116,3 +116,37 @@ def test_gated_mlp_layer_tolerance(ctx):
                               [f64(w) for w in inp["W_row"]], gated=True)
     for r in range(cfg.P):
         assert_close(f64(to_bits(Z[r])), ref[r], f"gated MLP rank {r}")
+
+
+def test_silu_mul_standalone(ctx):
+    # layer glue on its own: H = SiLU(G) * U from the bf16 gate/up block, rounded once
+    P, M, F = 2, 256, 384
+    g = torch.Generator().manual_seed(31)
+    GU = [wl.gaussian_bf16(g, (M, 2 * F), 3.0) for _ in range(P)]
+    H = [torch.empty((M, F), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    ctx.silu_mul([to_dev(x) for x in GU], H)
+    torch.cuda.synchronize()
+    for r in range(P):
+        ref = ops.silu_mul(f64(GU[r])[:, :F], f64(GU[r])[:, F:])
+        assert_close(f64(to_bits(H[r])), ref, f"silu_mul rank {r}")
+
+
+def test_gated_fused_epilogue_matches_unfused(ctx):
+    # the fused Flash-AG epilogue (SiLU(gate)*up) against the unfused AG GEMM + glue kernel
+    cfg = wl.MLPConfig("fused", 1, P=2, tokens=256, hidden=512, ffn=768, gated=True, integer=False)
+    inp = wl.mlp_inputs(cfg)
+    X = [to_dev(x) for x in inp["X_shards"]]
+    Wc = [to_dev(w) for w in inp["W_col"]]
+    Wr = [to_dev(w) for w in inp["W_row"]]
+    Z = [torch.empty((cfg.m, cfg.hidden), dtype=torch.bfloat16, device="cuda") for _ in range(cfg.P)]
+    ctx.mlp_layer(X, Wc, Wr, Z, gated=True)
+    Y = [torch.empty((cfg.tokens, cfg.n_col), dtype=torch.bfloat16, device="cuda") for _ in range(cfg.P)]
+    H = [torch.empty((cfg.tokens, cfg.k_row), dtype=torch.bfloat16, device="cuda") for _ in range(cfg.P)]
+    Z2 = [torch.empty_like(z) for z in Z]
+    ctx.ag_gemm(X, Wc, Y)
+    ctx.silu_mul(Y, H)
+    ctx.gemm_rs(H, Wr, Z2)
+    torch.cuda.synchronize()
+    ctx.poll()
+    for r in range(cfg.P):
+        assert np.array_equal(to_bits(Z[r]), to_bits(Z2[r])), f"rank {r}: fused and unfused glue differ"
