@@ -93,6 +93,12 @@ typedef enum {
                             FO_ERR_TIMEOUT from fo_ctx_poll and the context stays usable */
 } fo_fault;
 
+typedef enum {
+  FO_EPI_PLAIN = 0,      /* Y = X W^T (bf16)                                                */
+  FO_EPI_SILU_GATE = 1   /* W_col[r] = [gate rows; up rows] ([2F, K]); Y[r] = SiLU(gate) * up,
+                            [M, F], each of gate/up rounded to bf16 first (MLP glue fused)  */
+} fo_epilogue;
+
 typedef struct {
   int32_t order;        /* fo_order                                                   */
   int32_t link;         /* fo_link; all-gather hops are always copy-engine copies      */
@@ -101,7 +107,7 @@ typedef struct {
   int32_t causal_prune; /* attention: forward a K/V slice only to ranks that use it   */
   int32_t num_sms;      /* persistent grid size cap (0 = every SM)                    */
   int32_t fault;        /* fo_fault                                                   */
-  int32_t reserved;
+  int32_t epilogue;     /* fo_epilogue (fo_ag_gemm only)                              */
 } fo_opts;
 
 /* Version of this ABI (major*100 + minor). */

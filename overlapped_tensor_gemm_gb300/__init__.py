@@ -26,6 +26,7 @@ FO_BF16, FO_F32 = 0, 1
 ORDERS = {"flash": 0, "naive": 1, "slicing": 2, "serial": 3}
 LINKS = {"default": 0, "ce": 1, "push": 2}
 FAULTS = {"none": 0, "skip_hop": 1}
+EPILOGUES = {"plain": 0, "silu": 1}
 
 # Every entry point declared in include/fo.h.
 ABI_SYMBOLS = ("fo_version", "fo_last_error_string", "fo_ctx_create", "fo_ctx_destroy", "fo_ctx_poll",
@@ -41,7 +42,7 @@ class FoMat(ctypes.Structure):
 class FoOpts(ctypes.Structure):
     _fields_ = [("order", ctypes.c_int32), ("link", ctypes.c_int32), ("n_slices", ctypes.c_int32),
                 ("timeout_us", ctypes.c_uint32), ("causal_prune", ctypes.c_int32), ("num_sms", ctypes.c_int32),
-                ("fault", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("fault", ctypes.c_int32), ("epilogue", ctypes.c_int32)]
 
 
 class FoError(RuntimeError):
@@ -121,8 +122,9 @@ def _mats(ts: Sequence) -> ctypes.Array:
 
 
 def opts(order: str = "flash", link: str = "default", n_slices: int = 0, timeout_us: int = 0,
-         causal_prune: bool = False, num_sms: int = 0, fault: str = "none") -> FoOpts:
-    return FoOpts(ORDERS[order], LINKS[link], n_slices, timeout_us, int(causal_prune), num_sms, FAULTS[fault], 0)
+         causal_prune: bool = False, num_sms: int = 0, fault: str = "none", epilogue: str = "plain") -> FoOpts:
+    return FoOpts(ORDERS[order], LINKS[link], n_slices, timeout_us, int(causal_prune), num_sms, FAULTS[fault],
+                  EPILOGUES[epilogue])
 
 
 def _stream(stream) -> ctypes.c_void_p:

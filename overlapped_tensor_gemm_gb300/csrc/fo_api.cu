@@ -197,6 +197,8 @@ fo_status check_common(fo_ctx* ctx, int P, const fo_opts* opts) {
     if (opts->fault < FO_FAULT_NONE || opts->fault > FO_FAULT_SKIP_HOP)
       return fail(FO_ERR_INVALID_ARG, "unknown fault %d", opts->fault);
     if (opts->num_sms < 0) return fail(FO_ERR_INVALID_ARG, "num_sms < 0");
+    if (opts->epilogue < FO_EPI_PLAIN || opts->epilogue > FO_EPI_SILU_GATE)
+      return fail(FO_ERR_INVALID_ARG, "unknown epilogue %d", opts->epilogue);
   }
   return FO_OK;
 }
@@ -924,7 +926,7 @@ fo_status fo_ag_gemm(fo_ctx* ctx, const fo_mat* X_shards, const fo_mat* W_col, i
   FO_CUDA(cudaSetDevice(ctx->device));
   const fo_opts o = opts ? *opts : default_opts();
   if (o.order == FO_ORDER_NAIVE) return fail(FO_ERR_INVALID_ARG, "FO_ORDER_NAIVE applies to reduce-scatter only");
-  return ag_run(ctx, X_shards, W_col, P, Y, o, static_cast<cudaStream_t>(stream));
+  return ag_run(ctx, X_shards, W_col, P, Y, o, static_cast<cudaStream_t>(stream), o.epilogue == FO_EPI_SILU_GATE);
 }
 
 fo_status fo_gemm_rs(fo_ctx* ctx, const fo_mat* X, const fo_mat* W_row, int P, const fo_mat* Y,
