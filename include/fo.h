@@ -205,6 +205,30 @@ FO_API fo_status fo_qsplit_attn(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K_sh
                          const fo_mat* V_shards, int P, int heads, int head_dim, int causal,
                          const fo_mat* O, const fo_opts* opts, void* stream);
 
+/* Flash-RS (as fo_gemm_rs, FO_ORDER_FLASH) for callers that cannot allocate
+ * device memory.  (No counterpart on the pages: this is a deployment variant.)
+ * fo_gemm_rs keeps its ring scratch -- fp32 receive slots and per-tile flags --
+ * in a context that allocates it with cudaMalloc.  Callers whose device memory
+ * is owned entirely by their own allocator, or that must not pay the
+ * device-wide synchronisation of cudaMalloc/cudaFree on a latency-critical
+ * path, cannot do that.  This entry point allocates nothing and needs no
+ * context: its scratch is a fixed 64 MiB device array inside the library,
+ * which every GPU that loads the library holds until the process exits.
+ *   X, W_row, Y, P  as fo_gemm_rs (device pointers, caller-owned).
+ *   timeout_us      limit of every device-side wait (0 = 1 second).
+ *   status          optional device uint32: receives 0 or FO_ERR_TIMEOUT when
+ *                   the call's work has completed on `stream` (NULL: none).
+ * Shapes whose receive slots (P*(P-1)*m*N*4 bytes) or flags exceed the static
+ * area are rejected with FO_ERR_UNSUPPORTED.  The first call on a device does a
+ * one-time set-up (it resolves the array's device address with that device
+ * current); make that first call before any stream capture.  Every call shares
+ * the array and keeps the previous call's contents (flags are epoch-valued and
+ * the control words are cleared per call); calls whose work overlaps on the
+ * GPU race, so order them on one stream.  Not thread-safe across host threads
+ * using the same device concurrently with overlapping work. */
+FO_API fo_status fo_gemm_rs_noalloc(const fo_mat* X, const fo_mat* W_row, int P, const fo_mat* Y,
+                                    uint32_t timeout_us, uint32_t* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

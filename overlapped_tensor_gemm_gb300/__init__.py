@@ -31,7 +31,7 @@ EPILOGUES = {"plain": 0, "silu": 1}
 # Every entry point declared in include/fo.h.
 ABI_SYMBOLS = ("fo_version", "fo_last_error_string", "fo_ctx_create", "fo_ctx_destroy", "fo_ctx_poll",
                "fo_ctx_phase_ms", "fo_gemm", "fo_ag_gemm", "fo_gemm_rs", "fo_silu_mul", "fo_mlp_layer",
-               "fo_mlp_layer_host", "fo_qsplit_attn", "fo_step_order")
+               "fo_mlp_layer_host", "fo_qsplit_attn", "fo_step_order", "fo_gemm_rs_noalloc")
 
 
 class FoMat(ctypes.Structure):
@@ -82,6 +82,8 @@ def load() -> ctypes.CDLL:
                                        ctypes.c_int, ctypes.c_int, P(FoMat), P(FoOpts), vp]
         lib.fo_step_order.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P(ctypes.c_int32),
                                       P(ctypes.c_int32), ctypes.c_int]
+        lib.fo_gemm_rs_noalloc.argtypes = [P(FoMat), P(FoMat), ctypes.c_int, P(FoMat), ctypes.c_uint32,
+                                           vp, vp]
         for name in ABI_SYMBOLS:
             if name not in ("fo_version", "fo_last_error_string", "fo_step_order"):
                 getattr(lib, name).restype = ctypes.c_int
