@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--workload", default="llama8b")
     ap.add_argument("--no-extras", action="store_true", help="skip baselines, attention and e2e")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--attn-order", default="flash", choices=["flash", "serial"],
+                    help="order of the attention workload's main timing ('serial' for ncu, as --ag-order)")
     ap.add_argument("--ag-order", default="flash", choices=["flash", "serial"],
                     help="order of the AG projection; 'serial' (ring first, same GEMM kernel after) is what "
                          "runs under ncu, which serialises copy-engine work against kernels")
@@ -61,6 +63,21 @@ def peaks():
         return {"bf16_burst": d["bf16_tflops"], "bf16_sustained": d["bf16_tflops_sustained"],
                 "hbm_gbs": d["hbm_gbs"], "source": "measured"}
     return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def profiled_traffic(profile: str, source: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source is unchanged."""
+    import hashlib
+    import re
+    try:
+        text = open(os.path.join(ROOT, "profiles", profile)).read()
+        want = re.search(r"sha256 prefix `([0-9a-f]+)`", text).group(1)
+        have = hashlib.sha256(open(os.path.join(ROOT, source), "rb").read()).hexdigest()[:len(want)]
+        if have != want:
+            return None
+        return int(re.search(r"traffic_bytes_per_launch: (\d+)", text).group(1))
+    except (OSError, AttributeError):
+        return None
 
 
 def aggregate(flop_per_rank: float, ms_per_rank: float, world: int, reduce_max) -> tuple[float, float]:
@@ -285,7 +302,11 @@ def run_ours(args, rank: int, world: int, device: int):
     out["roofline"] = {"bound": "tensor", "kernel": f"gemm_kernel (Flash-AG launch, {epi} epilogue)",
                        "achieved": round(ag_tflops, 2),
                        "peak": pk["bf16_burst"], "unit": "TFLOP/s", "frac": round(ag_tflops / pk["bf16_burst"], 4),
-                       "peak_kind": f"bf16 burst ({pk['source']})", "traffic": None}
+                       "peak_kind": f"bf16 burst ({pk['source']})",
+                       "traffic": (profiled_traffic("gemm_kernel_llama8b_mlp.md",
+                                                    "overlapped_tensor_gemm_gb300/csrc/fo_gemm.cu")
+                                   if cfg.name == "llama8b" else None),
+                       "traffic_unit": "bytes per launch (dram read + write, ncu)"}
     breakdown = {"ag_flash_ms": round(t_ag, 4), "rs_flash_ms": round(t_rs, 4),
                  "ag_tflops": round(ag_tflops, 2), "rs_tflops": round(flops["rs"] / (t_rs * 1e-3) / 1e12, 2)}
     if not args.no_extras:
@@ -349,7 +370,7 @@ def run_ours(args, rank: int, world: int, device: int):
     return out
 
 
-def attention_bench(ctx, pk, iters: int):
+def attention_bench(ctx, pk, iters: int, order: str = "flash", baselines: bool = True):
     import torch
     c = wl.ATTN
     g = torch.Generator(device="cuda")
@@ -360,22 +381,36 @@ def attention_bench(ctx, pk, iters: int):
     V = [torch.randn(shape, generator=g, device="cuda").to(torch.bfloat16) for _ in range(c.P)]
     O = [torch.empty(shape, dtype=torch.bfloat16, device="cuda") for _ in range(c.P)]
     stream = torch.cuda.current_stream()
-    for _ in range(2):
-        ctx.qsplit_attn(Q, K, V, O, heads=c.heads, head_dim=c.head_dim)
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(iters):
-        ctx.qsplit_attn(Q, K, V, O, heads=c.heads, head_dim=c.head_dim)
-    b.record(stream)
-    torch.cuda.synchronize()
-    ctx.poll()
-    ms = a.elapsed_time(b) / iters
+
+    def timed(o):
+        for _ in range(2):
+            ctx.qsplit_attn(Q, K, V, O, heads=c.heads, head_dim=c.head_dim, order=o)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(iters):
+            ctx.qsplit_attn(Q, K, V, O, heads=c.heads, head_dim=c.head_dim, order=o)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ctx.poll()
+        return a.elapsed_time(b) / iters
+
+    ms = timed(order)
     tf = c.flops() / (ms * 1e-3) / 1e12
-    return {"workload": f"query-split causal attention, P={c.P}, seq {c.seq}, {c.heads} heads, head_dim "
-                        f"{c.head_dim}", "ms": round(ms, 4), "tflops": round(tf, 2),
-            "frac_of_bf16_peak": round(tf / pk["bf16_burst"], 4), "flop": c.flops(),
-            "flop_counting": "causal triangle only (QK^T and PV)"}
+    out = {"workload": f"query-split causal attention, P={c.P}, seq {c.seq}, {c.heads} heads, head_dim "
+                       f"{c.head_dim}", "order": order, "ms": round(ms, 4), "tflops": round(tf, 2),
+           "frac_of_bf16_peak": round(tf / pk["bf16_burst"], 4), "flop": c.flops(),
+           "flop_counting": "causal triangle only (QK^T and PV)"}
+    if baselines:
+        t_serial = timed("serial")
+        ctx.qsplit_attn(Q, K, V, O, heads=c.heads, head_dim=c.head_dim, order="serial")
+        torch.cuda.synchronize()
+        ring_ms, kernel_ms = ctx.phase_ms()
+        out.update({"serial_ms": round(t_serial, 4), "serial_phases_ms": {"ring": round(ring_ms, 4),
+                                                                           "kernel": round(kernel_ms, 4)},
+                    "exposed_copy_ms": round(ms - kernel_ms, 4),
+                    "exposed_frac": round((ms - kernel_ms) / ms, 4)})
+    return out
 
 
 def run_tail_rs(args, world, device, pk):
@@ -429,7 +464,7 @@ def run_tail_rs(args, world, device, pk):
 def run_attention_only(args, rank, world, device, pk, barrier, max_over_ranks):
     import overlapped_tensor_gemm_gb300 as fo
     ctx = fo.Context(device)
-    res = attention_bench(ctx, pk, args.steps)
+    res = attention_bench(ctx, pk, args.steps, args.attn_order, baselines=not args.no_extras)
     ctx.close()
     return {"metric": "query-split attention TFLOP/s", "value": res["tflops"], "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"],

@@ -108,6 +108,9 @@ typedef struct {
   int32_t num_sms;      /* persistent grid size cap (0 = every SM)                    */
   int32_t fault;        /* fo_fault                                                   */
   int32_t epilogue;     /* fo_epilogue (fo_ag_gemm only)                              */
+  int32_t sm_pairs;     /* GEMM tiles: 0 = automatic (256x256 tiles on SM pairs when every
+                           unit's rows are a multiple of 256), 1 = single-SM 128x256 tiles */
+  int32_t reserved;
 } fo_opts;
 
 /* Version of this ABI (major*100 + minor). */
@@ -200,7 +203,9 @@ FO_API fo_status fo_mlp_layer_host(fo_ctx* ctx, const fo_mat* X_shards, const fo
  *   head_dim contiguous.  head_dim == 128.  Scale 1/sqrt(head_dim).
  *   causal != 0: key j attends query i only if j <= i (global token indices);
  *   slices wholly above the diagonal are skipped.
- * Softmax statistics and the output accumulator are fp32 (online softmax). */
+ * Softmax statistics and the output accumulator are fp32 (online softmax).
+ * opts->order: FO_ORDER_FLASH (the ring runs while the kernel computes) or
+ * FO_ORDER_SERIAL (baseline: the whole K/V ring first, then the kernel). */
 FO_API fo_status fo_qsplit_attn(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K_shards,
                          const fo_mat* V_shards, int P, int heads, int head_dim, int causal,
                          const fo_mat* O, const fo_opts* opts, void* stream);

@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfo.so")
-SOURCES = ["fo_api.cu", "fo_gemm.cu", "fo_attn.cu", "fo_elem.cu", "fo_static.cu"]
+SOURCES = ["fo_api.cu", "fo_gemm.cu", "fo_gemm2.cu", "fo_attn.cu", "fo_elem.cu", "fo_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden", "--expt-relaxed-constexpr"]
 

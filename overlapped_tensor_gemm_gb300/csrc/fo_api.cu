@@ -134,6 +134,7 @@ struct fo_ctx {
   bool phase_gemm_first = false;  // RS serial: GEMM phase precedes the collective
   uint32_t* ctrl = nullptr;
   uint32_t epoch = 0;
+  int pair_clusters = 0;  // resident SM pairs for the 256x256-tile kernel (0: unavailable)
   std::map<int, Buffer> bufs;
 };
 
@@ -199,6 +200,7 @@ fo_status check_common(fo_ctx* ctx, int P, const fo_opts* opts) {
     if (opts->num_sms < 0) return fail(FO_ERR_INVALID_ARG, "num_sms < 0");
     if (opts->epilogue < FO_EPI_PLAIN || opts->epilogue > FO_EPI_SILU_GATE)
       return fail(FO_ERR_INVALID_ARG, "unknown epilogue %d", opts->epilogue);
+    if (opts->sm_pairs < 0 || opts->sm_pairs > 1) return fail(FO_ERR_INVALID_ARG, "sm_pairs must be 0 or 1");
   }
   return FO_OK;
 }
@@ -238,8 +240,15 @@ fo_status encode_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t co
   return FO_OK;
 }
 
+struct MapSpec {
+  const void* ptr;
+  int64_t rows, cols, ld;
+  int box_rows;
+};
+
 struct Launch {
   GemmParams p;
+  MapSpec spec[kMaxMaps];
   int num_units = 0;
   int num_groups = 0;
   int num_maps = 0;
@@ -251,7 +260,21 @@ struct Launch {
       return -1;
     }
     *st = encode_map(&p.maps[num_maps], ptr, rows, cols, ld, box_rows);
+    spec[num_maps] = MapSpec{ptr, rows, cols, ld, box_rows};
     return num_maps++;
+  }
+
+  // SM-pair tiles: each CTA stages 128 rows of B (its half of the 256-wide tile), so
+  // every B operand map is re-encoded with 128-row boxes.
+  fo_status pair_boxes() {
+    bool is_b[kMaxMaps] = {};
+    for (int u = 0; u < num_units; ++u) is_b[p.units[u].b_map] = true;
+    for (int m = 0; m < num_maps; ++m) {
+      if (!is_b[m] || spec[m].box_rows == kBN / 2) continue;
+      FO_TRY(encode_map(&p.maps[m], spec[m].ptr, spec[m].rows, spec[m].cols, spec[m].ld, kBN / 2));
+      spec[m].box_rows = kBN / 2;
+    }
+    return FO_OK;
   }
   void begin_group() {
     p.group_unit_begin[num_groups] = num_units;
@@ -259,11 +282,9 @@ struct Launch {
   }
   GemmUnit& add_unit() { return p.units[num_units++]; }
 
-  // Finalises group boundaries and tile counts.  All units of a group share one tile grid.
-  fo_status finish(uint32_t epoch, uint64_t tmo, uint32_t* flags, uint32_t* ctrl, int mblock_major) {
-    if (num_units > kMaxUnits || num_groups > kMaxGroups)
-      return fail(FO_ERR_UNSUPPORTED, "too many units (%d) or groups (%d)", num_units, num_groups);
-    p.group_unit_begin[num_groups] = num_units;
+  // Tile grids for tiles of `bm` rows (128: single SM, 256: SM pair).  All units of a
+  // group share one tile grid.
+  fo_status retile(int bm) {
     int64_t tiles = 0;
     for (int g = 0; g < num_groups; ++g) {
       p.group_tile_begin[g] = static_cast<int32_t>(tiles);
@@ -271,7 +292,7 @@ struct Launch {
       for (int u = u0; u < u1; ++u) {
         GemmUnit& x = p.units[u];
         const int bn = x.gated ? kBN / 2 : kBN;  // output columns per tile
-        x.tiles_m = (x.m_rows + kBM - 1) / kBM;
+        x.tiles_m = (x.m_rows + bm - 1) / bm;
         x.tiles_n = (x.n_cols + bn - 1) / bn;
         if (x.tiles_m != p.units[u0].tiles_m || x.tiles_n != p.units[u0].tiles_n)
           return fail(FO_ERR_SHAPE, "units of one step must share a tile grid");
@@ -280,9 +301,25 @@ struct Launch {
     }
     if (tiles > (1ll << 30)) return fail(FO_ERR_UNSUPPORTED, "too many tiles");
     p.group_tile_begin[num_groups] = static_cast<int32_t>(tiles);
+    p.total_tiles = static_cast<int32_t>(tiles);
+    return FO_OK;
+  }
+
+  // Every unit's rows are a multiple of 256: the SM-pair kernel wastes no rows.
+  bool pair_friendly() const {
+    for (int u = 0; u < num_units; ++u)
+      if (p.units[u].m_rows % (2 * kBM) != 0) return false;
+    return num_units > 0;
+  }
+
+  // Finalises group boundaries and tile counts (single-SM tiles).
+  fo_status finish(uint32_t epoch, uint64_t tmo, uint32_t* flags, uint32_t* ctrl, int mblock_major) {
+    if (num_units > kMaxUnits || num_groups > kMaxGroups)
+      return fail(FO_ERR_UNSUPPORTED, "too many units (%d) or groups (%d)", num_units, num_groups);
+    p.group_unit_begin[num_groups] = num_units;
+    FO_TRY(retile(kBM));
     p.num_groups = num_groups;
     p.num_maps = num_maps;
-    p.total_tiles = static_cast<int32_t>(tiles);
     p.mblock_major = mblock_major;
     p.epoch = epoch;
     p.timeout_ns = tmo;
@@ -303,6 +340,16 @@ GemmUnit blank_unit() {
 
 fo_status launch_gemm(fo_ctx* ctx, Launch& L, const fo_opts& o, cudaStream_t stream) {
   if (L.p.total_tiles == 0) return FO_OK;
+  if (o.sm_pairs == 0 && ctx->pair_clusters > 0 && L.pair_friendly()) {
+    // 256x256 tiles on SM pairs; the persistent grid never exceeds the resident clusters
+    FO_TRY(L.retile(2 * kBM));
+    FO_TRY(L.pair_boxes());
+    int clusters = ctx->pair_clusters;
+    if (o.num_sms > 0 && o.num_sms / 2 < clusters) clusters = o.num_sms / 2 > 0 ? o.num_sms / 2 : 1;
+    if (L.p.total_tiles < clusters) clusters = L.p.total_tiles;
+    FO_CUDA(gemm_pair_launch(L.p, clusters, stream));
+    return FO_OK;
+  }
   FO_CUDA(gemm_launch(L.p, grid_size(ctx, o, L.p.total_tiles), stream));
   return FO_OK;
 }
@@ -789,6 +836,12 @@ fo_status fo_ctx_create(int device, fo_ctx** out) {
     return st;
   };
   if (gemm_configure() != cudaSuccess) return cleanup(fail(FO_ERR_CUDA, "gemm kernel configuration failed"));
+  if (gemm_pair_configure() == cudaSuccess) {
+    c->pair_clusters = gemm_pair_max_clusters();
+  } else {
+    cudaGetLastError();
+    c->pair_clusters = 0;
+  }
   for (int r = 0; r < kMaxP; ++r) {
     if (cudaStreamCreateWithFlags(&c->link[r], cudaStreamNonBlocking) != cudaSuccess)
       return cleanup(fail(FO_ERR_CUDA, "stream creation failed"));
@@ -1053,4 +1106,9 @@ fo_status host_check_mat(const fo_mat& a, int32_t dtype, const char* what, int r
 fo_status host_fail(fo_status st, const char* msg) { return fail(st, "%s", msg); }
 uint64_t host_timeout_ns(const fo_opts& o) { return timeout_ns(o); }
 int host_grid(fo_ctx* ctx, const fo_opts& o, int work) { return grid_size(ctx, o, work); }
+void host_phase_record(fo_ctx* ctx, int i, cudaStream_t s) { cudaEventRecord(ctx->ev_phase[i], s); }
+void host_phase_done(fo_ctx* ctx, bool gemm_first) {
+  ctx->phase_valid = true;
+  ctx->phase_gemm_first = gemm_first;
+}
 }  // namespace fo

@@ -11,17 +11,20 @@
 // online-softmax state: row max and sum in registers, the output accumulator
 // in TMEM.
 //
-// CTA layout (192 threads, one CTA per SM):
-//   warp 0      TMA: Q block once per item, then K and V^T blocks (2 stages);
-//               waits for the slice's arrival flag before reading it.
+// CTA layout (320 threads, one CTA per SM):
+//   warp 0      TMA: Q block once per item, then K and V^T blocks in two
+//               rings of 2 stages each, K one block ahead of V; waits for the
+//               slice's arrival flag before reading it.
 //   warp 1      tcgen05.mma: S = Q K^T into one of two TMEM score buffers
 //               (the next block's scores overlap this block's softmax), then
 //               O += P V into the TMEM accumulator.
-//   warps 2-5   softmax: thread i owns query row i; loads its score row,
-//               masks the diagonal block, updates max/sum, rescales its O row
-//               only when the max grew by more than 2^8 (the final division
-//               by the sum uses the same reference max, so this is exact), and
-//               writes P into shared memory in the MMA's operand layout.
+//   warps 2-9   softmax: two warps per query row (one per 64-key half); they
+//               load their half of the score row, mask the diagonal block,
+//               combine the row maximum, update max/sum, rescale their half
+//               of the O row only when the max grew by more than 2^8 (the
+//               final division by the sum uses the same reference max, so this
+//               is exact), and write P into shared memory in the MMA's operand
+//               layout.
 // V is transposed once per rank (V^T [heads*128, tokens]) before the ring so
 // that both MMAs read K-major operands.  The P.V product runs in fp16: the
 // transpose converts V's bf16 values to fp16 (exact for |v| within fp16's
@@ -44,16 +47,18 @@ namespace {
 constexpr int kHd = 128;                 // head_dim
 constexpr int kQB = 128;                 // queries per block
 constexpr int kKB = 128;                 // keys per block
-constexpr int kAttnThreads = 192;
+constexpr int kAttnThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 softmax
 constexpr uint32_t kTileBytes = 128 * 128 * 2;   // one 128x128 bf16 operand (two 64-column swizzle halves)
 constexpr uint32_t kHalfBytes = kTileBytes / 2;
-constexpr int kKvStages = 2;
+constexpr int kKStages = 2;
+constexpr int kVStages = 2;
 constexpr uint32_t kTmemCols = 512;      // S0 [0,128), S1 [128,256), O [256,384)
 constexpr uint32_t kOCol = 256;
 constexpr uint32_t kIdescS = umma_idesc_bf16(128, 128);   // S = Q K^T, bf16 operands
 constexpr uint32_t kIdescO = umma_idesc_f16(128, 128);    // O += P V, fp16 operands
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kPolyEvery = 0;              // 0: every softmax weight through MUFU ex2
 
 struct AttnParams {
   CUtensorMap maps[4 * kMaxP];  // per rank r: Q = r, K local = P+r, K received = 2P+r, V^T = 3P+r
@@ -67,22 +72,28 @@ struct AttnParams {
   uint64_t timeout_ns;
   uint32_t* flags;              // arrival flags, index rank*P + slice
   uint32_t* ctrl;
+  int32_t wait_flags;           // 0: every slice is already in place (serial order)
+  int32_t pad;
 };
 
 struct alignas(8) AttnCtl {
   uint64_t q_full, q_empty;
-  uint64_t kv_full[kKvStages], kv_empty[kKvStages];
+  uint64_t k_full[kKStages], k_empty[kKStages];
+  uint64_t v_full[kVStages], v_empty[kVStages];
   uint64_t s_full[2], s_empty[2];
   uint64_t p_full, o_done, drain;
+  uint64_t xchg[4][2];   // per lane quadrant, two slots: the column halves' partial max / sum exchange
   uint32_t tmem_base;
   uint32_t pad;
 };
 
-// Shared memory: Q | K stage 0 | V^T stage 0 | K stage 1 | V^T stage 1 | P | control
+// Shared memory: Q | K stages | V^T stages | P | exchange | control
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffKv = kTileBytes;
-constexpr uint32_t kOffP = kOffKv + kKvStages * 2 * kTileBytes;
-constexpr uint32_t kOffCtl = kOffP + kTileBytes;
+constexpr uint32_t kOffK = kTileBytes;
+constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
+constexpr uint32_t kOffP = kOffV + kVStages * kTileBytes;
+constexpr uint32_t kOffXch = kOffP + kTileBytes;             // float [2 slots][2 halves][128 rows]
+constexpr uint32_t kOffCtl = kOffXch + 2 * 2 * 128 * 4;
 constexpr int kAttnSmem = static_cast<int>(kOffCtl + sizeof(AttnCtl) + 1024);
 
 struct Item {
@@ -112,66 +123,116 @@ __device__ __forceinline__ int item_blocks(const AttnParams& p, const Item& it) 
 
 // ---------------------------------------------------------------------------
 
-__device__ void attn_producer(const AttnParams& p, uint8_t* smem, AttnCtl* ctl) {
-  int stage = 0;
-  uint32_t phase = 0;
-  uint32_t q_uses = 0;
-  uint64_t seen = 0;  // bit r*P+s: arrival of slice s at rank r already observed
-  uint32_t armed = 0, armed_phase = 0;
-  bool q_armed = false;
-  uint32_t q_armed_phase = 0;
-  bool ok = true;
-  for (int i = blockIdx.x; ok && i < p.total_items; i += gridDim.x) {
-    const Item it = decode_item(p, i);
-    if (!mbar_wait(&ctl->q_empty, (q_uses & 1u) ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty, i)) break;
-    mbar_arrive_expect_tx(&ctl->q_full, kTileBytes);
-    for (int c = 0; c < 2; ++c)
-      tma_load_2d(&p.maps[it.r], smem + kOffQ + c * kHalfBytes, &ctl->q_full, it.h * kHd + c * 64, it.qb * kQB);
-    q_armed = true;
-    q_armed_phase = q_uses & 1u;
-    ++q_uses;
-    const int nsteps = steps_of(p, it.r);
-    for (int t = 0; ok && t < nsteps; ++t) {
-      const int s = slice_of(p, it.r, t);
-      const int fidx = it.r * p.P + s;
-      if (t > 0 && !((seen >> fidx) & 1ull)) {
-        if (!flag_wait(p.flags + fidx, p.epoch, p.ctrl, p.timeout_ns, kSiteAttnFlag, fidx)) {
-          ok = false;
-          break;
-        }
-        fence_proxy_async_global();
-        seen |= 1ull << fidx;
-      }
-      const CUtensorMap* kmap = t == 0 ? &p.maps[p.P + it.r] : &p.maps[2 * p.P + it.r];
-      const int krow0 = t == 0 ? 0 : s * p.m;
-      const CUtensorMap* vmap = &p.maps[3 * p.P + it.r];
-      const int vrow0 = (s * p.heads + it.h) * kHd;
-      const int nb = blocks_of(p, it, t);
-      for (int kb = 0; kb < nb; ++kb) {
-        if (!mbar_wait(&ctl->kv_empty[stage], phase ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty, i)) {
-          ok = false;
-          break;
-        }
-        uint8_t* kt = smem + kOffKv + stage * 2 * kTileBytes;
-        uint8_t* vt = kt + kTileBytes;
-        mbar_arrive_expect_tx(&ctl->kv_full[stage], 2 * kTileBytes);
-        for (int c = 0; c < 2; ++c) {
-          tma_load_2d(kmap, kt + c * kHalfBytes, &ctl->kv_full[stage], it.h * kHd + c * 64, krow0 + kb * kKB);
-          tma_load_2d(vmap, vt + c * kHalfBytes, &ctl->kv_full[stage], kb * kKB + c * 64, vrow0);
-        }
-        armed |= 1u << stage;
-        armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
-        if (++stage == kKvStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
+// Walks this CTA's key blocks in schedule order: items (stride gridDim.x), ring
+// steps (local slice first), 128-key blocks.
+struct BlockIter {
+  int i, t, kb, nsteps, nb;
+  Item it;
+  __device__ void start(const AttnParams& p) {
+    i = blockIdx.x;
+    t = kb = 0;
+    if (i < p.total_items) load(p);
+  }
+  __device__ void load(const AttnParams& p) {
+    it = decode_item(p, i);
+    nsteps = steps_of(p, it.r);
+    nb = blocks_of(p, it, 0);
+  }
+  __device__ bool valid(const AttnParams& p) const { return i < p.total_items; }
+  __device__ bool first_of_item() const { return t == 0 && kb == 0; }
+  __device__ void next(const AttnParams& p) {
+    if (++kb < nb) return;
+    kb = 0;
+    if (++t < nsteps) {
+      nb = blocks_of(p, it, t);
+      return;
     }
+    t = 0;
+    i += gridDim.x;
+    if (i < p.total_items) load(p);
+  }
+};
+
+// K runs one block ahead of V: a K stage is refilled as soon as the score MMA
+// that read it completes, a V stage once the P.V MMA that read it completes.
+__device__ void attn_producer(const AttnParams& p, uint8_t* smem, AttnCtl* ctl) {
+  int kst = 0, vst = 0;
+  uint32_t kph = 0, vph = 0, q_uses = 0;
+  uint64_t seen = 0;  // bit r*P+s: arrival of slice s at rank r already observed
+  uint32_t karmed = 0, karmed_ph = 0, varmed = 0, varmed_ph = 0;
+  bool q_armed = false;
+  uint32_t q_armed_ph = 0;
+  BlockIter kit, vit;
+  kit.start(p);
+  vit.start(p);
+  bool ok = true;
+  auto issue_k = [&]() -> bool {
+    const Item& it = kit.it;
+    if (kit.first_of_item()) {
+      if (!mbar_wait(&ctl->q_empty, (q_uses & 1u) ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty, kit.i)) return false;
+      mbar_arrive_expect_tx(&ctl->q_full, kTileBytes);
+      for (int c = 0; c < 2; ++c)
+        tma_load_2d(&p.maps[it.r], smem + kOffQ + c * kHalfBytes, &ctl->q_full, it.h * kHd + c * 64,
+                    it.qb * kQB);
+      q_armed = true;
+      q_armed_ph = q_uses & 1u;
+      ++q_uses;
+    }
+    const int s = slice_of(p, it.r, kit.t);
+    const int fidx = it.r * p.P + s;
+    if (kit.t > 0 && p.wait_flags && !((seen >> fidx) & 1ull)) {
+      if (!flag_wait(p.flags + fidx, p.epoch, p.ctrl, p.timeout_ns, kSiteAttnFlag, fidx)) return false;
+      fence_proxy_async_global();
+      seen |= 1ull << fidx;
+    }
+    if (!mbar_wait(&ctl->k_empty[kst], kph ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty, kit.i)) return false;
+    const CUtensorMap* kmap = kit.t == 0 ? &p.maps[p.P + it.r] : &p.maps[2 * p.P + it.r];
+    const int krow0 = kit.t == 0 ? 0 : s * p.m;
+    uint8_t* kt = smem + kOffK + kst * kTileBytes;
+    mbar_arrive_expect_tx(&ctl->k_full[kst], kTileBytes);
+    for (int c = 0; c < 2; ++c)
+      tma_load_2d(kmap, kt + c * kHalfBytes, &ctl->k_full[kst], it.h * kHd + c * 64, krow0 + kit.kb * kKB);
+    karmed |= 1u << kst;
+    karmed_ph = (karmed_ph & ~(1u << kst)) | (kph << kst);
+    if (++kst == kKStages) {
+      kst = 0;
+      kph ^= 1u;
+    }
+    kit.next(p);
+    return true;
+  };
+  auto issue_v = [&]() -> bool {
+    const Item& it = vit.it;
+    const int s = slice_of(p, it.r, vit.t);  // arrival already observed by the K walk
+    if (!mbar_wait(&ctl->v_empty[vst], vph ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty, vit.i)) return false;
+    uint8_t* vt = smem + kOffV + vst * kTileBytes;
+    mbar_arrive_expect_tx(&ctl->v_full[vst], kTileBytes);
+    for (int c = 0; c < 2; ++c)
+      tma_load_2d(&p.maps[3 * p.P + it.r], vt + c * kHalfBytes, &ctl->v_full[vst], vit.kb * kKB + c * 64,
+                  (s * p.heads + it.h) * kHd);
+    varmed |= 1u << vst;
+    varmed_ph = (varmed_ph & ~(1u << vst)) | (vph << vst);
+    if (++vst == kVStages) {
+      vst = 0;
+      vph ^= 1u;
+    }
+    vit.next(p);
+    return true;
+  };
+  if (kit.valid(p)) ok = issue_k();
+  while (ok && vit.valid(p)) {
+    if (kit.valid(p) && !issue_k()) {
+      ok = false;
+      break;
+    }
+    if (!issue_v()) ok = false;
   }
   if (!ok) {
-    if (q_armed) mbar_wait_drain(&ctl->q_full, q_armed_phase, kDrainNs);
-    for (int s = 0; s < kKvStages; ++s)
-      if ((armed >> s) & 1u) mbar_wait_drain(&ctl->kv_full[s], (armed_phase >> s) & 1u, kDrainNs);
+    if (q_armed) mbar_wait_drain(&ctl->q_full, q_armed_ph, kDrainNs);
+    for (int s = 0; s < kKStages; ++s)
+      if ((karmed >> s) & 1u) mbar_wait_drain(&ctl->k_full[s], (karmed_ph >> s) & 1u, kDrainNs);
+    for (int s = 0; s < kVStages; ++s)
+      if ((varmed >> s) & 1u) mbar_wait_drain(&ctl->v_full[s], (varmed_ph >> s) & 1u, kDrainNs);
   }
 }
 
@@ -205,13 +266,14 @@ __device__ void attn_mma(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, uint3
     tc_fence_after();
     // S for block j: K of kv stage (g+j) % 2, score buffer (g+j) % 2
     auto issue_scores = [&](uint32_t gj) -> bool {
-      const uint32_t st = gj % kKvStages, sb = gj & 1u;
-      if (!mbar_wait(&ctl->kv_full[st], (gj / kKvStages) & 1u, p.ctrl, p.timeout_ns, kSiteFull, i)) return false;
+      const uint32_t st = gj % kKStages, sb = gj & 1u;
+      if (!mbar_wait(&ctl->k_full[st], (gj / kKStages) & 1u, p.ctrl, p.timeout_ns, kSiteFull, i)) return false;
       if (!mbar_wait(&ctl->s_empty[sb], ((gj >> 1) & 1u) ^ 1u, p.ctrl, p.timeout_ns, kSiteTmemEmpty, i))
         return false;
       tc_fence_after();
-      issue_s(tmem_base + sb * 128, sbase + kOffQ, sbase + kOffKv + st * 2 * kTileBytes);
+      issue_s(tmem_base + sb * 128, sbase + kOffQ, sbase + kOffK + st * kTileBytes);
       issued = true;
+      umma_commit(&ctl->k_empty[st]);  // the K stage is free once these scores are computed
       umma_commit(&ctl->s_full[sb]);
       return true;
     };
@@ -235,9 +297,14 @@ __device__ void attn_mma(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, uint3
       }
       ++p_uses;
       tc_fence_after();
-      const uint32_t st = gj % kKvStages;
-      issue_pv(tmem_base + kOCol, sbase + kOffP, sbase + kOffKv + st * 2 * kTileBytes + kTileBytes, j == 0);
-      umma_commit(&ctl->kv_empty[st]);
+      const uint32_t vs = gj % kVStages;
+      if (!mbar_wait(&ctl->v_full[vs], (gj / kVStages) & 1u, p.ctrl, p.timeout_ns, kSiteFull, i)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      issue_pv(tmem_base + kOCol, sbase + kOffP, sbase + kOffV + vs * kTileBytes, j == 0);
+      umma_commit(&ctl->v_empty[vs]);
       umma_commit(&ctl->o_done);
     }
     g += n;
@@ -255,19 +322,51 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// exp2 on the FMA pipe (offloads the MUFU unit): range reduction
+// x = i + f, f in [0, 1), 2^f by the least-squares cubic derived in
+// poly_exp2_fit.py (relative error < 7.8e-5), 2^i added to the exponent field.
+// Inputs below -126 return 2^-126 * p(f), which rounds to 0 in fp16.
+__device__ __forceinline__ float poly_exp2(float x) {
+  x = fmaxf(x, -126.0f);
+  const float fi = floorf(x);
+  const float f = x - fi;
+  const float p = fmaf(fmaf(fmaf(0.07790716f, f, 0.22623319f), f, 0.69577710f), f, 0.99992783f);
+  return __int_as_float(__float_as_int(p) + (static_cast<int>(fi) << 23));
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
+// Softmax warps 2-9.  Warp w serves TMEM lane quadrant q = w % 4 (query rows
+// 32q..32q+31) and column half hf = (w - 2) / 4 (keys 64hf..64hf+63 of each
+// block).  The two warps of a quadrant combine their partial row maxima (and,
+// at the end, row sums) through shared memory, each exchange closed by a
+// bounded mbarrier wait.
+__device__ __forceinline__ bool exchange(AttnCtl* ctl, float* xch, uint32_t& uses, int q, int hf, int row,
+                                         float mine, float* other, const AttnParams& p, int lane, int item) {
+  const uint32_t slot = uses & 1u;
+  xch[(slot * 2 + hf) * 128 + row] = mine;
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&ctl->xchg[q][slot]);
+  if (!warp_wait(&ctl->xchg[q][slot], (uses >> 1) & 1u, p, kSiteAttnBar, item, lane)) return false;
+  *other = xch[(slot * 2 + (hf ^ 1)) * 128 + row];
+  ++uses;
+  return true;
+}
+
 __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, uint32_t tmem_base, int warp,
                              int lane) {
   const int q = warp & 3;
+  const int hf = (warp - 2) >> 2;
   const int row = q * 32 + lane;  // query row inside the block == TMEM lane
   const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-  uint8_t* prow = smem + kOffP + row * 128;
-  uint32_t g = 0;
+  const uint32_t col0 = static_cast<uint32_t>(hf * 64);  // this warp's key / output columns
+  uint8_t* prow = smem + kOffP + hf * kHalfBytes + row * 128;
+  float* xch = reinterpret_cast<float*>(smem + kOffXch);
+  uint32_t g = 0, xuses = 0;
   for (int i = blockIdx.x; i < p.total_items; i += gridDim.x) {
     const Item it = decode_item(p, i);
     float m_ref = -INFINITY, l = 0.f;
@@ -280,11 +379,11 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
         const uint32_t sb = gj & 1u;
         if (!warp_wait(&ctl->s_full[sb], (gj >> 1) & 1u, p, kSiteTmemFull, i, lane)) return;
         tc_fence_after();
-        float s[128];
+        float s[64];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
-          tmem_ld32(lane_base + sb * 128 + c * 32, v);
+          tmem_ld32(lane_base + sb * 128 + col0 + c * 32, v);
           tmem_wait_ld();
 #pragma unroll
           for (int k = 0; k < 32; ++k) s[c * 32 + k] = __uint_as_float(v[k]) * p.scale_log2;
@@ -295,10 +394,13 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
         const bool diag = p.causal && t == 0 && kb == it.qb;
         float mx = -INFINITY;
 #pragma unroll
-        for (int k = 0; k < 128; ++k) {
-          if (diag && k > row) s[k] = -INFINITY;
+        for (int k = 0; k < 64; ++k) {
+          if (diag && static_cast<int>(col0) + k > row) s[k] = -INFINITY;
           mx = fmaxf(mx, s[k]);
         }
+        float other;
+        if (!exchange(ctl, xch, xuses, q, hf, row, mx, &other, p, lane, i)) return;
+        mx = fmaxf(mx, other);  // the row's block maximum (finite: the diagonal key is never masked)
         float alpha = 1.f;
         bool rescale = false;
         if (j == 0) {
@@ -311,12 +413,14 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
         }
         // the row sum uses the fp16-rounded weights that the P.V product sees
         float sum = 0.f;
-        uint32_t packed[64];
+        uint32_t packed[32];
 #pragma unroll
-        for (int k = 0; k < 64; ++k) {
-          packed[k] = pack_f16x2(fast_exp2(s[2 * k] - m_ref), fast_exp2(s[2 * k + 1] - m_ref));
-          const __half2 h = *reinterpret_cast<const __half2*>(&packed[k]);
-          const float2 f = __half22float2(h);
+        for (int k = 0; k < 32; ++k) {
+          // every kPolyEvery-th pair of weights is computed on the FMA pipe, the rest on MUFU
+          const bool poly = kPolyEvery > 0 && (k % kPolyEvery) == kPolyEvery - 1;
+          packed[k] = poly ? pack_f16x2(poly_exp2(s[2 * k] - m_ref), poly_exp2(s[2 * k + 1] - m_ref))
+                           : pack_f16x2(fast_exp2(s[2 * k] - m_ref), fast_exp2(s[2 * k + 1] - m_ref));
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&packed[k]));
           sum += f.x + f.y;
         }
         l += sum;
@@ -327,21 +431,20 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
         }
         if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 2; ++c) {
             uint32_t v[32];
-            tmem_ld32(lane_base + kOCol + c * 32, v);
+            tmem_ld32(lane_base + kOCol + col0 + c * 32, v);
             tmem_wait_ld();
 #pragma unroll
             for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
-            tmem_st32(lane_base + kOCol + c * 32, v);
+            tmem_st32(lane_base + kOCol + col0 + c * 32, v);
           }
           tmem_wait_st();
         }
-        // P row -> two 128-byte-swizzled halves (keys 0-63, 64-127), 16-byte chunks
+        // this half of the P row: one 128-byte-swizzled half tile, 16-byte chunks
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int half = c >> 3, chunk = c & 7;
-          uint4* dst = reinterpret_cast<uint4*>(prow + half * kHalfBytes + ((chunk ^ (row & 7)) << 4));
+        for (int c = 0; c < 8; ++c) {
+          uint4* dst = reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4));
           *dst = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
         }
         fence_proxy_async_shared();
@@ -350,16 +453,18 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
         if (lane == 0) mbar_arrive(&ctl->p_full);
       }
     }
-    // epilogue: O row / l -> bf16
+    // epilogue: row sum of both halves, O row / l -> bf16 (this warp's 64 columns)
+    float other_l;
+    if (!exchange(ctl, xch, xuses, q, hf, row, l, &other_l, p, lane, i)) return;
     const uint32_t glast = g + j - 1;
     if (!warp_wait(&ctl->o_done, glast & 1u, p, kSiteDrain, i, lane)) return;
     tc_fence_after();
-    const float inv = 1.f / l;
-    uint16_t* orow = p.out[it.r] + static_cast<int64_t>(it.qb * kQB + row) * p.ld_out[it.r] + it.h * kHd;
+    const float inv = 1.f / (l + other_l);
+    uint16_t* orow = p.out[it.r] + static_cast<int64_t>(it.qb * kQB + row) * p.ld_out[it.r] + it.h * kHd + col0;
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 2; ++c) {
       uint32_t v[32];
-      tmem_ld32(lane_base + kOCol + c * 32, v);
+      tmem_ld32(lane_base + kOCol + col0 + c * 32, v);
       tmem_wait_ld();
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -384,15 +489,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   if (threadIdx.x == 0) {
     mbar_init(&ctl->q_full, 1);
     mbar_init(&ctl->q_empty, 1);
-    for (int s = 0; s < kKvStages; ++s) {
-      mbar_init(&ctl->kv_full[s], 1);
-      mbar_init(&ctl->kv_empty[s], 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&ctl->k_full[s], 1);
+      mbar_init(&ctl->k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&ctl->v_full[s], 1);
+      mbar_init(&ctl->v_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&ctl->s_full[b], 1);
-      mbar_init(&ctl->s_empty[b], 4);
+      mbar_init(&ctl->s_empty[b], 8);
     }
-    mbar_init(&ctl->p_full, 4);
+    mbar_init(&ctl->p_full, 8);
+    for (int q = 0; q < 4; ++q)
+      for (int b = 0; b < 2; ++b) mbar_init(&ctl->xchg[q][b], 2);
     mbar_init(&ctl->o_done, 1);
     mbar_init(&ctl->drain, 1);
     fence_barrier_init();
@@ -459,7 +570,8 @@ fo_status attn_run(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K, const fo_mat* 
   } else {
     std::memset(&o, 0, sizeof(o));
   }
-  if (o.order != FO_ORDER_FLASH) return host_fail(FO_ERR_UNSUPPORTED, "attention runs the ring order only");
+  if (o.order != FO_ORDER_FLASH && o.order != FO_ORDER_SERIAL)
+    return host_fail(FO_ERR_UNSUPPORTED, "attention runs the ring order or the serial baseline");
   if (head_dim != kHd) return host_fail(FO_ERR_UNSUPPORTED, "head_dim must be 128");
   if (heads < 1) return host_fail(FO_ERR_INVALID_ARG, "heads must be positive");
   const int64_t m = Q[0].rows, HD = static_cast<int64_t>(heads) * kHd;
@@ -526,9 +638,15 @@ fo_status attn_run(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K, const fo_mat* 
     if (cudaGetLastError() != cudaSuccess) return host_fail(FO_ERR_CUDA, "transpose launch failed");
   }
   // 2) the attention kernel, then 3) the K/V ring on the link streams, concurrently
+  //    (serial baseline: the whole ring first, then the kernel without flag waits)
+  const bool serial = o.order == FO_ORDER_SERIAL;
+  p.wait_flags = serial ? 0 : 1;
+  if (serial) host_phase_record(ctx, 0, stream);
   if ((st = host_fork(ctx, P, stream)) != FO_OK) return st;
-  attn_kernel<<<host_grid(ctx, o, p.total_items), kAttnThreads, kAttnSmem, stream>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return host_fail(FO_ERR_CUDA, "attention kernel launch failed");
+  if (!serial) {
+    attn_kernel<<<host_grid(ctx, o, p.total_items), kAttnThreads, kAttnSmem, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return host_fail(FO_ERR_CUDA, "attention kernel launch failed");
+  }
   const bool prune = o.causal_prune && causal;
   for (int t = 1; t < P; ++t) {
     for (int r = 0; r < P; ++r) {
@@ -548,7 +666,15 @@ fo_status attn_run(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K, const fo_mat* 
       if (cudaEventRecord(host_ev_hop(ctx, r, t), ls) != cudaSuccess) return host_fail(FO_ERR_CUDA, "event failed");
     }
   }
-  return host_join(ctx, P, stream);
+  if ((st = host_join(ctx, P, stream)) != FO_OK) return st;
+  if (serial) {
+    host_phase_record(ctx, 1, stream);
+    attn_kernel<<<host_grid(ctx, o, p.total_items), kAttnThreads, kAttnSmem, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return host_fail(FO_ERR_CUDA, "attention kernel launch failed");
+    host_phase_record(ctx, 2, stream);
+    host_phase_done(ctx, false);
+  }
+  return FO_OK;
 }
 
 }  // namespace fo

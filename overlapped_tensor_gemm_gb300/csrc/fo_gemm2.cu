@@ -1,0 +1,299 @@
+// Persistent GEMM on SM pairs (tcgen05 cta_group::2): the same ring schedules
+// and epilogues as fo_gemm.cu, with 256x256 tiles computed by a cluster of two
+// CTAs.  Each CTA stages its own 128 rows of A and one half (128 rows) of B per
+// 64-wide K step, so an SM receives 32 KiB per step instead of 48 KiB for the
+// same work per SM, and six stages fit in shared memory instead of four.
+//
+// Pair roles: the CTA of rank 0 in the cluster (the leader) owns the "full"
+// barriers of the operand ring (its producer posts the expected bytes of both
+// CTAs; both CTAs' TMA loads complete on it) and issues the pair MMAs; every
+// MMA commit is multicast to the "empty" barriers of both CTAs.  Each CTA's
+// TMEM holds its 128 rows of the 256x256 fp32 accumulator (two buffers), its
+// epilogue warps read them and report to the leader's "tmem empty" barrier.
+#include <cuda_bf16.h>
+
+#include "fo_gemm_common.cuh"
+#include "fo_internal.h"
+#include "fo_ptx.cuh"
+
+namespace fo {
+namespace {
+
+constexpr int kPairStages = 6;
+constexpr uint32_t kPA = 128 * kBK * 2;      // 16 KiB: this CTA's 128 rows of A
+constexpr uint32_t kPB = 128 * kBK * 2;      // 16 KiB: this CTA's half of B
+constexpr uint32_t kPStage = kPA + kPB;
+constexpr uint32_t kPTmemCols = 2 * kBN;     // two 128x256 accumulators per CTA
+constexpr uint32_t kPIdesc = umma_idesc_bf16(2 * kBM, kBN);  // M = 256 over the pair, N = 256
+constexpr uint64_t kPDrainNs = 200ull * 1000 * 1000;
+
+struct alignas(8) PairCtl {
+  uint64_t full[kPairStages];   // leader: both CTAs' operands of the stage have landed
+  uint64_t empty[kPairStages];  // each CTA: the pair MMAs reading the stage are done
+  uint64_t tmem_full[2];        // each CTA: accumulator complete
+  uint64_t tmem_empty[2];       // leader: both CTAs' epilogues have read the accumulator
+  uint64_t drain;
+  uint32_t tmem_base;
+  uint32_t pad;
+};
+
+constexpr int kPairSmem = kPairStages * kPStage + 1024 + static_cast<int>(sizeof(PairCtl));
+
+__device__ void pair_producer(const GemmParams& p, uint8_t* tiles, PairCtl* ctl, uint32_t cta) {
+  const uint32_t leader_full = map_to_cta(smem_u32(&ctl->full[0]), 0);
+  const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+  int stage = 0;
+  uint32_t phase = 0, armed = 0, armed_phase = 0;
+  int waited_unit = -1;
+  bool ok = true;
+  for (int tile = cluster; ok && tile < p.total_tiles; tile += nclusters) {
+    const TileCoord tc = decode_tile(p, tile);
+    const GemmUnit& u = p.units[tc.unit];
+    if (u.wait_flag >= 0 && tc.unit != waited_unit) {
+      ok = flag_wait(p.flags + u.wait_flag, p.epoch, p.ctrl, p.timeout_ns, kSiteAgFlag,
+                     static_cast<uint32_t>(u.wait_flag));
+      if (!ok) break;
+      fence_proxy_async_global();
+      waited_unit = tc.unit;
+    }
+    const int nk = (u.k + kBK - 1) / kBK;
+    const int a_row = u.a_row0 + tc.mb * 2 * kBM + static_cast<int>(cta) * kBM;
+    // B rows of this CTA: gated tiles put the gate rows in the leader and the up rows in the peer
+    const int b_row = u.gated ? (cta == 0 ? u.b_row0 : u.b_row1) + tc.nb * (kBN / 2)
+                              : u.b_row0 + tc.nb * kBN + static_cast<int>(cta) * (kBN / 2);
+    for (int kb = 0; kb < nk; ++kb) {
+      if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty,
+                     static_cast<uint32_t>(tile))) {
+        ok = false;
+        break;
+      }
+      uint8_t* a = tiles + stage * kPStage;
+      uint8_t* b = a + kPA;
+      if (cta == 0) mbar_arrive_expect_tx(&ctl->full[stage], 2 * kPStage);
+      const uint32_t bar = leader_full + stage * static_cast<uint32_t>(sizeof(uint64_t));
+      tma_load_2d_pair(&p.maps[u.a_map], a, bar, kb * kBK, a_row);
+      tma_load_2d_pair(&p.maps[u.b_map], b, bar, kb * kBK, b_row);
+      armed |= 1u << stage;
+      armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+      if (++stage == kPairStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+  if (!ok) {
+    if (cta == 0) {
+      for (int s = 0; s < kPairStages; ++s)
+        if ((armed >> s) & 1u) mbar_wait_drain(&ctl->full[s], (armed_phase >> s) & 1u, kPDrainNs);
+    } else {
+      // this CTA's loads complete on the leader's barriers: give them time to land
+      const uint64_t t0 = global_timer_ns();
+      while (global_timer_ns() - t0 < 50000ull) __nanosleep(1000);
+    }
+  }
+}
+
+__device__ void pair_mma(const GemmParams& p, uint8_t* tiles, PairCtl* ctl, uint32_t tmem_base) {
+  const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+  int stage = 0, acc = 0;
+  uint32_t phase = 0, acc_phase = 0;
+  bool issued = false, ok = true;
+  const uint32_t tiles_addr = smem_u32(tiles);
+  for (int tile = cluster; ok && tile < p.total_tiles; tile += nclusters) {
+    const TileCoord tc = decode_tile(p, tile);
+    const GemmUnit& u = p.units[tc.unit];
+    if (!mbar_wait(&ctl->tmem_empty[acc], acc_phase ^ 1u, p.ctrl, p.timeout_ns, kSiteTmemEmpty,
+                   static_cast<uint32_t>(tile))) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+    const int nk = (u.k + kBK - 1) / kBK;
+    for (int kb = 0; kb < nk; ++kb) {
+      if (!mbar_wait(&ctl->full[stage], phase, p.ctrl, p.timeout_ns, kSiteFull, static_cast<uint32_t>(tile))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t a_addr = tiles_addr + stage * kPStage;
+      const uint32_t b_addr = a_addr + kPA;
+#pragma unroll
+      for (int k = 0; k < kBK / 16; ++k) {
+        umma_bf16_pair(d_tmem, umma_sdesc_sw128(a_addr + k * 32), umma_sdesc_sw128(b_addr + k * 32), kPIdesc,
+                       (kb | k) != 0 ? 1u : 0u);
+      }
+      issued = true;
+      umma_commit_pair_mc(&ctl->empty[stage], 0x3);  // frees the stage in both CTAs
+      if (++stage == kPairStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok) break;
+    umma_commit_pair_mc(&ctl->tmem_full[acc], 0x3);
+    acc ^= 1;
+    if (acc == 0) acc_phase ^= 1u;
+  }
+  if (!ok && issued) {
+    umma_commit_pair(&ctl->drain);
+    mbar_wait_drain(&ctl->drain, 0, kPDrainNs);
+  }
+}
+
+__device__ void pair_epilogue(const GemmParams& p, PairCtl* ctl, uint32_t tmem_base, uint32_t cta, int warp,
+                              int lane) {
+  const int q = warp & 3;
+  const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+  const uint32_t leader_tmem_empty = map_to_cta(smem_u32(&ctl->tmem_empty[0]), 0);
+  int acc = 0;
+  uint32_t acc_phase = 0;
+  for (int tile = cluster; tile < p.total_tiles; tile += nclusters) {
+    const TileCoord tc = decode_tile(p, tile);
+    const GemmUnit& u = p.units[tc.unit];
+    if (!warp_mbar_wait(&ctl->tmem_full[acc], acc_phase, p, kSiteTmemFull, static_cast<uint32_t>(tile), lane))
+      return;
+    tc_fence_after();
+    // flags per (tile, CTA half, lane quadrant): the same rows on both sides of a hop
+    const int flag_slot = ((tc.mb * u.tiles_n + tc.nb) * 2 + static_cast<int>(cta)) * 4 + q;
+    if (u.in_flag_base >= 0) {
+      const int f = u.in_flag_base + flag_slot;
+      if (!warp_flag_wait(p.flags + f, p, kSiteAccInFlag, static_cast<uint32_t>(f), lane)) return;
+    }
+    const int row = tc.mb * 2 * kBM + static_cast<int>(cta) * kBM + q * 32 + lane;
+    const bool row_ok = row < u.m_rows;
+    const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
+    if (u.epi == kEpiSiluMul) {
+#pragma unroll 1
+      for (int c = 0; c < kBN / 64; ++c) {
+        uint32_t g[32], v[32];
+        tmem_ld32(tbase + c * 32, g);
+        tmem_ld32(tbase + kBN / 2 + c * 32, v);
+        tmem_wait_ld();
+        const int col = tc.nb * (kBN / 2) + c * 32;
+        if (row_ok && col < u.n_cols) store_silu_chunk(u, row, col, g, v);
+      }
+    } else {
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tbase + c * 32, v);
+        tmem_wait_ld();
+        const int col = tc.nb * kBN + c * 32;
+        if (row_ok && col < u.n_cols) store_chunk(u, row, col, v);
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      if (cta == 0) {
+        mbar_arrive(&ctl->tmem_empty[acc]);
+      } else {
+        mbar_arrive_cluster(leader_tmem_empty + acc * static_cast<uint32_t>(sizeof(uint64_t)));
+      }
+    }
+    if (u.out_flag_base >= 0) {
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) st_release_gpu(p.flags + u.out_flag_base + flag_slot, p.epoch);
+    }
+    acc ^= 1;
+    if (acc == 0) acc_phase ^= 1u;
+  }
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_pair_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t base = smem_u32(smem_raw);
+  uint8_t* tiles = smem_raw + ((1024u - (base & 1023u)) & 1023u);
+  PairCtl* ctl = reinterpret_cast<PairCtl*>(tiles + kPairStages * kPStage);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t cta = cluster_ctarank();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&ctl->tmem_full[b], 1);
+      mbar_init(&ctl->tmem_empty[b], 8);  // 4 epilogue warps in each CTA of the pair
+    }
+    mbar_init(&ctl->drain, 1);
+    fence_barrier_init();
+    fence_proxy_async_shared();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < p.num_maps; ++i) tma_prefetch_desc(&p.maps[i]);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&ctl->tmem_base, kPTmemCols);  // one warp of each CTA, collectively
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();  // barriers of both CTAs initialised, TMEM allocated
+  tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) pair_producer(p, tiles, ctl, cta);
+  } else if (warp == 1) {
+    if (lane == 0 && cta == 0) pair_mma(p, tiles, ctl, tmem_base);
+    __syncwarp();
+  } else {
+    pair_epilogue(p, ctl, tmem_base, cta, warp, lane);
+  }
+
+  tc_fence_before();
+  cluster_sync_all();  // no CTA leaves while its peer may still signal its barriers
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kPTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t gemm_pair_configure() {
+  return cudaFuncSetAttribute(gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
+}
+
+// Number of SM pairs that can be resident at once (the persistent grid must not exceed it).
+int gemm_pair_max_clusters() {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = kPairSmem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+cudaError_t gemm_pair_launch(const GemmParams& p, int clusters, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = kPairSmem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel, p);
+}
+
+}  // namespace fo

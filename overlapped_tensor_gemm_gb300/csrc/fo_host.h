@@ -22,4 +22,6 @@ fo_status host_check_mat(const fo_mat& a, int32_t dtype, const char* what, int r
 fo_status host_fail(fo_status st, const char* msg);
 uint64_t host_timeout_ns(const fo_opts& o);
 int host_grid(fo_ctx* ctx, const fo_opts& o, int work);
+void host_phase_record(fo_ctx* ctx, int i, cudaStream_t s);     // serial baselines' phase events
+void host_phase_done(fo_ctx* ctx, bool gemm_first);
 }  // namespace fo

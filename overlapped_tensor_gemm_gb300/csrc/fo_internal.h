@@ -96,10 +96,13 @@ enum WaitSite : uint32_t {
   kSiteAttnBar = 9
 };
 
-// host launchers (fo_gemm.cu)
+// host launchers (fo_gemm.cu: single-SM 128x256 tiles; fo_gemm2.cu: SM-pair 256x256 tiles)
 cudaError_t gemm_configure();
 cudaError_t gemm_launch(const GemmParams& p, int grid, cudaStream_t s);
 int gemm_smem_bytes();
+cudaError_t gemm_pair_configure();
+int gemm_pair_max_clusters();
+cudaError_t gemm_pair_launch(const GemmParams& p, int clusters, cudaStream_t s);
 
 // elementwise kernels (fo_elem.cu); bf16 data is passed as raw uint16_t
 struct SiluMulArgs {

@@ -42,6 +42,24 @@ def test_gemm_integer_bit_exact(ctx, M, N, K):
     assert_bits_equal(to_bits(C), ref, f"gemm {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K", [(256, 256, 64), (512, 768, 1024), (1024, 1000, 264)])
+def test_sm_pair_tiles_match_single_sm_tiles(ctx, M, N, K):
+    """256x256 tiles on SM pairs (tcgen05 cta_group::2) give the same bits as the
+    single-SM 128x256 tiles, and both match the oracle on integer inputs."""
+    g = torch.Generator().manual_seed(M + N + K)
+    A = wl.integer_bf16(g, (M, K))
+    B = wl.integer_bf16(g, (N, K))
+    C1 = padded(M, N, torch.bfloat16)
+    C2 = padded(M, N, torch.bfloat16)
+    ctx.gemm(to_dev(A), to_dev(B), C1)                      # rows % 256 == 0: SM pairs
+    ctx.gemm(to_dev(A), to_dev(B), C2, single_sm=True)
+    torch.cuda.synchronize()
+    ctx.poll()
+    ref = ops.gemm(f64(A), f64(B))
+    assert_bits_equal(to_bits(C1), ref, "pair tiles")
+    assert_bits_equal(to_bits(C2), ref, "single-SM tiles")
+
+
 @pytest.mark.parametrize("M,N,K", [(200, 300, 136), (1, 8, 8), (129, 257, 72), (64, 1000, 200)])
 def test_gemm_ragged_integer(ctx, M, N, K):
     C, ref = _run_gemm(ctx, M, N, K, integer=True, seed=1)
