@@ -36,6 +36,10 @@ sys.path.insert(0, ROOT)
 import fo_workloads as wl  # noqa: E402
 
 METRIC = "overlapped AG-GEMM/GEMM-RS TFLOP/s, % of bf16 tensor peak; exposed copy time"
+# sources whose digest a committed ncu summary records (traffic is reported only while they match)
+PAIR_KERNEL_SOURCES = ("overlapped_tensor_gemm_gb300/csrc/fo_gemm2.cu",
+                       "overlapped_tensor_gemm_gb300/csrc/fo_gemm_common.cuh",
+                       "overlapped_tensor_gemm_gb300/csrc/fo_ptx.cuh")
 
 
 def parse():
@@ -45,7 +49,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama8b")
-    ap.add_argument("--no-extras", action="store_true", help="skip baselines, attention and e2e")
+    ap.add_argument("--no-extras", action="store_true", help="skip baselines, attention, e2e and the CPU leg")
+    ap.add_argument("--no-attn", action="store_true", help="skip the attention sub-benchmark")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     ap.add_argument("--attn-order", default="flash", choices=["flash", "serial"],
                     help="order of the attention workload's main timing ('serial' for ncu, as --ag-order)")
@@ -65,14 +71,22 @@ def peaks():
     return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
-def profiled_traffic(profile: str, source: str):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel source is unchanged."""
+def source_digest(sources) -> str:
     import hashlib
+    h = hashlib.sha256()
+    for src in sources:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(profile: str, sources):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel sources are unchanged."""
     import re
     try:
         text = open(os.path.join(ROOT, "profiles", profile)).read()
         want = re.search(r"sha256 prefix `([0-9a-f]+)`", text).group(1)
-        have = hashlib.sha256(open(os.path.join(ROOT, source), "rb").read()).hexdigest()[:len(want)]
+        have = source_digest(sources)[:len(want)]
         if have != want:
             return None
         return int(re.search(r"traffic_bytes_per_launch: (\d+)", text).group(1))
@@ -299,13 +313,14 @@ def run_ours(args, rank: int, world: int, device: int):
     t_ag = timed(lambda: ctx.ag_gemm(X, Wc, H, order=args.ag_order, epilogue=epi), iters)
     t_rs = timed(lambda: ctx.gemm_rs(H, Wr, Z), iters)
     ag_tflops = flops["ag"] / (t_ag * 1e-3) / 1e12
-    out["roofline"] = {"bound": "tensor", "kernel": f"gemm_kernel (Flash-AG launch, {epi} epilogue)",
+    pair = cfg.m % 256 == 0  # 256-row tiles on SM pairs when every slice is a multiple of 256 rows
+    out["roofline"] = {"bound": "tensor",
+                       "kernel": f"{'gemm_pair_kernel' if pair else 'gemm_kernel'} (Flash-AG launch, {epi} epilogue)",
                        "achieved": round(ag_tflops, 2),
                        "peak": pk["bf16_burst"], "unit": "TFLOP/s", "frac": round(ag_tflops / pk["bf16_burst"], 4),
                        "peak_kind": f"bf16 burst ({pk['source']})",
-                       "traffic": (profiled_traffic("gemm_kernel_llama8b_mlp.md",
-                                                    "overlapped_tensor_gemm_gb300/csrc/fo_gemm.cu")
-                                   if cfg.name == "llama8b" else None),
+                       "traffic": (profiled_traffic("gemm_pair_kernel_llama8b_mlp.md", PAIR_KERNEL_SOURCES)
+                                   if cfg.name == "llama8b" and pair else None),
                        "traffic_unit": "bytes per launch (dram read + write, ncu)"}
     breakdown = {"ag_flash_ms": round(t_ag, 4), "rs_flash_ms": round(t_rs, 4),
                  "ag_tflops": round(ag_tflops, 2), "rs_tflops": round(flops["rs"] / (t_rs * 1e-3) / 1e12, 2)}
@@ -355,11 +370,12 @@ def run_ours(args, rank: int, world: int, device: int):
                       "ms_per_step": round(t_e2e, 4), "h2d_bytes_per_step": nbytes,
                       "d2h_bytes_per_step": sum(z.numel() * 2 for z in Zh)}
         # ---- query-split attention (config 5) -------------------------------
-        out["attention"] = attention_bench(ctx, pk, max(3, args.steps // 4))
+        if not args.no_attn:
+            out["attention"] = attention_bench(ctx, pk, max(3, args.steps // 4))
     out["breakdown"] = breakdown
     ctx.close()
 
-    if rank == 0 and not args.no_extras:
+    if rank == 0 and not args.no_extras and not args.no_cpu:
         inp_f64 = decode_inputs(inp)
         rows = calibrate_rows(cfg, inp_f64, args.cpu_seconds)
         dt, fl = oracle_mlp_sample(cfg, inp_f64, rows, 1)
@@ -397,6 +413,19 @@ def attention_bench(ctx, pk, iters: int, order: str = "flash", baselines: bool =
 
     ms = timed(order)
     tf = c.flops() / (ms * 1e-3) / 1e12
+    pruned_ms = None
+    if baselines:
+        for _ in range(2):
+            ctx.qsplit_attn(Q, K, V, O, heads=c.heads, head_dim=c.head_dim, causal_prune=True)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(iters):
+            ctx.qsplit_attn(Q, K, V, O, heads=c.heads, head_dim=c.head_dim, causal_prune=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ctx.poll()
+        pruned_ms = a.elapsed_time(b) / iters
     out = {"workload": f"query-split causal attention, P={c.P}, seq {c.seq}, {c.heads} heads, head_dim "
                        f"{c.head_dim}", "order": order, "ms": round(ms, 4), "tflops": round(tf, 2),
            "frac_of_bf16_peak": round(tf / pk["bf16_burst"], 4), "flop": c.flops(),
@@ -406,7 +435,8 @@ def attention_bench(ctx, pk, iters: int, order: str = "flash", baselines: bool =
         ctx.qsplit_attn(Q, K, V, O, heads=c.heads, head_dim=c.head_dim, order="serial")
         torch.cuda.synchronize()
         ring_ms, kernel_ms = ctx.phase_ms()
-        out.update({"serial_ms": round(t_serial, 4), "serial_phases_ms": {"ring": round(ring_ms, 4),
+        out.update({"pruned_ring_ms": round(pruned_ms, 4),
+                    "serial_ms": round(t_serial, 4), "serial_phases_ms": {"ring": round(ring_ms, 4),
                                                                            "kernel": round(kernel_ms, 4)},
                     "exposed_copy_ms": round(ms - kernel_ms, 4),
                     "exposed_frac": round((ms - kernel_ms) / ms, 4)})
