@@ -334,6 +334,31 @@ __device__ __forceinline__ float poly_exp2(float x) {
   return __int_as_float(__float_as_int(p) + (static_cast<int>(fi) << 23));
 }
 
+// Packed fp32 pairs (sm_100-family f32x2 instructions): two scores per instruction.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t x, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -379,28 +404,29 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
         const uint32_t sb = gj & 1u;
         if (!warp_wait(&ctl->s_full[sb], (gj >> 1) & 1u, p, kSiteTmemFull, i, lane)) return;
         tc_fence_after();
-        float s[64];
+        float s[64];  // raw scores of this warp's 64 keys (scale applied in the exponent)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
           tmem_ld32(lane_base + sb * 128 + col0 + c * 32, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < 32; ++k) s[c * 32 + k] = __uint_as_float(v[k]) * p.scale_log2;
+          for (int k = 0; k < 32; ++k) s[c * 32 + k] = __uint_as_float(v[k]);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->s_empty[sb]);
-        const bool diag = p.causal && t == 0 && kb == it.qb;
+        if (p.causal && t == 0 && kb == it.qb) {  // diagonal block: key j > query i is masked
+#pragma unroll
+          for (int k = 0; k < 64; ++k)
+            if (static_cast<int>(col0) + k > row) s[k] = -INFINITY;
+        }
         float mx = -INFINITY;
 #pragma unroll
-        for (int k = 0; k < 64; ++k) {
-          if (diag && static_cast<int>(col0) + k > row) s[k] = -INFINITY;
-          mx = fmaxf(mx, s[k]);
-        }
+        for (int k = 0; k < 32; ++k) mx = fmax3(mx, s[2 * k], s[2 * k + 1]);
         float other;
         if (!exchange(ctl, xch, xuses, q, hf, row, mx, &other, p, lane, i)) return;
-        mx = fmaxf(mx, other);  // the row's block maximum (finite: the diagonal key is never masked)
+        mx = fmaxf(mx, other) * p.scale_log2;  // the row's block maximum, log2 units (finite)
         float alpha = 1.f;
         bool rescale = false;
         if (j == 0) {
@@ -411,19 +437,26 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
           l *= alpha;
           rescale = true;
         }
-        // the row sum uses the fp16-rounded weights that the P.V product sees
-        float sum = 0.f;
+        // p = 2^(s * scale - m_ref): one packed FMA per pair, ex2 per weight, packed sums
+        const uint64_t c2 = pack2(p.scale_log2, p.scale_log2);
+        const uint64_t nm2 = pack2(-m_ref, -m_ref);
+        uint64_t sum2 = pack2(0.f, 0.f);
         uint32_t packed[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          // every kPolyEvery-th pair of weights is computed on the FMA pipe, the rest on MUFU
+          float x0, x1;
+          unpack2(ffma2(pack2(s[2 * k], s[2 * k + 1]), c2, nm2), x0, x1);
           const bool poly = kPolyEvery > 0 && (k % kPolyEvery) == kPolyEvery - 1;
-          packed[k] = poly ? pack_f16x2(poly_exp2(s[2 * k] - m_ref), poly_exp2(s[2 * k + 1] - m_ref))
-                           : pack_f16x2(fast_exp2(s[2 * k] - m_ref), fast_exp2(s[2 * k + 1] - m_ref));
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&packed[k]));
-          sum += f.x + f.y;
+          const float e0 = poly ? poly_exp2(x0) : fast_exp2(x0);
+          const float e1 = poly ? poly_exp2(x1) : fast_exp2(x1);
+          sum2 = fadd2(sum2, pack2(e0, e1));
+          packed[k] = pack_f16x2(e0, e1);
         }
-        l += sum;
+        {
+          float s0, s1;
+          unpack2(sum2, s0, s1);
+          l += s0 + s1;
+        }
         if (j > 0) {
           // the previous P.V must be complete before P is overwritten or O rescaled
           if (!warp_wait(&ctl->o_done, (gj - 1) & 1u, p, kSiteDrain, i, lane)) return;
