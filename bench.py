@@ -57,7 +57,7 @@ def parse():
                     help="order of the attention workload's main timing ('serial' for ncu, as --ag-order)")
     ap.add_argument("--ag-order", default="flash", choices=["flash", "serial"],
                     help="order of the AG projection; 'serial' (ring first, same GEMM kernel after) is what "
-                         "runs under ncu, which serialises copy-engine work against kernels")
+                         "runs under ncu, which serialises the ring copies against kernels")
     return ap.parse_args()
 
 

@@ -12,7 +12,8 @@
  *
  * Here all P "ranks" live on ONE GPU: rank r is a set of caller buffers plus a
  * disjoint arena of the context's workspace, and a ring hop is a device-local
- * copy (copy engine) or an epilogue store into the successor's arena, signalled
+ * copy (cudaMemcpyAsync on a link stream) or an epilogue store into the
+ * successor's arena, signalled
  * through per-slice / per-tile flags in device memory.
  *
  * Conventions for every entry point
@@ -80,7 +81,7 @@ typedef enum {
 
 typedef enum {
   FO_LINK_DEFAULT = 0, /* all-gather: FO_LINK_CE; fused reduce-scatter: FO_LINK_PUSH      */
-  FO_LINK_CE = 1,      /* hop = copy-engine copy on a per-rank link stream               */
+  FO_LINK_CE = 1,      /* hop = device-to-device cudaMemcpyAsync on a per-rank link stream */
   FO_LINK_PUSH = 2     /* RS only: the epilogue stores the partial sum straight into the
                           successor's receive slot and releases a per-tile flag          */
 } fo_link;
@@ -101,7 +102,7 @@ typedef enum {
 
 typedef struct {
   int32_t order;        /* fo_order                                                   */
-  int32_t link;         /* fo_link; all-gather hops are always copy-engine copies      */
+  int32_t link;         /* fo_link; all-gather hops are always cudaMemcpyAsync copies   */
   int32_t n_slices;     /* FO_ORDER_SLICING: number of slices (0 = P)                 */
   uint32_t timeout_us;  /* limit of every device-side wait (0 = 1 second)             */
   int32_t causal_prune; /* attention: forward a K/V slice only to ranks that use it   */

@@ -1,5 +1,5 @@
 // Host side of the Flash-Overlap library: context and workspace, argument
-// validation, the ring step engine (per-rank link streams, copy-engine hops,
+// validation, the ring step engine (per-rank link streams, device-to-device copies,
 // stream memory operations that publish per-slice flags), the step schedules
 // of Flash-AG / Flash-RS and of the two baselines, and the C ABI of fo.h.
 //
@@ -651,7 +651,7 @@ fo_status rs_flash(fo_ctx* ctx, const RsArgs& a, const fo_opts& o, cudaStream_t 
   return launch_gemm(ctx, L, o, stream);
 }
 
-// Baselines: partial GEMMs into `part`, then a ring reduce with copy-engine hops
+// Baselines: partial GEMMs into `part`, then a ring reduce with device-to-device hops
 // and fp32 add kernels.  Rows [row0, row0 + rows) of every chunk.
 fo_status rs_partials(fo_ctx* ctx, const RsArgs& a, const fo_opts& o, cudaStream_t stream, int64_t row0,
                       int64_t rows, uint32_t* flags, uint32_t epoch) {

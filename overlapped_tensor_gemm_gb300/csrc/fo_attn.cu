@@ -3,7 +3,7 @@
 // with sequence length).
 //
 // Rank r keeps its query slice; K and V slices travel the ring local-first,
-// like Flash-AG slices, as copy-engine hops that publish a per-(rank, slice)
+// like Flash-AG slices, as device-to-device copies that publish a per-(rank, slice)
 // arrival flag.  One persistent kernel processes work items (rank r, 128-query
 // block qb, head h).  An item walks the ring steps t = 0, 1, ... (slice
 // s = (r - t) mod P: its own slice first), skips slices that lie wholly above
@@ -58,7 +58,7 @@ constexpr uint32_t kIdescS = umma_idesc_bf16(128, 128);   // S = Q K^T, bf16 ope
 constexpr uint32_t kIdescO = umma_idesc_f16(128, 128);    // O += P V, fp16 operands
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr int kPolyEvery = 0;              // 0: every softmax weight through MUFU ex2
+constexpr int kPolyEvery = 0;              // 0: every weight on MUFU ex2 (the cubic measured slower: issue-bound)
 
 struct AttnParams {
   CUtensorMap maps[4 * kMaxP];  // per rank r: Q = r, K local = P+r, K received = 2P+r, V^T = 3P+r
@@ -95,6 +95,13 @@ constexpr uint32_t kOffP = kOffV + kVStages * kTileBytes;
 constexpr uint32_t kOffXch = kOffP + kTileBytes;             // float [2 slots][2 halves][128 rows]
 constexpr uint32_t kOffCtl = kOffXch + 2 * 2 * 128 * 4;
 constexpr int kAttnSmem = static_cast<int>(kOffCtl + sizeof(AttnCtl) + 1024);
+// Every persistent kernel of this library leaves shared memory and registers of
+// its SM free: the ring's device-to-device copies may run as a small copy kernel
+// that must be able to start while the persistent grid occupies every SM.  The
+// register share of one SM sub-partition (16K) holds up to three of this
+// kernel's ten warps; the kernel is therefore kept at <= 136 registers per thread
+// (3 warps x 32 x 136 = 13056, leaving 3328), checked at context set-up.
+static_assert(kAttnSmem <= 232448 - 24 * 1024, "attention kernel must leave 24 KiB of shared memory free");
 
 struct Item {
   int r, qb, h;
@@ -513,7 +520,7 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
   }
 }
 
-__global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __maxnreg__(136) attn_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (base & 1023u)) & 1023u);
@@ -633,9 +640,18 @@ fo_status attn_run(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K, const fo_mat* 
   auto vt_slot = [&](int r, int s) { return vtb + (static_cast<int64_t>(r) * P + s) * HD * m * 2; };
 
   static bool configured = false;
+  static int reserve_sms = 0;
   if (!configured) {
     if (cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem) != cudaSuccess)
       return host_fail(FO_ERR_CUDA, "attention kernel configuration failed");
+    // Register headroom per SM sub-partition (16K registers, up to 3 of the 10 warps):
+    // if the build ever exceeds it, leave SMs free for the ring's copies instead.
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, attn_kernel) != cudaSuccess)
+      return host_fail(FO_ERR_CUDA, "attention kernel attributes unavailable");
+    const int regs = (fa.numRegs + 7) / 8 * 8;
+    const int warps_per_quarter = (kAttnThreads / 32 + 3) / 4;
+    reserve_sms = warps_per_quarter * 32 * regs > 16384 - 3072 ? 8 : 0;
     configured = true;
   }
   AttnParams p;
@@ -673,12 +689,15 @@ fo_status attn_run(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K, const fo_mat* 
   // 2) the attention kernel, then 3) the K/V ring on the link streams, concurrently
   //    (serial baseline: the whole ring first, then the kernel without flag waits)
   const bool serial = o.order == FO_ORDER_SERIAL;
+  int grid = host_grid(ctx, o, p.total_items);
+  if (!serial && reserve_sms > 0 && grid > host_num_sms(ctx) - reserve_sms) grid = host_num_sms(ctx) - reserve_sms;
   p.wait_flags = serial ? 0 : 1;
   if (serial) host_phase_record(ctx, 0, stream);
   if ((st = host_fork(ctx, P, stream)) != FO_OK) return st;
   if (!serial) {
-    attn_kernel<<<host_grid(ctx, o, p.total_items), kAttnThreads, kAttnSmem, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return host_fail(FO_ERR_CUDA, "attention kernel launch failed");
+    attn_kernel<<<grid, kAttnThreads, kAttnSmem, stream>>>(p);
+    const cudaError_t le = cudaGetLastError();
+    if (le != cudaSuccess) return host_fail(FO_ERR_CUDA, cudaGetErrorString(le));
   }
   const bool prune = o.causal_prune && causal;
   for (int t = 1; t < P; ++t) {
@@ -702,8 +721,9 @@ fo_status attn_run(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K, const fo_mat* 
   if ((st = host_join(ctx, P, stream)) != FO_OK) return st;
   if (serial) {
     host_phase_record(ctx, 1, stream);
-    attn_kernel<<<host_grid(ctx, o, p.total_items), kAttnThreads, kAttnSmem, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return host_fail(FO_ERR_CUDA, "attention kernel launch failed");
+    attn_kernel<<<grid, kAttnThreads, kAttnSmem, stream>>>(p);
+    const cudaError_t le = cudaGetLastError();
+    if (le != cudaSuccess) return host_fail(FO_ERR_CUDA, cudaGetErrorString(le));
     host_phase_record(ctx, 2, stream);
     host_phase_done(ctx, false);
   }

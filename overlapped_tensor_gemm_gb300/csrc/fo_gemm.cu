@@ -45,6 +45,9 @@ struct alignas(8) SmemCtl {
 };
 
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 + static_cast<int>(sizeof(SmemCtl));
+// The ring's device-to-device copies may run as a small copy kernel next to this
+// persistent grid: leave shared memory free on every SM.
+static_assert(kSmemBytes <= 232448 - 24 * 1024, "the persistent GEMM must leave 24 KiB of shared memory free");
 
 // ---------------------------------------------------------------------------
 // warp roles
@@ -64,7 +67,7 @@ __device__ void producer_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl)
       ok = flag_wait(p.flags + u.wait_flag, p.epoch, p.ctrl, p.timeout_ns, kSiteAgFlag,
                      static_cast<uint32_t>(u.wait_flag));
       if (!ok) break;
-      // the slice was written by the copy engine; order the TMA reads after the acquire
+      // the slice was written by a ring copy; order the TMA reads after the acquire
       fence_proxy_async_global();
       waited_unit = tc.unit;
     }

@@ -38,6 +38,9 @@ struct alignas(8) PairCtl {
 };
 
 constexpr int kPairSmem = kPairStages * kPStage + 1024 + static_cast<int>(sizeof(PairCtl));
+// The ring's device-to-device copies may run as a small copy kernel next to this
+// persistent grid: leave shared memory free on every SM.
+static_assert(kPairSmem <= 232448 - 24 * 1024, "the persistent GEMM must leave 24 KiB of shared memory free");
 
 __device__ void pair_producer(const GemmParams& p, uint8_t* tiles, PairCtl* ctl, uint32_t cta) {
   const uint32_t leader_full = map_to_cta(smem_u32(&ctl->full[0]), 0);
