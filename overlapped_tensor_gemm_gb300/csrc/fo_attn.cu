@@ -13,18 +13,18 @@
 //
 // CTA layout (320 threads, one CTA per SM):
 //   warp 0      TMA: Q block once per item, then K and V^T blocks in two
-//               rings of 2 stages each, K one block ahead of V; waits for the
-//               slice's arrival flag before reading it.
+//               stage rings, K ahead of V; waits for the slice's arrival flag
+//               before reading it.
 //   warp 1      tcgen05.mma: S = Q K^T into one of two TMEM score buffers
 //               (the next block's scores overlap this block's softmax), then
-//               O += P V into the TMEM accumulator.
+//               O += P V into the TMEM accumulator, with P read from TMEM.
 //   warps 2-9   softmax: two warps per query row (one per 64-key half); they
 //               load their half of the score row, mask the diagonal block,
-//               combine the row maximum, update max/sum, rescale their half
+//               exchange the row maximum, update max/sum, rescale their half
 //               of the O row only when the max grew by more than 2^8 (the
 //               final division by the sum uses the same reference max, so this
-//               is exact), and write P into shared memory in the MMA's operand
-//               layout.
+//               is exact), and write P as fp16 into one of two TMEM buffers, so
+//               a block's softmax does not wait for the previous block's P.V.
 // V is transposed once per rank (V^T [heads*128, tokens]) before the ring so
 // that both MMAs read K-major operands.  The P.V product runs in fp16: the
 // transpose converts V's bf16 values to fp16 (exact for |v| within fp16's
@@ -52,13 +52,13 @@ constexpr uint32_t kTileBytes = 128 * 128 * 2;   // one 128x128 bf16 operand (tw
 constexpr uint32_t kHalfBytes = kTileBytes / 2;
 constexpr int kKStages = 2;
 constexpr int kVStages = 2;
-constexpr uint32_t kTmemCols = 512;      // S0 [0,128), S1 [128,256), O [256,384)
+constexpr uint32_t kTmemCols = 512;      // S0 [0,128), S1 [128,256), O [256,384), P0 [384,448), P1 [448,512)
 constexpr uint32_t kOCol = 256;
+constexpr uint32_t kPCol = 384;          // P as packed fp16 pairs: 128 keys in 64 columns
 constexpr uint32_t kIdescS = umma_idesc_bf16(128, 128);   // S = Q K^T, bf16 operands
 constexpr uint32_t kIdescO = umma_idesc_f16(128, 128);    // O += P V, fp16 operands
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr int kPolyEvery = 0;              // 0: every weight on MUFU ex2 (the cubic measured slower: issue-bound)
 
 struct AttnParams {
   CUtensorMap maps[4 * kMaxP];  // per rank r: Q = r, K local = P+r, K received = 2P+r, V^T = 3P+r
@@ -81,18 +81,18 @@ struct alignas(8) AttnCtl {
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
   uint64_t s_full[2], s_empty[2];
-  uint64_t p_full, o_done, drain;
+  uint64_t p_full[2], pv_done[2];   // per P buffer (TMEM): written by softmax / read by the P.V MMA
+  uint64_t drain;
   uint64_t xchg[4][2];   // per lane quadrant, two slots: the column halves' partial max / sum exchange
   uint32_t tmem_base;
   uint32_t pad;
 };
 
-// Shared memory: Q | K stages | V^T stages | P | exchange | control
+// Shared memory: Q | K stages | V^T stages | exchange | control  (S, O and P live in TMEM)
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kTileBytes;
 constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
-constexpr uint32_t kOffP = kOffV + kVStages * kTileBytes;
-constexpr uint32_t kOffXch = kOffP + kTileBytes;             // float [2 slots][2 halves][128 rows]
+constexpr uint32_t kOffXch = kOffV + kVStages * kTileBytes;  // float [2 slots][2 halves][128 rows]
 constexpr uint32_t kOffCtl = kOffXch + 2 * 2 * 128 * 4;
 constexpr int kAttnSmem = static_cast<int>(kOffCtl + sizeof(AttnCtl) + 1024);
 // Every persistent kernel of this library leaves shared memory and registers of
@@ -251,18 +251,31 @@ __device__ __forceinline__ void issue_s(uint32_t tmem_s, uint32_t q_addr, uint32
   }
 }
 
-__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t p_addr, uint32_t v_addr, bool first) {
+// D (TMEM) += A (TMEM) * B (shared memory descriptor), A = [128 rows in lanes, 16 fp16
+// per 8 columns]: the form whose A operand never passes through shared memory.
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// O += P V for one 128-key block: P from TMEM (column c holds keys 2c, 2c+1), V^T
+// from the two 64-key swizzle halves of the stage.
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr, bool first) {
 #pragma unroll
   for (int k = 0; k < kKB / 16; ++k) {
     const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
-    umma_bf16_ss(tmem_o, umma_sdesc_sw128(p_addr + off), umma_sdesc_sw128(v_addr + off), kIdescO,
-                 (first && k == 0) ? 0u : 1u);
+    umma_f16_ts(tmem_o, tmem_p + k * 8, umma_sdesc_sw128(v_addr + off), kIdescO, (first && k == 0) ? 0u : 1u);
   }
 }
 
 __device__ void attn_mma(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, uint32_t tmem_base) {
   const uint32_t sbase = smem_u32(smem);
-  uint32_t q_uses = 0, p_uses = 0;
+  uint32_t q_uses = 0;
   uint32_t g = 0;  // global key-block counter of this CTA
   bool issued = false, ok = true;
   for (int i = blockIdx.x; ok && i < p.total_items; i += gridDim.x) {
@@ -298,21 +311,20 @@ __device__ void attn_mma(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, uint3
       } else {
         umma_commit(&ctl->q_empty);  // Q is free once every score MMA of this item completes
       }
-      if (!mbar_wait(&ctl->p_full, p_uses & 1u, p.ctrl, p.timeout_ns, kSiteFull, i)) {
+      const uint32_t pb = gj & 1u;  // P buffer of block gj
+      if (!mbar_wait(&ctl->p_full[pb], (gj >> 1) & 1u, p.ctrl, p.timeout_ns, kSiteFull, i)) {
         ok = false;
         break;
       }
-      ++p_uses;
-      tc_fence_after();
       const uint32_t vs = gj % kVStages;
       if (!mbar_wait(&ctl->v_full[vs], (gj / kVStages) & 1u, p.ctrl, p.timeout_ns, kSiteFull, i)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      issue_pv(tmem_base + kOCol, sbase + kOffP, sbase + kOffV + vs * kTileBytes, j == 0);
+      issue_pv(tmem_base + kOCol, tmem_base + kPCol + pb * 64, sbase + kOffV + vs * kTileBytes, j == 0);
       umma_commit(&ctl->v_empty[vs]);
-      umma_commit(&ctl->o_done);
+      umma_commit(&ctl->pv_done[pb]);
     }
     g += n;
   }
@@ -327,18 +339,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   uint32_t ok = 0;
   if (lane == 0) ok = mbar_wait(bar, parity, p.ctrl, p.timeout_ns, site, detail) ? 1u : 0u;
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
-
-// exp2 on the FMA pipe (offloads the MUFU unit): range reduction
-// x = i + f, f in [0, 1), 2^f by the least-squares cubic derived in
-// poly_exp2_fit.py (relative error < 7.8e-5), 2^i added to the exponent field.
-// Inputs below -126 return 2^-126 * p(f), which rounds to 0 in fp16.
-__device__ __forceinline__ float poly_exp2(float x) {
-  x = fmaxf(x, -126.0f);
-  const float fi = floorf(x);
-  const float f = x - fi;
-  const float p = fmaf(fmaf(fmaf(0.07790716f, f, 0.22623319f), f, 0.69577710f), f, 0.99992783f);
-  return __int_as_float(__float_as_int(p) + (static_cast<int>(fi) << 23));
 }
 
 // Packed fp32 pairs (sm_100-family f32x2 instructions): two scores per instruction.
@@ -377,12 +377,16 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // block).  The two warps of a quadrant combine their partial row maxima (and,
 // at the end, row sums) through shared memory, each exchange closed by a
 // bounded mbarrier wait.
-__device__ __forceinline__ bool exchange(AttnCtl* ctl, float* xch, uint32_t& uses, int q, int hf, int row,
-                                         float mine, float* other, const AttnParams& p, int lane, int item) {
+__device__ __forceinline__ void xch_publish(AttnCtl* ctl, float* xch, uint32_t uses, int q, int hf, int row,
+                                            float mine, int lane) {
   const uint32_t slot = uses & 1u;
   xch[(slot * 2 + hf) * 128 + row] = mine;
   __syncwarp();
   if (lane == 0) mbar_arrive(&ctl->xchg[q][slot]);
+}
+__device__ __forceinline__ bool xch_collect(AttnCtl* ctl, const float* xch, uint32_t& uses, int q, int hf, int row,
+                                            float* other, const AttnParams& p, int lane, int item) {
+  const uint32_t slot = uses & 1u;
   if (!warp_wait(&ctl->xchg[q][slot], (uses >> 1) & 1u, p, kSiteAttnBar, item, lane)) return false;
   *other = xch[(slot * 2 + (hf ^ 1)) * 128 + row];
   ++uses;
@@ -396,9 +400,9 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
   const int row = q * 32 + lane;  // query row inside the block == TMEM lane
   const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
   const uint32_t col0 = static_cast<uint32_t>(hf * 64);  // this warp's key / output columns
-  uint8_t* prow = smem + kOffP + hf * kHalfBytes + row * 128;
   float* xch = reinterpret_cast<float*>(smem + kOffXch);
   uint32_t g = 0, xuses = 0;
+  const uint64_t c2 = pack2(p.scale_log2, p.scale_log2);
   for (int i = blockIdx.x; i < p.total_items; i += gridDim.x) {
     const Item it = decode_item(p, i);
     float m_ref = -INFINITY, l = 0.f;
@@ -406,70 +410,94 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
     const int nsteps = steps_of(p, it.r);
     for (int t = 0; t < nsteps; ++t) {
       const int nb = blocks_of(p, it, t);
+      const bool diag_step = p.causal && t == 0;
       for (int kb = 0; kb < nb; ++kb, ++j) {
         const uint32_t gj = g + j;
-        const uint32_t sb = gj & 1u;
+        const uint32_t sb = gj & 1u;  // score buffer and P buffer of this block
+        const bool diag = diag_step && kb == it.qb;
         if (!warp_wait(&ctl->s_full[sb], (gj >> 1) & 1u, p, kSiteTmemFull, i, lane)) return;
         tc_fence_after();
-        float s[64];  // raw scores of this warp's 64 keys (scale applied in the exponent)
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t v[32];
-          tmem_ld32(lane_base + sb * 128 + col0 + c * 32, v);
+        // raw scores of this warp's 64 keys (scale applied in the exponent); on the
+        // diagonal block key > query is masked
+        auto load_scores = [&](float (&s)[64]) {
+          uint32_t v[2][32];
+          tmem_ld32(lane_base + sb * 128 + col0, v[0]);
+          tmem_ld32(lane_base + sb * 128 + col0 + 32, v[1]);
           tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < 32; ++k) s[c * 32 + k] = __uint_as_float(v[k]);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->s_empty[sb]);
-        if (p.causal && t == 0 && kb == it.qb) {  // diagonal block: key j > query i is masked
+          for (int c = 0; c < 2; ++c)
 #pragma unroll
-          for (int k = 0; k < 64; ++k)
-            if (static_cast<int>(col0) + k > row) s[k] = -INFINITY;
-        }
+            for (int k = 0; k < 32; ++k) s[c * 32 + k] = __uint_as_float(v[c][k]);
+          if (diag) {
+#pragma unroll
+            for (int k = 0; k < 64; ++k)
+              if (static_cast<int>(col0) + k > row) s[k] = -INFINITY;
+          }
+        };
+        // p = 2^(s * scale - m): one packed FMA per pair, ex2 per weight, packed sums
+        auto weights = [&](const float (&s)[64], float m, uint32_t (&packed)[32]) -> float {
+          const uint64_t nm2 = pack2(-m, -m);
+          uint64_t sum2 = pack2(0.f, 0.f);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            float x0, x1;
+            unpack2(ffma2(pack2(s[2 * k], s[2 * k + 1]), c2, nm2), x0, x1);
+            const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+            sum2 = fadd2(sum2, pack2(e0, e1));
+            packed[k] = pack_f16x2(e0, e1);
+          }
+          float s0, s1;
+          unpack2(sum2, s0, s1);
+          return s0 + s1;
+        };
+        float s[64];
+        load_scores(s);
         float mx = -INFINITY;
 #pragma unroll
         for (int k = 0; k < 32; ++k) mx = fmax3(mx, s[2 * k], s[2 * k + 1]);
+        // The partner warp (other key half of the same rows) needs this row maximum.  The
+        // weights are computed against the running reference while the exchange is in
+        // flight; a block whose row maximum exceeds the reference by more than the
+        // threshold recomputes them against the new reference (rare: lazy rescaling).
+        xch_publish(ctl, xch, xuses, q, hf, row, mx, lane);
         float other;
-        if (!exchange(ctl, xch, xuses, q, hf, row, mx, &other, p, lane, i)) return;
-        mx = fmaxf(mx, other) * p.scale_log2;  // the row's block maximum, log2 units (finite)
-        float alpha = 1.f;
-        bool rescale = false;
-        if (j == 0) {
-          m_ref = mx;
-        } else if (mx > m_ref + kRescaleThreshold) {
-          alpha = fast_exp2(m_ref - mx);
-          m_ref = mx;
-          l *= alpha;
-          rescale = true;
-        }
-        // p = 2^(s * scale - m_ref): one packed FMA per pair, ex2 per weight, packed sums
-        const uint64_t c2 = pack2(p.scale_log2, p.scale_log2);
-        const uint64_t nm2 = pack2(-m_ref, -m_ref);
-        uint64_t sum2 = pack2(0.f, 0.f);
         uint32_t packed[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          float x0, x1;
-          unpack2(ffma2(pack2(s[2 * k], s[2 * k + 1]), c2, nm2), x0, x1);
-          const bool poly = kPolyEvery > 0 && (k % kPolyEvery) == kPolyEvery - 1;
-          const float e0 = poly ? poly_exp2(x0) : fast_exp2(x0);
-          const float e1 = poly ? poly_exp2(x1) : fast_exp2(x1);
-          sum2 = fadd2(sum2, pack2(e0, e1));
-          packed[k] = pack_f16x2(e0, e1);
+        float bsum = 0.f;
+        bool rescale = false;
+        float alpha = 1.f;
+        if (j == 0) {
+          if (!xch_collect(ctl, xch, xuses, q, hf, row, &other, p, lane, i)) return;
+          m_ref = fmaxf(mx, other) * p.scale_log2;  // block 0 holds key 0 <= every query: finite
+          bsum = weights(s, m_ref, packed);
+        } else {
+          bsum = weights(s, m_ref, packed);
+          if (!xch_collect(ctl, xch, xuses, q, hf, row, &other, p, lane, i)) return;
+          const float bm = fmaxf(mx, other) * p.scale_log2;
+          if (bm > m_ref + kRescaleThreshold) {
+            alpha = fast_exp2(m_ref - bm);
+            m_ref = bm;
+            l *= alpha;
+            rescale = true;
+          }
+          if (__any_sync(0xffffffffu, rescale)) {
+            load_scores(s);  // the score buffer is still held
+            bsum = weights(s, m_ref, packed);
+          }
         }
-        {
-          float s0, s1;
-          unpack2(sum2, s0, s1);
-          l += s0 + s1;
-        }
-        if (j > 0) {
-          // the previous P.V must be complete before P is overwritten or O rescaled
-          if (!warp_wait(&ctl->o_done, (gj - 1) & 1u, p, kSiteDrain, i, lane)) return;
+        l += bsum;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->s_empty[sb]);
+        // P buffer sb was last read by the P.V of block gj - 2
+        if (gj >= 2) {
+          if (!warp_wait(&ctl->pv_done[sb], ((gj >> 1) & 1u) ^ 1u, p, kSiteDrain, i, lane)) return;
           tc_fence_after();
         }
         if (__any_sync(0xffffffffu, rescale)) {
+          // O must hold every earlier block (P.V of block gj - 1 complete) before it is rescaled
+          const uint32_t pb = (gj - 1) & 1u;
+          if (!warp_wait(&ctl->pv_done[pb], ((gj - 1) >> 1) & 1u, p, kSiteDrain, i, lane)) return;
+          tc_fence_after();
 #pragma unroll 1
           for (int c = 0; c < 2; ++c) {
             uint32_t v[32];
@@ -479,25 +507,20 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
             for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
             tmem_st32(lane_base + kOCol + col0 + c * 32, v);
           }
-          tmem_wait_st();
         }
-        // this half of the P row: one 128-byte-swizzled half tile, 16-byte chunks
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint4* dst = reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4));
-          *dst = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
-        }
-        fence_proxy_async_shared();
+        tmem_st32(lane_base + kPCol + sb * 64 + col0 / 2, packed);
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->p_full);
+        if (lane == 0) mbar_arrive(&ctl->p_full[sb]);
       }
     }
     // epilogue: row sum of both halves, O row / l -> bf16 (this warp's 64 columns)
     float other_l;
-    if (!exchange(ctl, xch, xuses, q, hf, row, l, &other_l, p, lane, i)) return;
+    xch_publish(ctl, xch, xuses, q, hf, row, l, lane);
+    if (!xch_collect(ctl, xch, xuses, q, hf, row, &other_l, p, lane, i)) return;
     const uint32_t glast = g + j - 1;
-    if (!warp_wait(&ctl->o_done, glast & 1u, p, kSiteDrain, i, lane)) return;
+    if (!warp_wait(&ctl->pv_done[glast & 1u], (glast >> 1) & 1u, p, kSiteDrain, i, lane)) return;
     tc_fence_after();
     const float inv = 1.f / (l + other_l);
     uint16_t* orow = p.out[it.r] + static_cast<int64_t>(it.qb * kQB + row) * p.ld_out[it.r] + it.h * kHd + col0;
@@ -540,11 +563,11 @@ __global__ void __maxnreg__(136) attn_kernel(const __grid_constant__ AttnParams 
     for (int b = 0; b < 2; ++b) {
       mbar_init(&ctl->s_full[b], 1);
       mbar_init(&ctl->s_empty[b], 8);
+      mbar_init(&ctl->p_full[b], 8);
+      mbar_init(&ctl->pv_done[b], 1);
     }
-    mbar_init(&ctl->p_full, 8);
     for (int q = 0; q < 4; ++q)
       for (int b = 0; b < 2; ++b) mbar_init(&ctl->xchg[q][b], 2);
-    mbar_init(&ctl->o_done, 1);
     mbar_init(&ctl->drain, 1);
     fence_barrier_init();
     fence_proxy_async_shared();

@@ -32,7 +32,7 @@ def _attn(ctx, P, m, H, seed, causal=True, **kw):
     return inp, got
 
 
-@pytest.mark.parametrize("P,m,H", [(1, 128, 1), (2, 128, 2), (4, 256, 3), (3, 384, 2)])
+@pytest.mark.parametrize("P,m,H", [(1, 128, 1), (2, 128, 2), (4, 256, 3), (3, 384, 2), (2, 768, 2), (1, 512, 1)])
 def test_attention_matches_definition(ctx, P, m, H):
     inp, got = _attn(ctx, P, m, H, 300 + P)
     ref = ops.attention_definition(np.concatenate([f64(x) for x in inp["Q"]]),
@@ -41,8 +41,9 @@ def test_attention_matches_definition(ctx, P, m, H):
     assert_close(np.concatenate(got), ref, f"attention P={P}")
 
 
-def test_attention_matches_ring_simulation_pruned(ctx):
-    P, m, H = 4, 128, 2
+@pytest.mark.parametrize("m", [128, 256])
+def test_attention_matches_ring_simulation_pruned(ctx, m):
+    P, H = 4, 2
     inp, got = _attn(ctx, P, m, H, 41, causal_prune=True)
     ref, _ = ops.qsplit_attention_ring([f64(x) for x in inp["Q"]], [f64(x) for x in inp["K"]],
                                        [f64(x) for x in inp["V"]], prune=True)
@@ -59,9 +60,10 @@ def test_attention_non_causal(ctx):
     assert_close(np.concatenate(got), ref, "non-causal attention")
 
 
-def test_attention_constant_v_is_exact(ctx):
+@pytest.mark.parametrize("m", [128, 384])
+def test_attention_constant_v_is_exact(ctx, m):
     # closed form: a constant V gives that constant at every query
-    P, m, H = 2, 128, 1
+    P, H = 2, 1
     inp = wl.attn_inputs(P, P * m, H, 128, 43)
     c = wl.gaussian_bf16(torch.Generator().manual_seed(5), (1, H, 128))
     V = [np.repeat(c, m, axis=0) for _ in range(P)]

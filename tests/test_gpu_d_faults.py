@@ -39,9 +39,10 @@ def test_skipped_hop_times_out_and_context_recovers():
             assert_bits_equal(to_bits(Y[r]), ref[r], f"after recovery rank {r}")
 
 
-def test_skipped_kv_hop_times_out_in_attention():
+@pytest.mark.parametrize("m", [128, 384])
+def test_skipped_kv_hop_times_out_in_attention(m):
     import overlapped_tensor_gemm_gb300 as fo
-    P, m, H = 3, 128, 1
+    P, H = 3, 1
     inp = wl.attn_inputs(P, P * m, H, 128, 78)
     Q = [to_dev(x).reshape(m, 128) for x in inp["Q"]]
     K = [to_dev(x).reshape(m, 128) for x in inp["K"]]
