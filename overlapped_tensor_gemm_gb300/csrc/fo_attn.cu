@@ -50,7 +50,7 @@ constexpr int kKB = 128;                 // keys per block
 constexpr int kAttnThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 softmax
 constexpr uint32_t kTileBytes = 128 * 128 * 2;   // one 128x128 bf16 operand (two 64-column swizzle halves)
 constexpr uint32_t kHalfBytes = kTileBytes / 2;
-constexpr int kKStages = 2;
+constexpr int kKStages = 2;              // K runs kKStages - 1 blocks ahead of V (3 measured no faster)
 constexpr int kVStages = 2;
 constexpr uint32_t kTmemCols = 512;      // S0 [0,128), S1 [128,256), O [256,384), P0 [384,448), P1 [448,512)
 constexpr uint32_t kOCol = 256;
@@ -160,7 +160,7 @@ struct BlockIter {
   }
 };
 
-// K runs one block ahead of V: a K stage is refilled as soon as the score MMA
+// K runs kKStages - 1 blocks ahead of V: a K stage is refilled as soon as the score MMA
 // that read it completes, a V stage once the P.V MMA that read it completes.
 __device__ void attn_producer(const AttnParams& p, uint8_t* smem, AttnCtl* ctl) {
   int kst = 0, vst = 0;
@@ -226,7 +226,7 @@ __device__ void attn_producer(const AttnParams& p, uint8_t* smem, AttnCtl* ctl) 
     vit.next(p);
     return true;
   };
-  if (kit.valid(p)) ok = issue_k();
+  for (int a = 0; ok && a < kKStages - 1 && kit.valid(p); ++a) ok = issue_k();
   while (ok && vit.valid(p)) {
     if (kit.valid(p) && !issue_k()) {
       ok = false;
@@ -273,6 +273,19 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
   }
 }
 
+// Non-blocking test of the phase of parity `parity`.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ void attn_mma(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, uint32_t tmem_base) {
   const uint32_t sbase = smem_u32(smem);
   uint32_t q_uses = 0;
@@ -284,7 +297,7 @@ __device__ void attn_mma(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, uint3
     if (!mbar_wait(&ctl->q_full, q_uses & 1u, p.ctrl, p.timeout_ns, kSiteFull, i)) break;
     ++q_uses;
     tc_fence_after();
-    // S for block j: K of kv stage (g+j) % 2, score buffer (g+j) % 2
+    // S for block j: K of stage (g+j) % kKStages, score buffer (g+j) % 2
     auto issue_scores = [&](uint32_t gj) -> bool {
       const uint32_t st = gj % kKStages, sb = gj & 1u;
       if (!mbar_wait(&ctl->k_full[st], (gj / kKStages) & 1u, p.ctrl, p.timeout_ns, kSiteFull, i)) return false;
@@ -301,30 +314,49 @@ __device__ void attn_mma(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, uint3
       ok = false;
       break;
     }
-    for (int j = 0; j < n; ++j) {
+    if (n == 1) umma_commit(&ctl->q_empty);
+    // Block j's step: the scores of block j + 1 and the P.V of block j, the two
+    // independent, issued in whichever order their operands become ready (scores
+    // first when both are), so a late K block does not hold back a ready P.V.
+    for (int j = 0; ok && j < n; ++j) {
       const uint32_t gj = g + j;
-      if (j + 1 < n) {
-        if (!issue_scores(gj + 1)) {
-          ok = false;
-          break;
+      const uint32_t gs = gj + 1, st = gs % kKStages, sb = gs & 1u;
+      const uint32_t pb = gj & 1u, vs = gj % kVStages;  // P buffer and V stage of block gj
+      bool need_s = j + 1 < n, need_pv = true;
+      const uint64_t t0 = global_timer_ns();
+      for (uint32_t spin = 1; need_s || need_pv; ++spin) {
+        bool progressed = false;
+        if (need_s && mbar_test(&ctl->k_full[st], (gs / kKStages) & 1u) &&
+            mbar_test(&ctl->s_empty[sb], ((gs >> 1) & 1u) ^ 1u)) {
+          tc_fence_after();
+          issue_s(tmem_base + sb * 128, sbase + kOffQ, sbase + kOffK + st * kTileBytes);
+          umma_commit(&ctl->k_empty[st]);
+          umma_commit(&ctl->s_full[sb]);
+          // Q is free once the item's last score MMA completes: the producer, K blocks
+          // ahead, may already wait for it to load the next item's Q
+          if (j + 2 == n) umma_commit(&ctl->q_empty);
+          need_s = false;
+          progressed = true;
         }
-      } else {
-        umma_commit(&ctl->q_empty);  // Q is free once every score MMA of this item completes
+        if (need_pv && mbar_test(&ctl->p_full[pb], (gj >> 1) & 1u) &&
+            mbar_test(&ctl->v_full[vs], (gj / kVStages) & 1u)) {
+          tc_fence_after();
+          issue_pv(tmem_base + kOCol, tmem_base + kPCol + pb * 64, sbase + kOffV + vs * kTileBytes, j == 0);
+          umma_commit(&ctl->v_empty[vs]);
+          umma_commit(&ctl->pv_done[pb]);
+          need_pv = false;
+          progressed = true;
+        }
+        if (!progressed && (spin & 63u) == 0u) {
+          if (aborted(p.ctrl)) {
+            ok = false;
+          } else if (global_timer_ns() - t0 > p.timeout_ns) {
+            raise_error(p.ctrl, FO_ERR_TIMEOUT, need_pv ? kSiteFull : kSiteTmemEmpty, static_cast<uint32_t>(i));
+            ok = false;
+          }
+          if (!ok) break;
+        }
       }
-      const uint32_t pb = gj & 1u;  // P buffer of block gj
-      if (!mbar_wait(&ctl->p_full[pb], (gj >> 1) & 1u, p.ctrl, p.timeout_ns, kSiteFull, i)) {
-        ok = false;
-        break;
-      }
-      const uint32_t vs = gj % kVStages;
-      if (!mbar_wait(&ctl->v_full[vs], (gj / kVStages) & 1u, p.ctrl, p.timeout_ns, kSiteFull, i)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      issue_pv(tmem_base + kOCol, tmem_base + kPCol + pb * 64, sbase + kOffV + vs * kTileBytes, j == 0);
-      umma_commit(&ctl->v_empty[vs]);
-      umma_commit(&ctl->pv_done[pb]);
     }
     g += n;
   }

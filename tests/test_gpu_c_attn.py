@@ -51,6 +51,18 @@ def test_attention_matches_ring_simulation_pruned(ctx, m):
         assert_close(got[r], ref[r], f"pruned ring rank {r}")
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_attention_several_items_per_cta(ctx, causal):
+    # a grid of 3 CTAs: every CTA walks several (rank, query block, head) items, so the
+    # producer's look-ahead crosses item boundaries (next Q while the last blocks run)
+    P, m, H = 2, 384, 2
+    inp, got = _attn(ctx, P, m, H, 44, causal=causal, num_sms=3)
+    ref = ops.attention_definition(np.concatenate([f64(x) for x in inp["Q"]]),
+                                   np.concatenate([f64(x) for x in inp["K"]]),
+                                   np.concatenate([f64(x) for x in inp["V"]]), causal=causal)
+    assert_close(np.concatenate(got), ref, f"attention, 3 CTAs, causal={causal}")
+
+
 def test_attention_non_causal(ctx):
     P, m, H = 2, 256, 2
     inp, got = _attn(ctx, P, m, H, 42, causal=False)
