@@ -108,14 +108,19 @@ struct Item {
 };
 
 // Items in decreasing cost order: ranks with more visible slices first, then
-// later query blocks (longer causal rows), then heads.
+// groups of kHeadGroup heads, then later query blocks (longer causal rows), then
+// the heads of the group.  Grouping heads keeps the CTAs that run at the same time
+// on fewer heads' K/V blocks, which then stay in L2 for all their query blocks.
+constexpr int kHeadGroup = 8;
 __device__ __forceinline__ Item decode_item(const AttnParams& p, int i) {
   const int per_rank = p.nkb * p.heads;
+  const int grp = p.heads % kHeadGroup == 0 ? kHeadGroup : p.heads;
   Item it;
   it.r = p.P - 1 - i / per_rank;
   const int rem = i % per_rank;
-  it.qb = p.nkb - 1 - rem / p.heads;
-  it.h = rem % p.heads;
+  const int in_grp = rem % (p.nkb * grp);
+  it.qb = p.nkb - 1 - in_grp / grp;
+  it.h = rem / (p.nkb * grp) * grp + in_grp % grp;
   return it;
 }
 
