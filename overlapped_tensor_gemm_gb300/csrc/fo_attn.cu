@@ -12,19 +12,21 @@
 // in TMEM.
 //
 // CTA layout (320 threads, one CTA per SM):
-//   warp 0      TMA: Q block once per item, then K and V^T blocks in two
-//               stage rings, K ahead of V; waits for the slice's arrival flag
+//   warp 0      TMA: K and V^T blocks in two stage rings of three stages, K
+//               two blocks ahead of V; waits for the slice's arrival flag
 //               before reading it.
 //   warp 1      tcgen05.mma: S = Q K^T into one of two TMEM score buffers
 //               (the next block's scores overlap this block's softmax), then
-//               O += P V into the TMEM accumulator, with P read from TMEM.
+//               O += P V into the TMEM accumulator; Q and P are read from TMEM,
+//               so shared memory holds only the K and V^T rings.
 //   warps 2-9   softmax: two warps per query row (one per 64-key half); they
-//               load their half of the score row, mask the diagonal block,
-//               exchange the row maximum, update max/sum, rescale their half
-//               of the O row only when the max grew by more than 2^8 (the
-//               final division by the sum uses the same reference max, so this
-//               is exact), and write P as fp16 into one of two TMEM buffers, so
-//               a block's softmax does not wait for the previous block's P.V.
+//               write the item's Q rows into TMEM, load their half of the score
+//               row, mask the diagonal block, exchange the row maximum, update
+//               max/sum, rescale their half of the O row only when the max grew
+//               by more than 2^8 (the final division by the sum uses the same
+//               reference max, so this is exact), and write P as fp16 over the
+//               scores they have read, so a block's softmax does not wait for
+//               the previous block's P.V.
 // V is transposed once per rank (V^T [heads*128, tokens]) before the ring so
 // that both MMAs read K-major operands.  The P.V product runs in fp16: the
 // transpose converts V's bf16 values to fp16 (exact for |v| within fp16's
@@ -48,20 +50,24 @@ constexpr int kHd = 128;                 // head_dim
 constexpr int kQB = 128;                 // queries per block
 constexpr int kKB = 128;                 // keys per block
 constexpr int kAttnThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 softmax
-constexpr uint32_t kTileBytes = 128 * 128 * 2;   // one 128x128 bf16 operand (two 64-column swizzle halves)
+constexpr uint32_t kTileBytes = 128 * 128 * 2;   // one 128x128 16-bit operand (two 64-column swizzle halves)
 constexpr uint32_t kHalfBytes = kTileBytes / 2;
-constexpr int kKStages = 2;              // K runs kKStages - 1 blocks ahead of V (3 measured no faster)
-constexpr int kVStages = 2;
-constexpr uint32_t kTmemCols = 512;      // S0 [0,128), S1 [128,256), O [256,384), P0 [384,448), P1 [448,512)
+constexpr int kKStages = 3;              // K runs kKStages - 1 blocks ahead of V
+constexpr int kVStages = 3;
+// TMEM: S0 [0,128), S1 [128,256), O [256,384), Q [384,448).  P of a block is
+// written over the first 32 columns of each warp's 64 score columns of its S buffer.
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 256;
-constexpr uint32_t kPCol = 384;          // P as packed fp16 pairs: 128 keys in 64 columns
+constexpr uint32_t kQCol = 384;          // Q as packed bf16 pairs: 128 head dims in 64 columns
 constexpr uint32_t kIdescS = umma_idesc_bf16(128, 128);   // S = Q K^T, bf16 operands
 constexpr uint32_t kIdescO = umma_idesc_f16(128, 128);    // O += P V, fp16 operands
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct AttnParams {
-  CUtensorMap maps[4 * kMaxP];  // per rank r: Q = r, K local = P+r, K received = 2P+r, V^T = 3P+r
+  CUtensorMap maps[3 * kMaxP];  // per rank r: K local = r, K received = P+r, V^T = 2P+r
+  const uint16_t* q[kMaxP];     // Q shards (read by the softmax warps into TMEM)
+  int64_t ld_q[kMaxP];
   uint16_t* out[kMaxP];
   int64_t ld_out[kMaxP];
   int32_t P, heads, nkb, causal;
@@ -77,20 +83,20 @@ struct AttnParams {
 };
 
 struct alignas(8) AttnCtl {
-  uint64_t q_full, q_empty;
+  uint64_t q_full;                  // the item's Q is in TMEM (the softmax warps wrote it)
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
-  uint64_t s_full[2], s_empty[2];
-  uint64_t p_full[2], pv_done[2];   // per P buffer (TMEM): written by softmax / read by the P.V MMA
+  uint64_t s_full[2];               // per S buffer: scores computed
+  uint64_t p_full[2];               // per S buffer: P written over the scores
+  uint64_t pv_done[2];              // per S buffer: the P.V that read its P completed
   uint64_t drain;
   uint64_t xchg[4][2];   // per lane quadrant, two slots: the column halves' partial max / sum exchange
   uint32_t tmem_base;
   uint32_t pad;
 };
 
-// Shared memory: Q | K stages | V^T stages | exchange | control  (S, O and P live in TMEM)
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kTileBytes;
+// Shared memory: K stages | V^T stages | exchange | control  (Q, S, P and O live in TMEM)
+constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
 constexpr uint32_t kOffXch = kOffV + kVStages * kTileBytes;  // float [2 slots][2 halves][128 rows]
 constexpr uint32_t kOffCtl = kOffXch + 2 * 2 * 128 * 4;
@@ -151,7 +157,6 @@ struct BlockIter {
     nb = blocks_of(p, it, 0);
   }
   __device__ bool valid(const AttnParams& p) const { return i < p.total_items; }
-  __device__ bool first_of_item() const { return t == 0 && kb == 0; }
   __device__ void next(const AttnParams& p) {
     if (++kb < nb) return;
     kb = 0;
@@ -169,27 +174,15 @@ struct BlockIter {
 // that read it completes, a V stage once the P.V MMA that read it completes.
 __device__ void attn_producer(const AttnParams& p, uint8_t* smem, AttnCtl* ctl) {
   int kst = 0, vst = 0;
-  uint32_t kph = 0, vph = 0, q_uses = 0;
+  uint32_t kph = 0, vph = 0;
   uint64_t seen = 0;  // bit r*P+s: arrival of slice s at rank r already observed
   uint32_t karmed = 0, karmed_ph = 0, varmed = 0, varmed_ph = 0;
-  bool q_armed = false;
-  uint32_t q_armed_ph = 0;
   BlockIter kit, vit;
   kit.start(p);
   vit.start(p);
   bool ok = true;
   auto issue_k = [&]() -> bool {
     const Item& it = kit.it;
-    if (kit.first_of_item()) {
-      if (!mbar_wait(&ctl->q_empty, (q_uses & 1u) ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty, kit.i)) return false;
-      mbar_arrive_expect_tx(&ctl->q_full, kTileBytes);
-      for (int c = 0; c < 2; ++c)
-        tma_load_2d(&p.maps[it.r], smem + kOffQ + c * kHalfBytes, &ctl->q_full, it.h * kHd + c * 64,
-                    it.qb * kQB);
-      q_armed = true;
-      q_armed_ph = q_uses & 1u;
-      ++q_uses;
-    }
     const int s = slice_of(p, it.r, kit.t);
     const int fidx = it.r * p.P + s;
     if (kit.t > 0 && p.wait_flags && !((seen >> fidx) & 1ull)) {
@@ -198,7 +191,7 @@ __device__ void attn_producer(const AttnParams& p, uint8_t* smem, AttnCtl* ctl) 
       seen |= 1ull << fidx;
     }
     if (!mbar_wait(&ctl->k_empty[kst], kph ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty, kit.i)) return false;
-    const CUtensorMap* kmap = kit.t == 0 ? &p.maps[p.P + it.r] : &p.maps[2 * p.P + it.r];
+    const CUtensorMap* kmap = kit.t == 0 ? &p.maps[it.r] : &p.maps[p.P + it.r];
     const int krow0 = kit.t == 0 ? 0 : s * p.m;
     uint8_t* kt = smem + kOffK + kst * kTileBytes;
     mbar_arrive_expect_tx(&ctl->k_full[kst], kTileBytes);
@@ -220,7 +213,7 @@ __device__ void attn_producer(const AttnParams& p, uint8_t* smem, AttnCtl* ctl) 
     uint8_t* vt = smem + kOffV + vst * kTileBytes;
     mbar_arrive_expect_tx(&ctl->v_full[vst], kTileBytes);
     for (int c = 0; c < 2; ++c)
-      tma_load_2d(&p.maps[3 * p.P + it.r], vt + c * kHalfBytes, &ctl->v_full[vst], vit.kb * kKB + c * 64,
+      tma_load_2d(&p.maps[2 * p.P + it.r], vt + c * kHalfBytes, &ctl->v_full[vst], vit.kb * kKB + c * 64,
                   (s * p.heads + it.h) * kHd);
     varmed |= 1u << vst;
     varmed_ph = (varmed_ph & ~(1u << vst)) | (vph << vst);
@@ -240,7 +233,6 @@ __device__ void attn_producer(const AttnParams& p, uint8_t* smem, AttnCtl* ctl) 
     if (!issue_v()) ok = false;
   }
   if (!ok) {
-    if (q_armed) mbar_wait_drain(&ctl->q_full, q_armed_ph, kDrainNs);
     for (int s = 0; s < kKStages; ++s)
       if ((karmed >> s) & 1u) mbar_wait_drain(&ctl->k_full[s], (karmed_ph >> s) & 1u, kDrainNs);
     for (int s = 0; s < kVStages; ++s)
@@ -248,18 +240,11 @@ __device__ void attn_producer(const AttnParams& p, uint8_t* smem, AttnCtl* ctl) 
   }
 }
 
-__device__ __forceinline__ void issue_s(uint32_t tmem_s, uint32_t q_addr, uint32_t k_addr) {
-#pragma unroll
-  for (int k = 0; k < kHd / 16; ++k) {
-    const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
-    umma_bf16_ss(tmem_s, umma_sdesc_sw128(q_addr + off), umma_sdesc_sw128(k_addr + off), kIdescS, k > 0 ? 1u : 0u);
-  }
-}
-
-// D (TMEM) += A (TMEM) * B (shared memory descriptor), A = [128 rows in lanes, 16 fp16
-// per 8 columns]: the form whose A operand never passes through shared memory.
-__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                            uint32_t accumulate) {
+// D (TMEM) += A (TMEM) * B (shared memory descriptor), A = [128 rows in lanes, 16
+// 16-bit elements per 8 columns]: the form whose A operand never passes through
+// shared memory.
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
@@ -268,13 +253,24 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
-// O += P V for one 128-key block: P from TMEM (column c holds keys 2c, 2c+1), V^T
-// from the two 64-key swizzle halves of the stage.
+// S = Q K^T for one 128-key block: Q from TMEM (column c holds head dims 2c, 2c+1),
+// K from the two 64-dim swizzle halves of the stage (16 head dims per MMA).
+__device__ __forceinline__ void issue_s(uint32_t tmem_s, uint32_t tmem_q, uint32_t k_addr) {
+#pragma unroll
+  for (int k = 0; k < kHd / 16; ++k) {
+    const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
+    umma_ts(tmem_s, tmem_q + k * 8, umma_sdesc_sw128(k_addr + off), kIdescS, k > 0 ? 1u : 0u);
+  }
+}
+
+// O += P V for one 128-key block: P from the S buffer (keys 64h + 2c, 64h + 2c + 1 in
+// column 64h + c, c < 32), V^T from the two 64-key swizzle halves of the stage.
 __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr, bool first) {
 #pragma unroll
   for (int k = 0; k < kKB / 16; ++k) {
     const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
-    umma_f16_ts(tmem_o, tmem_p + k * 8, umma_sdesc_sw128(v_addr + off), kIdescO, (first && k == 0) ? 0u : 1u);
+    umma_ts(tmem_o, tmem_p + (k >> 2) * 64 + (k & 3) * 8, umma_sdesc_sw128(v_addr + off), kIdescO,
+            (first && k == 0) ? 0u : 1u);
   }
 }
 
@@ -291,6 +287,10 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// S buffer b of block gs may be overwritten once the P.V of block gs - 2 (whose P
+// lives there) has completed.
+__device__ __forceinline__ uint32_t s_free_parity(uint32_t gs) { return ((gs >> 1) & 1u) ^ 1u; }
+
 __device__ void attn_mma(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, uint32_t tmem_base) {
   const uint32_t sbase = smem_u32(smem);
   uint32_t q_uses = 0;
@@ -302,51 +302,43 @@ __device__ void attn_mma(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, uint3
     if (!mbar_wait(&ctl->q_full, q_uses & 1u, p.ctrl, p.timeout_ns, kSiteFull, i)) break;
     ++q_uses;
     tc_fence_after();
-    // S for block j: K of stage (g+j) % kKStages, score buffer (g+j) % 2
-    auto issue_scores = [&](uint32_t gj) -> bool {
-      const uint32_t st = gj % kKStages, sb = gj & 1u;
-      if (!mbar_wait(&ctl->k_full[st], (gj / kKStages) & 1u, p.ctrl, p.timeout_ns, kSiteFull, i)) return false;
-      if (!mbar_wait(&ctl->s_empty[sb], ((gj >> 1) & 1u) ^ 1u, p.ctrl, p.timeout_ns, kSiteTmemEmpty, i))
-        return false;
+    {  // scores of the item's first block
+      const uint32_t st = g % kKStages, sb = g & 1u;
+      if (!mbar_wait(&ctl->k_full[st], (g / kKStages) & 1u, p.ctrl, p.timeout_ns, kSiteFull, i) ||
+          !mbar_wait(&ctl->pv_done[sb], s_free_parity(g), p.ctrl, p.timeout_ns, kSiteTmemEmpty, i)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
-      issue_s(tmem_base + sb * 128, sbase + kOffQ, sbase + kOffK + st * kTileBytes);
+      issue_s(tmem_base + sb * 128, tmem_base + kQCol, sbase + kOffK + st * kTileBytes);
       issued = true;
       umma_commit(&ctl->k_empty[st]);  // the K stage is free once these scores are computed
       umma_commit(&ctl->s_full[sb]);
-      return true;
-    };
-    if (!issue_scores(g)) {
-      ok = false;
-      break;
     }
-    if (n == 1) umma_commit(&ctl->q_empty);
     // Block j's step: the scores of block j + 1 and the P.V of block j, the two
     // independent, issued in whichever order their operands become ready (scores
     // first when both are), so a late K block does not hold back a ready P.V.
     for (int j = 0; ok && j < n; ++j) {
       const uint32_t gj = g + j;
       const uint32_t gs = gj + 1, st = gs % kKStages, sb = gs & 1u;
-      const uint32_t pb = gj & 1u, vs = gj % kVStages;  // P buffer and V stage of block gj
+      const uint32_t pb = gj & 1u, vs = gj % kVStages;  // S buffer (holding P) and V stage of block gj
       bool need_s = j + 1 < n, need_pv = true;
       const uint64_t t0 = global_timer_ns();
       for (uint32_t spin = 1; need_s || need_pv; ++spin) {
         bool progressed = false;
         if (need_s && mbar_test(&ctl->k_full[st], (gs / kKStages) & 1u) &&
-            mbar_test(&ctl->s_empty[sb], ((gs >> 1) & 1u) ^ 1u)) {
+            mbar_test(&ctl->pv_done[sb], s_free_parity(gs))) {
           tc_fence_after();
-          issue_s(tmem_base + sb * 128, sbase + kOffQ, sbase + kOffK + st * kTileBytes);
+          issue_s(tmem_base + sb * 128, tmem_base + kQCol, sbase + kOffK + st * kTileBytes);
           umma_commit(&ctl->k_empty[st]);
           umma_commit(&ctl->s_full[sb]);
-          // Q is free once the item's last score MMA completes: the producer, K blocks
-          // ahead, may already wait for it to load the next item's Q
-          if (j + 2 == n) umma_commit(&ctl->q_empty);
           need_s = false;
           progressed = true;
         }
         if (need_pv && mbar_test(&ctl->p_full[pb], (gj >> 1) & 1u) &&
             mbar_test(&ctl->v_full[vs], (gj / kVStages) & 1u)) {
           tc_fence_after();
-          issue_pv(tmem_base + kOCol, tmem_base + kPCol + pb * 64, sbase + kOffV + vs * kTileBytes, j == 0);
+          issue_pv(tmem_base + kOCol, tmem_base + pb * 128, sbase + kOffV + vs * kTileBytes, j == 0);
           umma_commit(&ctl->v_empty[vs]);
           umma_commit(&ctl->pv_done[pb]);
           need_pv = false;
@@ -411,9 +403,9 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 // Softmax warps 2-9.  Warp w serves TMEM lane quadrant q = w % 4 (query rows
 // 32q..32q+31) and column half hf = (w - 2) / 4 (keys 64hf..64hf+63 of each
-// block).  The two warps of a quadrant combine their partial row maxima (and,
-// at the end, row sums) through shared memory, each exchange closed by a
-// bounded mbarrier wait.
+// block, head dims 64hf..64hf+63 of Q and O).  The two warps of a quadrant combine
+// their partial row maxima (and, at the end, row sums) through shared memory, each
+// exchange closed by a bounded mbarrier wait.
 __device__ __forceinline__ void xch_publish(AttnCtl* ctl, float* xch, uint32_t uses, int q, int hf, int row,
                                             float mine, int lane) {
   const uint32_t slot = uses & 1u;
@@ -430,6 +422,33 @@ __device__ __forceinline__ bool xch_collect(AttnCtl* ctl, const float* xch, uint
   return true;
 }
 
+// This thread's query row of item `it` (its warp's 64 head dims) into the TMEM Q
+// region, then the warp's arrival on q_full.  The caller guarantees that no score
+// MMA still reads the region.
+__device__ __forceinline__ void write_q(const AttnParams& p, AttnCtl* ctl, const Item& it, uint32_t lane_base,
+                                        int row, int hf, int lane) {
+  const uint16_t* src = p.q[it.r] + static_cast<int64_t>(it.qb * kQB + row) * p.ld_q[it.r] + it.h * kHd + hf * 64;
+  uint32_t v[32];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint4 x = *reinterpret_cast<const uint4*>(src + 8 * k);
+    v[4 * k] = x.x;
+    v[4 * k + 1] = x.y;
+    v[4 * k + 2] = x.z;
+    v[4 * k + 3] = x.w;
+  }
+  tmem_st32(lane_base + kQCol + hf * 32, v);
+  tmem_wait_st();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&ctl->q_full);
+}
+
+__device__ __forceinline__ void prefetch_row_l2(const AttnParams& p, const Item& it, int row, int hf) {
+  const uint16_t* src = p.q[it.r] + static_cast<int64_t>(it.qb * kQB + row) * p.ld_q[it.r] + it.h * kHd + hf * 64;
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
+}
+
 __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, uint32_t tmem_base, int warp,
                              int lane) {
   const int q = warp & 3;
@@ -440,17 +459,26 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
   float* xch = reinterpret_cast<float*>(smem + kOffXch);
   uint32_t g = 0, xuses = 0;
   const uint64_t c2 = pack2(p.scale_log2, p.scale_log2);
+  if (blockIdx.x < p.total_items) write_q(p, ctl, decode_item(p, blockIdx.x), lane_base, row, hf, lane);
   for (int i = blockIdx.x; i < p.total_items; i += gridDim.x) {
     const Item it = decode_item(p, i);
+    const int inext = i + static_cast<int>(gridDim.x);
+    const bool has_next = inext < p.total_items;
+    Item nx = it;
+    if (has_next) {
+      nx = decode_item(p, inext);
+      prefetch_row_l2(p, nx, row, hf);
+    }
     float m_ref = -INFINITY, l = 0.f;
     int j = 0;
     const int nsteps = steps_of(p, it.r);
+    const int n = item_blocks(p, it);
     for (int t = 0; t < nsteps; ++t) {
       const int nb = blocks_of(p, it, t);
       const bool diag_step = p.causal && t == 0;
       for (int kb = 0; kb < nb; ++kb, ++j) {
         const uint32_t gj = g + j;
-        const uint32_t sb = gj & 1u;  // score buffer and P buffer of this block
+        const uint32_t sb = gj & 1u;  // S buffer of this block (P is written over it)
         const bool diag = diag_step && kb == it.qb;
         if (!warp_wait(&ctl->s_full[sb], (gj >> 1) & 1u, p, kSiteTmemFull, i, lane)) return;
         tc_fence_after();
@@ -517,19 +545,14 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
             rescale = true;
           }
           if (__any_sync(0xffffffffu, rescale)) {
-            load_scores(s);  // the score buffer is still held
+            load_scores(s);  // the scores are still in TMEM (P not yet written)
             bsum = weights(s, m_ref, packed);
           }
         }
         l += bsum;
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->s_empty[sb]);
-        // P buffer sb was last read by the P.V of block gj - 2
-        if (gj >= 2) {
-          if (!warp_wait(&ctl->pv_done[sb], ((gj >> 1) & 1u) ^ 1u, p, kSiteDrain, i, lane)) return;
-          tc_fence_after();
-        }
+        // The item's last scores are read: every score MMA of the item has completed, so
+        // the next item's Q can take the TMEM Q region now, ahead of this item's end.
+        if (j + 1 == n && has_next) write_q(p, ctl, nx, lane_base, row, hf, lane);
         if (__any_sync(0xffffffffu, rescale)) {
           // O must hold every earlier block (P.V of block gj - 1 complete) before it is rescaled
           const uint32_t pb = (gj - 1) & 1u;
@@ -545,7 +568,8 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
             tmem_st32(lane_base + kOCol + col0 + c * 32, v);
           }
         }
-        tmem_st32(lane_base + kPCol + sb * 64 + col0 / 2, packed);
+        // P over the first half of this warp's (already read) score columns
+        tmem_st32(lane_base + sb * 128 + col0, packed);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -587,8 +611,7 @@ __global__ void __maxnreg__(136) attn_kernel(const __grid_constant__ AttnParams 
   AttnCtl* ctl = reinterpret_cast<AttnCtl*>(smem + kOffCtl);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(&ctl->q_full, 1);
-    mbar_init(&ctl->q_empty, 1);
+    mbar_init(&ctl->q_full, 8);
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&ctl->k_full[s], 1);
       mbar_init(&ctl->k_empty[s], 1);
@@ -599,7 +622,6 @@ __global__ void __maxnreg__(136) attn_kernel(const __grid_constant__ AttnParams 
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&ctl->s_full[b], 1);
-      mbar_init(&ctl->s_empty[b], 8);
       mbar_init(&ctl->p_full[b], 8);
       mbar_init(&ctl->pv_done[b], 1);
     }
@@ -610,7 +632,7 @@ __global__ void __maxnreg__(136) attn_kernel(const __grid_constant__ AttnParams 
     fence_proxy_async_shared();
   }
   if (warp == 0 && lane == 0)
-    for (int i = 0; i < 4 * p.P; ++i) tma_prefetch_desc(&p.maps[i]);
+    for (int i = 0; i < 3 * p.P; ++i) tma_prefetch_desc(&p.maps[i]);
   if (warp == 1) {
     tmem_alloc(&ctl->tmem_base, kTmemCols);
     tmem_relinquish();
@@ -717,12 +739,13 @@ fo_status attn_run(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K, const fo_mat* 
   AttnParams p;
   std::memset(&p, 0, sizeof(p));
   for (int r = 0; r < P; ++r) {
-    if ((st = host_encode_map(&p.maps[r], Q[r].ptr, m, HD, Q[r].ld, kQB)) != FO_OK) return st;
-    if ((st = host_encode_map(&p.maps[P + r], K[r].ptr, m, HD, K[r].ld, kKB)) != FO_OK) return st;
-    if ((st = host_encode_map(&p.maps[2 * P + r], k_slot(r, 0), M, HD, HD, kKB)) != FO_OK) return st;
-    if ((st = host_encode_map(&p.maps[3 * P + r], vt_slot(r, 0), static_cast<int64_t>(P) * HD, m, m, kHd,
+    if ((st = host_encode_map(&p.maps[r], K[r].ptr, m, HD, K[r].ld, kKB)) != FO_OK) return st;
+    if ((st = host_encode_map(&p.maps[P + r], k_slot(r, 0), M, HD, HD, kKB)) != FO_OK) return st;
+    if ((st = host_encode_map(&p.maps[2 * P + r], vt_slot(r, 0), static_cast<int64_t>(P) * HD, m, m, kHd,
                               CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != FO_OK)
       return st;
+    p.q[r] = static_cast<const uint16_t*>(Q[r].ptr);
+    p.ld_q[r] = Q[r].ld;
     p.out[r] = static_cast<uint16_t*>(O[r].ptr);
     p.ld_out[r] = O[r].ld;
   }
