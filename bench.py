@@ -8,7 +8,7 @@ A step is one layer over one batch; inputs stay resident in HBM.  The timed
 weights (336 MiB) and activations exceed the 126 MiB L2, so no flush is used.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload llama8b|tiny|sweep1k..sweep16k|tail_rs|attn]
+                  [--workload llama8b|tiny|sweep1k..sweep16k|tail_rs|attn|attn1k..attn16k|attn_layer]
 
 With N > 1 (torchrun, one process per GPU) every rank runs an independent
 replica of the workload ("replicas only": the virtual ranks of one layer never
@@ -231,10 +231,12 @@ def run_ours(args, rank: int, world: int, device: int):
         return float(t.item())
 
     pk = peaks()
-    if args.workload == "attn":
+    if args.workload == "attn" or (args.workload.startswith("attn") and args.workload.endswith("k")):
         return run_attention_only(args, rank, world, device, pk, barrier, max_over_ranks)
     if args.workload == "tail_rs":
         return run_tail_rs(args, world, device, pk)
+    if args.workload == "attn_layer":
+        return run_attn_layer(args, world, device, pk)
     cfg = mlp_config(args.workload)
     inp = wl.mlp_inputs(cfg)
 
@@ -386,9 +388,9 @@ def run_ours(args, rank: int, world: int, device: int):
     return out
 
 
-def attention_bench(ctx, pk, iters: int, order: str = "flash", baselines: bool = True):
+def attention_bench(ctx, pk, iters: int, order: str = "flash", baselines: bool = True, c=None):
     import torch
-    c = wl.ATTN
+    c = c or wl.ATTN
     g = torch.Generator(device="cuda")
     g.manual_seed(c.seed)
     shape = (c.m, c.heads * c.head_dim)
@@ -491,10 +493,63 @@ def run_tail_rs(args, world, device, pk):
             "exposed_ms": {k: round(v - gemm_ms, 4) for k, v in t.items()}}
 
 
+def run_attn_layer(args, world, device, pk):
+    """Attention block (Flash-AG QKV projection -> per-rank causal attention of the rank's
+    heads -> Flash-RS output projection), Llama-3-8B-shaped, against its serial and
+    data-slicing baselines."""
+    import torch
+    import overlapped_tensor_gemm_gb300 as fo
+    c = wl.ATTN_LAYER
+    g = torch.Generator(device="cuda")
+    g.manual_seed(c.seed)
+    hd = c.heads * c.head_dim
+    X = [torch.randn((c.m, c.hidden), generator=g, device="cuda").to(torch.bfloat16) for _ in range(c.P)]
+    Wq = [(torch.randn((3 * hd, c.hidden), generator=g, device="cuda") * wl.W_STD).to(torch.bfloat16)
+          for _ in range(c.P)]
+    Wo = [(torch.randn((c.hidden, hd), generator=g, device="cuda") * wl.W_STD).to(torch.bfloat16)
+          for _ in range(c.P)]
+    Z = [torch.empty((c.m, c.hidden), dtype=torch.bfloat16, device="cuda") for _ in range(c.P)]
+    ctx = fo.Context(device)
+    stream = torch.cuda.current_stream()
+
+    def timed(order, iters):
+        for _ in range(max(args.warmup, 1)):
+            ctx.attn_layer(X, Wq, Wo, Z, heads=c.heads, order=order)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(iters):
+            ctx.attn_layer(X, Wq, Wo, Z, heads=c.heads, order=order)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ctx.poll()
+        return a.elapsed_time(b) / iters
+
+    with ClockSampler(device) as clk:
+        ms = timed("flash", args.steps)
+    clocks = clk.summary()
+    fl = c.flops()
+    tf = fl["total"] / (ms * 1e-3) / 1e12
+    res = {"metric": "attention block TFLOP/s (Flash-AG QKV, attention, Flash-RS out-projection)",
+           "value": round(tf, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights)",
+           "config": {"workload": f"attention block, P={c.P}, tokens {c.tokens}, hidden {c.hidden}, "
+                                  f"{c.heads * c.P} heads of {c.head_dim} ({c.heads} per rank)",
+                      "l2": "inputs larger than L2 (no flush)"},
+           "pct_of_peak": round(100 * tf / pk["bf16_burst"], 2), "clocks": clocks,
+           "flop": fl}
+    if not args.no_extras:
+        res["baselines_ms"] = {o: round(timed(o, args.steps), 4) for o in ("serial", "slicing", "naive")}
+    ctx.close()
+    return res
+
+
 def run_attention_only(args, rank, world, device, pk, barrier, max_over_ranks):
     import overlapped_tensor_gemm_gb300 as fo
     ctx = fo.Context(device)
-    res = attention_bench(ctx, pk, args.steps, args.attn_order, baselines=not args.no_extras)
+    c = wl.ATTN if args.workload == "attn" else wl.attn_sweep(int(args.workload[4:-1]) * 1024)
+    res = attention_bench(ctx, pk, args.steps, args.attn_order, baselines=not args.no_extras, c=c)
     ctx.close()
     return {"metric": "query-split attention TFLOP/s", "value": res["tflops"], "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"],
@@ -507,7 +562,7 @@ def run_attention_only(args, rank, world, device, pk, barrier, max_over_ranks):
 # --------------------------------------------------------------------------
 
 def run_reference(args):
-    cfg = mlp_config(args.workload if args.workload != "attn" else "llama8b")
+    cfg = mlp_config(args.workload if not args.workload.startswith("attn") else "llama8b")  # incl. attn_layer
     inp = wl.mlp_inputs(cfg)
     inp_f64 = decode_inputs(inp)
     per_step = max(2.0, min(20.0, 60.0 / max(1, args.steps + args.warmup)))

@@ -18,7 +18,11 @@ configurations of the build):
 * ``tail_rs`` -- GEMM-RS only, P=8, tokens 512, hidden (out) 8192,
   in-features 28672.
 * ``attn``   -- query-split causal attention, P=4, seq 16384, 32 heads,
-  head_dim 128, Q,K,V~N(0,1).
+  head_dim 128, Q,K,V~N(0,1); ``attn1k``..``attn16k`` the same at other lengths.
+* ``attn_layer`` -- attention block (Flash-AG QKV projection, per-rank causal
+  attention of the rank's heads, Flash-RS output projection), Llama-3-8B-shaped:
+  P=4, tokens 4096, hidden 4096, 32 heads of 128 (8 per rank), X~N(0,1),
+  W~N(0,0.02).
 
 Seeds are ``1234 + config index``.  Generation uses the torch CPU generator
 (a library PRNG); conversion to bf16 uses torch's round-to-nearest-even cast.
@@ -138,6 +142,42 @@ TAIL_RS = RSConfig("tail_rs", 3, P=8, tokens=512, n_out=8192, k_total=28672, int
 ATTN = AttnConfig("attn", 4, P=4, seq=16384, heads=32, head_dim=128)
 
 
+@dataclasses.dataclass(frozen=True)
+class AttnLayerConfig:
+    name: str
+    index: int
+    P: int
+    tokens: int
+    hidden: int
+    heads: int          # heads per rank
+    head_dim: int = 128
+
+    @property
+    def seed(self) -> int:
+        return 1234 + self.index
+
+    @property
+    def m(self) -> int:
+        return self.tokens // self.P
+
+    def flops(self) -> dict:
+        """Algorithmic FLOP: QKV and output projections (2*M*K*N each), causal attention
+        (QK^T and PV over the i>=j triangle) of all P*heads heads."""
+        hd = self.heads * self.head_dim
+        qkv = 2 * self.tokens * self.hidden * 3 * hd * self.P
+        attn = 4 * (self.tokens * (self.tokens + 1) // 2) * self.heads * self.P * self.head_dim
+        out = 2 * self.tokens * hd * self.P * self.hidden
+        return {"qkv": qkv, "attn": attn, "out": out, "total": qkv + attn + out}
+
+
+ATTN_LAYER = AttnLayerConfig("attn_layer", 5, P=4, tokens=4096, hidden=4096, heads=8)
+
+
+def attn_sweep(seq: int) -> AttnConfig:
+    """The query-split attention workload at another sequence length (P=4, 32 heads)."""
+    return AttnConfig(f"attn{seq // 1024}k", 4, P=4, seq=seq, heads=32, head_dim=128)
+
+
 # --------------------------------------------------------------------------
 # generators
 # --------------------------------------------------------------------------
@@ -223,6 +263,18 @@ def attn_inputs(P: int, seq: int, heads: int, head_dim: int, seed: int) -> dict:
     K = [gaussian_bf16(g, (m, heads, head_dim)) for _ in range(P)]
     V = [gaussian_bf16(g, (m, heads, head_dim)) for _ in range(P)]
     return {"Q": Q, "K": K, "V": V}
+
+
+def attn_layer_inputs(P: int, tokens: int, hidden: int, heads: int, head_dim: int, seed: int) -> dict:
+    """X shards [tokens/P, hidden] ~N(0,1); per rank W_qkv [3*heads*head_dim, hidden] and
+    W_o [hidden, heads*head_dim] ~N(0, 0.02); bf16 bits."""
+    g = _gen(seed)
+    m = tokens // P
+    hd = heads * head_dim
+    X = [gaussian_bf16(g, (m, hidden)) for _ in range(P)]
+    W_qkv = [gaussian_bf16(g, (3 * hd, hidden), W_STD) for _ in range(P)]
+    W_o = [gaussian_bf16(g, (hidden, hd), W_STD) for _ in range(P)]
+    return {"X_shards": X, "W_qkv": W_qkv, "W_o": W_o}
 
 
 def sample_rows(n_rows: int, block: int, per_block: int, seed: int) -> np.ndarray:

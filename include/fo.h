@@ -211,6 +211,25 @@ FO_API fo_status fo_qsplit_attn(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K_sh
                          const fo_mat* V_shards, int P, int heads, int head_dim, int causal,
                          const fo_mat* O, const fo_opts* opts, void* stream);
 
+/* One attention block in the layout of the MLP layer (technical summary section 2:
+ * the QKV projection is a column-parallel GEMM after an all-gather, the output
+ * projection a row-parallel GEMM before a reduce-scatter): Flash-AG with W_qkv,
+ * causal multi-head attention of every rank's own heads over all M = P*m tokens
+ * (independent per rank, no ring: a rank holds the whole sequence of its heads),
+ * then Flash-RS with W_o.
+ *   X_shards[r] [m, Hd] bf16 (rank r's token slice of the block input)
+ *   W_qkv[r]    [3*heads*head_dim, Hd] bf16: rank r's heads, Q rows, then K rows,
+ *               then V rows (head h at rows h*head_dim.. of each part)
+ *   W_o[r]      [Hd, heads*head_dim] bf16: the output projection's columns of
+ *               rank r's heads
+ *   Z[r]        [m, Hd] bf16 (rank r's token slice of the block output)
+ * heads = heads per rank, head_dim == 128, M % 128 == 0.  QKV (bf16) and the
+ * attention output (bf16) live in the context's workspace.  opts->order applies to
+ * the two GEMMs as in fo_mlp_layer. */
+FO_API fo_status fo_attn_layer(fo_ctx* ctx, const fo_mat* X_shards, const fo_mat* W_qkv,
+                        const fo_mat* W_o, int P, int heads, int head_dim, int causal,
+                        const fo_mat* Z, const fo_opts* opts, void* stream);
+
 /* Flash-RS (as fo_gemm_rs, FO_ORDER_FLASH) for callers that cannot allocate
  * device memory.  (No counterpart on the pages: this is a deployment variant.)
  * fo_gemm_rs keeps its ring scratch -- fp32 receive slots and per-tile flags --

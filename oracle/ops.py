@@ -312,3 +312,46 @@ def qsplit_attention_ring(Q_shards, K_shards, V_shards, causal: bool = True, pru
     ring.check_drained()
     O = [np.transpose(acc[r] / lsum[r][:, :, None], (1, 0, 2)) for r in range(P)]
     return O, log
+
+
+# --------------------------------------------------------------------------
+# attention block (QKV projection -> attention -> output projection)
+# --------------------------------------------------------------------------
+
+def attn_layer(X_slices, W_qkv, W_o, heads: int, causal: bool = True, decomposed: bool = True):
+    """One attention block on P ranks; every operation output is rounded to bf16.
+
+    Technical summary, section 2 (architectural instantiations): the QKV
+    projection is the column-parallel GEMM after the all-gather, the output
+    projection the row-parallel GEMM before the reduce-scatter; attention itself
+    needs no communication because rank r owns ``heads`` whole heads for every
+    token.  W_qkv[r] = [Q rows; K rows; V rows] of rank r's heads ([3*heads*D, Hd]),
+    W_o[r] = the output projection's columns of rank r's heads ([Hd, heads*D]).
+
+    Returns (QKV, O, Z): QKV[r] [M, 3*heads*D], O[r] [M, heads*D] (attention of
+    rank r's heads over all M tokens) and Z[d] [m, Hd] (rank d's token slice).
+    """
+    P = len(W_qkv)
+    if decomposed:
+        QKV, _ = ag_gemm_ring(X_slices, W_qkv)
+    else:
+        QKV = ag_gemm_definition(X_slices, W_qkv)
+    QKV = [bf16.round_f64(y) for y in QKV]
+    O = []
+    for r in range(P):
+        M, three_hd = QKV[r].shape
+        HD = three_hd // 3
+        D = HD // heads
+        q = QKV[r][:, :HD].reshape(M, heads, D)
+        k = QKV[r][:, HD:2 * HD].reshape(M, heads, D)
+        v = QKV[r][:, 2 * HD:].reshape(M, heads, D)
+        O.append(bf16.round_f64(attention_definition(q, k, v, causal).reshape(M, HD)))
+    rows = [np.asarray(x).shape[0] for x in X_slices]
+    offs = np.cumsum([0] + rows)
+    chunks = [[o[offs[c]:offs[c + 1]] for c in range(P)] for o in O]
+    if decomposed:
+        Z, _ = gemm_rs_ring(chunks, W_o)
+    else:
+        Z = gemm_rs_definition(chunks, W_o)
+    Z = [bf16.round_f64(z) for z in Z]
+    return QKV, O, Z

@@ -31,7 +31,7 @@ EPILOGUES = {"plain": 0, "silu": 1}
 # Every entry point declared in include/fo.h.
 ABI_SYMBOLS = ("fo_version", "fo_last_error_string", "fo_ctx_create", "fo_ctx_destroy", "fo_ctx_poll",
                "fo_ctx_phase_ms", "fo_gemm", "fo_ag_gemm", "fo_gemm_rs", "fo_silu_mul", "fo_mlp_layer",
-               "fo_mlp_layer_host", "fo_qsplit_attn", "fo_step_order", "fo_gemm_rs_noalloc")
+               "fo_mlp_layer_host", "fo_qsplit_attn", "fo_attn_layer", "fo_step_order", "fo_gemm_rs_noalloc")
 
 
 class FoMat(ctypes.Structure):
@@ -81,6 +81,8 @@ def load() -> ctypes.CDLL:
                                            P(FoMat), P(FoOpts), vp]
         lib.fo_qsplit_attn.argtypes = [vp, P(FoMat), P(FoMat), P(FoMat), ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_int, P(FoMat), P(FoOpts), vp]
+        lib.fo_attn_layer.argtypes = [vp, P(FoMat), P(FoMat), P(FoMat), ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_int, ctypes.c_int, P(FoMat), P(FoOpts), vp]
         lib.fo_step_order.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P(ctypes.c_int32),
                                       P(ctypes.c_int32), ctypes.c_int]
         lib.fo_gemm_rs_noalloc.argtypes = [P(FoMat), P(FoMat), ctypes.c_int, P(FoMat), ctypes.c_uint32,
@@ -212,6 +214,14 @@ class Context:
         o = opts(**kw)
         _check(self._lib.fo_qsplit_attn(self._h, _mats(Q), _mats(K), _mats(V), P, heads, head_dim, int(causal),
                                         _mats(O), ctypes.byref(o), _stream(stream)))
+
+    def attn_layer(self, X_shards, W_qkv, W_o, Z, heads: int, head_dim: int = 128, causal: bool = True,
+                   stream=None, **kw) -> None:
+        """Flash-AG QKV projection -> per-rank causal attention -> Flash-RS output projection."""
+        P = len(X_shards)
+        o = opts(**kw)
+        _check(self._lib.fo_attn_layer(self._h, _mats(X_shards), _mats(W_qkv), _mats(W_o), P, heads, head_dim,
+                                       int(causal), _mats(Z), ctypes.byref(o), _stream(stream)))
 
 
 def step_order(op: str, P: int, order: str = "flash") -> list[list[tuple[int, int]]]:

@@ -21,7 +21,7 @@
 
 namespace fo {
 fo_status attn_run(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K, const fo_mat* V, int P, int heads,
-                   int head_dim, int causal, const fo_mat* O, const fo_opts* opts, cudaStream_t stream);
+                   int head_dim, int causal, const fo_mat* O, const fo_opts* opts, cudaStream_t stream, bool ring);
 }
 
 using namespace fo;
@@ -101,6 +101,8 @@ enum BufId : int {
   kBufMlpH,
   kBufHostX,
   kBufHostZ,
+  kBufLayerQkv,
+  kBufLayerO,
   kBufAttnRecv,
 };
 
@@ -1068,7 +1070,43 @@ fo_status fo_qsplit_attn(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K_shards, c
   if (!Q || !K_shards || !V_shards || !O) return fail(FO_ERR_INVALID_ARG, "null matrix array");
   FO_CUDA(cudaSetDevice(ctx->device));
   return attn_run(ctx, Q, K_shards, V_shards, P, heads, head_dim, causal, O, opts,
-                  static_cast<cudaStream_t>(stream));
+                  static_cast<cudaStream_t>(stream), true);
+}
+
+fo_status fo_attn_layer(fo_ctx* ctx, const fo_mat* X_shards, const fo_mat* W_qkv, const fo_mat* W_o, int P,
+                        int heads, int head_dim, int causal, const fo_mat* Z, const fo_opts* opts, void* stream) {
+  FO_TRY(check_common(ctx, P, opts));
+  if (!X_shards || !W_qkv || !W_o || !Z) return fail(FO_ERR_INVALID_ARG, "null matrix array");
+  if (heads < 1) return fail(FO_ERR_INVALID_ARG, "heads must be positive");
+  if (head_dim != 128) return fail(FO_ERR_UNSUPPORTED, "head_dim must be 128");
+  FO_CUDA(cudaSetDevice(ctx->device));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const fo_opts o = opts ? *opts : default_opts();
+  const int64_t m = X_shards[0].rows, M = m * P, HD = static_cast<int64_t>(heads) * head_dim;
+  for (int r = 0; r < P; ++r) {
+    FO_TRY(check_mat(W_qkv[r], FO_BF16, "W_qkv", r));
+    FO_TRY(check_mat(W_o[r], FO_BF16, "W_o", r));
+    if (W_qkv[r].rows != 3 * HD) return fail(FO_ERR_SHAPE, "W_qkv[%d] must have 3*heads*head_dim rows", r);
+    if (W_o[r].cols != HD) return fail(FO_ERR_SHAPE, "W_o[%d] must have heads*head_dim columns", r);
+  }
+  if (M % 128 != 0) return fail(FO_ERR_UNSUPPORTED, "P*m must be a multiple of 128");
+  void *qkv_v = nullptr, *o_v = nullptr;
+  FO_TRY(ensure_buf(ctx, kBufLayerQkv, static_cast<size_t>(P) * M * 3 * HD * 2 + 16, &qkv_v));
+  FO_TRY(ensure_buf(ctx, kBufLayerO, static_cast<size_t>(P) * M * HD * 2 + 16, &o_v));
+  fo_mat QKV[kMaxP], Qm[kMaxP], Km[kMaxP], Vm[kMaxP], Om[kMaxP];
+  for (int r = 0; r < P; ++r) {
+    char* base = static_cast<char*>(qkv_v) + static_cast<int64_t>(r) * M * 3 * HD * 2;
+    QKV[r] = fo_mat{base, FO_BF16, 0, M, 3 * HD, 3 * HD};
+    Qm[r] = fo_mat{base, FO_BF16, 0, M, HD, 3 * HD};
+    Km[r] = fo_mat{base + HD * 2, FO_BF16, 0, M, HD, 3 * HD};
+    Vm[r] = fo_mat{base + 2 * HD * 2, FO_BF16, 0, M, HD, 3 * HD};
+    Om[r] = fo_mat{static_cast<char*>(o_v) + static_cast<int64_t>(r) * M * HD * 2, FO_BF16, 0, M, HD, HD};
+  }
+  fo_opts oa = o;
+  if (oa.order == FO_ORDER_NAIVE) oa.order = FO_ORDER_FLASH;  // the naive order concerns the RS step
+  FO_TRY(ag_run(ctx, X_shards, W_qkv, P, QKV, oa, s));
+  FO_TRY(attn_run(ctx, Qm, Km, Vm, P, heads, head_dim, causal, Om, &oa, s, false));
+  return rs_run(ctx, Om, W_o, P, Z, o, s);
 }
 
 }  // extern "C"

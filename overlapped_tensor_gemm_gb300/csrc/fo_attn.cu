@@ -79,7 +79,7 @@ struct AttnParams {
   uint32_t* flags;              // arrival flags, index rank*P + slice
   uint32_t* ctrl;
   int32_t wait_flags;           // 0: every slice is already in place (serial order)
-  int32_t pad;
+  int32_t ring;                 // 1: query split (K/V ring); 0: P independent problems (own slice only)
 };
 
 struct alignas(8) AttnCtl {
@@ -130,13 +130,13 @@ __device__ __forceinline__ Item decode_item(const AttnParams& p, int i) {
   return it;
 }
 
-__device__ __forceinline__ int steps_of(const AttnParams& p, int r) { return p.causal ? r + 1 : p.P; }
+__device__ __forceinline__ int steps_of(const AttnParams& p, int r) { return !p.ring ? 1 : p.causal ? r + 1 : p.P; }
 __device__ __forceinline__ int slice_of(const AttnParams& p, int r, int t) { return (r - t + p.P) % p.P; }
 __device__ __forceinline__ int blocks_of(const AttnParams& p, const Item& it, int t) {
   return (p.causal && t == 0) ? it.qb + 1 : p.nkb;
 }
 __device__ __forceinline__ int item_blocks(const AttnParams& p, const Item& it) {
-  return p.causal ? it.r * p.nkb + it.qb + 1 : p.P * p.nkb;
+  return (steps_of(p, it.r) - 1) * p.nkb + blocks_of(p, it, 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -685,14 +685,14 @@ __global__ void transpose_kernel(const uint16_t* __restrict__ v, int64_t ld, uin
 // ---------------------------------------------------------------------------
 
 fo_status attn_run(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K, const fo_mat* V, int P, int heads, int head_dim,
-                   int causal, const fo_mat* O, const fo_opts* opts_in, cudaStream_t stream) {
+                   int causal, const fo_mat* O, const fo_opts* opts_in, cudaStream_t stream, bool ring) {
   fo_opts o;
   if (opts_in) {
     o = *opts_in;
   } else {
     std::memset(&o, 0, sizeof(o));
   }
-  if (o.order != FO_ORDER_FLASH && o.order != FO_ORDER_SERIAL)
+  if (ring && o.order != FO_ORDER_FLASH && o.order != FO_ORDER_SERIAL)
     return host_fail(FO_ERR_UNSUPPORTED, "attention runs the ring order or the serial baseline");
   if (head_dim != kHd) return host_fail(FO_ERR_UNSUPPORTED, "head_dim must be 128");
   if (heads < 1) return host_fail(FO_ERR_INVALID_ARG, "heads must be positive");
@@ -712,7 +712,7 @@ fo_status attn_run(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K, const fo_mat* 
   const int64_t M = m * P;
   void *kv = nullptr, *vt = nullptr;
   fo_status st;
-  if ((st = host_buffer(ctx, 0, static_cast<size_t>(P) * M * HD * 2, &kv)) != FO_OK) return st;  // K received
+  if (ring && (st = host_buffer(ctx, 0, static_cast<size_t>(P) * M * HD * 2, &kv)) != FO_OK) return st;  // K received
   if ((st = host_buffer(ctx, 1, static_cast<size_t>(P) * P * HD * m * 2, &vt)) != FO_OK) return st;  // V^T slots
   uint32_t* flags = nullptr;
   if ((st = host_flags(ctx, &flags)) != FO_OK) return st;
@@ -740,7 +740,11 @@ fo_status attn_run(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K, const fo_mat* 
   std::memset(&p, 0, sizeof(p));
   for (int r = 0; r < P; ++r) {
     if ((st = host_encode_map(&p.maps[r], K[r].ptr, m, HD, K[r].ld, kKB)) != FO_OK) return st;
-    if ((st = host_encode_map(&p.maps[P + r], k_slot(r, 0), M, HD, HD, kKB)) != FO_OK) return st;
+    if (ring) {
+      if ((st = host_encode_map(&p.maps[P + r], k_slot(r, 0), M, HD, HD, kKB)) != FO_OK) return st;
+    } else {
+      p.maps[P + r] = p.maps[r];  // no received slices
+    }
     if ((st = host_encode_map(&p.maps[2 * P + r], vt_slot(r, 0), static_cast<int64_t>(P) * HD, m, m, kHd,
                               CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != FO_OK)
       return st;
@@ -761,6 +765,7 @@ fo_status attn_run(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K, const fo_mat* 
   p.timeout_ns = host_timeout_ns(o);
   p.flags = flags;
   p.ctrl = host_ctrl(ctx);
+  p.ring = ring ? 1 : 0;
 
   // 1) every rank lays out its own V slice transposed (slot r of its V^T buffer)
   for (int r = 0; r < P; ++r) {
@@ -770,7 +775,15 @@ fo_status attn_run(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K, const fo_mat* 
     if (cudaGetLastError() != cudaSuccess) return host_fail(FO_ERR_CUDA, "transpose launch failed");
   }
   // 2) the attention kernel, then 3) the K/V ring on the link streams, concurrently
-  //    (serial baseline: the whole ring first, then the kernel without flag waits)
+  //    (serial baseline: the whole ring first, then the kernel without flag waits);
+  //    independent problems: the kernel alone
+  if (!ring) {
+    p.wait_flags = 0;
+    attn_kernel<<<host_grid(ctx, o, p.total_items), kAttnThreads, kAttnSmem, stream>>>(p);
+    const cudaError_t le = cudaGetLastError();
+    if (le != cudaSuccess) return host_fail(FO_ERR_CUDA, cudaGetErrorString(le));
+    return FO_OK;
+  }
   const bool serial = o.order == FO_ORDER_SERIAL;
   int grid = host_grid(ctx, o, p.total_items);
   if (!serial && reserve_sms > 0 && grid > host_num_sms(ctx) - reserve_sms) grid = host_num_sms(ctx) - reserve_sms;

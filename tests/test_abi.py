@@ -40,6 +40,7 @@ def test_null_arguments_are_rejected(lib):
     assert lib.fo_ag_gemm(null, mats, mats, 2, mats, ctypes.byref(o), null) == fo.FO_ERR_INVALID_ARG
     assert b"context" in lib.fo_last_error_string()
     assert lib.fo_gemm_rs(null, mats, mats, 2, mats, ctypes.byref(o), null) == fo.FO_ERR_INVALID_ARG
+    assert lib.fo_attn_layer(null, mats, mats, mats, 2, 1, 128, 1, mats, ctypes.byref(o), null) == fo.FO_ERR_INVALID_ARG
     assert lib.fo_ctx_poll(null) == fo.FO_ERR_INVALID_ARG
     assert lib.fo_ctx_create(0, None) == fo.FO_ERR_INVALID_ARG
     assert lib.fo_ctx_destroy(null) == fo.FO_OK

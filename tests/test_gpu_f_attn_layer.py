@@ -1,0 +1,64 @@
+"""Parity of the attention block (fo_attn_layer: Flash-AG QKV projection, causal
+attention of every rank's own heads, Flash-RS output projection) against the oracle
+(FlashOverlap technical summary, section 2, architectural instantiations)."""
+import numpy as np
+import pytest
+import torch
+
+import fo_workloads as wl
+from helpers import assert_close, f64, to_bits, to_dev
+from oracle import ops
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    import overlapped_tensor_gemm_gb300 as fo
+    c = fo.Context(0)
+    yield c
+    c.close()
+
+
+def _run(ctx, P, tokens, hidden, heads, seed, causal=True, **kw):
+    inp = wl.attn_layer_inputs(P, tokens, hidden, heads, 128, seed)
+    X = [to_dev(x) for x in inp["X_shards"]]
+    Wq = [to_dev(w) for w in inp["W_qkv"]]
+    Wo = [to_dev(w) for w in inp["W_o"]]
+    m = tokens // P
+    Z = [torch.full((m, hidden), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    ctx.attn_layer(X, Wq, Wo, Z, heads=heads, causal=causal, **kw)
+    torch.cuda.synchronize()
+    ctx.poll()
+    _, _, ref = ops.attn_layer([f64(x) for x in inp["X_shards"]], [f64(w) for w in inp["W_qkv"]],
+                               [f64(w) for w in inp["W_o"]], heads, causal=causal)
+    for d in range(P):
+        assert_close(f64(to_bits(Z[d])), ref[d], f"attention block rank {d}")
+
+
+# P=2, 128-row slices: single-SM GEMM tiles, 2 attention query blocks per head;
+# P=4, 256-row slices: SM-pair GEMM tiles, 8 query blocks per head, 2 heads per rank.
+@pytest.mark.parametrize("P,tokens,hidden,heads", [(2, 256, 256, 1), (4, 1024, 1024, 2)])
+def test_attention_block_matches_oracle(ctx, P, tokens, hidden, heads):
+    _run(ctx, P, tokens, hidden, heads, 500 + P)
+
+
+@pytest.mark.parametrize("order", ["naive", "serial", "slicing"])
+def test_attention_block_baseline_orders(ctx, order):
+    _run(ctx, 2, 512, 256, 1, 510, order=order)
+
+
+def test_attention_block_non_causal(ctx):
+    _run(ctx, 2, 256, 256, 1, 520, causal=False)
+
+
+def test_attention_block_rejects_bad_shapes(ctx):
+    import overlapped_tensor_gemm_gb300 as fo
+    inp = wl.attn_layer_inputs(2, 256, 256, 1, 128, 530)
+    X = [to_dev(x) for x in inp["X_shards"]]
+    Wq = [to_dev(w) for w in inp["W_qkv"]]
+    Wo = [to_dev(w) for w in inp["W_o"]]
+    Z = [torch.empty((128, 256), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    with pytest.raises(fo.FoError) as e:
+        ctx.attn_layer(X, Wq, Wo, Z, heads=2)  # W_qkv has 3*1*128 rows, not 3*2*128
+    assert e.value.status == fo.FO_ERR_SHAPE
