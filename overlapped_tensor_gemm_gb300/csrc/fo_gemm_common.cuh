@@ -20,7 +20,12 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int tile) 
   const int tm = p.units[u0].tiles_m;
   const int tn = p.units[u0].tiles_n;
   TileCoord c;
-  if (p.mblock_major) {
+  if ((p.group_nb_major >> g) & 1) {
+    c.nb = j / (nu * tm);
+    const int rem = j - c.nb * nu * tm;
+    c.unit = u0 + rem / tm;
+    c.mb = rem % tm;
+  } else if (p.mblock_major) {
     c.mb = j / (nu * tn);
     const int rem = j - c.mb * nu * tn;
     c.unit = u0 + rem / tn;

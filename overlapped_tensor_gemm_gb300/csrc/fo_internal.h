@@ -70,6 +70,7 @@ struct GemmParams {
   int32_t num_maps;            // maps[0, num_maps) are valid
   int32_t mblock_major;        // 1: tiles of a group ordered (m-block, unit, n-block);
                                // 0: unit by unit, n-block outer, m-block inner
+  int32_t group_nb_major;      // bit g: group g ordered (n-block, unit, m-block) instead
   int32_t total_tiles;
   uint32_t epoch;
   uint64_t timeout_ns;
