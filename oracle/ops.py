@@ -28,7 +28,7 @@ import numpy as np
 
 from . import bf16
 from .ring import Ring
-from .schedule import ag_slice, rs_chunk, rs_hop
+from .schedule import a2a_block, a2a_source, ag_slice, rs_chunk, rs_hop
 
 
 def gemm(A: np.ndarray, B: np.ndarray) -> np.ndarray:
@@ -355,3 +355,105 @@ def attn_layer(X_slices, W_qkv, W_o, heads: int, causal: bool = True, decomposed
         Z = gemm_rs_definition(chunks, W_o)
     Z = [bf16.round_f64(z) for z in Z]
     return QKV, O, Z
+
+
+# --------------------------------------------------------------------------
+# Flash all-to-all (Ulysses parallelism): GEMM -> A2A and A2A -> GEMM
+# --------------------------------------------------------------------------
+
+def gemm_a2a_definition(X_slices, W):
+    """Undecomposed producer side: rank r's output X_r @ W_r^T is split into P column
+    blocks of N/P; block d belongs to rank d, which stacks the blocks by source rank.
+
+    X_slices[r] [m, K]; W[r] [N, K].  Returns Y[d] [P*m, N/P] (rows r*m.. from rank r).
+    """
+    P = len(W)
+    Nb = np.asarray(W[0]).shape[0] // P
+    return [np.concatenate([gemm(X_slices[r], np.asarray(W[r])[d * Nb:(d + 1) * Nb]) for r in range(P)])
+            for d in range(P)]
+
+
+def gemm_a2a_ring(X_slices, W, order: str = "flash", direction: int = 1, fault=None):
+    """Producer side through simulated P2P messages.  At step t rank r computes block
+    a2a_block(r, t) ('naive': block t) and sends it straight to that rank (its own block
+    stays).  Returns (Y, log); log entries (rank, step, block)."""
+    P = len(W)
+    Nb = np.asarray(W[0]).shape[0] // P
+    ring = Ring(P, direction, fault)
+    got = [dict() for _ in range(P)]
+    log = []
+    for t in range(P):
+        sent = []
+        for r in range(P):
+            d = a2a_block(r, t, P, direction) if order == "flash" else t
+            blk = gemm(X_slices[r], np.asarray(W[r])[d * Nb:(d + 1) * Nb])
+            log.append((r, t, d))
+            if d == r:
+                got[r][r] = blk
+            else:
+                ring.send_to(r, d, seq=t, item=r, payload=blk)
+                sent.append((d, r))
+        for d, r in sent:
+            got[d][r] = ring.recv(d, seq=t, item=r)
+    ring.check_drained()
+    return [np.concatenate([got[d][r] for r in range(P)]) for d in range(P)], log
+
+
+def a2a_gemm_definition(C, W):
+    """Undecomposed consumer side: rows d*m.. of every rank's C_s are rank d's K chunks;
+    rank d multiplies their column concatenation by W_d^T.
+
+    C[s] [P*m, Kc]; W[d] [N, P*Kc].  Returns Y[d] [m, N].
+    """
+    P = len(W)
+    m = np.asarray(C[0]).shape[0] // P
+    out = []
+    for d in range(P):
+        A = np.concatenate([np.asarray(C[s], np.float64)[d * m:(d + 1) * m] for s in range(P)], axis=1)
+        out.append(gemm(A, W[d]))
+    return out
+
+
+def a2a_gemm_ring(C, W, order: str = "flash", direction: int = 1, fault=None):
+    """Consumer side through simulated P2P messages.  At hop t (1..P-1) rank s sends its
+    chunk for rank d = s + t; rank d's GEMM is a sum over K chunks, one per source, folded
+    in the order a2a_source(d, t) ('flash': own chunk first, then each as it arrives) or
+    ascending source ('naive', after every hop).  Returns (Y, log); log entries
+    (rank, step, source)."""
+    P = len(W)
+    m = np.asarray(C[0]).shape[0] // P
+    Kc = np.asarray(C[0]).shape[1]
+    ring = Ring(P, direction, fault)
+    held = [{d: np.asarray(C[d], np.float64)[d * m:(d + 1) * m].copy()} for d in range(P)]
+    acc = [None] * P
+    log = []
+
+    def hop(t):
+        for s in range(P):
+            d = (s + direction * t) % P
+            ring.send_to(s, d, seq=t, item=s, payload=np.asarray(C[s], np.float64)[d * m:(d + 1) * m])
+        for d in range(P):
+            s = (d - direction * t) % P
+            held[d][s] = ring.recv(d, seq=t, item=s)
+
+    def fold(d, s, t):
+        part = gemm(held[d][s], np.asarray(W[d])[:, s * Kc:(s + 1) * Kc])
+        acc[d] = part if acc[d] is None else acc[d] + part
+        log.append((d, t, s))
+
+    if order == "flash":
+        for t in range(P):
+            if t > 0:
+                hop(t)
+            for d in range(P):
+                fold(d, a2a_source(d, t, P, direction), t)
+    elif order == "naive":
+        for t in range(1, P):
+            hop(t)
+        for t in range(P):
+            for d in range(P):
+                fold(d, t, t)
+    else:
+        raise ValueError(order)
+    ring.check_drained()
+    return acc, log

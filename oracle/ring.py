@@ -50,6 +50,14 @@ class Ring:
         self.inbox[dst].extend(msgs)
         self.log.append((src, dst, seq, item))
 
+    def send_to(self, src: int, dst: int, seq: int, item: int, payload: np.ndarray) -> None:
+        """A direct P2P message to any rank (the decomposed all-to-all's step t sends to
+        rank src + t); same tagging and fault hook as ``send``."""
+        msg = Message(seq, item, np.array(payload, copy=True))
+        msgs = [msg] if self.fault is None else self.fault(src, dst, msg)
+        self.inbox[dst].extend(msgs)
+        self.log.append((src, dst, seq, item))
+
     def recv(self, dst: int, seq: int, item: int) -> np.ndarray:
         q = self.inbox[dst]
         if not q:

@@ -8,6 +8,9 @@ Distributed LLM Training", technical summary section 2 (Methodology):
 * Flash-Reduce-Scatter decomposes the reduce-scatter into P2P steps; with
   rank-adaptive scheduling the slice that stays on the rank (needs no further
   transfer) is computed at the last step.
+* Flash All-to-All (section 2) extends the decomposition to the all-to-all of
+  Ulysses parallelism; the pages give no detail, the step orders below apply the
+  two rules above to its producer and consumer GEMMs.
 * Section 1 (Problem statement): data slicing interleaves chunks of compute and
   communication, but the communication of the last chunk cannot overlap.
 
@@ -36,6 +39,22 @@ def rs_chunk(r: int, t: int, P: int, direction: int = 1) -> int:
 def rs_chunk_naive(r: int, t: int, P: int) -> int:
     """Rank-oblivious order: every rank computes chunk t at step t."""
     return t % P
+
+
+def a2a_block(r: int, t: int, P: int, direction: int = 1) -> int:
+    """Flash all-to-all, producer side (a GEMM whose output block d belongs to rank d):
+    the block rank r computes at step t.  Remote blocks first, so each can be sent as
+    soon as it is done; the own block (no transfer) last, at t = P-1 -- the
+    rank-adaptive rule of Flash-RS applied to the all-to-all."""
+    return (r + direction * (t + 1)) % P
+
+
+def a2a_source(r: int, t: int, P: int, direction: int = 1) -> int:
+    """Flash all-to-all, consumer side (a GEMM whose K chunks come from every rank): the
+    source rank whose chunk rank r folds in at step t.  Own chunk first (no wait), then
+    the chunk that arrives at hop t (source r - t sends to r at step t) -- the
+    local-first rule of Flash-AG applied to the all-to-all."""
+    return (r - direction * t) % P
 
 
 def rs_hop(r: int, c: int, P: int, direction: int = 1) -> int:
