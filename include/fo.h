@@ -140,12 +140,14 @@ FO_API fo_status fo_ctx_poll(fo_ctx* ctx);
 FO_API fo_status fo_ctx_phase_ms(fo_ctx* ctx, float* collective_ms, float* gemm_ms);
 
 /* Launch order of the fused ring launches, for inspection (host only, no GPU):
- * op 0 = Flash-AG (order FO_ORDER_FLASH), op 1 = Flash-RS (FO_ORDER_FLASH or
- * FO_ORDER_NAIVE).  Unit i of step t is written at index t*P + i: rank[] gets
- * the rank, item[] the slice (AG) or chunk (RS) it computes.  Returns P*P, or
- * -1 on a bad argument (capacity < P*P included).  Follows the technical
- * summary's section 2: AG step 0 is the rank's own slice; RS step P-1 is the
- * rank's kept chunk. */
+ * op 0 = Flash-AG (order FO_ORDER_FLASH), op 1 = Flash-RS, op 2 = the all-to-all's
+ * producer GEMM (fo_gemm_a2a), op 3 = its consumer GEMM (fo_a2a_gemm); ops 1-3 take
+ * FO_ORDER_FLASH or FO_ORDER_NAIVE.  Unit i of step t is written at index t*P + i:
+ * rank[] gets the rank, item[] the slice (AG), chunk (RS), destination block (op 2) or
+ * source chunk (op 3) it computes.  Returns P*P, or -1 on a bad argument (capacity <
+ * P*P included).  Follows the technical summary's section 2: AG step 0 is the rank's
+ * own slice; RS step P-1 is the rank's kept chunk; the all-to-all's producer computes
+ * its own block last and its consumer its own chunk first. */
 FO_API int fo_step_order(int op, int P, int order, int32_t* rank, int32_t* item, int capacity);
 
 /* Plain GEMM on the tensor cores, C = A * B^T (no ring):
@@ -210,6 +212,31 @@ FO_API fo_status fo_mlp_layer_host(fo_ctx* ctx, const fo_mat* X_shards, const fo
 FO_API fo_status fo_qsplit_attn(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K_shards,
                          const fo_mat* V_shards, int P, int heads, int head_dim, int causal,
                          const fo_mat* O, const fo_opts* opts, void* stream);
+
+/* Flash all-to-all, producer side (technical summary section 2: Flash All-to-All,
+ * the extension of the decomposition to the all-to-all of Ulysses parallelism): a
+ * GEMM whose output blocks belong to other ranks.
+ *   X_shards[r] [m, K] bf16; W[r] [N, K] bf16, N = P*Nb; Y[d] [P*m, Nb] bf16.
+ *   Y[d][rows r*m..] = X_shards[r] W[r][rows d*Nb..]^T (rank r's block d goes to rank d).
+ * FO_ORDER_FLASH: at step t rank r computes the block of rank (r + t + 1) mod P, its
+ * own block last; each tile is stored straight into the destination's buffer (the hop
+ * is the epilogue store).  FO_ORDER_NAIVE: block t at step t.  FO_ORDER_SERIAL
+ * (baseline): the GEMM into a workspace buffer, then the all-to-all as copies. */
+FO_API fo_status fo_gemm_a2a(fo_ctx* ctx, const fo_mat* X_shards, const fo_mat* W, int P,
+                      const fo_mat* Y, const fo_opts* opts, void* stream);
+
+/* Flash all-to-all, consumer side: the all-to-all in front of a GEMM whose K
+ * dimension is split over the source ranks.
+ *   C[s] [P*m, Kc] bf16: rows d*m.. hold source s's K chunk for rank d (Kc % 64 == 0);
+ *   W[d] [N, P*Kc] bf16 (K chunk s at columns s*Kc..); Y[d] [m, N] bf16.
+ *   Y[d] = [C[0] rows d*m.. | ... | C[P-1] rows d*m..] W[d]^T.
+ * Hops: at step t (1..P-1) rank s copies its chunk for rank (s + t) mod P into that
+ * rank's receive slot and publishes an arrival flag.  FO_ORDER_FLASH: rank d folds in
+ * its own chunk first, then each received chunk as it arrives (source d-1, d-2, ...),
+ * inside one K loop.  FO_ORDER_NAIVE: chunks in ascending source order.
+ * FO_ORDER_SERIAL (baseline): every copy first, then the GEMM. */
+FO_API fo_status fo_a2a_gemm(fo_ctx* ctx, const fo_mat* C, const fo_mat* W, int P, const fo_mat* Y,
+                      const fo_opts* opts, void* stream);
 
 /* One attention block in the layout of the MLP layer (technical summary section 2:
  * the QKV projection is a column-parallel GEMM after an all-gather, the output

@@ -31,7 +31,8 @@ EPILOGUES = {"plain": 0, "silu": 1}
 # Every entry point declared in include/fo.h.
 ABI_SYMBOLS = ("fo_version", "fo_last_error_string", "fo_ctx_create", "fo_ctx_destroy", "fo_ctx_poll",
                "fo_ctx_phase_ms", "fo_gemm", "fo_ag_gemm", "fo_gemm_rs", "fo_silu_mul", "fo_mlp_layer",
-               "fo_mlp_layer_host", "fo_qsplit_attn", "fo_attn_layer", "fo_step_order", "fo_gemm_rs_noalloc")
+               "fo_mlp_layer_host", "fo_qsplit_attn", "fo_attn_layer", "fo_gemm_a2a", "fo_a2a_gemm", "fo_step_order",
+               "fo_gemm_rs_noalloc")
 
 
 class FoMat(ctypes.Structure):
@@ -73,7 +74,7 @@ def load() -> ctypes.CDLL:
         lib.fo_ctx_poll.argtypes = [vp]
         lib.fo_ctx_phase_ms.argtypes = [vp, P(ctypes.c_float), P(ctypes.c_float)]
         lib.fo_gemm.argtypes = [vp, P(FoMat), P(FoMat), P(FoMat), P(FoOpts), vp]
-        for name in ("fo_ag_gemm", "fo_gemm_rs"):
+        for name in ("fo_ag_gemm", "fo_gemm_rs", "fo_gemm_a2a", "fo_a2a_gemm"):
             getattr(lib, name).argtypes = [vp, P(FoMat), P(FoMat), ctypes.c_int, P(FoMat), P(FoOpts), vp]
         lib.fo_silu_mul.argtypes = [vp, P(FoMat), ctypes.c_int, P(FoMat), vp]
         for name in ("fo_mlp_layer", "fo_mlp_layer_host"):
@@ -193,6 +194,19 @@ class Context:
         _check(self._lib.fo_gemm_rs(self._h, _mats(X), _mats(W_row), P, _mats(Y), ctypes.byref(o),
                                     _stream(stream)))
 
+    def gemm_a2a(self, X_shards, W, Y, stream=None, **kw) -> None:
+        """Y[d][rows r*m..] = X_shards[r] W[r][rows d*Nb..]^T (the all-to-all's producer GEMM)."""
+        P = len(X_shards)
+        o = opts(**kw)
+        _check(self._lib.fo_gemm_a2a(self._h, _mats(X_shards), _mats(W), P, _mats(Y), ctypes.byref(o),
+                                     _stream(stream)))
+
+    def a2a_gemm(self, C, W, Y, stream=None, **kw) -> None:
+        """Y[d] = [C[0] rows d*m.. | ... | C[P-1] rows d*m..] W[d]^T (the all-to-all's consumer GEMM)."""
+        P = len(C)
+        o = opts(**kw)
+        _check(self._lib.fo_a2a_gemm(self._h, _mats(C), _mats(W), P, _mats(Y), ctypes.byref(o), _stream(stream)))
+
     def silu_mul(self, GU, H, stream=None) -> None:
         _check(self._lib.fo_silu_mul(self._h, _mats(GU), len(GU), _mats(H), _stream(stream)))
 
@@ -230,7 +244,7 @@ def step_order(op: str, P: int, order: str = "flash") -> list[list[tuple[int, in
     n = P * P
     rank = (ctypes.c_int32 * n)()
     item = (ctypes.c_int32 * n)()
-    got = lib.fo_step_order({"ag": 0, "rs": 1}[op], P, ORDERS[order], rank, item, n)
+    got = lib.fo_step_order({"ag": 0, "rs": 1, "gemm_a2a": 2, "a2a_gemm": 3}[op], P, ORDERS[order], rank, item, n)
     if got != n:
         raise FoError(FO_ERR_INVALID_ARG, "bad step-order request")
     return [[(rank[t * P + i], item[t * P + i]) for i in range(P)] for t in range(P)]

@@ -103,6 +103,8 @@ enum BufId : int {
   kBufHostZ,
   kBufLayerQkv,
   kBufLayerO,
+  kBufA2aRecv,
+  kBufA2aLocal,
   kBufAttnRecv,
 };
 
@@ -379,6 +381,21 @@ void rs_unit(int P, int order, int t, int i, int* rank, int* chunk) {
     *rank = mod(t + i, P);
     *chunk = mod(*rank - t - 1, P);
   }
+}
+
+//   Flash all-to-all, producer side (GEMM -> A2A): at step t rank r computes the output
+//             block of destination (r + t + 1) mod P, so its own block comes last
+//             (kept-last, as Flash-RS); naive: block t at step t.
+//   Flash all-to-all, consumer side (A2A -> GEMM): at step t rank r folds in the K chunk
+//             received from source (r - t) mod P, its own chunk first (local-first, as
+//             Flash-AG); naive: chunk t at step t.
+void a2a_block_unit(int P, int order, int t, int i, int* rank, int* block) {
+  *rank = i;
+  *block = order == FO_ORDER_NAIVE ? t : mod(i + t + 1, P);
+}
+void a2a_source_unit(int P, int order, int t, int i, int* rank, int* source) {
+  *rank = i;
+  *source = order == FO_ORDER_NAIVE ? t : mod(i - t, P);
 }
 
 char* bptr(const fo_mat& a, int64_t row) {
@@ -797,6 +814,186 @@ fo_status rs_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_
 }
 
 // --------------------------------------------------------------------------
+// Flash all-to-all (Ulysses parallelism): GEMM -> A2A and A2A -> GEMM
+// --------------------------------------------------------------------------
+
+// Y_d[rows r*m..] = X_r W_r[rows d*Nb..]^T: rank r's output block d belongs to rank d.
+// Flash / naive: one persistent launch; each unit's epilogue stores its tiles straight
+// into the destination's buffer (the hop of this all-to-all is the epilogue store), in
+// the step order of a2a_block_unit.  Serial baseline: the GEMM into a local buffer, then
+// the all-to-all as P*P copies.
+fo_status gemm_a2a_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_mat* Y, const fo_opts& o,
+                       cudaStream_t stream) {
+  const int64_t m = X[0].rows, K = X[0].cols, N = W[0].rows, M = m * P;
+  for (int r = 0; r < P; ++r) {
+    FO_TRY(check_mat(X[r], FO_BF16, "X_shards", r));
+    FO_TRY(check_mat(W[r], FO_BF16, "W", r));
+    FO_TRY(check_mat(Y[r], FO_BF16, "Y", r));
+    if (X[r].rows != m || X[r].cols != K) return fail(FO_ERR_SHAPE, "X_shards[%d] shape differs from rank 0", r);
+    if (W[r].rows != N || W[r].cols != K) return fail(FO_ERR_SHAPE, "W[%d] must be [N, K] like rank 0", r);
+  }
+  if (N % P != 0) return fail(FO_ERR_SHAPE, "N=%lld not divisible by P=%d", (long long)N, P);
+  const int64_t Nb = N / P;
+  for (int d = 0; d < P; ++d)
+    if (Y[d].rows != M || Y[d].cols != Nb) return fail(FO_ERR_SHAPE, "Y[%d] must be [P*m, N/P]", d);
+  if (K % 8 != 0) return fail(FO_ERR_UNSUPPORTED, "K=%lld must be a multiple of 8", (long long)K);
+  if (o.order == FO_ORDER_SLICING) return fail(FO_ERR_UNSUPPORTED, "no data-slicing baseline for the all-to-all");
+  if (m == 0 || Nb == 0) return FO_OK;
+  if (K == 0) return fail(FO_ERR_UNSUPPORTED, "K == 0");
+  void* flags_v = nullptr;
+  FO_TRY(ensure_buf(ctx, kBufFlags, 1 << 20, &flags_v));
+  const uint32_t epoch = ++ctx->epoch;
+  const bool serial = o.order == FO_ORDER_SERIAL;
+  char* local = nullptr;
+  if (serial) {
+    void* v = nullptr;
+    FO_TRY(ensure_buf(ctx, kBufA2aLocal, static_cast<size_t>(P) * m * N * 2, &v));
+    local = static_cast<char*>(v);
+  }
+  auto local_rank = [&](int r) { return local + static_cast<int64_t>(r) * m * N * 2; };
+  fo_status st = FO_OK;
+  Launch L;
+  int xmap[kMaxP], wmap[kMaxP];
+  for (int r = 0; r < P; ++r) {
+    xmap[r] = L.add_map(&st, X[r].ptr, m, K, X[r].ld, kBM);
+    if (st != FO_OK) return st;
+    wmap[r] = L.add_map(&st, W[r].ptr, N, K, W[r].ld, kBN);
+    if (st != FO_OK) return st;
+  }
+  for (int t = 0; t < (serial ? 1 : P); ++t) {
+    L.begin_group();
+    for (int i = 0; i < P; ++i) {
+      int r, d;
+      a2a_block_unit(P, o.order, t, i, &r, &d);
+      GemmUnit& u = L.add_unit();
+      u = blank_unit();
+      u.a_map = xmap[r];
+      u.b_map = wmap[r];
+      u.m_rows = static_cast<int32_t>(m);
+      u.k = static_cast<int32_t>(K);
+      u.epi = kEpiBF16;
+      if (serial) {  // the whole local output, all blocks
+        u.b_row0 = 0;
+        u.n_cols = static_cast<int32_t>(N);
+        u.c = local_rank(r);
+        u.ldc = N;
+      } else {
+        u.b_row0 = static_cast<int32_t>(d * Nb);
+        u.n_cols = static_cast<int32_t>(Nb);
+        u.c = bptr(Y[d], r * m);
+        u.ldc = Y[d].ld;
+      }
+    }
+  }
+  FO_TRY(L.finish(epoch, timeout_ns(o), static_cast<uint32_t*>(flags_v), ctx->ctrl, 0));
+  if (!serial) return launch_gemm(ctx, L, o, stream);
+  FO_CUDA(cudaEventRecord(ctx->ev_phase[0], stream));
+  FO_TRY(launch_gemm(ctx, L, o, stream));
+  FO_CUDA(cudaEventRecord(ctx->ev_phase[1], stream));
+  FO_TRY(fork_links(ctx, P, stream));
+  for (int t = 0; t < P; ++t) {
+    for (int r = 0; r < P; ++r) {
+      const int d = mod(r + t, P);  // t = 0: the own block, a local move
+      FO_TRY(copy_rows(bptr(Y[d], r * m), Y[d].ld, local_rank(r) + d * Nb * 2, N, m, Nb, 2, ctx->link[r]));
+    }
+  }
+  FO_TRY(join_links(ctx, P, stream));
+  FO_CUDA(cudaEventRecord(ctx->ev_phase[2], stream));
+  ctx->phase_valid = true;
+  ctx->phase_gemm_first = true;
+  return FO_OK;
+}
+
+// Y_d = [C_0 rows d*m.. | C_1 rows d*m.. | ... ] W_d^T: every source s holds, in rows
+// d*m.. of C_s, a K chunk of destination d's operand.  Hops: at step t source s copies its
+// block for destination (s + t) mod P into that rank's receive slot and publishes a
+// flag; the K-chunked GEMM folds in the own chunk first and each received chunk after its
+// flag (a2a_source_unit order).  Serial baseline: every copy first, then the GEMM.
+fo_status a2a_gemm_run(fo_ctx* ctx, const fo_mat* C, const fo_mat* W, int P, const fo_mat* Y, const fo_opts& o,
+                       cudaStream_t stream) {
+  const int64_t Mr = C[0].rows, Kc = C[0].cols, N = W[0].rows;
+  for (int r = 0; r < P; ++r) {
+    FO_TRY(check_mat(C[r], FO_BF16, "C", r));
+    FO_TRY(check_mat(W[r], FO_BF16, "W", r));
+    FO_TRY(check_mat(Y[r], FO_BF16, "Y", r));
+    if (C[r].rows != Mr || C[r].cols != Kc) return fail(FO_ERR_SHAPE, "C[%d] shape differs from rank 0", r);
+    if (W[r].rows != N || W[r].cols != P * Kc) return fail(FO_ERR_SHAPE, "W[%d] must be [N, P*Kc]", r);
+  }
+  if (Mr % P != 0) return fail(FO_ERR_SHAPE, "C rows=%lld not divisible by P=%d", (long long)Mr, P);
+  const int64_t m = Mr / P;
+  for (int d = 0; d < P; ++d)
+    if (Y[d].rows != m || Y[d].cols != N) return fail(FO_ERR_SHAPE, "Y[%d] must be [rows/P, N]", d);
+  if (Kc % kBK != 0) return fail(FO_ERR_UNSUPPORTED, "Kc=%lld must be a multiple of %d", (long long)Kc, kBK);
+  if (o.order == FO_ORDER_SLICING) return fail(FO_ERR_UNSUPPORTED, "no data-slicing baseline for the all-to-all");
+  if (m == 0 || N == 0) return FO_OK;
+  if (Kc == 0) return fail(FO_ERR_UNSUPPORTED, "Kc == 0");
+  void *flags_v = nullptr, *recv_v = nullptr;
+  FO_TRY(ensure_buf(ctx, kBufFlags, 1 << 20, &flags_v));
+  FO_TRY(ensure_buf(ctx, kBufA2aRecv, static_cast<size_t>(P) * Mr * Kc * 2, &recv_v));
+  uint32_t* flags = static_cast<uint32_t*>(flags_v);
+  auto recv = [&](int d) { return static_cast<char*>(recv_v) + static_cast<int64_t>(d) * Mr * Kc * 2; };
+  const uint32_t epoch = ++ctx->epoch;
+  const bool serial = o.order == FO_ORDER_SERIAL;
+  fo_status st = FO_OK;
+  Launch L;
+  L.begin_group();
+  for (int d = 0; d < P; ++d) {
+    const int cmap = L.add_map(&st, C[d].ptr, Mr, Kc, C[d].ld, kBM);
+    if (st != FO_OK) return st;
+    const int rmap = L.add_map(&st, recv(d), Mr, Kc, Kc, kBM);
+    if (st != FO_OK) return st;
+    const int wmap = L.add_map(&st, W[d].ptr, N, P * Kc, W[d].ld, kBN);
+    if (st != FO_OK) return st;
+    GemmUnit& u = L.add_unit();
+    u = blank_unit();
+    u.a_map = cmap;
+    u.a_row0 = static_cast<int32_t>(d * m);
+    u.a_map2 = rmap;
+    u.a2_row_stride = static_cast<int32_t>(m);
+    u.kchunk = static_cast<int32_t>(Kc);
+    u.chunk_self = d;
+    u.chunk_nsrc = P;
+    u.chunk_order = o.order == FO_ORDER_NAIVE ? 1 : 0;
+    u.chunk_flag_base = serial ? -1 : static_cast<int32_t>(kAgFlagBase + d * P);
+    u.b_map = wmap;
+    u.m_rows = static_cast<int32_t>(m);
+    u.n_cols = static_cast<int32_t>(N);
+    u.k = static_cast<int32_t>(P * Kc);
+    u.epi = kEpiBF16;
+    u.c = Y[d].ptr;
+    u.ldc = Y[d].ld;
+  }
+  FO_TRY(L.finish(epoch, timeout_ns(o), flags, ctx->ctrl, 0));
+  auto hops = [&](bool with_flags) -> fo_status {
+    for (int t = 1; t < P; ++t) {
+      for (int s = 0; s < P; ++s) {
+        const int d = mod(s + t, P);
+        if (o.fault == FO_FAULT_SKIP_HOP && with_flags && t == 1 && s == 0) continue;
+        FO_TRY(copy_rows(recv(d) + s * m * Kc * 2, Kc, bptr(C[s], d * m), C[s].ld, m, Kc, 2, ctx->link[s]));
+        if (with_flags) FO_TRY(write_flag(ctx->link[s], flags + kAgFlagBase + d * P + s, epoch));
+      }
+    }
+    return FO_OK;
+  };
+  if (serial) {
+    FO_CUDA(cudaEventRecord(ctx->ev_phase[0], stream));
+    FO_TRY(fork_links(ctx, P, stream));
+    FO_TRY(hops(false));
+    FO_TRY(join_links(ctx, P, stream));
+    FO_CUDA(cudaEventRecord(ctx->ev_phase[1], stream));
+    FO_TRY(launch_gemm(ctx, L, o, stream));
+    FO_CUDA(cudaEventRecord(ctx->ev_phase[2], stream));
+    ctx->phase_valid = true;
+    ctx->phase_gemm_first = false;
+    return FO_OK;
+  }
+  FO_TRY(fork_links(ctx, P, stream));  // the links start after the caller's prior work
+  FO_TRY(launch_gemm(ctx, L, o, stream));  // runs concurrently with the hops below
+  FO_TRY(hops(true));
+  return join_links(ctx, P, stream);
+}
+
+// --------------------------------------------------------------------------
 // MLP layer
 // --------------------------------------------------------------------------
 
@@ -928,7 +1125,7 @@ fo_status fo_ctx_poll(fo_ctx* ctx) {
 }
 
 int fo_step_order(int op, int P, int order, int32_t* rank, int32_t* item, int capacity) {
-  if (P < 1 || P > kMaxP || (op != 0 && op != 1) || !rank || !item) return -1;
+  if (P < 1 || P > kMaxP || op < 0 || op > 3 || !rank || !item) return -1;
   if (order != FO_ORDER_FLASH && order != FO_ORDER_NAIVE) return -1;
   if (op == 0 && order != FO_ORDER_FLASH) return -1;
   if (capacity < P * P) return -1;
@@ -937,8 +1134,12 @@ int fo_step_order(int op, int P, int order, int32_t* rank, int32_t* item, int ca
       int r, x;
       if (op == 0) {
         ag_unit(P, t, i, &r, &x);
-      } else {
+      } else if (op == 1) {
         rs_unit(P, order, t, i, &r, &x);
+      } else if (op == 2) {
+        a2a_block_unit(P, order, t, i, &r, &x);
+      } else {
+        a2a_source_unit(P, order, t, i, &r, &x);
       }
       rank[t * P + i] = r;
       item[t * P + i] = x;
@@ -1094,6 +1295,22 @@ fo_status fo_qsplit_attn(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K_shards, c
   FO_CUDA(cudaSetDevice(ctx->device));
   return attn_run(ctx, Q, K_shards, V_shards, P, heads, head_dim, causal, O, opts,
                   static_cast<cudaStream_t>(stream), true);
+}
+
+fo_status fo_gemm_a2a(fo_ctx* ctx, const fo_mat* X_shards, const fo_mat* W, int P, const fo_mat* Y,
+                      const fo_opts* opts, void* stream) {
+  FO_TRY(check_common(ctx, P, opts));
+  if (!X_shards || !W || !Y) return fail(FO_ERR_INVALID_ARG, "null matrix array");
+  FO_CUDA(cudaSetDevice(ctx->device));
+  return gemm_a2a_run(ctx, X_shards, W, P, Y, opts ? *opts : default_opts(), static_cast<cudaStream_t>(stream));
+}
+
+fo_status fo_a2a_gemm(fo_ctx* ctx, const fo_mat* C, const fo_mat* W, int P, const fo_mat* Y, const fo_opts* opts,
+                      void* stream) {
+  FO_TRY(check_common(ctx, P, opts));
+  if (!C || !W || !Y) return fail(FO_ERR_INVALID_ARG, "null matrix array");
+  FO_CUDA(cudaSetDevice(ctx->device));
+  return a2a_gemm_run(ctx, C, W, P, Y, opts ? *opts : default_opts(), static_cast<cudaStream_t>(stream));
 }
 
 fo_status fo_attn_layer(fo_ctx* ctx, const fo_mat* X_shards, const fo_mat* W_qkv, const fo_mat* W_o, int P,

@@ -81,15 +81,25 @@ __device__ void producer_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl)
         ok = false;
         break;
       }
+      int amap, arow, ax, bx, wait_src;
+      kblock_coords(u, kb, a_row, &amap, &arow, &ax, &bx, &wait_src);
+      if (wait_src >= 0) {  // a received K chunk: its copy must have landed
+        const int f = u.chunk_flag_base + wait_src;
+        if (!flag_wait(p.flags + f, p.epoch, p.ctrl, p.timeout_ns, kSiteAgFlag, static_cast<uint32_t>(f))) {
+          ok = false;
+          break;
+        }
+        fence_proxy_async_global();
+      }
       uint8_t* a = tiles + stage * kStageBytes;
       uint8_t* b = a + kABytes;
       mbar_arrive_expect_tx(&ctl->full[stage], kStageBytes);
-      tma_load_2d(&p.maps[u.a_map], a, &ctl->full[stage], kb * kBK, a_row);
+      tma_load_2d(&p.maps[amap], a, &ctl->full[stage], ax, arow);
       if (u.gated) {  // gate rows -> B rows [0,128), up rows -> B rows [128,256) (128-row boxes)
-        tma_load_2d(&p.maps[u.b_map], b, &ctl->full[stage], kb * kBK, b_row);
-        tma_load_2d(&p.maps[u.b_map], b + kBBytes / 2, &ctl->full[stage], kb * kBK, b_row_up);
+        tma_load_2d(&p.maps[u.b_map], b, &ctl->full[stage], bx, b_row);
+        tma_load_2d(&p.maps[u.b_map], b + kBBytes / 2, &ctl->full[stage], bx, b_row_up);
       } else {
-        tma_load_2d(&p.maps[u.b_map], b, &ctl->full[stage], kb * kBK, b_row);
+        tma_load_2d(&p.maps[u.b_map], b, &ctl->full[stage], bx, b_row);
       }
       armed |= 1u << stage;
       armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);

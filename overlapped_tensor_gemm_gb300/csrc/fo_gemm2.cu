@@ -70,12 +70,22 @@ __device__ void pair_producer(const GemmParams& p, uint8_t* tiles, PairCtl* ctl,
         ok = false;
         break;
       }
+      int amap, arow, ax, bx, wait_src;
+      kblock_coords(u, kb, a_row, &amap, &arow, &ax, &bx, &wait_src);
+      if (wait_src >= 0) {  // a received K chunk: its copy must have landed
+        const int f = u.chunk_flag_base + wait_src;
+        if (!flag_wait(p.flags + f, p.epoch, p.ctrl, p.timeout_ns, kSiteAgFlag, static_cast<uint32_t>(f))) {
+          ok = false;
+          break;
+        }
+        fence_proxy_async_global();
+      }
       uint8_t* a = tiles + stage * kPStage;
       uint8_t* b = a + kPA;
       if (cta == 0) mbar_arrive_expect_tx(&ctl->full[stage], 2 * kPStage);
       const uint32_t bar = leader_full + stage * static_cast<uint32_t>(sizeof(uint64_t));
-      tma_load_2d_pair(&p.maps[u.a_map], a, bar, kb * kBK, a_row);
-      tma_load_2d_pair(&p.maps[u.b_map], b, bar, kb * kBK, b_row);
+      tma_load_2d_pair(&p.maps[amap], a, bar, ax, arow);
+      tma_load_2d_pair(&p.maps[u.b_map], b, bar, bx, b_row);
       armed |= 1u << stage;
       armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
       if (++stage == kPairStages) {

@@ -11,6 +11,34 @@
 namespace fo {
 namespace {
 
+// Operand coordinates of K block kb of unit u.  `a_row` is the unit's A row for this
+// tile (own rows); for K-chunked units the A map, A row and K offsets follow the chunk's
+// source rank.  *wait_src >= 0: the first block of a received chunk (wait for its flag).
+__device__ __forceinline__ void kblock_coords(const GemmUnit& u, int kb, int a_row, int* amap, int* arow, int* ax,
+                                              int* bx, int* wait_src) {
+  *wait_src = -1;
+  if (u.kchunk <= 0) {
+    *amap = u.a_map;
+    *arow = a_row;
+    *ax = *bx = kb * kBK;
+    return;
+  }
+  const int cpk = u.kchunk / kBK;
+  const int ci = kb / cpk;
+  const int kk = (kb - ci * cpk) * kBK;
+  const int s = u.chunk_order == 1 ? ci : (u.chunk_self - ci + u.chunk_nsrc) % u.chunk_nsrc;
+  *ax = kk;
+  *bx = s * u.kchunk + kk;
+  if (s == u.chunk_self) {
+    *amap = u.a_map;
+    *arow = a_row;
+  } else {
+    *amap = u.a_map2;
+    *arow = a_row - u.a_row0 + s * u.a2_row_stride;
+    if (kk == 0 && u.chunk_flag_base >= 0) *wait_src = s;
+  }
+}
+
 __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int tile) {
   int g = 0;
   while (g + 1 < p.num_groups && tile >= p.group_tile_begin[g + 1]) ++g;

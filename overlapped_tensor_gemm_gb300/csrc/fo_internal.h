@@ -55,7 +55,15 @@ struct GemmUnit {
   int32_t epi;                 // EpiMode
   int32_t gated;               // 1: B tile = 128 gate rows at b_row0 + 128 up rows at b_row1 (kEpiSiluMul)
   int32_t b_row1;              // gated: row offset of the up half of B
-  int32_t pad0;
+  // K-chunked A (all-to-all consumer): K is split into chunks of `kchunk` columns, one per
+  // source rank.  Chunk 0 is the own block (a_map at a_row0); chunk ci > 0 comes from
+  // source s = (chunk_self - ci) mod chunk_nsrc (ascending s = ci when chunk_order == 1)
+  // at rows s * a2_row_stride of a_map2, after flag chunk_flag_base + s reaches `epoch`
+  // (chunk_flag_base < 0: no wait).  B's K offset of chunk ci is s * kchunk.
+  int32_t kchunk;              // 0: plain K
+  int32_t chunk_self, chunk_nsrc, chunk_order;
+  int32_t a_map2, a2_row_stride, chunk_flag_base;
+  int32_t pad1;
   void* c;                     // output
   const float* acc_in;         // fp32 partial sum to add (kEpiAdd*)
   int64_t ldc, ld_acc;         // leading dimensions in elements

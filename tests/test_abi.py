@@ -81,3 +81,22 @@ def test_library_step_order_follows_the_oracle_schedule(lib, P):
         for i, (r, c) in enumerate(rs[t]):
             assert rs[t - 1][i] == ((r - 1) % P, c)
     assert lib.fo_step_order(0, P, 1, (ctypes.c_int32 * 64)(), (ctypes.c_int32 * 64)(), 64) == -1
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 8])
+def test_library_all_to_all_order_follows_the_oracle_schedule(lib, P):
+    """The all-to-all launches' unit order (host logic, no GPU) against the oracle: the
+    producer computes its own block last, the consumer folds in its own chunk first."""
+    from oracle import schedule
+    prod = fo.step_order("gemm_a2a", P)
+    cons = fo.step_order("a2a_gemm", P)
+    for t in range(P):
+        for r, d in prod[t]:
+            assert d == schedule.a2a_block(r, t, P)
+        for r, s in cons[t]:
+            assert s == schedule.a2a_source(r, t, P)
+    for r in range(P):
+        assert prod[P - 1][r] == (r, r)
+        assert cons[0][r] == (r, r)
+        assert sorted(d for t in range(P) for rr, d in prod[t] if rr == r) == list(range(P))
+        assert sorted(s for t in range(P) for rr, s in cons[t] if rr == r) == list(range(P))

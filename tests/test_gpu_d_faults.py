@@ -57,3 +57,21 @@ def test_skipped_kv_hop_times_out_in_attention(m):
         ctx.qsplit_attn(Q, K, V, O, heads=H, head_dim=128)
         torch.cuda.synchronize()
         ctx.poll()
+
+
+def test_skipped_all_to_all_hop_times_out_and_context_recovers():
+    import overlapped_tensor_gemm_gb300 as fo
+    P, m, Kc, N = 3, 128, 64, 256
+    g = torch.Generator().manual_seed(79)
+    C = [to_dev(wl.integer_bf16(g, (P * m, Kc))) for _ in range(P)]
+    W = [to_dev(wl.integer_bf16(g, (N, P * Kc))) for _ in range(P)]
+    Y = [torch.zeros((m, N), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    with fo.Context(0) as ctx:
+        ctx.a2a_gemm(C, W, Y, fault="skip_hop", timeout_us=20000)
+        torch.cuda.synchronize()
+        with pytest.raises(fo.FoError) as e:
+            ctx.poll()
+        assert e.value.status == fo.FO_ERR_TIMEOUT
+        ctx.a2a_gemm(C, W, Y)
+        torch.cuda.synchronize()
+        ctx.poll()
