@@ -8,7 +8,7 @@ A step is one layer over one batch; inputs stay resident in HBM.  The timed
 weights (336 MiB) and activations exceed the 126 MiB L2, so no flush is used.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload llama8b|tiny|sweep1k..sweep16k|tail_rs|attn|attn1k..attn16k|attn_layer]
+                  [--workload llama8b|tiny|sweep1k..sweep16k|tail_rs|attn|attn1k..attn16k|attn_layer|a2a]
 
 With N > 1 (torchrun, one process per GPU) every rank runs an independent
 replica of the workload ("replicas only": the virtual ranks of one layer never
@@ -239,6 +239,8 @@ def run_ours(args, rank: int, world: int, device: int):
         return run_tail_rs(args, world, device, pk)
     if args.workload == "attn_layer":
         return run_attn_layer(args, world, device, pk)
+    if args.workload == "a2a":
+        return run_a2a(args, world, device, pk)
     cfg = mlp_config(args.workload)
     inp = wl.mlp_inputs(cfg)
 
@@ -547,6 +549,69 @@ def run_attn_layer(args, world, device, pk):
     return res
 
 
+def run_a2a(args, world, device, pk):
+    """Flash all-to-all, Ulysses-style: the QKV projection whose output head groups go
+    to their ranks (fo_gemm_a2a) and the output projection whose K chunks come from
+    every rank (fo_a2a_gemm), against the serial and naive orders."""
+    import torch
+    import overlapped_tensor_gemm_gb300 as fo
+    c = wl.A2A
+    P, m, H = c.P, c.m, c.hidden
+    g = torch.Generator(device="cuda")
+    g.manual_seed(c.seed)
+    rnd = lambda shape, sd=1.0: (torch.randn(shape, generator=g, device="cuda") * sd).to(torch.bfloat16)  # noqa: E731
+    X = [rnd((m, H)) for _ in range(P)]
+    Wqkv = [rnd((3 * H, H), wl.W_STD) for _ in range(P)]
+    Yq = [torch.empty((P * m, 3 * H // P), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    C = [rnd((P * m, H // P)) for _ in range(P)]
+    Wo = [rnd((H, H), wl.W_STD) for _ in range(P)]
+    Z = [torch.empty((m, H), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    ctx = fo.Context(device)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, iters):
+        for _ in range(max(args.warmup, 1)):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(iters):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ctx.poll()
+        return a.elapsed_time(b) / iters
+
+    prod = lambda o: (lambda: ctx.gemm_a2a(X, Wqkv, Yq, order=o))  # noqa: E731
+    cons = lambda o: (lambda: ctx.a2a_gemm(C, Wo, Z, order=o))  # noqa: E731
+    with ClockSampler(device) as clk:
+        t_prod = timed(prod("flash"), args.steps)
+        t_cons = timed(cons("flash"), args.steps)
+    fl = c.flops()
+    ms = t_prod + t_cons
+    tf = (fl["gemm_a2a"] + fl["a2a_gemm"]) / (ms * 1e-3) / 1e12
+    res = {"metric": "Flash all-to-all projections TFLOP/s (QKV -> A2A, A2A -> output projection)",
+           "value": round(tf, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "bf16", "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights)",
+           "config": {"workload": f"Ulysses projections, P={P}, tokens {c.tokens}, hidden {H}",
+                      "l2": "inputs larger than L2 (no flush)"},
+           "pct_of_peak": round(100 * tf / pk["bf16_burst"], 2), "clocks": clk.summary(),
+           "gemm_a2a": {"ms": round(t_prod, 4), "tflops": round(fl["gemm_a2a"] / (t_prod * 1e-3) / 1e12, 2)},
+           "a2a_gemm": {"ms": round(t_cons, 4), "tflops": round(fl["a2a_gemm"] / (t_cons * 1e-3) / 1e12, 2)}}
+    if not args.no_extras:
+        for name, fn in (("gemm_a2a", prod), ("a2a_gemm", cons)):
+            for o in ("serial", "naive"):
+                res[name][f"{o}_ms"] = round(timed(fn(o), args.steps), 4)
+            fn("serial")()
+            torch.cuda.synchronize()
+            coll, gemm_ms = ctx.phase_ms()
+            res[name]["serial_phases_ms"] = {"collective": round(coll, 4), "gemm": round(gemm_ms, 4)}
+            res[name]["exposed_ms"] = round(res[name]["ms"] - gemm_ms, 4)
+    ctx.close()
+    return res
+
+
 def run_attention_only(args, rank, world, device, pk, barrier, max_over_ranks):
     import overlapped_tensor_gemm_gb300 as fo
     ctx = fo.Context(device)
@@ -564,7 +629,7 @@ def run_attention_only(args, rank, world, device, pk, barrier, max_over_ranks):
 # --------------------------------------------------------------------------
 
 def run_reference(args):
-    cfg = mlp_config(args.workload if not args.workload.startswith("attn") else "llama8b")  # incl. attn_layer
+    cfg = mlp_config(args.workload if not (args.workload.startswith("attn") or args.workload == "a2a") else "llama8b")
     inp = wl.mlp_inputs(cfg)
     inp_f64 = decode_inputs(inp)
     per_step = max(2.0, min(20.0, 60.0 / max(1, args.steps + args.warmup)))

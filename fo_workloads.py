@@ -19,6 +19,8 @@ configurations of the build):
   in-features 28672.
 * ``attn``   -- query-split causal attention, P=4, seq 16384, 32 heads,
   head_dim 128, Q,K,V~N(0,1); ``attn1k``..``attn16k`` the same at other lengths.
+* ``a2a``    -- Flash all-to-all (Ulysses): QKV projection -> all-to-all and
+  all-to-all -> output projection, P=4, tokens 16384, hidden 4096.
 * ``attn_layer`` -- attention block (Flash-AG QKV projection, per-rank causal
   attention of the rank's heads, Flash-RS output projection), Llama-3-8B-shaped:
   P=4, tokens 4096, hidden 4096, 32 heads of 128 (8 per rank), X~N(0,1),
@@ -171,6 +173,34 @@ class AttnLayerConfig:
 
 
 ATTN_LAYER = AttnLayerConfig("attn_layer", 5, P=4, tokens=4096, hidden=4096, heads=8)
+
+
+@dataclasses.dataclass(frozen=True)
+class A2AConfig:
+    """Ulysses-style projections around attention: the QKV projection feeding the
+    all-to-all (producer, N = 3 * hidden split into P head groups) and the output
+    projection behind it (consumer, K = hidden split into P head groups)."""
+    name: str
+    index: int
+    P: int
+    tokens: int
+    hidden: int
+
+    @property
+    def seed(self) -> int:
+        return 1234 + self.index
+
+    @property
+    def m(self) -> int:
+        return self.tokens // self.P
+
+    def flops(self) -> dict:
+        prod = 2 * self.tokens * self.hidden * 3 * self.hidden
+        cons = 2 * self.tokens * self.hidden * self.hidden
+        return {"gemm_a2a": prod, "a2a_gemm": cons}
+
+
+A2A = A2AConfig("a2a", 6, P=4, tokens=16384, hidden=4096)
 
 
 def attn_sweep(seq: int) -> AttnConfig:
