@@ -173,12 +173,13 @@ fo_status ensure_buf(fo_ctx* ctx, int id, size_t bytes, void** out) {
 // --------------------------------------------------------------------------
 
 fo_status check_mat(const fo_mat& a, int32_t dtype, const char* what, int r) {
-  if (!a.ptr) return fail(FO_ERR_INVALID_ARG, "%s[%d]: null pointer", what, r);
+  if (!a.ptr && a.rows > 0 && a.cols > 0) return fail(FO_ERR_INVALID_ARG, "%s[%d]: null pointer", what, r);
   if (a.dtype != dtype)
     return fail(FO_ERR_INVALID_ARG, "%s[%d]: dtype %d, expected %d", what, r, a.dtype, dtype);
   if (a.rows < 0 || a.cols < 0 || a.ld < a.cols)
     return fail(FO_ERR_SHAPE, "%s[%d]: bad shape rows=%lld cols=%lld ld=%lld", what, r, (long long)a.rows,
                 (long long)a.cols, (long long)a.ld);
+  if (a.rows == 0 || a.cols == 0) return FO_OK;  // empty: no element is ever addressed
   if (reinterpret_cast<uintptr_t>(a.ptr) % 16 != 0)
     return fail(FO_ERR_UNSUPPORTED, "%s[%d]: pointer not 16-byte aligned", what, r);
   if ((a.ld * static_cast<int64_t>(elem_size(dtype))) % 16 != 0)
