@@ -457,3 +457,44 @@ def a2a_gemm_ring(C, W, order: str = "flash", direction: int = 1, fault=None):
         raise ValueError(order)
     ring.check_drained()
     return acc, log
+
+
+# --------------------------------------------------------------------------
+# training backward of the two projections
+# --------------------------------------------------------------------------
+
+def col_linear_backward(X_slices, W_col, dY, decomposed: bool = True):
+    """Backward of the column-parallel projection Y_r = AG(X) @ W_r^T.
+
+    The all-gather's adjoint is a reduce-scatter: dX (rank d's token slice) =
+    sum_r dY_r[rows of slice d] @ W_r, computed through the Flash-RS ring with the
+    transposed weight; dW_r = dY_r^T @ AG(X) is local.  Outputs rounded to bf16.
+    Returns (dX [P] of [m, K], dW [P] of [Nr, K]).
+    """
+    P = len(W_col)
+    Wt = [np.asarray(w, np.float64).T for w in W_col]
+    chunks = [split_chunks(np.asarray(d, np.float64), P) for d in dY]
+    if decomposed:
+        dX, _ = gemm_rs_ring(chunks, Wt)
+    else:
+        dX = gemm_rs_definition(chunks, Wt)
+    X_full = np.concatenate([np.asarray(x, np.float64) for x in X_slices])
+    dW = [gemm(np.asarray(d, np.float64).T, X_full.T) for d in dY]
+    return [bf16.round_f64(x) for x in dX], [bf16.round_f64(w) for w in dW]
+
+
+def row_linear_backward(H, W_row, dZ_slices, decomposed: bool = True):
+    """Backward of the row-parallel projection Z = RS(H_r @ W_r^T).
+
+    The reduce-scatter's adjoint is an all-gather: dH_r = AG(dZ) @ W_r, computed through
+    the Flash-AG ring with the transposed weight; dW_r = AG(dZ)^T @ H_r is local.
+    Outputs rounded to bf16.  Returns (dH [P] of [M, Fr], dW [P] of [N, Fr]).
+    """
+    Wt = [np.asarray(w, np.float64).T for w in W_row]
+    if decomposed:
+        dH, _ = ag_gemm_ring(dZ_slices, Wt)
+    else:
+        dH = ag_gemm_definition(dZ_slices, Wt)
+    dZ_full = np.concatenate([np.asarray(z, np.float64) for z in dZ_slices])
+    dW = [gemm(dZ_full.T, np.asarray(h, np.float64).T) for h in H]
+    return [bf16.round_f64(x) for x in dH], [bf16.round_f64(w) for w in dW]
