@@ -8,7 +8,7 @@ A step is one layer over one batch; inputs stay resident in HBM.  The timed
 weights (336 MiB) and activations exceed the 126 MiB L2, so no flush is used.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload llama8b|tiny|sweep1k..sweep16k|tail_rs|attn|attn1k..attn16k|attn_layer|a2a]
+                  [--workload llama8b|tiny|sweep1k..sweep16k|tail_rs|attn|attn1k..attn16k|attn_layer|a2a|mlp_bwd]
 
 With N > 1 (torchrun, one process per GPU) every rank runs an independent
 replica of the workload ("replicas only": the virtual ranks of one layer never
@@ -241,6 +241,8 @@ def run_ours(args, rank: int, world: int, device: int):
         return run_attn_layer(args, world, device, pk)
     if args.workload == "a2a":
         return run_a2a(args, world, device, pk)
+    if args.workload == "mlp_bwd":
+        return run_mlp_backward(args, world, device, pk)
     cfg = mlp_config(args.workload)
     inp = wl.mlp_inputs(cfg)
 
@@ -612,6 +614,65 @@ def run_a2a(args, world, device, pk):
     return res
 
 
+def run_mlp_backward(args, world, device, pk):
+    """Training backward of the Llama-3-8B MLP's two projections (P=4): the down
+    projection (row-parallel: dH by Flash-AG, dW local) and the gate/up projection
+    (column-parallel: dX by Flash-RS, dW local), against the serial order."""
+    import torch
+    import overlapped_tensor_gemm_gb300 as fo
+    cfg = wl.LLAMA8B
+    P, m, Hd, F = cfg.P, cfg.m, cfg.hidden, cfg.ffn // cfg.P
+    M = P * m
+    g = torch.Generator(device="cuda")
+    g.manual_seed(cfg.seed + 100)
+    rnd = lambda shape, sd=1.0: (torch.randn(shape, generator=g, device="cuda") * sd).to(torch.bfloat16)  # noqa: E731
+    X = [rnd((m, Hd)) for _ in range(P)]
+    Wc = [rnd((2 * F, Hd), wl.W_STD) for _ in range(P)]
+    dY = [rnd((M, 2 * F)) for _ in range(P)]
+    dX = [torch.empty((m, Hd), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    dWc = [torch.empty((2 * F, Hd), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    H = [rnd((M, F)) for _ in range(P)]
+    Wr = [rnd((Hd, F), wl.W_STD) for _ in range(P)]
+    dZ = [rnd((m, Hd)) for _ in range(P)]
+    dH = [torch.empty((M, F), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    dWr = [torch.empty((Hd, F), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    ctx = fo.Context(device)
+    stream = torch.cuda.current_stream()
+
+    def step(order):
+        ctx.row_linear_backward(H, Wr, dZ, dH, dWr, order=order)
+        ctx.col_linear_backward(X, Wc, dY, dX, dWc, order=order)
+
+    def timed(order, iters):
+        for _ in range(max(args.warmup, 1)):
+            step(order)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(iters):
+            step(order)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ctx.poll()
+        return a.elapsed_time(b) / iters
+
+    with ClockSampler(device) as clk:
+        ms = timed("flash", args.steps)
+    flop = 2 * (2 * M * Hd * F * P) + 2 * (2 * M * 2 * F * Hd * P)  # dH + dWr, dX + dWc
+    tf = flop / (ms * 1e-3) / 1e12
+    res = {"metric": "MLP backward TFLOP/s (dH by Flash-AG, dX by Flash-RS, local dW)", "value": round(tf, 2),
+           "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "bf16", "data": "synthetic (seeded N(0,1) activations and gradients, N(0,0.02) weights)",
+           "config": {"workload": f"llama8b MLP backward, P={P}, tokens {M}, hidden {Hd}, ffn {cfg.ffn}",
+                      "l2": "inputs larger than L2 (no flush)"},
+           "pct_of_peak": round(100 * tf / pk["bf16_burst"], 2), "clocks": clk.summary(), "flop": flop}
+    if not args.no_extras:
+        res["serial_ms"] = round(timed("serial", args.steps), 4)
+    ctx.close()
+    return res
+
+
 def run_attention_only(args, rank, world, device, pk, barrier, max_over_ranks):
     import overlapped_tensor_gemm_gb300 as fo
     ctx = fo.Context(device)
@@ -629,7 +690,8 @@ def run_attention_only(args, rank, world, device, pk, barrier, max_over_ranks):
 # --------------------------------------------------------------------------
 
 def run_reference(args):
-    cfg = mlp_config(args.workload if not (args.workload.startswith("attn") or args.workload == "a2a") else "llama8b")
+    cfg = mlp_config(args.workload if not (args.workload.startswith("attn") or args.workload in ("a2a", "mlp_bwd"))
+                     else "llama8b")
     inp = wl.mlp_inputs(cfg)
     inp_f64 = decode_inputs(inp)
     per_step = max(2.0, min(20.0, 60.0 / max(1, args.steps + args.warmup)))

@@ -238,6 +238,30 @@ FO_API fo_status fo_gemm_a2a(fo_ctx* ctx, const fo_mat* X_shards, const fo_mat* 
 FO_API fo_status fo_a2a_gemm(fo_ctx* ctx, const fo_mat* C, const fo_mat* W, int P, const fo_mat* Y,
                       const fo_opts* opts, void* stream);
 
+/* Training backward of a column-parallel projection (forward: Y[r] = AG(X) W_col[r]^T,
+ * as fo_ag_gemm).  The all-gather's adjoint is a reduce-scatter, so the input gradient is
+ * Flash-RS with the transposed weight (technical summary section 2: the same
+ * decomposed collectives; the title's training setting).
+ *   X_shards[r] [m, K]; W_col[r] [Nr, K]; dY[r] [P*m, Nr]            (inputs, bf16)
+ *   dX[d] [m, K] = sum_r dY[r][rows d*m..] W_col[r]                  (Flash-RS)
+ *   dW[r] [Nr, K] = dY[r]^T AG(X)                                     (local GEMM)
+ * Nr and P*m multiples of 8.  W_col^T, dY^T and AG(X)^T are laid out in the context's
+ * workspace by a transpose kernel; opts->order applies to the reduce-scatter. */
+FO_API fo_status fo_col_linear_backward(fo_ctx* ctx, const fo_mat* X_shards, const fo_mat* W_col,
+                                 const fo_mat* dY, int P, const fo_mat* dX, const fo_mat* dW,
+                                 const fo_opts* opts, void* stream);
+
+/* Training backward of a row-parallel projection (forward: Z = RS(H[r] W_row[r]^T), as
+ * fo_gemm_rs).  The reduce-scatter's adjoint is an all-gather: the input gradient is
+ * Flash-AG with the transposed weight.
+ *   H[r] [P*m, Fr]; W_row[r] [N, Fr]; dZ_shards[d] [m, N]            (inputs, bf16)
+ *   dH[r] [P*m, Fr] = AG(dZ) W_row[r]                                 (Flash-AG)
+ *   dW[r] [N, Fr] = AG(dZ)^T H[r]                                     (local GEMM)
+ * N and P*m multiples of 8; opts->order applies to the all-gather. */
+FO_API fo_status fo_row_linear_backward(fo_ctx* ctx, const fo_mat* H, const fo_mat* W_row,
+                                 const fo_mat* dZ_shards, int P, const fo_mat* dH, const fo_mat* dW,
+                                 const fo_opts* opts, void* stream);
+
 /* One attention block in the layout of the MLP layer (technical summary section 2:
  * the QKV projection is a column-parallel GEMM after an all-gather, the output
  * projection a row-parallel GEMM before a reduce-scatter): Flash-AG with W_qkv,

@@ -31,7 +31,8 @@ EPILOGUES = {"plain": 0, "silu": 1}
 # Every entry point declared in include/fo.h.
 ABI_SYMBOLS = ("fo_version", "fo_last_error_string", "fo_ctx_create", "fo_ctx_destroy", "fo_ctx_poll",
                "fo_ctx_phase_ms", "fo_gemm", "fo_ag_gemm", "fo_gemm_rs", "fo_silu_mul", "fo_mlp_layer",
-               "fo_mlp_layer_host", "fo_qsplit_attn", "fo_attn_layer", "fo_gemm_a2a", "fo_a2a_gemm", "fo_step_order",
+               "fo_mlp_layer_host", "fo_qsplit_attn", "fo_attn_layer", "fo_gemm_a2a", "fo_a2a_gemm", "fo_col_linear_backward",
+               "fo_row_linear_backward", "fo_step_order",
                "fo_gemm_rs_noalloc")
 
 
@@ -84,6 +85,9 @@ def load() -> ctypes.CDLL:
                                        ctypes.c_int, ctypes.c_int, P(FoMat), P(FoOpts), vp]
         lib.fo_attn_layer.argtypes = [vp, P(FoMat), P(FoMat), P(FoMat), ctypes.c_int, ctypes.c_int,
                                       ctypes.c_int, ctypes.c_int, P(FoMat), P(FoOpts), vp]
+        for name in ("fo_col_linear_backward", "fo_row_linear_backward"):
+            getattr(lib, name).argtypes = [vp, P(FoMat), P(FoMat), P(FoMat), ctypes.c_int, P(FoMat), P(FoMat),
+                                           P(FoOpts), vp]
         lib.fo_step_order.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P(ctypes.c_int32),
                                       P(ctypes.c_int32), ctypes.c_int]
         lib.fo_gemm_rs_noalloc.argtypes = [P(FoMat), P(FoMat), ctypes.c_int, P(FoMat), ctypes.c_uint32,
@@ -206,6 +210,20 @@ class Context:
         P = len(C)
         o = opts(**kw)
         _check(self._lib.fo_a2a_gemm(self._h, _mats(C), _mats(W), P, _mats(Y), ctypes.byref(o), _stream(stream)))
+
+    def col_linear_backward(self, X_shards, W_col, dY, dX, dW, stream=None, **kw) -> None:
+        """Backward of Y[r] = AG(X) W_col[r]^T: dX (token slices, Flash-RS) and dW (per rank)."""
+        P = len(X_shards)
+        o = opts(**kw)
+        _check(self._lib.fo_col_linear_backward(self._h, _mats(X_shards), _mats(W_col), _mats(dY), P, _mats(dX),
+                                                _mats(dW), ctypes.byref(o), _stream(stream)))
+
+    def row_linear_backward(self, H, W_row, dZ_shards, dH, dW, stream=None, **kw) -> None:
+        """Backward of Z = RS(H[r] W_row[r]^T): dH (Flash-AG) and dW (per rank)."""
+        P = len(H)
+        o = opts(**kw)
+        _check(self._lib.fo_row_linear_backward(self._h, _mats(H), _mats(W_row), _mats(dZ_shards), P, _mats(dH),
+                                                _mats(dW), ctypes.byref(o), _stream(stream)))
 
     def silu_mul(self, GU, H, stream=None) -> None:
         _check(self._lib.fo_silu_mul(self._h, _mats(GU), len(GU), _mats(H), _stream(stream)))

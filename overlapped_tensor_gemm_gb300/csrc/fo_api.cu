@@ -105,6 +105,9 @@ enum BufId : int {
   kBufLayerO,
   kBufA2aRecv,
   kBufA2aLocal,
+  kBufBwdWt,
+  kBufBwdAt,
+  kBufBwdBt,
   kBufAttnRecv,
 };
 
@@ -995,6 +998,121 @@ fo_status a2a_gemm_run(fo_ctx* ctx, const fo_mat* C, const fo_mat* W, int P, con
 }
 
 // --------------------------------------------------------------------------
+// Training backward of the two projections: the same collectives with the roles swapped
+// --------------------------------------------------------------------------
+
+// C[i] = A[i] B[i]^T (bf16) for i < n in one persistent launch.
+fo_status gemm_batch(fo_ctx* ctx, int n, const fo_mat* A, const fo_mat* B, const fo_mat* C, const fo_opts& o,
+                     cudaStream_t stream) {
+  Launch L;
+  fo_status st = FO_OK;
+  L.begin_group();
+  for (int i = 0; i < n; ++i) {
+    const int am = L.add_map(&st, A[i].ptr, A[i].rows, A[i].cols, A[i].ld, kBM);
+    FO_TRY(st);
+    const int bm = L.add_map(&st, B[i].ptr, B[i].rows, B[i].cols, B[i].ld, kBN);
+    FO_TRY(st);
+    GemmUnit& u = L.add_unit();
+    u = blank_unit();
+    u.a_map = am;
+    u.b_map = bm;
+    u.m_rows = static_cast<int32_t>(A[i].rows);
+    u.n_cols = static_cast<int32_t>(B[i].rows);
+    u.k = static_cast<int32_t>(A[i].cols);
+    u.epi = kEpiBF16;
+    u.c = C[i].ptr;
+    u.ldc = C[i].ld;
+  }
+  void* flags_v = nullptr;
+  FO_TRY(ensure_buf(ctx, kBufFlags, 1 << 20, &flags_v));
+  FO_TRY(L.finish(++ctx->epoch, timeout_ns(o), static_cast<uint32_t*>(flags_v), ctx->ctrl, 0));
+  return launch_gemm(ctx, L, o, stream);
+}
+
+fo_status transpose(const fo_mat& src, void* dst, int64_t dld, cudaStream_t s) {
+  FO_CUDA(launch_transpose16(src.ptr, src.ld, dst, dld, src.rows, src.cols, s));
+  return FO_OK;
+}
+
+// Column-parallel projection Y_r = AG(X) W_r^T, backward:
+//   dX (token slices) = reduce-scatter of dY_r W_r  -> Flash-RS with B = W_r^T
+//   dW_r = dY_r^T AG(X)                             -> local GEMM on transposed copies
+fo_status col_backward_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, const fo_mat* dY, int P, const fo_mat* dX,
+                           const fo_mat* dW, const fo_opts& o, cudaStream_t s) {
+  const int64_t m = X[0].rows, K = X[0].cols, Nr = W[0].rows, M = m * P;
+  for (int r = 0; r < P; ++r) {
+    FO_TRY(check_mat(X[r], FO_BF16, "X_shards", r));
+    FO_TRY(check_mat(W[r], FO_BF16, "W_col", r));
+    FO_TRY(check_mat(dY[r], FO_BF16, "dY", r));
+    FO_TRY(check_mat(dX[r], FO_BF16, "dX", r));
+    FO_TRY(check_mat(dW[r], FO_BF16, "dW", r));
+    if (X[r].rows != m || X[r].cols != K || W[r].rows != Nr || W[r].cols != K || dY[r].rows != M ||
+        dY[r].cols != Nr || dX[r].rows != m || dX[r].cols != K || dW[r].rows != Nr || dW[r].cols != K)
+      return fail(FO_ERR_SHAPE, "rank %d: need X [m, K], W_col [Nr, K], dY [P*m, Nr], dX [m, K], dW [Nr, K]", r);
+  }
+  if (Nr % 8 != 0 || M % 8 != 0) return fail(FO_ERR_UNSUPPORTED, "Nr and P*m must be multiples of 8");
+  if (m == 0 || K == 0 || Nr == 0) return FO_OK;
+  void *wt = nullptr, *at = nullptr, *bt = nullptr;
+  FO_TRY(ensure_buf(ctx, kBufBwdWt, static_cast<size_t>(P) * K * Nr * 2, &wt));
+  FO_TRY(ensure_buf(ctx, kBufBwdAt, static_cast<size_t>(P) * Nr * M * 2, &at));
+  FO_TRY(ensure_buf(ctx, kBufBwdBt, static_cast<size_t>(K) * M * 2, &bt));
+  fo_mat Wt[kMaxP], At[kMaxP], Bt[kMaxP];
+  for (int r = 0; r < P; ++r) {
+    char* w = static_cast<char*>(wt) + static_cast<int64_t>(r) * K * Nr * 2;
+    char* a = static_cast<char*>(at) + static_cast<int64_t>(r) * Nr * M * 2;
+    FO_TRY(transpose(W[r], w, Nr, s));
+    FO_TRY(transpose(dY[r], a, M, s));
+    FO_TRY(transpose(X[r], static_cast<char*>(bt) + r * m * 2, M, s));  // AG(X)^T, column block r
+    Wt[r] = fo_mat{w, FO_BF16, 0, K, Nr, Nr};
+    At[r] = fo_mat{a, FO_BF16, 0, Nr, M, M};
+    Bt[r] = fo_mat{bt, FO_BF16, 0, K, M, M};
+  }
+  FO_TRY(rs_run(ctx, dY, Wt, P, dX, o, s));
+  return gemm_batch(ctx, P, At, Bt, dW, o, s);
+}
+
+// Row-parallel projection Z = RS(H_r W_r^T), backward:
+//   dH_r = AG(dZ) W_r                 -> Flash-AG with B = W_r^T
+//   dW_r = AG(dZ)^T H_r               -> local GEMM on transposed copies
+fo_status row_backward_run(fo_ctx* ctx, const fo_mat* H, const fo_mat* W, const fo_mat* dZ, int P, const fo_mat* dH,
+                           const fo_mat* dW, const fo_opts& o, cudaStream_t s) {
+  const int64_t M = H[0].rows, Fr = H[0].cols, N = W[0].rows;
+  if (M % P != 0) return fail(FO_ERR_SHAPE, "H rows=%lld not divisible by P=%d", (long long)M, P);
+  const int64_t m = M / P;
+  for (int r = 0; r < P; ++r) {
+    FO_TRY(check_mat(H[r], FO_BF16, "H", r));
+    FO_TRY(check_mat(W[r], FO_BF16, "W_row", r));
+    FO_TRY(check_mat(dZ[r], FO_BF16, "dZ", r));
+    FO_TRY(check_mat(dH[r], FO_BF16, "dH", r));
+    FO_TRY(check_mat(dW[r], FO_BF16, "dW", r));
+    if (H[r].rows != M || H[r].cols != Fr || W[r].rows != N || W[r].cols != Fr || dZ[r].rows != m ||
+        dZ[r].cols != N || dH[r].rows != M || dH[r].cols != Fr || dW[r].rows != N || dW[r].cols != Fr)
+      return fail(FO_ERR_SHAPE, "rank %d: need H [P*m, Fr], W_row [N, Fr], dZ [m, N], dH [P*m, Fr], dW [N, Fr]", r);
+  }
+  if (N % 8 != 0 || M % 8 != 0) return fail(FO_ERR_UNSUPPORTED, "N and P*m must be multiples of 8");
+  if (m == 0 || Fr == 0 || N == 0) return FO_OK;
+  void *wt = nullptr, *at = nullptr, *bt = nullptr;
+  FO_TRY(ensure_buf(ctx, kBufBwdWt, static_cast<size_t>(P) * Fr * N * 2, &wt));
+  FO_TRY(ensure_buf(ctx, kBufBwdAt, static_cast<size_t>(N) * M * 2, &at));
+  FO_TRY(ensure_buf(ctx, kBufBwdBt, static_cast<size_t>(P) * Fr * M * 2, &bt));
+  fo_mat Wt[kMaxP], At[kMaxP], Bt[kMaxP];
+  for (int r = 0; r < P; ++r) {
+    char* w = static_cast<char*>(wt) + static_cast<int64_t>(r) * Fr * N * 2;
+    char* b = static_cast<char*>(bt) + static_cast<int64_t>(r) * Fr * M * 2;
+    FO_TRY(transpose(W[r], w, N, s));
+    FO_TRY(transpose(H[r], b, M, s));
+    FO_TRY(transpose(dZ[r], static_cast<char*>(at) + r * m * 2, M, s));  // AG(dZ)^T, column block r
+    Wt[r] = fo_mat{w, FO_BF16, 0, Fr, N, N};
+    At[r] = fo_mat{at, FO_BF16, 0, N, M, M};
+    Bt[r] = fo_mat{b, FO_BF16, 0, Fr, M, M};
+  }
+  fo_opts oa = o;
+  if (oa.order == FO_ORDER_NAIVE) oa.order = FO_ORDER_FLASH;  // the naive order concerns the RS step
+  FO_TRY(ag_run(ctx, dZ, Wt, P, dH, oa, s));
+  return gemm_batch(ctx, P, At, Bt, dW, o, s);
+}
+
+// --------------------------------------------------------------------------
 // MLP layer
 // --------------------------------------------------------------------------
 
@@ -1296,6 +1414,24 @@ fo_status fo_qsplit_attn(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K_shards, c
   FO_CUDA(cudaSetDevice(ctx->device));
   return attn_run(ctx, Q, K_shards, V_shards, P, heads, head_dim, causal, O, opts,
                   static_cast<cudaStream_t>(stream), true);
+}
+
+fo_status fo_col_linear_backward(fo_ctx* ctx, const fo_mat* X_shards, const fo_mat* W_col, const fo_mat* dY, int P,
+                                 const fo_mat* dX, const fo_mat* dW, const fo_opts* opts, void* stream) {
+  FO_TRY(check_common(ctx, P, opts));
+  if (!X_shards || !W_col || !dY || !dX || !dW) return fail(FO_ERR_INVALID_ARG, "null matrix array");
+  FO_CUDA(cudaSetDevice(ctx->device));
+  return col_backward_run(ctx, X_shards, W_col, dY, P, dX, dW, opts ? *opts : default_opts(),
+                          static_cast<cudaStream_t>(stream));
+}
+
+fo_status fo_row_linear_backward(fo_ctx* ctx, const fo_mat* H, const fo_mat* W_row, const fo_mat* dZ_shards, int P,
+                                 const fo_mat* dH, const fo_mat* dW, const fo_opts* opts, void* stream) {
+  FO_TRY(check_common(ctx, P, opts));
+  if (!H || !W_row || !dZ_shards || !dH || !dW) return fail(FO_ERR_INVALID_ARG, "null matrix array");
+  FO_CUDA(cudaSetDevice(ctx->device));
+  return row_backward_run(ctx, H, W_row, dZ_shards, P, dH, dW, opts ? *opts : default_opts(),
+                          static_cast<cudaStream_t>(stream));
 }
 
 fo_status fo_gemm_a2a(fo_ctx* ctx, const fo_mat* X_shards, const fo_mat* W, int P, const fo_mat* Y,
