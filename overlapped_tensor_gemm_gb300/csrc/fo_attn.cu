@@ -53,14 +53,23 @@ constexpr int kAttnThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 softmax
 constexpr uint32_t kTileBytes = 128 * 128 * 2;   // one 128x128 16-bit operand (two 64-column swizzle halves)
 constexpr uint32_t kHalfBytes = kTileBytes / 2;
 constexpr int kKStages = 3;              // K runs kKStages - 1 blocks ahead of V
-constexpr int kVStages = 3;
-// TMEM: S0 [0,128), S1 [128,256), O [256,384), Q [384,448).  P of a block is
-// written over the first 32 columns of each warp's 64 score columns of its S buffer.
+constexpr int kVStages = 2;
+// The P.V MMA also produces the softmax row sums: every V^T stage carries 16 extra
+// rows below its 128 head dims, the first all ones and the rest zero (written once at
+// start, never overwritten by the loads), so O gains 16 columns whose first is
+// sum_j P_ij, accumulated and rescaled exactly like the output itself.
+constexpr int kVRows = kHd + 16;
+constexpr uint32_t kVHalfBytes = kVRows * 128;           // [144 rows x 64 keys] swizzled
+constexpr uint32_t kVStageBytes = 2 * kVHalfBytes;
+// TMEM: S0 [0,128), S1 [128,256), O [256,400) (column 384 = row sum), Q [448,512).
+// P of a block is written over the first 32 columns of each warp's 64 score columns
+// of its S buffer.
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 256;
-constexpr uint32_t kQCol = 384;          // Q as packed bf16 pairs: 128 head dims in 64 columns
+constexpr uint32_t kSumCol = kOCol + kHd;
+constexpr uint32_t kQCol = 448;          // Q as packed bf16 pairs: 128 head dims in 64 columns
 constexpr uint32_t kIdescS = umma_idesc_bf16(128, 128);   // S = Q K^T, bf16 operands
-constexpr uint32_t kIdescO = umma_idesc_f16(128, 128);    // O += P V, fp16 operands
+constexpr uint32_t kIdescO = umma_idesc_f16(128, kVRows); // [O | sums] += P [V | 1 0..0], fp16
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -98,7 +107,7 @@ struct alignas(8) AttnCtl {
 // Shared memory: K stages | V^T stages | exchange | control  (Q, S, P and O live in TMEM)
 constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
-constexpr uint32_t kOffXch = kOffV + kVStages * kTileBytes;  // float [2 slots][2 halves][128 rows]
+constexpr uint32_t kOffXch = kOffV + kVStages * kVStageBytes;  // float [2 slots][2 halves][128 rows]
 constexpr uint32_t kOffCtl = kOffXch + 2 * 2 * 128 * 4;
 constexpr int kAttnSmem = static_cast<int>(kOffCtl + sizeof(AttnCtl) + 1024);
 // Every persistent kernel of this library leaves shared memory and registers of
@@ -210,10 +219,10 @@ __device__ void attn_producer(const AttnParams& p, uint8_t* smem, AttnCtl* ctl) 
     const Item& it = vit.it;
     const int s = slice_of(p, it.r, vit.t);  // arrival already observed by the K walk
     if (!mbar_wait(&ctl->v_empty[vst], vph ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty, vit.i)) return false;
-    uint8_t* vt = smem + kOffV + vst * kTileBytes;
-    mbar_arrive_expect_tx(&ctl->v_full[vst], kTileBytes);
+    uint8_t* vt = smem + kOffV + vst * kVStageBytes;
+    mbar_arrive_expect_tx(&ctl->v_full[vst], kTileBytes);  // the 128 head-dim rows of both key halves
     for (int c = 0; c < 2; ++c)
-      tma_load_2d(&p.maps[2 * p.P + it.r], vt + c * kHalfBytes, &ctl->v_full[vst], vit.kb * kKB + c * 64,
+      tma_load_2d(&p.maps[2 * p.P + it.r], vt + c * kVHalfBytes, &ctl->v_full[vst], vit.kb * kKB + c * 64,
                   (s * p.heads + it.h) * kHd);
     varmed |= 1u << vst;
     varmed_ph = (varmed_ph & ~(1u << vst)) | (vph << vst);
@@ -263,15 +272,28 @@ __device__ __forceinline__ void issue_s(uint32_t tmem_s, uint32_t tmem_q, uint32
   }
 }
 
-// O += P V for one 128-key block: P from the S buffer (keys 64h + 2c, 64h + 2c + 1 in
-// column 64h + c, c < 32), V^T from the two 64-key swizzle halves of the stage.
+// [O | sums] += P [V | 1 0..0] for one 128-key block: P from the S buffer (keys 64h + 2c,
+// 64h + 2c + 1 in column 64h + c, c < 32), V^T (and the ones row) from the two 64-key
+// swizzle halves of the stage.
 __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr, bool first) {
 #pragma unroll
   for (int k = 0; k < kKB / 16; ++k) {
-    const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
+    const uint32_t off = (k >> 2) * kVHalfBytes + (k & 3) * 32;
     umma_ts(tmem_o, tmem_p + (k >> 2) * 64 + (k & 3) * 8, umma_sdesc_sw128(v_addr + off), kIdescO,
             (first && k == 0) ? 0u : 1u);
   }
+}
+
+// One 32-bit TMEM column of this warp's 32 lanes (load waits for completion; store does too).
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+  uint32_t v;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v) : "r"(taddr) : "memory");
+  tmem_wait_ld();
+  return v;
+}
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+  tmem_wait_st();
 }
 
 // Non-blocking test of the phase of parity `parity`.
@@ -338,7 +360,7 @@ __device__ void attn_mma(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, uint3
         if (need_pv && mbar_test(&ctl->p_full[pb], (gj >> 1) & 1u) &&
             mbar_test(&ctl->v_full[vs], (gj / kVStages) & 1u)) {
           tc_fence_after();
-          issue_pv(tmem_base + kOCol, tmem_base + pb * 128, sbase + kOffV + vs * kTileBytes, j == 0);
+          issue_pv(tmem_base + kOCol, tmem_base + pb * 128, sbase + kOffV + vs * kVStageBytes, j == 0);
           umma_commit(&ctl->v_empty[vs]);
           umma_commit(&ctl->pv_done[pb]);
           need_pv = false;
@@ -469,7 +491,7 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
       nx = decode_item(p, inext);
       prefetch_row_l2(p, nx, row, hf);
     }
-    float m_ref = -INFINITY, l = 0.f;
+    float m_ref = -INFINITY;
     int j = 0;
     const int nsteps = steps_of(p, it.r);
     const int n = item_blocks(p, it);
@@ -499,21 +521,16 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
               if (static_cast<int>(col0) + k > row) s[k] = -INFINITY;
           }
         };
-        // p = 2^(s * scale - m): one packed FMA per pair, ex2 per weight, packed sums
-        auto weights = [&](const float (&s)[64], float m, uint32_t (&packed)[32]) -> float {
+        // p = 2^(s * scale - m): one packed FMA per pair, ex2 per weight (the row sums
+        // come out of the P.V MMA)
+        auto weights = [&](const float (&s)[64], float m, uint32_t (&packed)[32]) {
           const uint64_t nm2 = pack2(-m, -m);
-          uint64_t sum2 = pack2(0.f, 0.f);
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
             float x0, x1;
             unpack2(ffma2(pack2(s[2 * k], s[2 * k + 1]), c2, nm2), x0, x1);
-            const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
-            sum2 = fadd2(sum2, pack2(e0, e1));
-            packed[k] = pack_f16x2(e0, e1);
+            packed[k] = pack_f16x2(fast_exp2(x0), fast_exp2(x1));
           }
-          float s0, s1;
-          unpack2(sum2, s0, s1);
-          return s0 + s1;
         };
         float s[64];
         load_scores(s);
@@ -527,29 +544,26 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
         xch_publish(ctl, xch, xuses, q, hf, row, mx, lane);
         float other;
         uint32_t packed[32];
-        float bsum = 0.f;
         bool rescale = false;
         float alpha = 1.f;
         if (j == 0) {
           if (!xch_collect(ctl, xch, xuses, q, hf, row, &other, p, lane, i)) return;
           m_ref = fmaxf(mx, other) * p.scale_log2;  // block 0 holds key 0 <= every query: finite
-          bsum = weights(s, m_ref, packed);
+          weights(s, m_ref, packed);
         } else {
-          bsum = weights(s, m_ref, packed);
+          weights(s, m_ref, packed);
           if (!xch_collect(ctl, xch, xuses, q, hf, row, &other, p, lane, i)) return;
           const float bm = fmaxf(mx, other) * p.scale_log2;
           if (bm > m_ref + kRescaleThreshold) {
             alpha = fast_exp2(m_ref - bm);
             m_ref = bm;
-            l *= alpha;
             rescale = true;
           }
           if (__any_sync(0xffffffffu, rescale)) {
             load_scores(s);  // the scores are still in TMEM (P not yet written)
-            bsum = weights(s, m_ref, packed);
+            weights(s, m_ref, packed);
           }
         }
-        l += bsum;
         // The item's last scores are read: every score MMA of the item has completed, so
         // the next item's Q can take the TMEM Q region now, ahead of this item's end.
         if (j + 1 == n && has_next) write_q(p, ctl, nx, lane_base, row, hf, lane);
@@ -567,6 +581,10 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
             for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
             tmem_st32(lane_base + kOCol + col0 + c * 32, v);
           }
+          if (hf == 1) {  // and the row-sum column
+            const uint32_t v = tmem_ld1(lane_base + kSumCol);
+            tmem_st1(lane_base + kSumCol, __float_as_uint(__uint_as_float(v) * alpha));
+          }
         }
         // P over the first half of this warp's (already read) score columns
         tmem_st32(lane_base + sb * 128 + col0, packed);
@@ -576,14 +594,11 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
         if (lane == 0) mbar_arrive(&ctl->p_full[sb]);
       }
     }
-    // epilogue: row sum of both halves, O row / l -> bf16 (this warp's 64 columns)
-    float other_l;
-    xch_publish(ctl, xch, xuses, q, hf, row, l, lane);
-    if (!xch_collect(ctl, xch, xuses, q, hf, row, &other_l, p, lane, i)) return;
+    // epilogue: O row / row sum -> bf16 (this warp's 64 columns)
     const uint32_t glast = g + j - 1;
     if (!warp_wait(&ctl->pv_done[glast & 1u], (glast >> 1) & 1u, p, kSiteDrain, i, lane)) return;
     tc_fence_after();
-    const float inv = 1.f / (l + other_l);
+    const float inv = 1.f / __uint_as_float(tmem_ld1(lane_base + kSumCol));
     uint16_t* orow = p.out[it.r] + static_cast<int64_t>(it.qb * kQB + row) * p.ld_out[it.r] + it.h * kHd + col0;
 #pragma unroll 1
     for (int c = 0; c < 2; ++c) {
@@ -633,6 +648,15 @@ __global__ void __maxnreg__(136) attn_kernel(const __grid_constant__ AttnParams 
   }
   if (warp == 0 && lane == 0)
     for (int i = 0; i < 3 * p.P; ++i) tma_prefetch_desc(&p.maps[i]);
+  // the row-sum rows below every V^T stage half: row kHd all ones (fp16), the rest zero
+  // (a row of equal 16-byte chunks is invariant under the 128-byte swizzle)
+  for (int i = threadIdx.x; i < kVStages * 2 * 16 * 8; i += blockDim.x) {
+    const int chunk = i & 7, rrow = (i >> 3) & 15, half = i >> 7;
+    const uint32_t v = rrow == 0 ? 0x3C003C00u : 0u;
+    *reinterpret_cast<uint4*>(smem + kOffV + half * kVHalfBytes + (kHd + rrow) * 128 + chunk * 16) =
+        make_uint4(v, v, v, v);
+  }
+  fence_proxy_async_shared();
   if (warp == 1) {
     tmem_alloc(&ctl->tmem_base, kTmemCols);
     tmem_relinquish();
