@@ -388,7 +388,8 @@ __device__ void attn_mma(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, uint3
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const AttnParams& p, uint32_t site,
                                           uint32_t detail, int lane) {
   uint32_t ok = 0;
-  if (lane == 0) ok = mbar_wait(bar, parity, p.ctrl, p.timeout_ns, site, detail) ? 1u : 0u;
+  // the phase is usually complete already: test it inline before the bounded wait loop
+  if (lane == 0) ok = (mbar_try_wait(bar, parity) || mbar_wait(bar, parity, p.ctrl, p.timeout_ns, site, detail)) ? 1u : 0u;
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
