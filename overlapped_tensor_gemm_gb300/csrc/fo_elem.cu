@@ -116,6 +116,18 @@ cudaError_t launch_add_f32(const float* a, int64_t lda, const float* b, int64_t 
   return cudaGetLastError();
 }
 
+// With lazy module loading a kernel is loaded at its first launch; a helper kernel first
+// launched on a side stream while a persistent kernel that waits for its result occupies
+// the device was measured to stall until that kernel gave up.  Querying the attributes
+// loads the kernels up front.
+cudaError_t preload_helper_kernels() {
+  cudaFuncAttributes a;
+  cudaError_t e = cudaFuncGetAttributes(&a, transpose16_kernel);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, silu_mul_kernel);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, add_f32_kernel);
+  return e;
+}
+
 cudaError_t launch_transpose16(const void* src, int64_t sld, void* dst, int64_t dld, int64_t rows, int64_t cols,
                                cudaStream_t s) {
   if (rows == 0 || cols == 0) return cudaSuccess;

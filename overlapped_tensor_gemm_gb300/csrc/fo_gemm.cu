@@ -274,8 +274,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 
 int gemm_smem_bytes() { return kSmemBytes; }
 
+// Called once at context creation, before any persistent kernel runs: also loads the
+// helper kernels (see preload_helper_kernels).
 cudaError_t gemm_configure() {
-  return cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  const cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  return e != cudaSuccess ? e : preload_helper_kernels();
 }
 
 cudaError_t gemm_launch(const GemmParams& p, int grid, cudaStream_t s) {

@@ -123,6 +123,8 @@ struct SiluMulArgs {
 };
 cudaError_t launch_silu_mul(const SiluMulArgs& a, cudaStream_t s);
 // c = a + b (fp32 inputs); c is fp32 (c_f32) or bf16 (c_bf16), exactly one non-null
+// loads the helper kernels (copies, transposes, glue) before any persistent kernel runs
+cudaError_t preload_helper_kernels();
 // dst[c][r] = src[r][c] for a [rows, cols] block of 16-bit elements (leading dimensions in elements)
 cudaError_t launch_transpose16(const void* src, int64_t sld, void* dst, int64_t dld, int64_t rows, int64_t cols,
                                cudaStream_t s);
