@@ -105,9 +105,7 @@ enum BufId : int {
   kBufLayerO,
   kBufA2aRecv,
   kBufA2aLocal,
-  kBufBwdWt,
-  kBufBwdAt,
-  kBufBwdBt,
+  kBufBwdStack,
   kBufAttnRecv,
 };
 
@@ -248,10 +246,23 @@ fo_status encode_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t co
   return FO_OK;
 }
 
+// An MN-major operand stored [k_rows][mn_cols] (MN contiguous): boxes of 64 MN elements
+// (one 128-byte swizzled row) x 64 K rows.
+fo_status encode_map_mn(CUtensorMap* map, const void* ptr, int64_t k_rows, int64_t mn_cols, int64_t ld) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(mn_cols), static_cast<cuuint64_t>(k_rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
+  cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(kBK)};
+  cuuint32_t estr[2] = {1, 1};
+  FO_CU(driver()->encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
+  return FO_OK;
+}
+
 struct MapSpec {
   const void* ptr;
   int64_t rows, cols, ld;
-  int box_rows;
+  int box_rows;  // 0: MN-major map (fixed 64 x 64 boxes)
 };
 
 struct Launch {
@@ -271,6 +282,16 @@ struct Launch {
     spec[num_maps] = MapSpec{ptr, rows, cols, ld, box_rows};
     return num_maps++;
   }
+  // An operand stored transposed, [K][M or N]; the unit reading it sets its mn_major bit.
+  int add_map_mn(fo_status* st, const void* ptr, int64_t k_rows, int64_t mn_cols, int64_t ld) {
+    if (num_maps >= kMaxMaps) {
+      *st = fail(FO_ERR_UNSUPPORTED, "too many operand maps");
+      return -1;
+    }
+    *st = encode_map_mn(&p.maps[num_maps], ptr, k_rows, mn_cols, ld);
+    spec[num_maps] = MapSpec{ptr, k_rows, mn_cols, ld, 0};
+    return num_maps++;
+  }
 
   // SM-pair tiles: each CTA stages 128 rows of B (its half of the 256-wide tile), so
   // every B operand map is re-encoded with 128-row boxes.
@@ -278,7 +299,7 @@ struct Launch {
     bool is_b[kMaxMaps] = {};
     for (int u = 0; u < num_units; ++u) is_b[p.units[u].b_map] = true;
     for (int m = 0; m < num_maps; ++m) {
-      if (!is_b[m] || spec[m].box_rows == kBN / 2) continue;
+      if (!is_b[m] || spec[m].box_rows == kBN / 2 || spec[m].box_rows == 0) continue;
       FO_TRY(encode_map(&p.maps[m], spec[m].ptr, spec[m].rows, spec[m].cols, spec[m].ld, kBN / 2));
       spec[m].box_rows = kBN / 2;
     }
@@ -450,6 +471,7 @@ struct AgArgs {
   int P;
   int64_t m, K, N;
   char* recv;  // rank r's gathered copy: recv + r*M*K*2, slice s at row s*m
+  bool w_kn;   // W[r] given as [K, N] (the transposed weight of a backward pass)
 };
 
 char* ag_slot(const AgArgs& a, int r, int s, int64_t row_in_slice) {
@@ -520,6 +542,7 @@ fo_status add_ag_units(Launch& L, const AgArgs& a, const int* xmap, const int* r
         if (flash) u.wait_flag = static_cast<int32_t>(kAgFlagBase + r * P + s);
       }
       u.b_map = wmap[r];
+      u.mn_major = a.w_kn ? 2 : 0;
       u.m_rows = static_cast<int32_t>(rows);
       u.k = static_cast<int32_t>(a.K);
       if (gated_f > 0) {
@@ -538,17 +561,20 @@ fo_status add_ag_units(Launch& L, const AgArgs& a, const int* xmap, const int* r
   return FO_OK;
 }
 
+// w_kn: W[r] is given as [K, N] (read MN-major by the MMA; not with `gated`).
 fo_status ag_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_mat* Y, const fo_opts& o,
-                 cudaStream_t stream, bool gated = false) {
-  const int64_t m = X[0].rows, K = X[0].cols, N = W[0].rows, M = m * P;
+                 cudaStream_t stream, bool gated = false, bool w_kn = false) {
+  const int64_t m = X[0].rows, K = X[0].cols, N = w_kn ? W[0].cols : W[0].rows, M = m * P;
   const int64_t gated_f = gated ? N / 2 : 0;
   if (gated && N % 2 != 0) return fail(FO_ERR_SHAPE, "gated weight must have 2F rows");
+  if (gated && w_kn) return fail(FO_ERR_UNSUPPORTED, "gated projection with a transposed weight");
   for (int r = 0; r < P; ++r) {
     FO_TRY(check_mat(X[r], FO_BF16, "X_shards", r));
     FO_TRY(check_mat(W[r], FO_BF16, "W_col", r));
     FO_TRY(check_mat(Y[r], FO_BF16, "Y", r));
     if (X[r].rows != m || X[r].cols != K) return fail(FO_ERR_SHAPE, "X_shards[%d] shape differs from rank 0", r);
-    if (W[r].rows != N || W[r].cols != K) return fail(FO_ERR_SHAPE, "W_col[%d] must be [N, K] like rank 0", r);
+    if ((w_kn ? W[r].cols : W[r].rows) != N || (w_kn ? W[r].rows : W[r].cols) != K)
+      return fail(FO_ERR_SHAPE, "W_col[%d] must be %s like rank 0", r, w_kn ? "[K, N]" : "[N, K]");
     if (Y[r].rows != M || Y[r].cols != (gated ? gated_f : N))
       return fail(FO_ERR_SHAPE, "Y[%d] must be [P*m, %s]", r, gated ? "F" : "N");
   }
@@ -560,7 +586,7 @@ fo_status ag_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_
   FO_TRY(ensure_buf(ctx, kBufFlags, 1 << 20, &flags_v));
   FO_TRY(ensure_buf(ctx, kBufAgRecv, static_cast<size_t>(P) * M * K * 2, &recv_v));
   uint32_t* flags = static_cast<uint32_t*>(flags_v);
-  AgArgs a{X, W, Y, P, m, K, N, static_cast<char*>(recv_v)};
+  AgArgs a{X, W, Y, P, m, K, N, static_cast<char*>(recv_v), w_kn};
   const uint32_t epoch = ++ctx->epoch;
   const uint64_t tmo = timeout_ns(o);
 
@@ -572,7 +598,8 @@ fo_status ag_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_
       if (st != FO_OK) return st;
       rmap[r] = L.add_map(&st, ag_slot(a, r, 0, 0), M, K, K, kBM);
       if (st != FO_OK) return st;
-      wmap[r] = L.add_map(&st, W[r].ptr, N, K, W[r].ld, gated ? kBN / 2 : kBN);
+      wmap[r] = w_kn ? L.add_map_mn(&st, W[r].ptr, K, N, W[r].ld)
+                     : L.add_map(&st, W[r].ptr, N, K, W[r].ld, gated ? kBN / 2 : kBN);
       if (st != FO_OK) return st;
     }
     FO_TRY(add_ag_units(L, a, xmap, rmap, wmap, row0, rows, flash, gated_f, weight_major));
@@ -637,7 +664,13 @@ struct RsArgs {
   int64_t M, m, Kr, N;
   float* recv;  // rank r's receive slot for hop h: recv + ((r*P + h)*m)*N
   float* part;  // baselines: partial of rank r for chunk c: part + ((r*P + c)*m)*N
+  bool w_kn;    // W[r] given as [Kr, N] (the transposed weight of a backward pass)
 };
+
+int add_rs_weight(Launch& L, fo_status* st, const RsArgs& a, int r) {
+  return a.w_kn ? L.add_map_mn(st, a.W[r].ptr, a.Kr, a.N, a.W[r].ld)
+                : L.add_map(st, a.W[r].ptr, a.N, a.Kr, a.W[r].ld, kBN);
+}
 
 float* rs_slot(const RsArgs& a, float* base, int r, int h) {
   return base + (static_cast<int64_t>(r) * a.P + h) * a.m * a.N;
@@ -652,7 +685,7 @@ fo_status rs_flash(fo_ctx* ctx, const RsArgs& a, const fo_opts& o, cudaStream_t 
   for (int r = 0; r < P; ++r) {
     xmap[r] = L.add_map(&st, a.X[r].ptr, a.M, a.Kr, a.X[r].ld, kBM);
     if (st != FO_OK) return st;
-    wmap[r] = L.add_map(&st, a.W[r].ptr, a.N, a.Kr, a.W[r].ld, kBN);
+    wmap[r] = add_rs_weight(L, &st, a, r);
     if (st != FO_OK) return st;
   }
   const int64_t tm = (a.m + kBM - 1) / kBM, tn = (a.N + kBN - 1) / kBN;
@@ -665,6 +698,7 @@ fo_status rs_flash(fo_ctx* ctx, const RsArgs& a, const fo_opts& o, cudaStream_t 
     u.a_map = xmap[r];
     u.a_row0 = static_cast<int32_t>(c * a.m);
     u.b_map = wmap[r];
+    u.mn_major = a.w_kn ? 2 : 0;
     u.m_rows = static_cast<int32_t>(a.m);
     u.n_cols = static_cast<int32_t>(a.N);
     u.k = static_cast<int32_t>(a.Kr);
@@ -708,7 +742,7 @@ fo_status rs_partials(fo_ctx* ctx, const RsArgs& a, const fo_opts& o, cudaStream
   for (int r = 0; r < P; ++r) {
     xmap[r] = L.add_map(&st, a.X[r].ptr, a.M, a.Kr, a.X[r].ld, kBM);
     if (st != FO_OK) return st;
-    wmap[r] = L.add_map(&st, a.W[r].ptr, a.N, a.Kr, a.W[r].ld, kBN);
+    wmap[r] = add_rs_weight(L, &st, a, r);
     if (st != FO_OK) return st;
   }
   L.begin_group();
@@ -719,6 +753,7 @@ fo_status rs_partials(fo_ctx* ctx, const RsArgs& a, const fo_opts& o, cudaStream
       u.a_map = xmap[r];
       u.a_row0 = static_cast<int32_t>(c * a.m + row0);
       u.b_map = wmap[r];
+      u.mn_major = a.w_kn ? 2 : 0;
       u.m_rows = static_cast<int32_t>(rows);
       u.n_cols = static_cast<int32_t>(a.N);
       u.k = static_cast<int32_t>(a.Kr);
@@ -760,15 +795,17 @@ fo_status rs_ring_reduce(fo_ctx* ctx, const RsArgs& a, cudaStream_t rs, int64_t 
   return FO_OK;
 }
 
+// w_kn: W[r] is given as [Kr, N] (read MN-major by the MMA).
 fo_status rs_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_mat* Y, const fo_opts& o,
-                 cudaStream_t stream) {
-  const int64_t M = X[0].rows, Kr = X[0].cols, N = W[0].rows;
+                 cudaStream_t stream, bool w_kn = false) {
+  const int64_t M = X[0].rows, Kr = X[0].cols, N = w_kn ? W[0].cols : W[0].rows;
   for (int r = 0; r < P; ++r) {
     FO_TRY(check_mat(X[r], FO_BF16, "X", r));
     FO_TRY(check_mat(W[r], FO_BF16, "W_row", r));
     FO_TRY(check_mat(Y[r], FO_BF16, "Y", r));
     if (X[r].rows != M || X[r].cols != Kr) return fail(FO_ERR_SHAPE, "X[%d] shape differs from rank 0", r);
-    if (W[r].rows != N || W[r].cols != Kr) return fail(FO_ERR_SHAPE, "W_row[%d] must be [N, Kr] like rank 0", r);
+    if ((w_kn ? W[r].cols : W[r].rows) != N || (w_kn ? W[r].rows : W[r].cols) != Kr)
+      return fail(FO_ERR_SHAPE, "W_row[%d] must be %s like rank 0", r, w_kn ? "[Kr, N]" : "[N, Kr]");
   }
   if (M % P != 0) return fail(FO_ERR_SHAPE, "M=%lld not divisible by P=%d", (long long)M, P);
   const int64_t m = M / P;
@@ -781,7 +818,7 @@ fo_status rs_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_
   void *flags_v = nullptr, *recv_v = nullptr;
   FO_TRY(ensure_buf(ctx, kBufFlags, 1 << 20, &flags_v));
   FO_TRY(ensure_buf(ctx, kBufRsRecv, static_cast<size_t>(P) * P * m * N * 4, &recv_v));
-  RsArgs a{X, W, Y, P, M, m, Kr, N, static_cast<float*>(recv_v), nullptr};
+  RsArgs a{X, W, Y, P, M, m, Kr, N, static_cast<float*>(recv_v), nullptr, w_kn};
   uint32_t* flags = static_cast<uint32_t*>(flags_v);
   const uint32_t epoch = ++ctx->epoch;
   if (o.order == FO_ORDER_FLASH || o.order == FO_ORDER_NAIVE || P == 1) {
@@ -1001,24 +1038,28 @@ fo_status a2a_gemm_run(fo_ctx* ctx, const fo_mat* C, const fo_mat* W, int P, con
 // Training backward of the two projections: the same collectives with the roles swapped
 // --------------------------------------------------------------------------
 
-// C[i] = A[i] B[i]^T (bf16) for i < n in one persistent launch.
-fo_status gemm_batch(fo_ctx* ctx, int n, const fo_mat* A, const fo_mat* B, const fo_mat* C, const fo_opts& o,
-                     cudaStream_t stream) {
+// C[i] = A[i] B[i]^T (bf16) for i < n in one persistent launch.  a_mn: A[i] is given as
+// its transpose, [K, M]; b_mn: B[i] as [K, N] (both read MN-major by the MMA, no copy).
+fo_status gemm_batch(fo_ctx* ctx, int n, const fo_mat* A, bool a_mn, const fo_mat* B, bool b_mn, const fo_mat* C,
+                     const fo_opts& o, cudaStream_t stream) {
   Launch L;
   fo_status st = FO_OK;
   L.begin_group();
   for (int i = 0; i < n; ++i) {
-    const int am = L.add_map(&st, A[i].ptr, A[i].rows, A[i].cols, A[i].ld, kBM);
+    const int64_t M = a_mn ? A[i].cols : A[i].rows, K = a_mn ? A[i].rows : A[i].cols;
+    const int64_t N = b_mn ? B[i].cols : B[i].rows;
+    const int am = a_mn ? L.add_map_mn(&st, A[i].ptr, K, M, A[i].ld) : L.add_map(&st, A[i].ptr, M, K, A[i].ld, kBM);
     FO_TRY(st);
-    const int bm = L.add_map(&st, B[i].ptr, B[i].rows, B[i].cols, B[i].ld, kBN);
+    const int bm = b_mn ? L.add_map_mn(&st, B[i].ptr, K, N, B[i].ld) : L.add_map(&st, B[i].ptr, N, K, B[i].ld, kBN);
     FO_TRY(st);
     GemmUnit& u = L.add_unit();
     u = blank_unit();
     u.a_map = am;
     u.b_map = bm;
-    u.m_rows = static_cast<int32_t>(A[i].rows);
-    u.n_cols = static_cast<int32_t>(B[i].rows);
-    u.k = static_cast<int32_t>(A[i].cols);
+    u.mn_major = (a_mn ? 1 : 0) | (b_mn ? 2 : 0);
+    u.m_rows = static_cast<int32_t>(M);
+    u.n_cols = static_cast<int32_t>(N);
+    u.k = static_cast<int32_t>(K);
     u.epi = kEpiBF16;
     u.c = C[i].ptr;
     u.ldc = C[i].ld;
@@ -1029,14 +1070,21 @@ fo_status gemm_batch(fo_ctx* ctx, int n, const fo_mat* A, const fo_mat* B, const
   return launch_gemm(ctx, L, o, stream);
 }
 
-fo_status transpose(const fo_mat& src, void* dst, int64_t dld, cudaStream_t s) {
-  FO_CUDA(launch_transpose16(src.ptr, src.ld, dst, dld, src.rows, src.cols, s));
+// The P token slices stacked into one [P*m, cols] buffer (the operand that the weight
+// gradient contracts over all tokens).
+fo_status stack_slices(const fo_mat* S, int P, void** buf, fo_ctx* ctx, int id, cudaStream_t s) {
+  const int64_t m = S[0].rows, cols = S[0].cols;
+  FO_TRY(ensure_buf(ctx, id, static_cast<size_t>(P) * m * cols * 2, buf));
+  for (int r = 0; r < P; ++r)
+    FO_TRY(copy_rows(static_cast<char*>(*buf) + r * m * cols * 2, cols, S[r].ptr, S[r].ld, m, cols, 2, s));
   return FO_OK;
 }
 
 // Column-parallel projection Y_r = AG(X) W_r^T, backward:
-//   dX (token slices) = reduce-scatter of dY_r W_r  -> Flash-RS with B = W_r^T
-//   dW_r = dY_r^T AG(X)                             -> local GEMM on transposed copies
+//   dX (token slices) = reduce-scatter of dY_r W_r  -> Flash-RS, W_r read as the [Nr, K]
+//                                                     B^T it already is
+//   dW_r = dY_r^T AG(X)                             -> local GEMM, dY_r and the stacked X
+//                                                     read MN-major
 fo_status col_backward_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, const fo_mat* dY, int P, const fo_mat* dX,
                            const fo_mat* dW, const fo_opts& o, cudaStream_t s) {
   const int64_t m = X[0].rows, K = X[0].cols, Nr = W[0].rows, M = m * P;
@@ -1052,28 +1100,17 @@ fo_status col_backward_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, const 
   }
   if (Nr % 8 != 0 || M % 8 != 0) return fail(FO_ERR_UNSUPPORTED, "Nr and P*m must be multiples of 8");
   if (m == 0 || K == 0 || Nr == 0) return FO_OK;
-  void *wt = nullptr, *at = nullptr, *bt = nullptr;
-  FO_TRY(ensure_buf(ctx, kBufBwdWt, static_cast<size_t>(P) * K * Nr * 2, &wt));
-  FO_TRY(ensure_buf(ctx, kBufBwdAt, static_cast<size_t>(P) * Nr * M * 2, &at));
-  FO_TRY(ensure_buf(ctx, kBufBwdBt, static_cast<size_t>(K) * M * 2, &bt));
-  fo_mat Wt[kMaxP], At[kMaxP], Bt[kMaxP];
-  for (int r = 0; r < P; ++r) {
-    char* w = static_cast<char*>(wt) + static_cast<int64_t>(r) * K * Nr * 2;
-    char* a = static_cast<char*>(at) + static_cast<int64_t>(r) * Nr * M * 2;
-    FO_TRY(transpose(W[r], w, Nr, s));
-    FO_TRY(transpose(dY[r], a, M, s));
-    FO_TRY(transpose(X[r], static_cast<char*>(bt) + r * m * 2, M, s));  // AG(X)^T, column block r
-    Wt[r] = fo_mat{w, FO_BF16, 0, K, Nr, Nr};
-    At[r] = fo_mat{a, FO_BF16, 0, Nr, M, M};
-    Bt[r] = fo_mat{bt, FO_BF16, 0, K, M, M};
-  }
-  FO_TRY(rs_run(ctx, dY, Wt, P, dX, o, s));
-  return gemm_batch(ctx, P, At, Bt, dW, o, s);
+  void* xs = nullptr;
+  FO_TRY(stack_slices(X, P, &xs, ctx, kBufBwdStack, s));
+  fo_mat Xs[kMaxP];
+  for (int r = 0; r < P; ++r) Xs[r] = fo_mat{xs, FO_BF16, 0, M, K, K};
+  FO_TRY(rs_run(ctx, dY, W, P, dX, o, s, /*w_kn=*/true));
+  return gemm_batch(ctx, P, dY, /*a_mn=*/true, Xs, /*b_mn=*/true, dW, o, s);
 }
 
 // Row-parallel projection Z = RS(H_r W_r^T), backward:
-//   dH_r = AG(dZ) W_r                 -> Flash-AG with B = W_r^T
-//   dW_r = AG(dZ)^T H_r               -> local GEMM on transposed copies
+//   dH_r = AG(dZ) W_r                 -> Flash-AG, W_r read MN-major
+//   dW_r = AG(dZ)^T H_r               -> local GEMM, the stacked dZ and H_r read MN-major
 fo_status row_backward_run(fo_ctx* ctx, const fo_mat* H, const fo_mat* W, const fo_mat* dZ, int P, const fo_mat* dH,
                            const fo_mat* dW, const fo_opts& o, cudaStream_t s) {
   const int64_t M = H[0].rows, Fr = H[0].cols, N = W[0].rows;
@@ -1091,25 +1128,14 @@ fo_status row_backward_run(fo_ctx* ctx, const fo_mat* H, const fo_mat* W, const 
   }
   if (N % 8 != 0 || M % 8 != 0) return fail(FO_ERR_UNSUPPORTED, "N and P*m must be multiples of 8");
   if (m == 0 || Fr == 0 || N == 0) return FO_OK;
-  void *wt = nullptr, *at = nullptr, *bt = nullptr;
-  FO_TRY(ensure_buf(ctx, kBufBwdWt, static_cast<size_t>(P) * Fr * N * 2, &wt));
-  FO_TRY(ensure_buf(ctx, kBufBwdAt, static_cast<size_t>(N) * M * 2, &at));
-  FO_TRY(ensure_buf(ctx, kBufBwdBt, static_cast<size_t>(P) * Fr * M * 2, &bt));
-  fo_mat Wt[kMaxP], At[kMaxP], Bt[kMaxP];
-  for (int r = 0; r < P; ++r) {
-    char* w = static_cast<char*>(wt) + static_cast<int64_t>(r) * Fr * N * 2;
-    char* b = static_cast<char*>(bt) + static_cast<int64_t>(r) * Fr * M * 2;
-    FO_TRY(transpose(W[r], w, N, s));
-    FO_TRY(transpose(H[r], b, M, s));
-    FO_TRY(transpose(dZ[r], static_cast<char*>(at) + r * m * 2, M, s));  // AG(dZ)^T, column block r
-    Wt[r] = fo_mat{w, FO_BF16, 0, Fr, N, N};
-    At[r] = fo_mat{at, FO_BF16, 0, N, M, M};
-    Bt[r] = fo_mat{b, FO_BF16, 0, Fr, M, M};
-  }
+  void* zs = nullptr;
+  FO_TRY(stack_slices(dZ, P, &zs, ctx, kBufBwdStack, s));
+  fo_mat Zs[kMaxP];
+  for (int r = 0; r < P; ++r) Zs[r] = fo_mat{zs, FO_BF16, 0, M, N, N};
   fo_opts oa = o;
   if (oa.order == FO_ORDER_NAIVE) oa.order = FO_ORDER_FLASH;  // the naive order concerns the RS step
-  FO_TRY(ag_run(ctx, dZ, Wt, P, dH, oa, s));
-  return gemm_batch(ctx, P, At, Bt, dW, o, s);
+  FO_TRY(ag_run(ctx, dZ, W, P, dH, oa, s, /*gated=*/false, /*w_kn=*/true));
+  return gemm_batch(ctx, P, Zs, /*a_mn=*/true, H, /*b_mn=*/true, dW, o, s);
 }
 
 // --------------------------------------------------------------------------

@@ -65,23 +65,6 @@ __global__ void add_f32_kernel(const float* __restrict__ a, int64_t lda, const f
   }
 }
 
-// dst[c][r] = src[r][c] for a [rows, cols] 16-bit block: 64x64 tiles through shared
-// memory (coalesced reads along src rows, writes along dst rows).
-__global__ void transpose16_kernel(const uint16_t* __restrict__ src, int64_t sld, uint16_t* __restrict__ dst,
-                                   int64_t dld, int64_t rows, int64_t cols) {
-  __shared__ uint16_t tile[64][66];
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 64, c0 = static_cast<int64_t>(blockIdx.x) * 64;
-  for (int i = threadIdx.y; i < 64; i += blockDim.y) {
-    const int64_t r = r0 + i, c = c0 + threadIdx.x;
-    if (r < rows && c < cols) tile[i][threadIdx.x] = src[r * sld + c];
-  }
-  __syncthreads();
-  for (int i = threadIdx.y; i < 64; i += blockDim.y) {
-    const int64_t c = c0 + i, r = r0 + threadIdx.x;
-    if (r < rows && c < cols) dst[c * dld + r] = tile[threadIdx.x][i];
-  }
-}
-
 int sm_count() {
   static int n = 0;
   if (n == 0) {
@@ -122,20 +105,9 @@ cudaError_t launch_add_f32(const float* a, int64_t lda, const float* b, int64_t 
 // loads the kernels up front.
 cudaError_t preload_helper_kernels() {
   cudaFuncAttributes a;
-  cudaError_t e = cudaFuncGetAttributes(&a, transpose16_kernel);
-  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, silu_mul_kernel);
+  cudaError_t e = cudaFuncGetAttributes(&a, silu_mul_kernel);
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, add_f32_kernel);
   return e;
-}
-
-cudaError_t launch_transpose16(const void* src, int64_t sld, void* dst, int64_t dld, int64_t rows, int64_t cols,
-                               cudaStream_t s) {
-  if (rows == 0 || cols == 0) return cudaSuccess;
-  if ((cols + 63) / 64 > 2147483647 || (rows + 63) / 64 > 65535) return cudaErrorInvalidValue;
-  const dim3 grid(static_cast<unsigned>((cols + 63) / 64), static_cast<unsigned>((rows + 63) / 64));
-  transpose16_kernel<<<grid, dim3(64, 8), 0, s>>>(static_cast<const uint16_t*>(src), sld, static_cast<uint16_t*>(dst),
-                                                  dld, rows, cols);
-  return cudaGetLastError();
 }
 
 }  // namespace fo

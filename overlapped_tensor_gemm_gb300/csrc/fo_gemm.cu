@@ -94,8 +94,16 @@ __device__ void producer_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl)
       uint8_t* a = tiles + stage * kStageBytes;
       uint8_t* b = a + kABytes;
       mbar_arrive_expect_tx(&ctl->full[stage], kStageBytes);
-      tma_load_2d(&p.maps[amap], a, &ctl->full[stage], ax, arow);
-      if (u.gated) {  // gate rows -> B rows [0,128), up rows -> B rows [128,256) (128-row boxes)
+      if (u.mn_major & 1) {  // A stored [K][M]: x runs along M
+        for (int h = 0; h < kBM / 64; ++h)
+          tma_load_2d(&p.maps[amap], a + h * kMnBox, &ctl->full[stage], arow + h * 64, ax);
+      } else {
+        tma_load_2d(&p.maps[amap], a, &ctl->full[stage], ax, arow);
+      }
+      if (u.mn_major & 2) {  // B stored [K][N]
+        for (int h = 0; h < kBN / 64; ++h)
+          tma_load_2d(&p.maps[u.b_map], b + h * kMnBox, &ctl->full[stage], b_row + h * 64, bx);
+      } else if (u.gated) {  // gate rows -> B rows [0,128), up rows -> B rows [128,256) (128-row boxes)
         tma_load_2d(&p.maps[u.b_map], b, &ctl->full[stage], bx, b_row);
         tma_load_2d(&p.maps[u.b_map], b + kBBytes / 2, &ctl->full[stage], bx, b_row_up);
       } else {
@@ -135,6 +143,8 @@ __device__ void mma_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl, uint
     tc_fence_after();
     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
     const int nk = (u.k + kBK - 1) / kBK;
+    const bool amn = (u.mn_major & 1) != 0, bmn = (u.mn_major & 2) != 0;
+    const uint32_t idesc = kIdesc | (amn ? kIdescAMn : 0u) | (bmn ? kIdescBMn : 0u);
     for (int kb = 0; kb < nk; ++kb) {
       if (!mbar_wait(&ctl->full[stage], phase, p.ctrl, p.timeout_ns, kSiteFull, static_cast<uint32_t>(tile))) {
         ok = false;
@@ -145,8 +155,7 @@ __device__ void mma_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl, uint
       const uint32_t b_addr = a_addr + kABytes;
 #pragma unroll
       for (int k = 0; k < kBK / 16; ++k) {
-        // K advance inside the 128-byte swizzle atom: +32 bytes per UMMA_K=16
-        umma_bf16_ss(d_tmem, umma_sdesc_sw128(a_addr + k * 32), umma_sdesc_sw128(b_addr + k * 32), kIdesc,
+        umma_bf16_ss(d_tmem, operand_desc(a_addr, k, amn), operand_desc(b_addr, k, bmn), idesc,
                      (kb | k) != 0 ? 1u : 0u);
       }
       issued = true;

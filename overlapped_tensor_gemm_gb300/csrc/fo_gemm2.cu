@@ -84,8 +84,17 @@ __device__ void pair_producer(const GemmParams& p, uint8_t* tiles, PairCtl* ctl,
       uint8_t* b = a + kPA;
       if (cta == 0) mbar_arrive_expect_tx(&ctl->full[stage], 2 * kPStage);
       const uint32_t bar = leader_full + stage * static_cast<uint32_t>(sizeof(uint64_t));
-      tma_load_2d_pair(&p.maps[amap], a, bar, ax, arow);
-      tma_load_2d_pair(&p.maps[u.b_map], b, bar, bx, b_row);
+      if (u.mn_major & 1) {  // A stored [K][M]: x runs along M
+        for (int h = 0; h < kBM / 64; ++h) tma_load_2d_pair(&p.maps[amap], a + h * kMnBox, bar, arow + h * 64, ax);
+      } else {
+        tma_load_2d_pair(&p.maps[amap], a, bar, ax, arow);
+      }
+      if (u.mn_major & 2) {  // B stored [K][N]: this CTA's 128 columns
+        for (int h = 0; h < kBN / 128; ++h)
+          tma_load_2d_pair(&p.maps[u.b_map], b + h * kMnBox, bar, b_row + h * 64, bx);
+      } else {
+        tma_load_2d_pair(&p.maps[u.b_map], b, bar, bx, b_row);
+      }
       armed |= 1u << stage;
       armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
       if (++stage == kPairStages) {
@@ -123,6 +132,8 @@ __device__ void pair_mma(const GemmParams& p, uint8_t* tiles, PairCtl* ctl, uint
     tc_fence_after();
     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
     const int nk = (u.k + kBK - 1) / kBK;
+    const bool amn = (u.mn_major & 1) != 0, bmn = (u.mn_major & 2) != 0;
+    const uint32_t idesc = kPIdesc | (amn ? kIdescAMn : 0u) | (bmn ? kIdescBMn : 0u);
     for (int kb = 0; kb < nk; ++kb) {
       if (!mbar_wait(&ctl->full[stage], phase, p.ctrl, p.timeout_ns, kSiteFull, static_cast<uint32_t>(tile))) {
         ok = false;
@@ -133,7 +144,7 @@ __device__ void pair_mma(const GemmParams& p, uint8_t* tiles, PairCtl* ctl, uint
       const uint32_t b_addr = a_addr + kPA;
 #pragma unroll
       for (int k = 0; k < kBK / 16; ++k) {
-        umma_bf16_pair(d_tmem, umma_sdesc_sw128(a_addr + k * 32), umma_sdesc_sw128(b_addr + k * 32), kPIdesc,
+        umma_bf16_pair(d_tmem, operand_desc(a_addr, k, amn), operand_desc(b_addr, k, bmn), idesc,
                        (kb | k) != 0 ? 1u : 0u);
       }
       issued = true;

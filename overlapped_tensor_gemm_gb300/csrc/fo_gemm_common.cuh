@@ -39,6 +39,18 @@ __device__ __forceinline__ void kblock_coords(const GemmUnit& u, int kb, int a_r
   }
 }
 
+// An MN-major operand block in shared memory: `nblk` boxes of 64 MN elements (one
+// 128-byte swizzled row per K index) x 64 K rows, kMnBox bytes apart.
+constexpr uint32_t kMnBox = 64 * kBK * 2;
+constexpr uint32_t kIdescAMn = 1u << 15;  // instruction descriptor: A is MN-major
+constexpr uint32_t kIdescBMn = 1u << 16;  // B is MN-major
+
+// Shared-memory descriptor of the K=16 slice k of a staged operand: K-major atoms
+// advance 32 bytes inside the 128-byte row, MN-major ones by two 8-row groups.
+__device__ __forceinline__ uint64_t operand_desc(uint32_t addr, int k, bool mn) {
+  return mn ? umma_sdesc_sw128_mn(addr + k * 2048, kMnBox) : umma_sdesc_sw128(addr + k * 32);
+}
+
 __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int tile) {
   int g = 0;
   while (g + 1 < p.num_groups && tile >= p.group_tile_begin[g + 1]) ++g;

@@ -63,7 +63,10 @@ struct GemmUnit {
   int32_t kchunk;              // 0: plain K
   int32_t chunk_self, chunk_nsrc, chunk_order;
   int32_t a_map2, a2_row_stride, chunk_flag_base;
-  int32_t pad1;
+  // Operand orientation: bit 0 set: A is stored [K][M] (M contiguous), bit 1 set: B is
+  // stored [K][N] (a transposed weight).  Such operands are staged as 64 (M or N) x 64 (K)
+  // boxes, one per 64-wide block, and read by the MMA as MN-major (no K chunks, no gating).
+  int32_t mn_major;
   void* c;                     // output
   const float* acc_in;         // fp32 partial sum to add (kEpiAdd*)
   int64_t ldc, ld_acc;         // leading dimensions in elements
@@ -122,12 +125,9 @@ struct SiluMulArgs {
   int32_t P;
 };
 cudaError_t launch_silu_mul(const SiluMulArgs& a, cudaStream_t s);
-// c = a + b (fp32 inputs); c is fp32 (c_f32) or bf16 (c_bf16), exactly one non-null
-// loads the helper kernels (copies, transposes, glue) before any persistent kernel runs
+// loads the helper kernels (glue, reduce adds) before any persistent kernel runs
 cudaError_t preload_helper_kernels();
-// dst[c][r] = src[r][c] for a [rows, cols] block of 16-bit elements (leading dimensions in elements)
-cudaError_t launch_transpose16(const void* src, int64_t sld, void* dst, int64_t dld, int64_t rows, int64_t cols,
-                               cudaStream_t s);
+// c = a + b (fp32 inputs); c is fp32 (c_f32) or bf16 (c_bf16), exactly one non-null
 cudaError_t launch_add_f32(const float* a, int64_t lda, const float* b, int64_t ldb, float* c_f32,
                            uint16_t* c_bf16, int64_t ldc, int64_t rows, int64_t cols, cudaStream_t s);
 

@@ -77,3 +77,18 @@ def test_row_parallel_backward_integer_exact(ctx, P, m, Fr, N, order):
 def test_backward_gaussian(ctx):
     _col(ctx, 4, 512, 1024, 768, 840, False)
     _row(ctx, 4, 512, 768, 1024, 841, False)
+
+
+def test_single_sm_tiles_match(ctx):
+    # both operands of the weight-gradient GEMM and the weight of the collective GEMM are
+    # read MN-major; the single-SM kernel stages 128-wide A and 256-wide B blocks of them
+    _col(ctx, 4, 256, 384, 512, 850, True, single_sm=True)
+    _row(ctx, 4, 256, 384, 512, 851, True, single_sm=True)
+
+
+@pytest.mark.parametrize("P,m,K,Nr", [(2, 256, 72, 264), (2, 128, 520, 8)])
+def test_ragged_transposed_operands(ctx, P, m, K, Nr):
+    # MN extents that end inside a 64-wide box (the box's tail reads zeros) and one block
+    # of only 8 columns
+    _col(ctx, P, m, K, Nr, 860 + K, True)
+    _row(ctx, P, m, Nr, K, 870 + K, True)
