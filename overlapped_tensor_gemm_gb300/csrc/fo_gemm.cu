@@ -60,6 +60,7 @@ __device__ void producer_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl)
   uint32_t armed_phase = 0;  // bit s: phase parity of the last arming of stage s
   int waited_unit = -1;
   bool ok = true;
+  const int mn = p.mn_major & 3;
   for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
     const TileCoord tc = decode_tile(p, tile);
     const GemmUnit& u = p.units[tc.unit];
@@ -73,41 +74,52 @@ __device__ void producer_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl)
     }
     const int nk = (u.k + kBK - 1) / kBK;
     const int a_row = u.a_row0 + tc.mb * kBM;
-    const int b_row = u.b_row0 + tc.nb * (u.gated ? kBN / 2 : kBN);
+    const bool gated = u.gated != 0;
+    const int b_row = u.b_row0 + tc.nb * (gated ? kBN / 2 : kBN);
     const int b_row_up = u.b_row1 + tc.nb * (kBN / 2);
+    // per-tile values in registers: the k loop below re-reads nothing from the parameters
+    const bool chunked = u.kchunk > 0;
+    const CUtensorMap* amap0 = &p.maps[u.a_map];
+    const CUtensorMap* bmap = &p.maps[u.b_map];
     for (int kb = 0; kb < nk; ++kb) {
-      if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty,
-                     static_cast<uint32_t>(tile))) {
+      if (!mbar_try_wait(&ctl->empty[stage], phase ^ 1u) &&
+          !mbar_wait(&ctl->empty[stage], phase ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty, static_cast<uint32_t>(tile))) {
         ok = false;
         break;
       }
-      int amap, arow, ax, bx, wait_src;
-      kblock_coords(u, kb, a_row, &amap, &arow, &ax, &bx, &wait_src);
-      if (wait_src >= 0) {  // a received K chunk: its copy must have landed
-        const int f = u.chunk_flag_base + wait_src;
-        if (!flag_wait(p.flags + f, p.epoch, p.ctrl, p.timeout_ns, kSiteAgFlag, static_cast<uint32_t>(f))) {
-          ok = false;
-          break;
+      const CUtensorMap* amap = amap0;
+      int arow = a_row, ax = kb * kBK, bx = kb * kBK;
+      if (chunked) {
+        int am, wait_src;
+        kblock_coords(u, kb, a_row, &am, &arow, &ax, &bx, &wait_src);
+        amap = &p.maps[am];
+        if (wait_src >= 0) {  // a received K chunk: its copy must have landed
+          const int f = u.chunk_flag_base + wait_src;
+          if (!flag_wait(p.flags + f, p.epoch, p.ctrl, p.timeout_ns, kSiteAgFlag, static_cast<uint32_t>(f))) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();
         }
-        fence_proxy_async_global();
       }
       uint8_t* a = tiles + stage * kStageBytes;
       uint8_t* b = a + kABytes;
-      mbar_arrive_expect_tx(&ctl->full[stage], kStageBytes);
-      if (u.mn_major & 1) {  // A stored [K][M]: x runs along M
-        for (int h = 0; h < kBM / 64; ++h)
-          tma_load_2d(&p.maps[amap], a + h * kMnBox, &ctl->full[stage], arow + h * 64, ax);
+      uint64_t* bar = &ctl->full[stage];
+      mbar_arrive_expect_tx(bar, kStageBytes);
+      if (mn & 1) {  // A stored [K][M]: x runs along M
+        tma_load_2d(amap, a, bar, arow, ax);
+        tma_load_2d(amap, a + kMnBox, bar, arow + 64, ax);
       } else {
-        tma_load_2d(&p.maps[amap], a, &ctl->full[stage], ax, arow);
+        tma_load_2d(amap, a, bar, ax, arow);
       }
-      if (u.mn_major & 2) {  // B stored [K][N]
-        for (int h = 0; h < kBN / 64; ++h)
-          tma_load_2d(&p.maps[u.b_map], b + h * kMnBox, &ctl->full[stage], b_row + h * 64, bx);
-      } else if (u.gated) {  // gate rows -> B rows [0,128), up rows -> B rows [128,256) (128-row boxes)
-        tma_load_2d(&p.maps[u.b_map], b, &ctl->full[stage], bx, b_row);
-        tma_load_2d(&p.maps[u.b_map], b + kBBytes / 2, &ctl->full[stage], bx, b_row_up);
+      if (mn & 2) {  // B stored [K][N]
+#pragma unroll
+        for (int h = 0; h < kBN / 64; ++h) tma_load_2d(bmap, b + h * kMnBox, bar, b_row + h * 64, bx);
+      } else if (gated) {  // gate rows -> B rows [0,128), up rows -> B rows [128,256) (128-row boxes)
+        tma_load_2d(bmap, b, bar, bx, b_row);
+        tma_load_2d(bmap, b + kBBytes / 2, bar, bx, b_row_up);
       } else {
-        tma_load_2d(&p.maps[u.b_map], b, &ctl->full[stage], bx, b_row);
+        tma_load_2d(bmap, b, bar, bx, b_row);
       }
       armed |= 1u << stage;
       armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
@@ -124,7 +136,11 @@ __device__ void producer_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl)
   }
 }
 
+// The operand orientation is a template argument: the instruction descriptor stays a
+// compile-time constant and the K loop carries no per-block dispatch.
+template <bool AMN, bool BMN>
 __device__ void mma_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl, uint32_t tmem_base) {
+  constexpr uint32_t idesc = kIdesc | (AMN ? kIdescAMn : 0u) | (BMN ? kIdescBMn : 0u);
   int stage = 0;
   uint32_t phase = 0;
   int acc = 0;
@@ -143,8 +159,6 @@ __device__ void mma_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl, uint
     tc_fence_after();
     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
     const int nk = (u.k + kBK - 1) / kBK;
-    const bool amn = (u.mn_major & 1) != 0, bmn = (u.mn_major & 2) != 0;
-    const uint32_t idesc = kIdesc | (amn ? kIdescAMn : 0u) | (bmn ? kIdescBMn : 0u);
     for (int kb = 0; kb < nk; ++kb) {
       if (!mbar_wait(&ctl->full[stage], phase, p.ctrl, p.timeout_ns, kSiteFull, static_cast<uint32_t>(tile))) {
         ok = false;
@@ -155,7 +169,8 @@ __device__ void mma_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl, uint
       const uint32_t b_addr = a_addr + kABytes;
 #pragma unroll
       for (int k = 0; k < kBK / 16; ++k) {
-        umma_bf16_ss(d_tmem, operand_desc(a_addr, k, amn), operand_desc(b_addr, k, bmn), idesc,
+        // K advance inside the swizzle atom: +32 bytes (K-major) or two 8-row groups (MN-major)
+        umma_bf16_ss(d_tmem, operand_desc(a_addr, k, AMN), operand_desc(b_addr, k, BMN), idesc,
                      (kb | k) != 0 ? 1u : 0u);
       }
       issued = true;
@@ -265,7 +280,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   if (warp == 0) {
     if (lane == 0) producer_loop(p, tiles, ctl);
   } else if (warp == 1) {
-    if (lane == 0) mma_loop(p, tiles, ctl, tmem_base);
+    if (lane == 0) {
+      switch (p.mn_major & 3) {
+        case 0: mma_loop<false, false>(p, tiles, ctl, tmem_base); break;
+        case 2: mma_loop<false, true>(p, tiles, ctl, tmem_base); break;
+        case 3: mma_loop<true, true>(p, tiles, ctl, tmem_base); break;
+        default: mma_loop<true, false>(p, tiles, ctl, tmem_base); break;
+      }
+    }
     __syncwarp();
   } else {
     epilogue_loop(p, ctl, tmem_base, warp, lane);

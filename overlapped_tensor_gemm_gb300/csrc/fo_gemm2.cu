@@ -49,6 +49,7 @@ __device__ void pair_producer(const GemmParams& p, uint8_t* tiles, PairCtl* ctl,
   uint32_t phase = 0, armed = 0, armed_phase = 0;
   int waited_unit = -1;
   bool ok = true;
+  const int mn = p.mn_major & 3;
   for (int tile = cluster; ok && tile < p.total_tiles; tile += nclusters) {
     const TileCoord tc = decode_tile(p, tile);
     const GemmUnit& u = p.units[tc.unit];
@@ -64,36 +65,51 @@ __device__ void pair_producer(const GemmParams& p, uint8_t* tiles, PairCtl* ctl,
     // B rows of this CTA: gated tiles put the gate rows in the leader and the up rows in the peer
     const int b_row = u.gated ? (cta == 0 ? u.b_row0 : u.b_row1) + tc.nb * (kBN / 2)
                               : u.b_row0 + tc.nb * kBN + static_cast<int>(cta) * (kBN / 2);
+    // per-tile values in registers: the k loop below re-reads nothing from the parameters
+    const bool chunked = u.kchunk > 0;
+    const CUtensorMap* amap0 = &p.maps[u.a_map];
+    const CUtensorMap* bmap = &p.maps[u.b_map];
     for (int kb = 0; kb < nk; ++kb) {
-      if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty,
-                     static_cast<uint32_t>(tile))) {
+      if (!mbar_try_wait(&ctl->empty[stage], phase ^ 1u) &&
+          !mbar_wait(&ctl->empty[stage], phase ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty, static_cast<uint32_t>(tile))) {
         ok = false;
         break;
       }
-      int amap, arow, ax, bx, wait_src;
-      kblock_coords(u, kb, a_row, &amap, &arow, &ax, &bx, &wait_src);
-      if (wait_src >= 0) {  // a received K chunk: its copy must have landed
-        const int f = u.chunk_flag_base + wait_src;
-        if (!flag_wait(p.flags + f, p.epoch, p.ctrl, p.timeout_ns, kSiteAgFlag, static_cast<uint32_t>(f))) {
-          ok = false;
-          break;
+      const CUtensorMap* amap = amap0;
+      int arow = a_row, ax = kb * kBK, bx = kb * kBK;
+      if (chunked) {
+        int am, wait_src;
+        kblock_coords(u, kb, a_row, &am, &arow, &ax, &bx, &wait_src);
+        amap = &p.maps[am];
+        if (wait_src >= 0) {  // a received K chunk: its copy must have landed
+          const int f = u.chunk_flag_base + wait_src;
+          if (!flag_wait(p.flags + f, p.epoch, p.ctrl, p.timeout_ns, kSiteAgFlag, static_cast<uint32_t>(f))) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();
         }
-        fence_proxy_async_global();
       }
       uint8_t* a = tiles + stage * kPStage;
       uint8_t* b = a + kPA;
       if (cta == 0) mbar_arrive_expect_tx(&ctl->full[stage], 2 * kPStage);
       const uint32_t bar = leader_full + stage * static_cast<uint32_t>(sizeof(uint64_t));
-      if (u.mn_major & 1) {  // A stored [K][M]: x runs along M
-        for (int h = 0; h < kBM / 64; ++h) tma_load_2d_pair(&p.maps[amap], a + h * kMnBox, bar, arow + h * 64, ax);
+      if (mn == 0) {
+        tma_load_2d_pair(amap, a, bar, ax, arow);
+        tma_load_2d_pair(bmap, b, bar, bx, b_row);
       } else {
-        tma_load_2d_pair(&p.maps[amap], a, bar, ax, arow);
-      }
-      if (u.mn_major & 2) {  // B stored [K][N]: this CTA's 128 columns
-        for (int h = 0; h < kBN / 128; ++h)
-          tma_load_2d_pair(&p.maps[u.b_map], b + h * kMnBox, bar, b_row + h * 64, bx);
-      } else {
-        tma_load_2d_pair(&p.maps[u.b_map], b, bar, bx, b_row);
+        if (mn & 1) {  // A stored [K][M]: x runs along M
+          tma_load_2d_pair(amap, a, bar, arow, ax);
+          tma_load_2d_pair(amap, a + kMnBox, bar, arow + 64, ax);
+        } else {
+          tma_load_2d_pair(amap, a, bar, ax, arow);
+        }
+        if (mn & 2) {  // B stored [K][N]: this CTA's 128 columns
+          tma_load_2d_pair(bmap, b, bar, b_row, bx);
+          tma_load_2d_pair(bmap, b + kMnBox, bar, b_row + 64, bx);
+        } else {
+          tma_load_2d_pair(bmap, b, bar, bx, b_row);
+        }
       }
       armed |= 1u << stage;
       armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
@@ -115,7 +131,11 @@ __device__ void pair_producer(const GemmParams& p, uint8_t* tiles, PairCtl* ctl,
   }
 }
 
+// The operand orientation is a template argument: the instruction descriptor stays a
+// compile-time constant and the K loop carries no per-block dispatch.
+template <bool AMN, bool BMN>
 __device__ void pair_mma(const GemmParams& p, uint8_t* tiles, PairCtl* ctl, uint32_t tmem_base) {
+  constexpr uint32_t idesc = kPIdesc | (AMN ? kIdescAMn : 0u) | (BMN ? kIdescBMn : 0u);
   const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
   int stage = 0, acc = 0;
   uint32_t phase = 0, acc_phase = 0;
@@ -132,8 +152,6 @@ __device__ void pair_mma(const GemmParams& p, uint8_t* tiles, PairCtl* ctl, uint
     tc_fence_after();
     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
     const int nk = (u.k + kBK - 1) / kBK;
-    const bool amn = (u.mn_major & 1) != 0, bmn = (u.mn_major & 2) != 0;
-    const uint32_t idesc = kPIdesc | (amn ? kIdescAMn : 0u) | (bmn ? kIdescBMn : 0u);
     for (int kb = 0; kb < nk; ++kb) {
       if (!mbar_wait(&ctl->full[stage], phase, p.ctrl, p.timeout_ns, kSiteFull, static_cast<uint32_t>(tile))) {
         ok = false;
@@ -144,7 +162,7 @@ __device__ void pair_mma(const GemmParams& p, uint8_t* tiles, PairCtl* ctl, uint
       const uint32_t b_addr = a_addr + kPA;
 #pragma unroll
       for (int k = 0; k < kBK / 16; ++k) {
-        umma_bf16_pair(d_tmem, operand_desc(a_addr, k, amn), operand_desc(b_addr, k, bmn), idesc,
+        umma_bf16_pair(d_tmem, operand_desc(a_addr, k, AMN), operand_desc(b_addr, k, BMN), idesc,
                        (kb | k) != 0 ? 1u : 0u);
       }
       issued = true;
@@ -263,7 +281,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_pair_kernel(const __grid
   if (warp == 0) {
     if (lane == 0) pair_producer(p, tiles, ctl, cta);
   } else if (warp == 1) {
-    if (lane == 0 && cta == 0) pair_mma(p, tiles, ctl, tmem_base);
+    if (lane == 0 && cta == 0) {
+      switch (p.mn_major & 3) {
+        case 0: pair_mma<false, false>(p, tiles, ctl, tmem_base); break;
+        case 2: pair_mma<false, true>(p, tiles, ctl, tmem_base); break;
+        case 3: pair_mma<true, true>(p, tiles, ctl, tmem_base); break;
+        default: pair_mma<true, false>(p, tiles, ctl, tmem_base); break;
+      }
+    }
     __syncwarp();
   } else {
     pair_epilogue(p, ctl, tmem_base, cta, warp, lane);

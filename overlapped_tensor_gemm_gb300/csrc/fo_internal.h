@@ -63,10 +63,7 @@ struct GemmUnit {
   int32_t kchunk;              // 0: plain K
   int32_t chunk_self, chunk_nsrc, chunk_order;
   int32_t a_map2, a2_row_stride, chunk_flag_base;
-  // Operand orientation: bit 0 set: A is stored [K][M] (M contiguous), bit 1 set: B is
-  // stored [K][N] (a transposed weight).  Such operands are staged as 64 (M or N) x 64 (K)
-  // boxes, one per 64-wide block, and read by the MMA as MN-major (no K chunks, no gating).
-  int32_t mn_major;
+  int32_t pad1;
   void* c;                     // output
   const float* acc_in;         // fp32 partial sum to add (kEpiAdd*)
   int64_t ldc, ld_acc;         // leading dimensions in elements
@@ -82,6 +79,11 @@ struct GemmParams {
   int32_t mblock_major;        // 1: tiles of a group ordered (m-block, unit, n-block);
                                // 0: unit by unit, n-block outer, m-block inner
   int32_t group_nb_major;      // bit g: group g ordered (n-block, unit, m-block) instead
+  // Operand orientation of every unit of the launch: bit 0 set: A is stored [K][M] (M
+  // contiguous), bit 1 set: B is stored [K][N] (a transposed weight).  Such operands are
+  // staged as 64 (M or N) x 64 (K) boxes, one per 64-wide block, and read by the MMA as
+  // MN-major (no K chunks, no gating).  The kernels instantiate their MMA loop per value.
+  int32_t mn_major;
   int32_t total_tiles;
   uint32_t epoch;
   uint64_t timeout_ns;
