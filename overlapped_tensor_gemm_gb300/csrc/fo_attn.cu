@@ -199,7 +199,7 @@ __device__ void attn_producer(const AttnParams& p, uint8_t* smem, AttnCtl* ctl) 
       fence_proxy_async_global();
       seen |= 1ull << fidx;
     }
-    if (!mbar_wait(&ctl->k_empty[kst], kph ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty, kit.i)) return false;
+    if (!mbar_wait_fast(&ctl->k_empty[kst], kph ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty, kit.i)) return false;
     const CUtensorMap* kmap = kit.t == 0 ? &p.maps[it.r] : &p.maps[p.P + it.r];
     const int krow0 = kit.t == 0 ? 0 : s * p.m;
     uint8_t* kt = smem + kOffK + kst * kTileBytes;
@@ -218,7 +218,7 @@ __device__ void attn_producer(const AttnParams& p, uint8_t* smem, AttnCtl* ctl) 
   auto issue_v = [&]() -> bool {
     const Item& it = vit.it;
     const int s = slice_of(p, it.r, vit.t);  // arrival already observed by the K walk
-    if (!mbar_wait(&ctl->v_empty[vst], vph ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty, vit.i)) return false;
+    if (!mbar_wait_fast(&ctl->v_empty[vst], vph ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty, vit.i)) return false;
     uint8_t* vt = smem + kOffV + vst * kVStageBytes;
     mbar_arrive_expect_tx(&ctl->v_full[vst], kTileBytes);  // the 128 head-dim rows of both key halves
     for (int c = 0; c < 2; ++c)
@@ -321,13 +321,13 @@ __device__ void attn_mma(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, uint3
   for (int i = blockIdx.x; ok && i < p.total_items; i += gridDim.x) {
     const Item it = decode_item(p, i);
     const int n = item_blocks(p, it);
-    if (!mbar_wait(&ctl->q_full, q_uses & 1u, p.ctrl, p.timeout_ns, kSiteFull, i)) break;
+    if (!mbar_wait_fast(&ctl->q_full, q_uses & 1u, p.ctrl, p.timeout_ns, kSiteFull, i)) break;
     ++q_uses;
     tc_fence_after();
     {  // scores of the item's first block
       const uint32_t st = g % kKStages, sb = g & 1u;
-      if (!mbar_wait(&ctl->k_full[st], (g / kKStages) & 1u, p.ctrl, p.timeout_ns, kSiteFull, i) ||
-          !mbar_wait(&ctl->pv_done[sb], s_free_parity(g), p.ctrl, p.timeout_ns, kSiteTmemEmpty, i)) {
+      if (!mbar_wait_fast(&ctl->k_full[st], (g / kKStages) & 1u, p.ctrl, p.timeout_ns, kSiteFull, i) ||
+          !mbar_wait_fast(&ctl->pv_done[sb], s_free_parity(g), p.ctrl, p.timeout_ns, kSiteTmemEmpty, i)) {
         ok = false;
         break;
       }
@@ -389,7 +389,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
                                           uint32_t detail, int lane) {
   uint32_t ok = 0;
   // the phase is usually complete already: test it inline before the bounded wait loop
-  if (lane == 0) ok = (mbar_try_wait(bar, parity) || mbar_wait(bar, parity, p.ctrl, p.timeout_ns, site, detail)) ? 1u : 0u;
+  if (lane == 0) ok = mbar_wait_fast(bar, parity, p.ctrl, p.timeout_ns, site, detail) ? 1u : 0u;
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 

@@ -82,8 +82,8 @@ __device__ void producer_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl)
     const CUtensorMap* amap0 = &p.maps[u.a_map];
     const CUtensorMap* bmap = &p.maps[u.b_map];
     for (int kb = 0; kb < nk; ++kb) {
-      if (!mbar_try_wait(&ctl->empty[stage], phase ^ 1u) &&
-          !mbar_wait(&ctl->empty[stage], phase ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty, static_cast<uint32_t>(tile))) {
+      if (!mbar_wait_fast(&ctl->empty[stage], phase ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty,
+                          static_cast<uint32_t>(tile))) {
         ok = false;
         break;
       }
@@ -151,7 +151,7 @@ __device__ void mma_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl, uint
   for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
     const TileCoord tc = decode_tile(p, tile);
     const GemmUnit& u = p.units[tc.unit];
-    if (!mbar_wait(&ctl->tmem_empty[acc], acc_phase ^ 1u, p.ctrl, p.timeout_ns, kSiteTmemEmpty,
+    if (!mbar_wait_fast(&ctl->tmem_empty[acc], acc_phase ^ 1u, p.ctrl, p.timeout_ns, kSiteTmemEmpty,
                    static_cast<uint32_t>(tile))) {
       ok = false;
       break;
@@ -160,7 +160,7 @@ __device__ void mma_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl, uint
     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
     const int nk = (u.k + kBK - 1) / kBK;
     for (int kb = 0; kb < nk; ++kb) {
-      if (!mbar_wait(&ctl->full[stage], phase, p.ctrl, p.timeout_ns, kSiteFull, static_cast<uint32_t>(tile))) {
+      if (!mbar_wait_fast(&ctl->full[stage], phase, p.ctrl, p.timeout_ns, kSiteFull, static_cast<uint32_t>(tile))) {
         ok = false;
         break;
       }

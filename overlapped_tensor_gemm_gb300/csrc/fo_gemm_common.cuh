@@ -168,7 +168,7 @@ __device__ __forceinline__ void store_silu_chunk(const GemmUnit& u, int row, int
 __device__ __forceinline__ bool warp_mbar_wait(uint64_t* bar, uint32_t parity, const GemmParams& p,
                                                uint32_t site, uint32_t detail, int lane) {
   uint32_t ok = 0;
-  if (lane == 0) ok = mbar_wait(bar, parity, p.ctrl, p.timeout_ns, site, detail) ? 1u : 0u;
+  if (lane == 0) ok = mbar_wait_fast(bar, parity, p.ctrl, p.timeout_ns, site, detail) ? 1u : 0u;
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
