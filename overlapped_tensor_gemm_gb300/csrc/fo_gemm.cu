@@ -44,10 +44,11 @@ struct alignas(8) SmemCtl {
   uint32_t pad;
 };
 
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 + static_cast<int>(sizeof(SmemCtl));
+// operand stages, then the four epilogue warps' staging buffers, then the barriers
+constexpr int kSmemBytes = kStages * kStageBytes + 4 * kEpiStageBytes + 1024 + static_cast<int>(sizeof(SmemCtl));
 // The ring's device-to-device copies may run as a small copy kernel next to this
 // persistent grid: leave shared memory free on every SM.
-static_assert(kSmemBytes <= 232448 - 24 * 1024, "the persistent GEMM must leave 24 KiB of shared memory free");
+static_assert(kSmemBytes <= 232448 - 16 * 1024, "the persistent GEMM must leave 16 KiB of shared memory free");
 
 // ---------------------------------------------------------------------------
 // warp roles
@@ -192,23 +193,28 @@ __device__ void mma_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl, uint
   }
 }
 
-__device__ void epilogue_loop(const GemmParams& p, SmemCtl* ctl, uint32_t tmem_base, int warp, int lane) {
+__device__ void epilogue_loop(const GemmParams& p, SmemCtl* ctl, uint32_t tmem_base, int warp, int lane,
+                              float* stage) {
   const int q = warp & 3;  // TMEM lanes [32q, 32q+32) are the only ones this warp may access
   int acc = 0;
   uint32_t acc_phase = 0;
   for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
     const TileCoord tc = decode_tile(p, tile);
     const GemmUnit& u = p.units[tc.unit];
-    if (!warp_mbar_wait(&ctl->tmem_full[acc], acc_phase, p, kSiteTmemFull, static_cast<uint32_t>(tile), lane))
-      return;
-    tc_fence_after();
     const int tile_in_unit = tc.mb * u.tiles_n + tc.nb;
+    const int row = tc.mb * kBM + q * 32 + lane;
+    const bool row_ok = row < u.m_rows;
+    // the partial sum's flag and first chunk are taken while the accumulator is computed
+    const bool add = u.epi == kEpiAddF32 || u.epi == kEpiAddBF16;
     if (u.in_flag_base >= 0) {
       const int f = u.in_flag_base + tile_in_unit * 4 + q;
       if (!warp_flag_wait(p.flags + f, p, kSiteAccInFlag, static_cast<uint32_t>(f), lane)) return;
     }
-    const int row = tc.mb * kBM + q * 32 + lane;
-    const bool row_ok = row < u.m_rows;
+    float4 part[8];
+    if (add) load_partial(u, row - lane, tc.nb * kBN, lane, part);
+    if (!warp_mbar_wait(&ctl->tmem_full[acc], acc_phase, p, kSiteTmemFull, static_cast<uint32_t>(tile), lane))
+      return;
+    tc_fence_after();
     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
     if (u.epi == kEpiSiluMul) {
 #pragma unroll 1
@@ -221,14 +227,7 @@ __device__ void epilogue_loop(const GemmParams& p, SmemCtl* ctl, uint32_t tmem_b
         if (row_ok && col < u.n_cols) store_silu_chunk(u, row, col, g, v);
       }
     } else {
-#pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tbase + c * 32, v);
-        tmem_wait_ld();
-        const int col = tc.nb * kBN + c * 32;
-        if (row_ok && col < u.n_cols) store_chunk(u, row, col, v);
-      }
+      store_rows(u, tbase, row - lane, tc.nb * kBN, lane, add, part, stage);
     }
     tc_fence_before();
     __syncwarp();
@@ -248,7 +247,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = smem_u32(smem_raw);
   uint8_t* tiles = smem_raw + ((1024u - (base & 1023u)) & 1023u);
-  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(tiles + kStages * kStageBytes);
+  float* epi_stage = reinterpret_cast<float*>(tiles + kStages * kStageBytes);
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(tiles + kStages * kStageBytes + 4 * kEpiStageBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     }
     __syncwarp();
   } else {
-    epilogue_loop(p, ctl, tmem_base, warp, lane);
+    epilogue_loop(p, ctl, tmem_base, warp, lane, epi_stage + (warp - 2) * (kEpiStageBytes / 4));
   }
 
   tc_fence_before();

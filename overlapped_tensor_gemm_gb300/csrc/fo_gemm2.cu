@@ -37,10 +37,11 @@ struct alignas(8) PairCtl {
   uint32_t pad;
 };
 
-constexpr int kPairSmem = kPairStages * kPStage + 1024 + static_cast<int>(sizeof(PairCtl));
+// operand stages, then the four epilogue warps' staging buffers, then the barriers
+constexpr int kPairSmem = kPairStages * kPStage + 4 * kEpiStageBytes + 1024 + static_cast<int>(sizeof(PairCtl));
 // The ring's device-to-device copies may run as a small copy kernel next to this
 // persistent grid: leave shared memory free on every SM.
-static_assert(kPairSmem <= 232448 - 24 * 1024, "the persistent GEMM must leave 24 KiB of shared memory free");
+static_assert(kPairSmem <= 232448 - 16 * 1024, "the persistent GEMM must leave 16 KiB of shared memory free");
 
 __device__ void pair_producer(const GemmParams& p, uint8_t* tiles, PairCtl* ctl, uint32_t cta) {
   const uint32_t leader_full = map_to_cta(smem_u32(&ctl->full[0]), 0);
@@ -184,7 +185,7 @@ __device__ void pair_mma(const GemmParams& p, uint8_t* tiles, PairCtl* ctl, uint
 }
 
 __device__ void pair_epilogue(const GemmParams& p, PairCtl* ctl, uint32_t tmem_base, uint32_t cta, int warp,
-                              int lane) {
+                              int lane, float* stage) {
   const int q = warp & 3;
   const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
   const uint32_t leader_tmem_empty = map_to_cta(smem_u32(&ctl->tmem_empty[0]), 0);
@@ -193,17 +194,21 @@ __device__ void pair_epilogue(const GemmParams& p, PairCtl* ctl, uint32_t tmem_b
   for (int tile = cluster; tile < p.total_tiles; tile += nclusters) {
     const TileCoord tc = decode_tile(p, tile);
     const GemmUnit& u = p.units[tc.unit];
-    if (!warp_mbar_wait(&ctl->tmem_full[acc], acc_phase, p, kSiteTmemFull, static_cast<uint32_t>(tile), lane))
-      return;
-    tc_fence_after();
     // flags per (tile, CTA half, lane quadrant): the same rows on both sides of a hop
     const int flag_slot = ((tc.mb * u.tiles_n + tc.nb) * 2 + static_cast<int>(cta)) * 4 + q;
+    const int row = tc.mb * 2 * kBM + static_cast<int>(cta) * kBM + q * 32 + lane;
+    const bool row_ok = row < u.m_rows;
+    // the partial sum's flag and first chunk are taken while the accumulator is computed
+    const bool add = u.epi == kEpiAddF32 || u.epi == kEpiAddBF16;
     if (u.in_flag_base >= 0) {
       const int f = u.in_flag_base + flag_slot;
       if (!warp_flag_wait(p.flags + f, p, kSiteAccInFlag, static_cast<uint32_t>(f), lane)) return;
     }
-    const int row = tc.mb * 2 * kBM + static_cast<int>(cta) * kBM + q * 32 + lane;
-    const bool row_ok = row < u.m_rows;
+    float4 part[8];
+    if (add) load_partial(u, row - lane, tc.nb * kBN, lane, part);
+    if (!warp_mbar_wait(&ctl->tmem_full[acc], acc_phase, p, kSiteTmemFull, static_cast<uint32_t>(tile), lane))
+      return;
+    tc_fence_after();
     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
     if (u.epi == kEpiSiluMul) {
 #pragma unroll 1
@@ -216,14 +221,7 @@ __device__ void pair_epilogue(const GemmParams& p, PairCtl* ctl, uint32_t tmem_b
         if (row_ok && col < u.n_cols) store_silu_chunk(u, row, col, g, v);
       }
     } else {
-#pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tbase + c * 32, v);
-        tmem_wait_ld();
-        const int col = tc.nb * kBN + c * 32;
-        if (row_ok && col < u.n_cols) store_chunk(u, row, col, v);
-      }
+      store_rows(u, tbase, row - lane, tc.nb * kBN, lane, add, part, stage);
     }
     tc_fence_before();
     __syncwarp();
@@ -248,7 +246,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_pair_kernel(const __grid
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = smem_u32(smem_raw);
   uint8_t* tiles = smem_raw + ((1024u - (base & 1023u)) & 1023u);
-  PairCtl* ctl = reinterpret_cast<PairCtl*>(tiles + kPairStages * kPStage);
+  float* epi_stage = reinterpret_cast<float*>(tiles + kPairStages * kPStage);
+  PairCtl* ctl = reinterpret_cast<PairCtl*>(tiles + kPairStages * kPStage + 4 * kEpiStageBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t cta = cluster_ctarank();
@@ -291,7 +290,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_pair_kernel(const __grid
     }
     __syncwarp();
   } else {
-    pair_epilogue(p, ctl, tmem_base, cta, warp, lane);
+    pair_epilogue(p, ctl, tmem_base, cta, warp, lane, epi_stage + (warp - 2) * (kEpiStageBytes / 4));
   }
 
   tc_fence_before();

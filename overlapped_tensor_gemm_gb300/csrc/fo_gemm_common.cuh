@@ -80,55 +80,142 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int tile) 
   return c;
 }
 
-// One 32-column chunk of one row: optional fp32 partial add, then store.
-__device__ __forceinline__ void store_chunk(const GemmUnit& u, int row, int col, const uint32_t (&v)[32]) {
-  float f[32];
+// ---------------------------------------------------------------------------
+// Partial-sum and fp32 epilogues through a per-warp staging buffer.
+//
+// tcgen05.ld (32x32b) hands each lane one accumulator row, so a lane-per-row global access
+// touches 32 rows per instruction.  Instead each epilogue warp writes its 32x32 fp32
+// chunk to shared memory row by row, reads it back so that 8 lanes cover one row's 32
+// columns (4 rows per instruction), and loads partial sums / stores results in that
+// row-contiguous layout.  Rows are 128 bytes; 16-byte granule g of row r sits at
+// g ^ (r & 7), which keeps both passes free of bank conflicts.
+// ---------------------------------------------------------------------------
+constexpr int kEpiStageBytes = 32 * 32 * 4;  // one warp's chunk
+
+__device__ __forceinline__ int stage_index(int row, int g) { return row * 32 + ((g ^ (row & 7)) << 2); }
+
+// Partial sums of one chunk in the coalesced layout: pf[i] = row 4i + lane/8 of the warp's
+// rows (first row `row0`), columns col + 4*(lane%8) .. +3; zero outside the unit.
+__device__ __forceinline__ void load_partial(const GemmUnit& u, int row0, int col, int lane, float4 (&pf)[8]) {
+  const int c = col + 4 * (lane & 7);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
-  const bool full = col + 32 <= u.n_cols;
-  const int ncol = full ? 32 : u.n_cols - col;
-  if (u.epi == kEpiAddF32 || u.epi == kEpiAddBF16) {
-    const float* src = u.acc_in + static_cast<int64_t>(row) * u.ld_acc + col;
-    if (full) {
+  for (int i = 0; i < 8; ++i) {
+    const int r = row0 + 4 * i + (lane >> 3);
+    float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (r < u.m_rows && c < u.n_cols) {
+      const float* src = u.acc_in + static_cast<int64_t>(r) * u.ld_acc + c;
+      if (c + 4 <= u.n_cols) {
+        x = ld_cg_f4(src);
+      } else {
+        x.x = __ldcg(src);
+        if (c + 1 < u.n_cols) x.y = __ldcg(src + 1);
+        if (c + 2 < u.n_cols) x.z = __ldcg(src + 2);
+      }
+    }
+    pf[i] = x;
+  }
+}
+
+// Stores one staged chunk (+ the partial sums when `add`) in the coalesced layout.
+__device__ __forceinline__ void store_staged(const GemmUnit& u, int row0, int col, int lane, const float* stage,
+                                             bool add, const float4 (&pf)[8]) {
+  const int c = col + 4 * (lane & 7);
+  const bool bf16_out = u.epi == kEpiBF16 || u.epi == kEpiAddBF16;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 a = ld_cg_f4(src + 4 * i);
-        f[4 * i + 0] += a.x;
-        f[4 * i + 1] += a.y;
-        f[4 * i + 2] += a.z;
-        f[4 * i + 3] += a.w;
+  for (int i = 0; i < 8; ++i) {
+    const int rl = 4 * i + (lane >> 3);
+    const int r = row0 + rl;
+    float4 x = *reinterpret_cast<const float4*>(stage + stage_index(rl, lane & 7));
+    if (add) {
+      x.x += pf[i].x;
+      x.y += pf[i].y;
+      x.z += pf[i].z;
+      x.w += pf[i].w;
+    }
+    if (r >= u.m_rows || c >= u.n_cols) continue;
+    const int ncol = u.n_cols - c;
+    if (bf16_out) {
+      uint16_t* dst = static_cast<uint16_t*>(u.c) + static_cast<int64_t>(r) * u.ldc + c;
+      if (ncol >= 4) {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w));
+      } else {
+        dst[0] = __bfloat16_as_ushort(__float2bfloat16_rn(x.x));
+        if (ncol > 1) dst[1] = __bfloat16_as_ushort(__float2bfloat16_rn(x.y));
+        if (ncol > 2) dst[2] = __bfloat16_as_ushort(__float2bfloat16_rn(x.z));
       }
     } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i < ncol) f[i] += __ldcg(src + i);
+      float* dst = static_cast<float*>(u.c) + static_cast<int64_t>(r) * u.ldc + c;
+      if (ncol >= 4) {
+        st_v4_u32(dst, __float_as_uint(x.x), __float_as_uint(x.y), __float_as_uint(x.z), __float_as_uint(x.w));
+      } else {
+        dst[0] = x.x;
+        if (ncol > 1) dst[1] = x.y;
+        if (ncol > 2) dst[2] = x.z;
+      }
     }
   }
-  if (u.epi == kEpiBF16 || u.epi == kEpiAddBF16) {
-    uint16_t* dst = static_cast<uint16_t*>(u.c) + static_cast<int64_t>(row) * u.ldc + col;
-    if (full) {
+}
+
+// A plain bf16 chunk of one row (lane = row), stored straight from registers: without
+// partial sums to load this was measured faster than the staged path.
+__device__ __forceinline__ void store_bf16_row_chunk(const GemmUnit& u, int row, int col, const uint32_t (&v)[32]) {
+  uint16_t* dst = static_cast<uint16_t*>(u.c) + static_cast<int64_t>(row) * u.ldc + col;
+  if (col + 32 <= u.n_cols) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        st_v4_u32(dst + 8 * i, pack_bf16x2(f[8 * i + 0], f[8 * i + 1]), pack_bf16x2(f[8 * i + 2], f[8 * i + 3]),
-                  pack_bf16x2(f[8 * i + 4], f[8 * i + 5]), pack_bf16x2(f[8 * i + 6], f[8 * i + 7]));
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i < ncol) dst[i] = __bfloat16_as_ushort(__float2bfloat16_rn(f[i]));
+    for (int i = 0; i < 4; ++i) {
+      st_v4_u32(dst + 8 * i,
+                pack_bf16x2(__uint_as_float(v[8 * i + 0]), __uint_as_float(v[8 * i + 1])),
+                pack_bf16x2(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3])),
+                pack_bf16x2(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
+                pack_bf16x2(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])));
     }
   } else {
-    float* dst = static_cast<float*>(u.c) + static_cast<int64_t>(row) * u.ldc + col;
-    if (full) {
+    const int ncol = u.n_cols - col;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        st_v4_u32(dst + 4 * i, __float_as_uint(f[4 * i + 0]), __float_as_uint(f[4 * i + 1]),
-                  __float_as_uint(f[4 * i + 2]), __float_as_uint(f[4 * i + 3]));
-      }
-    } else {
+    for (int i = 0; i < 32; ++i)
+      if (i < ncol) dst[i] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i])));
+  }
+}
+
+// The kBN columns of the warp's 32 accumulator rows (first row `row0`), chunk by chunk.
+// With a partial-sum add, `pf` holds chunk 0's partials on entry (loaded before the
+// accumulator was complete) and the loads of chunk c+1 are in flight while chunk c is
+// staged and stored.
+__device__ __forceinline__ void store_rows(const GemmUnit& u, uint32_t tbase, int row0, int col0, int lane, bool add,
+                                           float4 (&pf)[8], float* stage) {
+  if (u.epi == kEpiBF16) {
+    const int row = row0 + lane;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      const int col = col0 + c * 32;
+      if (col >= u.n_cols) break;
+      uint32_t v[32];
+      tmem_ld32(tbase + c * 32, v);
+      tmem_wait_ld();
+      if (row < u.m_rows) store_bf16_row_chunk(u, row, col, v);
+    }
+    return;
+  }
+#pragma unroll 1
+  for (int c = 0; c < kBN / 32; ++c) {
+    const int col = col0 + c * 32;
+    if (col >= u.n_cols) break;
+    uint32_t v[32];
+    float4 next[8];
+    tmem_ld32(tbase + c * 32, v);
+    if (add && c + 1 < kBN / 32) load_partial(u, row0, col + 32, lane, next);
+    tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i < ncol) dst[i] = f[i];
+    for (int g = 0; g < 8; ++g)
+      *reinterpret_cast<float4*>(stage + stage_index(lane, g)) =
+          make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]), __uint_as_float(v[4 * g + 2]),
+                      __uint_as_float(v[4 * g + 3]));
+    __syncwarp();
+    store_staged(u, row0, col, lane, stage, add, pf);
+    __syncwarp();  // the stage is rewritten by the next chunk
+    if (add) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) pf[i] = next[i];
     }
   }
 }
