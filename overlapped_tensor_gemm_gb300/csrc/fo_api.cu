@@ -472,6 +472,9 @@ struct AgArgs {
   int64_t m, K, N;
   char* recv;  // rank r's gathered copy: recv + r*M*K*2, slice s at row s*m
   bool w_kn;   // W[r] given as [K, N] (the transposed weight of a backward pass)
+  const fo_mat* Xh;  // non-null: X[r] is first uploaded from these host shards (flash order:
+                     // in rank order on the link streams, each slice's step-0 GEMM behind
+                     // the upload's flag)
 };
 
 char* ag_slot(const AgArgs& a, int r, int s, int64_t row_in_slice) {
@@ -481,6 +484,22 @@ char* ag_slot(const AgArgs& a, int r, int s, int64_t row_in_slice) {
 // The ring all-gather of rows [row0, row0 + rows) of every slice, on the link
 // streams.  Hop t: rank r forwards slice (r - t + 1) mod P (its own at t = 1)
 // to rank r+1 and, with `flags`, publishes arrival of that slice at r+1.
+// Uploads of the host shards a.Xh into X (flash order): one at a time in rank order on the
+// link streams, each publishing the (rank r, slice r) flag, which no ring hop uses, so the
+// GEMM of rank 0's own slice starts after one slice has crossed the host link instead of
+// all of them; each rank's first ring hop follows its upload on the same stream.
+fo_status enqueue_uploads(fo_ctx* ctx, const AgArgs& a, uint32_t epoch, uint32_t* flag_base) {
+  for (int r = 0; r < a.P; ++r) {
+    cudaStream_t ls = ctx->link[r];
+    if (r > 0) FO_CUDA(cudaStreamWaitEvent(ls, ctx->ev_hop[r - 1][0], 0));
+    FO_CUDA(cudaMemcpy2DAsync(a.X[r].ptr, a.X[r].ld * 2, a.Xh[r].ptr, a.Xh[r].ld * 2, a.K * 2, a.m,
+                              cudaMemcpyHostToDevice, ls));
+    FO_CUDA(cudaEventRecord(ctx->ev_hop[r][0], ls));
+    FO_TRY(write_flag(ls, flag_base + kAgFlagBase + r * a.P + r, epoch));
+  }
+  return FO_OK;
+}
+
 fo_status enqueue_ag_ring(fo_ctx* ctx, const AgArgs& a, int64_t row0, int64_t rows, bool flags, uint32_t epoch,
                           int fault, uint32_t* flag_base) {
   const int P = a.P;
@@ -536,6 +555,7 @@ fo_status add_ag_units(Launch& L, const AgArgs& a, const int* xmap, const int* r
       if (t == 0) {
         u.a_map = xmap[r];
         u.a_row0 = static_cast<int32_t>(row0);
+        if (flash && a.Xh) u.wait_flag = static_cast<int32_t>(kAgFlagBase + r * P + r);  // uploaded slice
       } else {
         u.a_map = rmap[r];
         u.a_row0 = static_cast<int32_t>(s * a.m + row0);
@@ -562,7 +582,7 @@ fo_status add_ag_units(Launch& L, const AgArgs& a, const int* xmap, const int* r
 
 // w_kn: W[r] is given as [K, N] (read MN-major by the MMA; not with `gated`).
 fo_status ag_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_mat* Y, const fo_opts& o,
-                 cudaStream_t stream, bool gated = false, bool w_kn = false) {
+                 cudaStream_t stream, bool gated = false, bool w_kn = false, const fo_mat* Xh = nullptr) {
   const int64_t m = X[0].rows, K = X[0].cols, N = w_kn ? W[0].cols : W[0].rows, M = m * P;
   const int64_t gated_f = gated ? N / 2 : 0;
   if (gated && N % 2 != 0) return fail(FO_ERR_SHAPE, "gated weight must have 2F rows");
@@ -585,7 +605,17 @@ fo_status ag_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_
   FO_TRY(ensure_buf(ctx, kBufFlags, 1 << 20, &flags_v));
   FO_TRY(ensure_buf(ctx, kBufAgRecv, static_cast<size_t>(P) * M * K * 2, &recv_v));
   uint32_t* flags = static_cast<uint32_t*>(flags_v);
-  AgArgs a{X, W, Y, P, m, K, N, static_cast<char*>(recv_v), w_kn};
+  AgArgs a{X, W, Y, P, m, K, N, static_cast<char*>(recv_v), w_kn, nullptr};
+  const bool flash = o.order == FO_ORDER_FLASH || o.order == FO_ORDER_NAIVE;
+  if (Xh) {
+    if (flash) {
+      a.Xh = Xh;
+    } else {  // the baselines upload everything first
+      for (int r = 0; r < P; ++r)
+        FO_CUDA(cudaMemcpy2DAsync(X[r].ptr, X[r].ld * 2, Xh[r].ptr, Xh[r].ld * 2, K * 2, m, cudaMemcpyHostToDevice,
+                                  stream));
+    }
+  }
   const uint32_t epoch = ++ctx->epoch;
   const uint64_t tmo = timeout_ns(o);
 
@@ -617,6 +647,7 @@ fo_status ag_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_
     FO_CUDA(cudaEventRecord(ctx->ev_fork, stream));
     FO_TRY(launch_gemm(ctx, L, o, stream));  // runs concurrently with the ring below
     for (int r = 0; r < P; ++r) FO_CUDA(cudaStreamWaitEvent(ctx->link[r], ctx->ev_fork, 0));
+    if (a.Xh) FO_TRY(enqueue_uploads(ctx, a, epoch, flags));
     FO_TRY(enqueue_ag_ring(ctx, a, 0, m, true, epoch, o.fault, flags));
     return join_links(ctx, P, stream);
   }
@@ -1147,8 +1178,9 @@ fo_status row_backward_run(fo_ctx* ctx, const fo_mat* H, const fo_mat* W, const 
 // MLP layer
 // --------------------------------------------------------------------------
 
+// Xh non-null: X are device buffers that the Flash-AG first fills from the host shards Xh.
 fo_status mlp_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* Wc, const fo_mat* Wr, int P, int gated,
-                  const fo_mat* Z, const fo_opts& o, cudaStream_t stream) {
+                  const fo_mat* Z, const fo_opts& o, cudaStream_t stream, const fo_mat* Xh = nullptr) {
   const int64_t m = X[0].rows, M = m * P, Nc = Wc[0].rows;
   if (gated && Nc % 16 != 0) return fail(FO_ERR_UNSUPPORTED, "gated layer needs 2F with F % 8 == 0");
   const int64_t F = gated ? Nc / 2 : Nc;
@@ -1167,9 +1199,9 @@ fo_status mlp_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* Wc, const fo_mat* 
     FO_TRY(ensure_buf(ctx, kBufMlpH, static_cast<size_t>(P) * M * F * 2 + 16, &h_v));
     for (int r = 0; r < P; ++r)
       H[r] = fo_mat{static_cast<char*>(h_v) + static_cast<int64_t>(r) * M * F * 2, FO_BF16, 0, M, F, F};
-    FO_TRY(ag_run(ctx, X, Wc, P, H, oa, stream, true));
+    FO_TRY(ag_run(ctx, X, Wc, P, H, oa, stream, true, false, Xh));
   } else {
-    FO_TRY(ag_run(ctx, X, Wc, P, Y, oa, stream));
+    FO_TRY(ag_run(ctx, X, Wc, P, Y, oa, stream, false, false, Xh));
     for (int r = 0; r < P; ++r) H[r] = Y[r];
   }
   return rs_run(ctx, H, Wr, P, Z, o, stream);
@@ -1429,10 +1461,13 @@ fo_status fo_mlp_layer_host(fo_ctx* ctx, const fo_mat* X_shards, const fo_mat* W
   for (int r = 0; r < P; ++r) {
     Xd[r] = fo_mat{static_cast<char*>(xv) + static_cast<int64_t>(r) * m * Hd * 2, FO_BF16, 0, m, Hd, Hd};
     Zd[r] = fo_mat{static_cast<char*>(zv) + static_cast<int64_t>(r) * m * Hd * 2, FO_BF16, 0, m, Hd, Hd};
-    FO_CUDA(cudaMemcpy2DAsync(Xd[r].ptr, Hd * 2, X_shards[r].ptr, X_shards[r].ld * 2, Hd * 2, m,
-                              cudaMemcpyHostToDevice, s));
+    FO_TRY(check_mat(W_col[r], FO_BF16, "W_col", r));
+    FO_TRY(check_mat(W_row[r], FO_BF16, "W_row", r));
+    const int64_t F = gated ? W_col[r].rows / 2 : W_col[r].rows;
+    if (W_row[r].cols != F) return fail(FO_ERR_SHAPE, "W_row[%d] must have F=%lld columns", r, (long long)F);
   }
-  FO_TRY(fo_mlp_layer(ctx, Xd, W_col, W_row, P, gated, Zd, opts, stream));
+  // the Flash-AG uploads the host shards itself, slice by slice, ahead of their GEMMs
+  FO_TRY(mlp_run(ctx, Xd, W_col, W_row, P, gated, Zd, opts ? *opts : default_opts(), s, X_shards));
   for (int r = 0; r < P; ++r)
     FO_CUDA(cudaMemcpy2DAsync(Z[r].ptr, Z[r].ld * 2, Zd[r].ptr, Hd * 2, Hd * 2, m, cudaMemcpyDeviceToHost, s));
   return FO_OK;
