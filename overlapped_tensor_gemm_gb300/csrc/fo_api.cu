@@ -52,11 +52,13 @@ typedef CUresult (*PfnEncodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 typedef CUresult (*PfnWriteValue32)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+typedef CUresult (*PfnWaitValue32)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
 typedef CUresult (*PfnGetErrorString)(CUresult, const char**);
 
 struct DriverFns {
   PfnEncodeTiled encode_tiled = nullptr;
   PfnWriteValue32 write_value32 = nullptr;
+  PfnWaitValue32 wait_value32 = nullptr;
   PfnGetErrorString get_error_string = nullptr;
 };
 
@@ -69,9 +71,11 @@ const DriverFns* driver() {
                                      cudaEnableDefault, &q);
     cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", reinterpret_cast<void**>(&fns.write_value32), 12000,
                                      cudaEnableDefault, &q);
+    cudaGetDriverEntryPointByVersion("cuStreamWaitValue32", reinterpret_cast<void**>(&fns.wait_value32), 12000,
+                                     cudaEnableDefault, &q);
     cudaGetDriverEntryPointByVersion("cuGetErrorString", reinterpret_cast<void**>(&fns.get_error_string), 12000,
                                      cudaEnableDefault, &q);
-    loaded = fns.encode_tiled && fns.write_value32 && fns.get_error_string;
+    loaded = fns.encode_tiled && fns.write_value32 && fns.wait_value32 && fns.get_error_string;
   }
   return loaded ? &fns : nullptr;
 }
@@ -111,8 +115,11 @@ enum BufId : int {
 
 // Flag layout (uint32 words, epoch-valued):
 //   [0, kMaxP*kMaxP)                AG / attention arrival: rank r holds slice s
+//   [kDoneBase, kDoneBase + kMaxP)  RS: per-rank completion counters of the kept chunk's
+//                                   tiles (running totals, not epochs)
 //   [kRsFlagBase, ...)             RS per-(rank, hop, tile, quadrant) partial-sum flags
 constexpr int64_t kAgFlagBase = 0;
+constexpr int64_t kDoneBase = 64;
 constexpr int64_t kRsFlagBase = 256;
 
 constexpr int kMaxSlices = 16;
@@ -140,6 +147,7 @@ struct fo_ctx {
   uint32_t* ctrl = nullptr;
   uint32_t epoch = 0;
   int pair_clusters = 0;  // resident SM pairs for the 256x256-tile kernel (0: unavailable)
+  uint32_t done_total[kMaxP] = {};  // running targets of the per-rank completion counters
   std::map<int, Buffer> bufs;
 };
 
@@ -268,6 +276,7 @@ struct MapSpec {
 struct Launch {
   GemmParams p;
   MapSpec spec[kMaxMaps];
+  int arrivals_per_tile = 4;  // epilogue warps that finish each tile (8 on SM pairs)
   int num_units = 0;
   int num_groups = 0;
   int num_maps = 0;
@@ -365,6 +374,7 @@ GemmUnit blank_unit() {
   u.wait_flag = -1;
   u.in_flag_base = -1;
   u.out_flag_base = -1;
+  u.done_counter = -1;
   return u;
 }
 
@@ -377,6 +387,7 @@ fo_status launch_gemm(fo_ctx* ctx, Launch& L, const fo_opts& o, cudaStream_t str
     int clusters = ctx->pair_clusters;
     if (o.num_sms > 0 && o.num_sms / 2 < clusters) clusters = o.num_sms / 2 > 0 ? o.num_sms / 2 : 1;
     if (L.p.total_tiles < clusters) clusters = L.p.total_tiles;
+    L.arrivals_per_tile = 8;
     FO_CUDA(gemm_pair_launch(L.p, clusters, stream));
     return FO_OK;
   }
@@ -703,12 +714,21 @@ int add_rs_weight(Launch& L, fo_status* st, const RsArgs& a, int r) {
                 : L.add_map(st, a.W[r].ptr, a.N, a.Kr, a.W[r].ld, kBN);
 }
 
+// Completion of each rank's kept chunk in the fused reduce-scatter, for copies that wait
+// on it (the host-buffer layer's copies back): the kept chunk's tiles count into
+// flags[kDoneBase + r], and after the launch the stream writes every target, so a
+// waiter is released even if the kernel gave up early.
+struct DoneSignal {
+  bool set = false;            // filled in by the flash launch
+  uint32_t target[kMaxP] = {};
+};
+
 float* rs_slot(const RsArgs& a, float* base, int r, int h) {
   return base + (static_cast<int64_t>(r) * a.P + h) * a.m * a.N;
 }
 
 fo_status rs_flash(fo_ctx* ctx, const RsArgs& a, const fo_opts& o, cudaStream_t stream, uint32_t* flags,
-                   uint32_t epoch) {
+                   uint32_t epoch, DoneSignal* done = nullptr) {
   const int P = a.P;
   Launch L;
   fo_status st = FO_OK;
@@ -747,6 +767,7 @@ fo_status rs_flash(fo_ctx* ctx, const RsArgs& a, const fo_opts& o, cudaStream_t 
       u.c = a.Y[r].ptr;
       u.ldc = a.Y[r].ld;
       u.epi = h == 0 ? kEpiBF16 : kEpiAddBF16;
+      if (done) u.done_counter = static_cast<int32_t>(kDoneBase + r);
     }
   };
   for (int t = 0; t < P; ++t) {
@@ -759,7 +780,20 @@ fo_status rs_flash(fo_ctx* ctx, const RsArgs& a, const fo_opts& o, cudaStream_t 
   }
   L.p.mn_major = a.w_kn ? 2 : 0;
   FO_TRY(L.finish(epoch, timeout_ns(o), flags, ctx->ctrl, 0));
-  return launch_gemm(ctx, L, o, stream);
+  FO_TRY(launch_gemm(ctx, L, o, stream));
+  if (done) {
+    for (int i = 0; i < L.num_units; ++i) {
+      const GemmUnit& u = L.p.units[i];
+      if (u.done_counter < 0) continue;
+      const int r = static_cast<int>(u.done_counter - kDoneBase);
+      const uint32_t n = static_cast<uint32_t>(u.tiles_m * u.tiles_n * L.arrivals_per_tile);
+      ctx->done_total[r] += n;
+      done->target[r] = ctx->done_total[r];
+      FO_TRY(write_flag(stream, flags + kDoneBase + r, done->target[r]));
+    }
+    done->set = true;
+  }
+  return FO_OK;
 }
 
 // Baselines: partial GEMMs into `part`, then a ring reduce with device-to-device hops
@@ -826,9 +860,10 @@ fo_status rs_ring_reduce(fo_ctx* ctx, const RsArgs& a, cudaStream_t rs, int64_t 
   return FO_OK;
 }
 
-// w_kn: W[r] is given as [Kr, N] (read MN-major by the MMA).
+// w_kn: W[r] is given as [Kr, N] (read MN-major by the MMA).  done: see DoneSignal (fused
+// order only; left unset otherwise).
 fo_status rs_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_mat* Y, const fo_opts& o,
-                 cudaStream_t stream, bool w_kn = false) {
+                 cudaStream_t stream, bool w_kn = false, DoneSignal* done = nullptr) {
   const int64_t M = X[0].rows, Kr = X[0].cols, N = w_kn ? W[0].cols : W[0].rows;
   for (int r = 0; r < P; ++r) {
     FO_TRY(check_mat(X[r], FO_BF16, "X", r));
@@ -855,7 +890,7 @@ fo_status rs_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_
   if (o.order == FO_ORDER_FLASH || o.order == FO_ORDER_NAIVE || P == 1) {
     if (o.link == FO_LINK_CE)
       return fail(FO_ERR_UNSUPPORTED, "fused reduce-scatter hops are epilogue pushes (FO_LINK_PUSH)");
-    return rs_flash(ctx, a, o, stream, flags, epoch);
+    return rs_flash(ctx, a, o, stream, flags, epoch, done);
   }
   void* part_v = nullptr;
   FO_TRY(ensure_buf(ctx, kBufPart, static_cast<size_t>(P) * P * m * N * 4, &part_v));
@@ -1180,7 +1215,8 @@ fo_status row_backward_run(fo_ctx* ctx, const fo_mat* H, const fo_mat* W, const 
 
 // Xh non-null: X are device buffers that the Flash-AG first fills from the host shards Xh.
 fo_status mlp_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* Wc, const fo_mat* Wr, int P, int gated,
-                  const fo_mat* Z, const fo_opts& o, cudaStream_t stream, const fo_mat* Xh = nullptr) {
+                  const fo_mat* Z, const fo_opts& o, cudaStream_t stream, const fo_mat* Xh = nullptr,
+                  DoneSignal* done = nullptr) {
   const int64_t m = X[0].rows, M = m * P, Nc = Wc[0].rows;
   if (gated && Nc % 16 != 0) return fail(FO_ERR_UNSUPPORTED, "gated layer needs 2F with F % 8 == 0");
   const int64_t F = gated ? Nc / 2 : Nc;
@@ -1204,7 +1240,7 @@ fo_status mlp_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* Wc, const fo_mat* 
     FO_TRY(ag_run(ctx, X, Wc, P, Y, oa, stream, false, false, Xh));
     for (int r = 0; r < P; ++r) H[r] = Y[r];
   }
-  return rs_run(ctx, H, Wr, P, Z, o, stream);
+  return rs_run(ctx, H, Wr, P, Z, o, stream, false, done);
 }
 
 }  // namespace
@@ -1466,11 +1502,25 @@ fo_status fo_mlp_layer_host(fo_ctx* ctx, const fo_mat* X_shards, const fo_mat* W
     const int64_t F = gated ? W_col[r].rows / 2 : W_col[r].rows;
     if (W_row[r].cols != F) return fail(FO_ERR_SHAPE, "W_row[%d] must have F=%lld columns", r, (long long)F);
   }
-  // the Flash-AG uploads the host shards itself, slice by slice, ahead of their GEMMs
-  FO_TRY(mlp_run(ctx, Xd, W_col, W_row, P, gated, Zd, opts ? *opts : default_opts(), s, X_shards));
-  for (int r = 0; r < P; ++r)
-    FO_CUDA(cudaMemcpy2DAsync(Z[r].ptr, Z[r].ld * 2, Zd[r].ptr, Hd * 2, Hd * 2, m, cudaMemcpyDeviceToHost, s));
-  return FO_OK;
+  // the Flash-AG uploads the host shards itself, slice by slice, ahead of their GEMMs; in
+  // the fused order each rank's output goes back as soon as its kept chunk is complete
+  DoneSignal done;
+  FO_TRY(mlp_run(ctx, Xd, W_col, W_row, P, gated, Zd, opts ? *opts : default_opts(), s, X_shards, &done));
+  if (!done.set) {
+    for (int r = 0; r < P; ++r)
+      FO_CUDA(cudaMemcpy2DAsync(Z[r].ptr, Z[r].ld * 2, Zd[r].ptr, Hd * 2, Hd * 2, m, cudaMemcpyDeviceToHost, s));
+    return FO_OK;
+  }
+  void* flags_v = nullptr;
+  FO_TRY(ensure_buf(ctx, kBufFlags, 1 << 20, &flags_v));
+  uint32_t* flags = static_cast<uint32_t*>(flags_v);
+  for (int r = 0; r < P; ++r) {
+    cudaStream_t ls = ctx->link[r];
+    FO_CU(driver()->wait_value32(reinterpret_cast<CUstream>(ls), reinterpret_cast<CUdeviceptr>(flags + kDoneBase + r),
+                                 done.target[r], CU_STREAM_WAIT_VALUE_GEQ));
+    FO_CUDA(cudaMemcpy2DAsync(Z[r].ptr, Z[r].ld * 2, Zd[r].ptr, Hd * 2, Hd * 2, m, cudaMemcpyDeviceToHost, ls));
+  }
+  return join_links(ctx, P, s);
 }
 
 fo_status fo_qsplit_attn(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K_shards, const fo_mat* V_shards, int P,

@@ -237,6 +237,12 @@ __device__ void pair_epilogue(const GemmParams& p, PairCtl* ctl, uint32_t tmem_b
       __syncwarp();
       if (lane == 0) st_release_gpu(p.flags + u.out_flag_base + flag_slot, p.epoch);
     }
+    if (u.done_counter >= 0) {
+      // this warp's rows of the tile are final: count them for a copy engine that waits
+      __threadfence_system();
+      __syncwarp();
+      if (lane == 0) red_release_sys_add(p.flags + u.done_counter, 1u);
+    }
     acc ^= 1;
     if (acc == 0) acc_phase ^= 1u;
   }

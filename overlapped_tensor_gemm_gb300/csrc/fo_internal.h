@@ -63,7 +63,8 @@ struct GemmUnit {
   int32_t kchunk;              // 0: plain K
   int32_t chunk_self, chunk_nsrc, chunk_order;
   int32_t a_map2, a2_row_stride, chunk_flag_base;
-  int32_t pad1;
+  int32_t done_counter;        // >= 0: every epilogue warp adds 1 to flags[done_counter] after its
+                               // part of a tile is stored (system-scope release)
   void* c;                     // output
   const float* acc_in;         // fp32 partial sum to add (kEpiAdd*)
   int64_t ldc, ld_acc;         // leading dimensions in elements

@@ -75,3 +75,38 @@ def test_skipped_all_to_all_hop_times_out_and_context_recovers():
         ctx.a2a_gemm(C, W, Y)
         torch.cuda.synchronize()
         ctx.poll()
+
+
+def test_host_layer_with_skipped_hop_releases_its_copies():
+    # The host-buffer layer copies each rank's output back on a link stream that waits for
+    # the reduce-scatter's completion counter of that rank.  With a skipped all-gather hop
+    # the GEMMs give up; the counters' final values, written on the stream after the
+    # reduce-scatter launch, still release those copies, so the call completes.
+    import time
+
+    import overlapped_tensor_gemm_gb300 as fo
+    cfg = wl.MLPConfig("host-f", 70, P=4, tokens=1024, hidden=256, ffn=512, gated=False, integer=True)
+    inp = wl.mlp_inputs(cfg)
+    Xh = [to_dev(x, "cpu").pin_memory() for x in inp["X_shards"]]
+    Wc = [to_dev(w) for w in inp["W_col"]]
+    Wr = [to_dev(w) for w in inp["W_row"]]
+    Zh = [torch.empty((cfg.m, cfg.hidden), dtype=torch.bfloat16).pin_memory() for _ in range(cfg.P)]
+    with fo.Context(0) as ctx:
+        ctx.mlp_layer_host(Xh, Wc, Wr, Zh, gated=False, fault="skip_hop", timeout_us=20000)
+        done = torch.cuda.Event()
+        done.record()
+        deadline = time.time() + 30.0
+        while not done.query():
+            assert time.time() < deadline, "a copy back to the host was not released"
+            time.sleep(0.005)
+        with pytest.raises(fo.FoError) as e:
+            ctx.poll()
+        assert e.value.status == fo.FO_ERR_TIMEOUT
+        ctx.poll()
+        ctx.mlp_layer_host(Xh, Wc, Wr, Zh, gated=False)
+        torch.cuda.synchronize()
+        ctx.poll()
+        _, _, ref = ops.mlp_layer([f64(x) for x in inp["X_shards"]], [f64(w) for w in inp["W_col"]],
+                                  [f64(w) for w in inp["W_row"]], gated=False)
+        for r in range(cfg.P):
+            assert_bits_equal(to_bits(Zh[r]), ref[r], f"host layer after recovery rank {r}")
