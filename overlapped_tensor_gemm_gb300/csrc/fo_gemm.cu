@@ -10,12 +10,18 @@
 // CTA layout (192 threads, one CTA per SM, persistent):
 //   warp 0      TMA producer: waits for a slice's arrival flag (AG), then streams
 //               128x64 A and 256x64 B bf16 tiles (128-byte swizzle) into a
-//               4-stage shared-memory ring.
+//               4-stage shared-memory ring; K-major operands as one box each,
+//               MN-major ones (transposed operands of the backward) as 64x64
+//               boxes, one per 64-wide block.
 //   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators) and
-//               issues tcgen05.mma (M=128, N=256, K=16) from one thread.
-//   warps 2-5   epilogue: tcgen05.ld of its 32-lane quadrant, optional fp32
-//               partial-sum add (RS, after acquiring the per-tile flag), store,
-//               then release of the per-tile flag read by the next rank.
+//               issues tcgen05.mma (M=128, N=256, K=16) from one thread: the
+//               kernel's critical path, so its loop is instantiated per operand
+//               orientation and its waits test the barrier phase inline.
+//   warps 2-5   epilogue: tcgen05.ld of its 32-lane quadrant; plain bf16 results
+//               are stored from registers, fp32 partial sums (RS, after acquiring
+//               the per-tile flag) go through a per-warp staging buffer so the
+//               partial-sum loads and the stores move whole row segments; then
+//               release of the per-tile flag read by the next rank.
 // Accumulators are double-buffered so the epilogue of tile i overlaps the
 // main loop of tile i+1.
 #include <cuda_bf16.h>

@@ -19,7 +19,8 @@ constexpr int kMaxP = 8;
 // A launch computes a list of "units".  A unit is one rank's GEMM on one ring
 // step: rows [a_row0, a_row0 + m_rows) of its A operand (via a TMA map)
 // times the rows [b_row0, b_row0 + n_cols) of its B operand (nn.Linear
-// layout, K contiguous), written through a per-unit epilogue.  Units are
+// layout, K contiguous; or both transposed, see GemmParams::mn_major), written
+// through a per-unit epilogue.  Units are
 // grouped (one group per ring step); the tiles of a launch are enumerated group
 // by group, and inside a group either unit by unit (n-block outer, m-block
 // inner: consecutive CTAs share the B tile, the whole A slice stays in L2) or
