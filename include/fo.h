@@ -111,7 +111,12 @@ typedef struct {
   int32_t epilogue;     /* fo_epilogue (fo_ag_gemm only)                              */
   int32_t sm_pairs;     /* GEMM tiles: 0 = automatic (256x256 tiles on SM pairs when every
                            unit's rows are a multiple of 256), 1 = single-SM 128x256 tiles */
-  int32_t reserved;
+  int32_t compute_only; /* timing diagnostic (fo_ag_gemm, fo_gemm_rs, fo_qsplit_attn): every
+                           kernel of the chosen order runs, every ring flag is published
+                           before the launch and no ring copy is enqueued, so the call takes
+                           the compute time of that order with the transfers removed.  The
+                           receive buffers keep whatever an earlier call left in them: the
+                           results are meaningless.  Not accepted with host buffers. */
 } fo_opts;
 
 /* Version of this ABI (major*100 + minor). */
@@ -245,8 +250,10 @@ FO_API fo_status fo_a2a_gemm(fo_ctx* ctx, const fo_mat* C, const fo_mat* W, int 
  *   X_shards[r] [m, K]; W_col[r] [Nr, K]; dY[r] [P*m, Nr]            (inputs, bf16)
  *   dX[d] [m, K] = sum_r dY[r][rows d*m..] W_col[r]                  (Flash-RS)
  *   dW[r] [Nr, K] = dY[r]^T AG(X)                                     (local GEMM)
- * Nr and P*m multiples of 8.  W_col^T, dY^T and AG(X)^T are laid out in the context's
- * workspace by a transpose kernel; opts->order applies to the reduce-scatter. */
+ * Nr and P*m multiples of 8.  W_col^T, dY^T and AG(X)^T are not materialised: the
+ * tensor cores read W_col, dY and the token slices in place as MN-major operands (only
+ * the P token slices are stacked into one workspace buffer for the weight gradient);
+ * opts->order applies to the reduce-scatter. */
 FO_API fo_status fo_col_linear_backward(fo_ctx* ctx, const fo_mat* X_shards, const fo_mat* W_col,
                                  const fo_mat* dY, int P, const fo_mat* dX, const fo_mat* dW,
                                  const fo_opts* opts, void* stream);
@@ -296,12 +303,19 @@ FO_API fo_status fo_attn_layer(fo_ctx* ctx, const fo_mat* X_shards, const fo_mat
  *                   the call's work has completed on `stream` (NULL: none).
  * Shapes whose receive slots (P*(P-1)*m*N*4 bytes) or flags exceed the static
  * area are rejected with FO_ERR_UNSUPPORTED.  The first call on a device does a
- * one-time set-up (it resolves the array's device address with that device
- * current); make that first call before any stream capture.  Every call shares
- * the array and keeps the previous call's contents (flags are epoch-valued and
- * the control words are cleared per call); calls whose work overlaps on the
- * GPU race, so order them on one stream.  Not thread-safe across host threads
- * using the same device concurrently with overlapping work. */
+ * one-time set-up (it configures the kernel with that device current); make that
+ * first call before any stream capture.  Every call asks for the array's device
+ * address with the caller's device current (in host code the array's name is
+ * only a stand-in).  Every call shares the array, which keeps the previous
+ * call's contents: each call first clears, on `stream`, the control words and
+ * the flag words it uses, so no call depends on what an earlier one left.  Calls
+ * whose work overlaps on the GPU race on the array, so order them on one stream;
+ * host threads that use one device at once must order their calls too.
+ * The persistent kernel's CTAs wait on one another (a tile waits for the partial
+ * sum of a tile of smaller index), so all of them must be resident at once: the
+ * call needs the whole GPU while it runs.  Kernels running beside it can leave
+ * some CTAs unscheduled; the waiting ones then give up after timeout_us and the
+ * status reads FO_ERR_TIMEOUT. */
 FO_API fo_status fo_gemm_rs_noalloc(const fo_mat* X, const fo_mat* W_row, int P, const fo_mat* Y,
                                     uint32_t timeout_us, uint32_t* status, void* stream);
 

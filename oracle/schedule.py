@@ -14,9 +14,9 @@ Distributed LLM Training", technical summary section 2 (Methodology):
 * Section 1 (Problem statement): data slicing interleaves chunks of compute and
   communication, but the communication of the last chunk cannot overlap.
 
-Readings where the pages are silent (listed in the design doc): the ring sends rank
-r -> r+1 (``direction=+1``; ``-1`` is the mirror ring); one slice per rank
-(M/P rows); the naive order computes chunks in ascending index on every rank.
+Readings taken where the pages are silent: the ring sends rank r -> r+1
+(``direction=+1``; ``-1`` is the mirror ring); one slice per rank (M/P rows);
+the naive order computes chunks in ascending index on every rank.
 """
 from __future__ import annotations
 

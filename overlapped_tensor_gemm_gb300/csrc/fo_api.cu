@@ -215,6 +215,8 @@ fo_status check_common(fo_ctx* ctx, int P, const fo_opts* opts) {
     if (opts->epilogue < FO_EPI_PLAIN || opts->epilogue > FO_EPI_SILU_GATE)
       return fail(FO_ERR_INVALID_ARG, "unknown epilogue %d", opts->epilogue);
     if (opts->sm_pairs < 0 || opts->sm_pairs > 1) return fail(FO_ERR_INVALID_ARG, "sm_pairs must be 0 or 1");
+    if (opts->compute_only < 0 || opts->compute_only > 1)
+      return fail(FO_ERR_INVALID_ARG, "compute_only must be 0 or 1");
   }
   return FO_OK;
 }
@@ -652,19 +654,28 @@ fo_status ag_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_
   // slices reused across all weight tiles) moves fewer bytes.
   const bool weight_major = static_cast<double>(P - 1) * m * K * 2 <= kWeightMajorMaxBytes;
 
+  const bool compute_only = o.compute_only != 0;
+  if (compute_only && a.Xh) return fail(FO_ERR_UNSUPPORTED, "compute_only is a device-buffer timing mode");
   if (o.order == FO_ORDER_FLASH || o.order == FO_ORDER_NAIVE) {
     Launch L;
     FO_TRY(build(L, 0, m, true, xmap, rmap, wmap, weight_major));
-    FO_CUDA(cudaEventRecord(ctx->ev_fork, stream));
-    FO_TRY(launch_gemm(ctx, L, o, stream));  // runs concurrently with the ring below
-    for (int r = 0; r < P; ++r) FO_CUDA(cudaStreamWaitEvent(ctx->link[r], ctx->ev_fork, 0));
+    if (compute_only) {  // the same launch with every arrival flag already published
+      FO_CUDA(launch_fill_u32(flags + kAgFlagBase, static_cast<int64_t>(P) * P, epoch, stream));
+      return launch_gemm(ctx, L, o, stream);
+    }
+    // The ring's copies are enqueued before the persistent GEMM that waits on them: they
+    // run concurrently, and an executor that serialises the work (a profiler) runs the
+    // copies first instead of a kernel that waits for copies queued behind it.
+    FO_TRY(fork_links(ctx, P, stream));
     if (a.Xh) FO_TRY(enqueue_uploads(ctx, a, epoch, flags));
     FO_TRY(enqueue_ag_ring(ctx, a, 0, m, true, epoch, o.fault, flags));
+    FO_TRY(launch_gemm(ctx, L, o, stream));
     return join_links(ctx, P, stream);
   }
   if (o.order == FO_ORDER_SERIAL) {
     Launch L;
     FO_TRY(build(L, 0, m, false, xmap, rmap, wmap, weight_major));
+    if (compute_only) return launch_gemm(ctx, L, o, stream);
     FO_CUDA(cudaEventRecord(ctx->ev_phase[0], stream));
     FO_TRY(fork_links(ctx, P, stream));
     FO_TRY(enqueue_ag_ring(ctx, a, 0, m, false, epoch, FO_FAULT_NONE, flags));
@@ -680,6 +691,14 @@ fo_status ag_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_
   const int n = o.n_slices ? o.n_slices : P;
   if (m % n != 0) return fail(FO_ERR_SHAPE, "slice rows m=%lld not divisible by n_slices=%d", (long long)m, n);
   const int64_t sub = m / n;
+  if (compute_only) {  // the per-slice launches alone
+    for (int i = 0; i < n; ++i) {
+      Launch L;
+      FO_TRY(build(L, i * sub, sub, false, xmap, rmap, wmap, false));
+      FO_TRY(launch_gemm(ctx, L, o, stream));
+    }
+    return FO_OK;
+  }
   FO_TRY(fork_links(ctx, P, stream));
   for (int i = 0; i < n; ++i) {
     FO_TRY(enqueue_ag_ring(ctx, a, i * sub, sub, false, epoch, FO_FAULT_NONE, flags));
@@ -780,6 +799,8 @@ fo_status rs_flash(fo_ctx* ctx, const RsArgs& a, const fo_opts& o, cudaStream_t 
   }
   L.p.mn_major = a.w_kn ? 2 : 0;
   FO_TRY(L.finish(epoch, timeout_ns(o), flags, ctx->ctrl, 0));
+  if (o.compute_only)  // every partial-sum flag published: no tile waits on another
+    FO_CUDA(launch_fill_u32(flags + kRsFlagBase, fbase(P - 1, P) - kRsFlagBase, epoch, stream));
   FO_TRY(launch_gemm(ctx, L, o, stream));
   if (done) {
     for (int i = 0; i < L.num_units; ++i) {
@@ -834,17 +855,20 @@ fo_status rs_partials(fo_ctx* ctx, const RsArgs& a, const fo_opts& o, cudaStream
 // Ring reduce of rows [row0, row0 + rows) of every chunk, issued on `rs` (adds)
 // and the link streams (hops).  Hop h: rank c+h sends its running sum of chunk c
 // to rank c+h+1, which adds its own partial (in place) or, at the owner, rounds
-// the final sum into Y[c].
-fo_status rs_ring_reduce(fo_ctx* ctx, const RsArgs& a, cudaStream_t rs, int64_t row0, int64_t rows) {
+// the final sum into Y[c].  copies == false: the adds alone (compute-only timing).
+fo_status rs_ring_reduce(fo_ctx* ctx, const RsArgs& a, cudaStream_t rs, int64_t row0, int64_t rows,
+                         bool copies = true) {
   const int P = a.P;  // P >= 2 (a single rank takes the fused path)
   for (int h = 1; h < P; ++h) {
-    FO_TRY(fork_links(ctx, P, rs));
-    for (int c = 0; c < P; ++c) {
-      const int s = mod(c + h, P), d = mod(c + h + 1, P);
-      FO_TRY(copy_rows(rs_slot(a, a.recv, d, h) + row0 * a.N, a.N, rs_slot(a, a.part, s, c) + row0 * a.N, a.N,
-                       rows, a.N, 4, ctx->link[s]));
+    if (copies) {
+      FO_TRY(fork_links(ctx, P, rs));
+      for (int c = 0; c < P; ++c) {
+        const int s = mod(c + h, P), d = mod(c + h + 1, P);
+        FO_TRY(copy_rows(rs_slot(a, a.recv, d, h) + row0 * a.N, a.N, rs_slot(a, a.part, s, c) + row0 * a.N, a.N,
+                         rows, a.N, 4, ctx->link[s]));
+      }
+      FO_TRY(join_links(ctx, P, rs));
     }
-    FO_TRY(join_links(ctx, P, rs));
     for (int c = 0; c < P; ++c) {
       const int d = mod(c + h + 1, P);
       float* mine = rs_slot(a, a.part, d, c) + row0 * a.N;
@@ -895,6 +919,15 @@ fo_status rs_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_
   void* part_v = nullptr;
   FO_TRY(ensure_buf(ctx, kBufPart, static_cast<size_t>(P) * P * m * N * 4, &part_v));
   a.part = static_cast<float*>(part_v);
+  if (o.compute_only) {  // the baselines' partial GEMMs and adds, no copies
+    const int n = o.order == FO_ORDER_SLICING ? (o.n_slices ? o.n_slices : P) : 1;
+    if (m % n != 0) return fail(FO_ERR_SHAPE, "slice rows m=%lld not divisible by n_slices=%d", (long long)m, n);
+    for (int i = 0; i < n; ++i) {
+      FO_TRY(rs_partials(ctx, a, o, stream, i * (m / n), m / n, flags, epoch));
+      FO_TRY(rs_ring_reduce(ctx, a, stream, i * (m / n), m / n, false));
+    }
+    return FO_OK;
+  }
   if (o.order == FO_ORDER_SERIAL) {
     FO_CUDA(cudaEventRecord(ctx->ev_phase[0], stream));
     FO_TRY(rs_partials(ctx, a, o, stream, 0, m, flags, epoch));
@@ -1094,9 +1127,11 @@ fo_status a2a_gemm_run(fo_ctx* ctx, const fo_mat* C, const fo_mat* W, int P, con
     ctx->phase_gemm_first = false;
     return FO_OK;
   }
+  // hops first in host order: they run concurrently with the GEMM that waits on them, and a
+  // serialising executor runs them before it
   FO_TRY(fork_links(ctx, P, stream));  // the links start after the caller's prior work
-  FO_TRY(launch_gemm(ctx, L, o, stream));  // runs concurrently with the hops below
   FO_TRY(hops(true));
+  FO_TRY(launch_gemm(ctx, L, o, stream));
   return join_links(ctx, P, stream);
 }
 
@@ -1478,6 +1513,7 @@ fo_status fo_mlp_layer(fo_ctx* ctx, const fo_mat* X_shards, const fo_mat* W_col,
 fo_status fo_mlp_layer_host(fo_ctx* ctx, const fo_mat* X_shards, const fo_mat* W_col, const fo_mat* W_row, int P,
                             int gated, const fo_mat* Z, const fo_opts* opts, void* stream) {
   FO_TRY(check_common(ctx, P, opts));
+  if (opts && opts->compute_only) return fail(FO_ERR_UNSUPPORTED, "compute_only is a device-buffer timing mode");
   if (!X_shards || !W_col || !W_row || !Z) return fail(FO_ERR_INVALID_ARG, "null matrix array");
   FO_CUDA(cudaSetDevice(ctx->device));
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -799,9 +799,11 @@ fo_status attn_run(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K, const fo_mat* 
                                                        reinterpret_cast<uint16_t*>(vt_slot(r, r)), m, HD);
     if (cudaGetLastError() != cudaSuccess) return host_fail(FO_ERR_CUDA, "transpose launch failed");
   }
-  // 2) the attention kernel, then 3) the K/V ring on the link streams, concurrently
+  // 2) the K/V ring on the link streams, then 3) the attention kernel, concurrently
   //    (serial baseline: the whole ring first, then the kernel without flag waits);
-  //    independent problems: the kernel alone
+  //    independent problems: the kernel alone.  The ring is enqueued first: an executor
+  //    that serialises the work (a profiler) then runs the copies before the kernel that
+  //    waits on them.
   if (!ring) {
     p.wait_flags = 0;
     attn_kernel<<<host_grid(ctx, o, p.total_items), kAttnThreads, kAttnSmem, stream>>>(p);
@@ -813,13 +815,15 @@ fo_status attn_run(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K, const fo_mat* 
   int grid = host_grid(ctx, o, p.total_items);
   if (!serial && reserve_sms > 0 && grid > host_num_sms(ctx) - reserve_sms) grid = host_num_sms(ctx) - reserve_sms;
   p.wait_flags = serial ? 0 : 1;
-  if (serial) host_phase_record(ctx, 0, stream);
-  if ((st = host_fork(ctx, P, stream)) != FO_OK) return st;
-  if (!serial) {
+  if (o.compute_only) {  // the kernel alone, every arrival flag already published
+    if (!serial && launch_fill_u32(flags, static_cast<int64_t>(P) * P, epoch, stream) != cudaSuccess)
+      return host_fail(FO_ERR_CUDA, "flag fill launch failed");
     attn_kernel<<<grid, kAttnThreads, kAttnSmem, stream>>>(p);
     const cudaError_t le = cudaGetLastError();
-    if (le != cudaSuccess) return host_fail(FO_ERR_CUDA, cudaGetErrorString(le));
+    return le != cudaSuccess ? host_fail(FO_ERR_CUDA, cudaGetErrorString(le)) : FO_OK;
   }
+  if (serial) host_phase_record(ctx, 0, stream);
+  if ((st = host_fork(ctx, P, stream)) != FO_OK) return st;
   const bool prune = o.causal_prune && causal;
   for (int t = 1; t < P; ++t) {
     for (int r = 0; r < P; ++r) {
@@ -838,6 +842,11 @@ fo_status attn_run(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K, const fo_mat* 
       if ((st = host_write_flag(ls, flags + d * P + s, epoch)) != FO_OK) return st;
       if (cudaEventRecord(host_ev_hop(ctx, r, t), ls) != cudaSuccess) return host_fail(FO_ERR_CUDA, "event failed");
     }
+  }
+  if (!serial) {
+    attn_kernel<<<grid, kAttnThreads, kAttnSmem, stream>>>(p);
+    const cudaError_t le = cudaGetLastError();
+    if (le != cudaSuccess) return host_fail(FO_ERR_CUDA, cudaGetErrorString(le));
   }
   if ((st = host_join(ctx, P, stream)) != FO_OK) return st;
   if (serial) {

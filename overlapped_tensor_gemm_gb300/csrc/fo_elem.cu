@@ -65,6 +65,13 @@ __global__ void add_f32_kernel(const float* __restrict__ a, int64_t lda, const f
   }
 }
 
+// Every word of flags[0, n) = value (the ring flags of a timing run with no transfers).
+__global__ void fill_u32_kernel(uint32_t* flags, int64_t n, uint32_t value) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    flags[i] = value;
+}
+
 int sm_count() {
   static int n = 0;
   if (n == 0) {
@@ -99,6 +106,12 @@ cudaError_t launch_add_f32(const float* a, int64_t lda, const float* b, int64_t 
   return cudaGetLastError();
 }
 
+cudaError_t launch_fill_u32(uint32_t* flags, int64_t n, uint32_t value, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  fill_u32_kernel<<<grid_for(n, 256), 256, 0, s>>>(flags, n, value);
+  return cudaGetLastError();
+}
+
 // With lazy module loading a kernel is loaded at its first launch; a helper kernel first
 // launched on a side stream while a persistent kernel that waits for its result occupies
 // the device was measured to stall until that kernel gave up.  Querying the attributes
@@ -107,6 +120,7 @@ cudaError_t preload_helper_kernels() {
   cudaFuncAttributes a;
   cudaError_t e = cudaFuncGetAttributes(&a, silu_mul_kernel);
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, add_f32_kernel);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, fill_u32_kernel);
   return e;
 }
 

@@ -131,6 +131,8 @@ struct SiluMulArgs {
 cudaError_t launch_silu_mul(const SiluMulArgs& a, cudaStream_t s);
 // loads the helper kernels (glue, reduce adds) before any persistent kernel runs
 cudaError_t preload_helper_kernels();
+// flags[0, n) = value
+cudaError_t launch_fill_u32(uint32_t* flags, int64_t n, uint32_t value, cudaStream_t s);
 // c = a + b (fp32 inputs); c is fp32 (c_f32) or bf16 (c_bf16), exactly one non-null
 cudaError_t launch_add_f32(const float* a, int64_t lda, const float* b, int64_t ldb, float* c_f32,
                            uint16_t* c_bf16, int64_t ldc, int64_t rows, int64_t cols, cudaStream_t s);

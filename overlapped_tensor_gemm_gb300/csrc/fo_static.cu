@@ -11,10 +11,11 @@
 //
 // The array below is part of the library image: every GPU that loads the
 // library holds kStaticScratchBytes of it until the process exits.  All calls
-// share it, and it keeps the previous call's contents: the control words are
-// cleared at the start of every call and the ring flags are epoch-valued (a
-// per-device counter), so nothing stale is ever read as fresh.  Calls whose
-// kernels overlap on the GPU race on the array.
+// share it, and it keeps the previous call's contents, so every call starts by
+// clearing, on its own stream, the control words and the flag words its shape
+// uses; its flags are then released with the fixed value 1.  Nothing a call
+// reads depends on what an earlier call left behind.  Calls whose kernels
+// overlap on the GPU race on the array.
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -35,9 +36,7 @@ constexpr size_t kSlotBytes = kStaticScratchBytes - kCtrlBytes - kFlagBytes;
 static __device__ __align__(256) unsigned char g_rs_scratch[kStaticScratchBytes];
 
 struct DeviceState {
-  bool ready = false;
-  unsigned char* scratch = nullptr;  // device address of g_rs_scratch on this device
-  uint32_t epoch = 0;
+  bool ready = false;  // the GEMM kernel is configured for this device
   int num_sms = 0;
 };
 
@@ -45,24 +44,30 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 DeviceState g_state[kMaxDevices];
 
-// Once per device, with that device current: resolve the array's device address
-// (in host code the symbol is only a stand-in) and configure the kernel.
+// Once per device, with that device current: configure the kernel (its shared-memory
+// size attribute) and read the SM count.
 fo_status device_setup(int dev, DeviceState** out) {
   if (dev < 0 || dev >= kMaxDevices) return host_fail(FO_ERR_UNSUPPORTED, "device index above 63");
   DeviceState& s = g_state[dev];
   if (!s.ready) {
-    void* ptr = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_rs_scratch);
-    if (e != cudaSuccess) return host_fail(FO_ERR_CUDA, cudaGetErrorString(e));
     if (gemm_configure() != cudaSuccess) return host_fail(FO_ERR_CUDA, "gemm kernel configuration failed");
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
       return host_fail(FO_ERR_CUDA, "cannot read the SM count");
-    s.scratch = static_cast<unsigned char*>(ptr);
     s.num_sms = sms;
     s.ready = true;
   }
   *out = &s;
+  return FO_OK;
+}
+
+// The array's address on the current device.  In host code the symbol is only a
+// stand-in, so the address is asked for on every call (cheap); it is never cached.
+fo_status scratch_address(unsigned char** out) {
+  void* ptr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_rs_scratch);
+  if (e != cudaSuccess) return host_fail(FO_ERR_CUDA, cudaGetErrorString(e));
+  *out = static_cast<unsigned char*>(ptr);
   return FO_OK;
 }
 
@@ -105,17 +110,21 @@ extern "C" FO_API fo_status fo_gemm_rs_noalloc(const fo_mat* X, const fo_mat* W_
   if (cudaGetDevice(&dev) != cudaSuccess) return host_fail(FO_ERR_CUDA, "no current device");
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState* ds = nullptr;
+  unsigned char* scratch = nullptr;
   {
-    const fo_status st = device_setup(dev, &ds);
+    fo_status st = device_setup(dev, &ds);
+    if (st == FO_OK) st = scratch_address(&scratch);
     if (st != FO_OK) return st;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint32_t* ctrl = reinterpret_cast<uint32_t*>(ds->scratch);
-  uint32_t* flags = reinterpret_cast<uint32_t*>(ds->scratch + kCtrlBytes);
-  float* slots = reinterpret_cast<float*>(ds->scratch + kCtrlBytes + kFlagBytes);
-  if (cudaMemsetAsync(ctrl, 0, kCtrlWords * sizeof(uint32_t), s) != cudaSuccess)
-    return host_fail(FO_ERR_CUDA, "control block reset failed");
-  const uint32_t epoch = ++ds->epoch;
+  uint32_t* ctrl = reinterpret_cast<uint32_t*>(scratch);
+  uint32_t* flags = reinterpret_cast<uint32_t*>(scratch + kCtrlBytes);
+  float* slots = reinterpret_cast<float*>(scratch + kCtrlBytes + kFlagBytes);
+  // this call's control words and flags start at zero, whatever an earlier call left
+  if (cudaMemsetAsync(ctrl, 0, kCtrlWords * sizeof(uint32_t), s) != cudaSuccess ||
+      cudaMemsetAsync(flags, 0, flag_bytes, s) != cudaSuccess)
+    return host_fail(FO_ERR_CUDA, "scratch reset failed");
+  const uint32_t epoch = 1;  // every flag of this call is released with the value 1
 
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
@@ -176,6 +185,8 @@ extern "C" FO_API fo_status fo_gemm_rs_noalloc(const fo_mat* X, const fo_mat* W_
   p.timeout_ns = (timeout_us ? static_cast<uint64_t>(timeout_us) : 1000000ull) * 1000ull;
   p.flags = flags;
   p.ctrl = ctrl;
+  // Tiles wait on tiles of smaller index owned by other CTAs, so every CTA of this grid must
+  // be resident at once: the call needs the whole GPU while it runs.
   const int grid = p.total_tiles < ds->num_sms ? p.total_tiles : ds->num_sms;
   if (gemm_launch(p, grid, s) != cudaSuccess) return host_fail(FO_ERR_CUDA, "gemm kernel launch failed");
   if (status && cudaMemcpyAsync(status, ctrl + kCtrlError, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s) !=

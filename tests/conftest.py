@@ -15,3 +15,11 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def repo_root():
     return ROOT
+
+
+@pytest.fixture(autouse=True)
+def _output_canary():
+    """After every test: the padding and guard rows around its guarded() outputs are intact."""
+    yield
+    from helpers import check_guards
+    check_guards()

@@ -50,10 +50,42 @@ def assert_close(got: np.ndarray, ref: np.ndarray, what: str = "", round_ref: bo
     assert mx <= lim, f"{what}: max-abs {mx:.3e} > {lim:.3e}"
 
 
-def padded(rows: int, cols: int, dtype, fill=float("nan"), device="cuda"):
-    """[rows, cols] view of a buffer whose row pitch is padded to 16 bytes."""
-    import torch
+# Output buffers whose surroundings are checked after every test (see check_guards).
+_GUARDED = []
+
+
+def guarded(shape, dtype, device="cuda"):
+    """A [rows, cols] output view inside a NaN-filled buffer: the row pitch carries at
+    least 16 bytes of padding and one guard row sits above and one below the view.
+    check_guards(), run after every test, asserts that all of them are still NaN -- a
+    cheap canary for out-of-bounds writes of the kernels."""
+    rows, cols = shape
     esz = torch.empty((), dtype=dtype).element_size()
     per = 16 // esz
-    ld = (cols + per - 1) // per * per
-    return torch.full((rows, ld), fill, dtype=dtype, device=device)[:, :cols]
+    ld = (cols + per - 1) // per * per + per
+    base = torch.full((rows + 2, ld), float("nan"), dtype=dtype, device=device)
+    _GUARDED.append((base, rows, cols))
+    return base[1:rows + 1, :cols]
+
+
+def padded(rows: int, cols: int, dtype, fill=float("nan"), device="cuda"):
+    """[rows, cols] view of a NaN-filled buffer with a padded row pitch and guard rows
+    (guarded()); `fill` is kept for the call sites' readability and must be NaN."""
+    assert fill != fill, "the canary needs a NaN fill"
+    return guarded((rows, cols), dtype, device)
+
+
+def check_guards():
+    """Asserts that the padding and guard rows of every guarded() buffer of the test that
+    just ran are untouched, then forgets the buffers."""
+    bad = []
+    try:
+        for base, rows, cols in _GUARDED:
+            pad = base[1:rows + 1, cols:]
+            ok = bool(torch.isnan(base[0]).all()) and bool(torch.isnan(base[rows + 1]).all())
+            ok = ok and (pad.numel() == 0 or bool(torch.isnan(pad).all()))
+            if not ok:
+                bad.append((rows, cols))
+    finally:
+        _GUARDED.clear()
+    assert not bad, f"out-of-bounds write next to output buffers of shape {bad}"

@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import fo_workloads as wl
-from helpers import assert_close, f64, to_bits, to_dev
+from helpers import assert_close, f64, to_bits, to_dev, guarded
 from oracle import bf16, ops
 
 pytestmark = pytest.mark.gpu
@@ -24,7 +24,7 @@ def _attn(ctx, P, m, H, seed, causal=True, **kw):
     Q = [to_dev(x).reshape(m, H * 128) for x in inp["Q"]]
     K = [to_dev(x).reshape(m, H * 128) for x in inp["K"]]
     V = [to_dev(x).reshape(m, H * 128) for x in inp["V"]]
-    O = [torch.full((m, H * 128), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    O = [guarded((m, H * 128), torch.bfloat16) for _ in range(P)]
     ctx.qsplit_attn(Q, K, V, O, heads=H, head_dim=128, causal=causal, **kw)
     torch.cuda.synchronize()
     ctx.poll()

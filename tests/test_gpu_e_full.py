@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import fo_workloads as wl
-from helpers import assert_close, f64, to_bits, to_dev
+from helpers import assert_close, f64, to_bits, to_dev, guarded
 from oracle import ops
 
 pytestmark = pytest.mark.gpu
@@ -29,7 +29,7 @@ def _mlp_check(ctx, cfg, X_bits, Wc_bits, Wr_bits, rows_per_slice, seed):
     X = [to_dev(x) for x in X_bits]
     Wc = [to_dev(w) for w in Wc_bits]
     Wr = [to_dev(w) for w in Wr_bits]
-    Z = [torch.full((cfg.m, cfg.hidden), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(cfg.P)]
+    Z = [guarded((cfg.m, cfg.hidden), torch.bfloat16) for _ in range(cfg.P)]
     ctx.mlp_layer(X, Wc, Wr, Z, gated=cfg.gated)
     torch.cuda.synchronize()
     ctx.poll()
@@ -73,7 +73,7 @@ def test_tail_rs_full(ctx, order):
     inp = wl.rs_inputs(c.P, c.tokens, c.n_out, c.k_row, c.seed, integer=False)
     X = [to_dev(x) for x in inp["X"]]
     W = [to_dev(w) for w in inp["W_row"]]
-    Y = [torch.full((c.m, c.n_out), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(c.P)]
+    Y = [guarded((c.m, c.n_out), torch.bfloat16) for _ in range(c.P)]
     ctx.gemm_rs(X, W, Y, order=order)
     torch.cuda.synchronize()
     ctx.poll()
@@ -90,7 +90,7 @@ def test_attention_full_sampled_rows(ctx):
     Q = [to_dev(x).reshape(shape) for x in inp["Q"]]
     K = [to_dev(x).reshape(shape) for x in inp["K"]]
     V = [to_dev(x).reshape(shape) for x in inp["V"]]
-    O = [torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(c.P)]
+    O = [guarded(shape, torch.bfloat16) for _ in range(c.P)]
     ctx.qsplit_attn(Q, K, V, O, heads=c.heads, head_dim=c.head_dim)
     torch.cuda.synchronize()
     ctx.poll()

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import fo_workloads as wl
-from helpers import assert_close, f64, to_bits, to_dev
+from helpers import assert_close, f64, to_bits, to_dev, guarded
 from oracle import ops
 
 pytestmark = pytest.mark.gpu
@@ -26,7 +26,7 @@ def _run(ctx, P, tokens, hidden, heads, seed, causal=True, **kw):
     Wq = [to_dev(w) for w in inp["W_qkv"]]
     Wo = [to_dev(w) for w in inp["W_o"]]
     m = tokens // P
-    Z = [torch.full((m, hidden), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    Z = [guarded((m, hidden), torch.bfloat16) for _ in range(P)]
     ctx.attn_layer(X, Wq, Wo, Z, heads=heads, causal=causal, **kw)
     torch.cuda.synchronize()
     ctx.poll()

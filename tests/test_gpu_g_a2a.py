@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import fo_workloads as wl
-from helpers import assert_bits_equal, assert_close, f64, to_bits, to_dev
+from helpers import assert_bits_equal, assert_close, f64, to_bits, to_dev, guarded
 from oracle import ops
 
 pytestmark = pytest.mark.gpu
@@ -40,7 +40,7 @@ def _check(got, ref, integer, what):
 def _gemm_a2a(ctx, P, m, K, Nb, seed, integer, **kw):
     X = _gen(seed, integer, [(m, K)] * P, [1.0] * P)
     W = _gen(seed + 1, integer, [(P * Nb, K)] * P, [wl.W_STD] * P)
-    Y = [torch.full((P * m, Nb), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    Y = [guarded((P * m, Nb), torch.bfloat16) for _ in range(P)]
     ctx.gemm_a2a([to_dev(x) for x in X], [to_dev(w) for w in W], Y, **kw)
     torch.cuda.synchronize()
     ctx.poll()
@@ -51,7 +51,7 @@ def _gemm_a2a(ctx, P, m, K, Nb, seed, integer, **kw):
 def _a2a_gemm(ctx, P, m, Kc, N, seed, integer, **kw):
     C = _gen(seed, integer, [(P * m, Kc)] * P, [1.0] * P)
     W = _gen(seed + 1, integer, [(N, P * Kc)] * P, [wl.W_STD] * P)
-    Y = [torch.full((m, N), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    Y = [guarded((m, N), torch.bfloat16) for _ in range(P)]
     ctx.a2a_gemm([to_dev(c) for c in C], [to_dev(w) for w in W], Y, **kw)
     torch.cuda.synchronize()
     ctx.poll()

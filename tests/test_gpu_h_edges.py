@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import fo_workloads as wl
-from helpers import assert_bits_equal, assert_close, f64, to_bits, to_dev
+from helpers import assert_bits_equal, assert_close, f64, to_bits, to_dev, guarded
 from oracle import ops
 
 pytestmark = pytest.mark.gpu
@@ -87,7 +87,7 @@ def test_eight_rank_query_split_attention(ctx):
     Q = [to_dev(x).reshape(m, 128) for x in inp["Q"]]
     K = [to_dev(x).reshape(m, 128) for x in inp["K"]]
     V = [to_dev(x).reshape(m, 128) for x in inp["V"]]
-    O = [torch.full((m, 128), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    O = [guarded((m, 128), torch.bfloat16) for _ in range(P)]
     ctx.qsplit_attn(Q, K, V, O, heads=H, head_dim=128)
     torch.cuda.synchronize()
     ctx.poll()

@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import fo_workloads as wl
-from helpers import assert_bits_equal, assert_close, f64, to_bits, to_dev
+from helpers import assert_bits_equal, assert_close, f64, to_bits, to_dev, guarded
 from oracle import ops
 
 pytestmark = pytest.mark.gpu
@@ -36,8 +36,8 @@ def _col(ctx, P, m, K, Nr, seed, integer, **kw):
     X = [_gen(g, (m, K), integer) for _ in range(P)]
     W = [_gen(g, (Nr, K), integer, wl.W_STD) for _ in range(P)]
     dY = [_gen(g, (P * m, Nr), integer) for _ in range(P)]
-    dX = [torch.full((m, K), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
-    dW = [torch.full((Nr, K), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    dX = [guarded((m, K), torch.bfloat16) for _ in range(P)]
+    dW = [guarded((Nr, K), torch.bfloat16) for _ in range(P)]
     ctx.col_linear_backward([to_dev(x) for x in X], [to_dev(w) for w in W], [to_dev(d) for d in dY], dX, dW, **kw)
     torch.cuda.synchronize()
     ctx.poll()
@@ -51,8 +51,8 @@ def _row(ctx, P, m, Fr, N, seed, integer, **kw):
     H = [_gen(g, (P * m, Fr), integer) for _ in range(P)]
     W = [_gen(g, (N, Fr), integer, wl.W_STD) for _ in range(P)]
     dZ = [_gen(g, (m, N), integer) for _ in range(P)]
-    dH = [torch.full((P * m, Fr), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
-    dW = [torch.full((N, Fr), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    dH = [guarded((P * m, Fr), torch.bfloat16) for _ in range(P)]
+    dW = [guarded((N, Fr), torch.bfloat16) for _ in range(P)]
     ctx.row_linear_backward([to_dev(h) for h in H], [to_dev(w) for w in W], [to_dev(z) for z in dZ], dH, dW, **kw)
     torch.cuda.synchronize()
     ctx.poll()
