@@ -58,7 +58,8 @@ typedef enum {
   FO_ERR_UNSUPPORTED = 3,   /* valid but outside what the kernels handle        */
   FO_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed                */
   FO_ERR_TIMEOUT = 5,       /* a device wait ran past opts.timeout_us           */
-  FO_ERR_OOM = 6            /* workspace growth failed                          */
+  FO_ERR_OOM = 6,           /* workspace growth failed                          */
+  FO_ERR_RANGE = 7          /* an input value outside what a kernel represents  */
 } fo_status;
 
 typedef enum { FO_BF16 = 0, FO_F32 = 1 } fo_dtype;
@@ -135,8 +136,9 @@ FO_API fo_status fo_ctx_create(int device, fo_ctx** out);
 FO_API fo_status fo_ctx_destroy(fo_ctx* ctx);
 
 /* Reads the device error word after the caller has synchronised the stream of
- * the previous calls, and clears it.  FO_OK, or FO_ERR_TIMEOUT when a device
- * wait gave up (the work of that call is then incomplete). */
+ * the previous calls, and clears it.  FO_OK; FO_ERR_TIMEOUT when a device wait
+ * gave up (the work of that call is then incomplete); FO_ERR_RANGE when an input
+ * held a value the kernels cannot represent (see fo_qsplit_attn). */
 FO_API fo_status fo_ctx_poll(fo_ctx* ctx);
 
 /* Device milliseconds of the two phases of the last FO_ORDER_SERIAL call on
@@ -212,6 +214,12 @@ FO_API fo_status fo_mlp_layer_host(fo_ctx* ctx, const fo_mat* X_shards, const fo
  *   causal != 0: key j attends query i only if j <= i (global token indices);
  *   slices wholly above the diagonal are skipped.
  * Softmax statistics and the output accumulator are fp32 (online softmax).
+ * The P.V product runs on fp16 tensor cores: V is converted from bf16 to fp16,
+ * which is exact for |v| in [2^-14, 65504] and for 0.  A finite |v| above 65504
+ * would become infinite: the conversion counts such values and the call then
+ * ends with FO_ERR_RANGE from fo_ctx_poll (the outputs of that call are not
+ * valid).  Nonzero |v| below 2^-14 keep fp16's subnormal precision (absolute
+ * error at most 2^-25 in V, hence in O). 
  * opts->order: FO_ORDER_FLASH (the ring runs while the kernel computes) or
  * FO_ORDER_SERIAL (baseline: the whole K/V ring first, then the kernel). */
 FO_API fo_status fo_qsplit_attn(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K_shards,

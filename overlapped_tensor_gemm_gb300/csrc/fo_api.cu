@@ -1373,6 +1373,9 @@ fo_status fo_ctx_poll(fo_ctx* ctx) {
   FO_CUDA(cudaMemcpy(w, ctx->ctrl, sizeof(w), cudaMemcpyDeviceToHost));
   if (w[kCtrlError] == 0) return FO_OK;
   FO_CUDA(cudaMemset(ctx->ctrl, 0, sizeof(w)));
+  if (w[kCtrlError] == FO_ERR_RANGE)
+    return fail(FO_ERR_RANGE, "input value out of the kernels' range (site %u, row %u): |V| above 65504, "
+                "the largest finite fp16 value", w[kCtrlWhere], w[kCtrlDetail]);
   return fail(static_cast<fo_status>(w[kCtrlError]), "device wait gave up (site %u, index %u)", w[kCtrlWhere],
               w[kCtrlDetail]);
 }

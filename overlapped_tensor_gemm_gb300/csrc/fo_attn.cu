@@ -683,19 +683,29 @@ __global__ void __maxnreg__(136) attn_kernel(const __grid_constant__ AttnParams 
 }
 
 // V [m, heads*128] bf16 (row pitch ld) -> V^T [heads*128, m] fp16, 64x64 tiles
-// through shared memory.  bf16 -> fp16 is exact inside fp16's normal range.
+// through shared memory.  bf16 -> fp16 is exact inside fp16's normal range; a finite
+// |v| above fp16's largest finite value (65504) would turn into infinity, so it is
+// recorded as FO_ERR_RANGE in the control block (detail: the token row).
 __global__ void transpose_kernel(const uint16_t* __restrict__ v, int64_t ld, uint16_t* __restrict__ vt, int64_t m,
-                                 int64_t hd) {
+                                 int64_t hd, uint32_t* ctrl) {
   __shared__ uint16_t tile[64][66];
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 64;  // token
   const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 64;  // feature
+  bool out_of_range = false;
+  int64_t bad_row = 0;
   for (int i = threadIdx.y; i < 64; i += blockDim.y) {
     const int64_t r = r0 + i, c = c0 + threadIdx.x;
     if (r < m && c < hd) {
       const float f = __uint_as_float(static_cast<uint32_t>(v[r * ld + c]) << 16);
+      const bool finite = (__float_as_uint(f) & 0x7f800000u) != 0x7f800000u;
+      if (finite && fabsf(f) > 65504.0f) {  // beyond fp16 (NaN and infinity stay what they are)
+        out_of_range = true;
+        bad_row = r;
+      }
       tile[i][threadIdx.x] = __half_as_ushort(__float2half_rn(f));
     }
   }
+  if (out_of_range) note_error(ctrl, FO_ERR_RANGE, kSiteVRange, static_cast<uint32_t>(bad_row));
   __syncthreads();
   for (int i = threadIdx.y; i < 64; i += blockDim.y) {
     const int64_t c = c0 + i, r = r0 + threadIdx.x;
@@ -796,7 +806,8 @@ fo_status attn_run(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K, const fo_mat* 
   for (int r = 0; r < P; ++r) {
     dim3 grid(static_cast<unsigned>((HD + 63) / 64), static_cast<unsigned>((m + 63) / 64));
     transpose_kernel<<<grid, dim3(64, 8), 0, stream>>>(static_cast<const uint16_t*>(V[r].ptr), V[r].ld,
-                                                       reinterpret_cast<uint16_t*>(vt_slot(r, r)), m, HD);
+                                                       reinterpret_cast<uint16_t*>(vt_slot(r, r)), m, HD,
+                                                       host_ctrl(ctx));
     if (cudaGetLastError() != cudaSuccess) return host_fail(FO_ERR_CUDA, "transpose launch failed");
   }
   // 2) the K/V ring on the link streams, then 3) the attention kernel, concurrently

@@ -81,6 +81,7 @@ __device__ void producer_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl)
     }
     const int nk = (u.k + kBK - 1) / kBK;
     const int a_row = u.a_row0 + tc.mb * kBM;
+    prefetch_partial(u, tc.mb * kBM, tc.nb * kBN);
     const bool gated = u.gated != 0;
     const int b_row = u.b_row0 + tc.nb * (gated ? kBN / 2 : kBN);
     const int b_row_up = u.b_row1 + tc.nb * (kBN / 2);

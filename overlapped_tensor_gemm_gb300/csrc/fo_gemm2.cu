@@ -63,6 +63,7 @@ __device__ void pair_producer(const GemmParams& p, uint8_t* tiles, PairCtl* ctl,
     }
     const int nk = (u.k + kBK - 1) / kBK;
     const int a_row = u.a_row0 + tc.mb * 2 * kBM + static_cast<int>(cta) * kBM;
+    prefetch_partial(u, tc.mb * 2 * kBM + static_cast<int>(cta) * kBM, tc.nb * kBN);
     // B rows of this CTA: gated tiles put the gate rows in the leader and the up rows in the peer
     const int b_row = u.gated ? (cta == 0 ? u.b_row0 : u.b_row1) + tc.nb * (kBN / 2)
                               : u.b_row0 + tc.nb * kBN + static_cast<int>(cta) * (kBN / 2);

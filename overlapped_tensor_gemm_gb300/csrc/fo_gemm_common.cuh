@@ -80,6 +80,23 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int tile) 
   return c;
 }
 
+// L2 prefetch of the fp32 partial sums that this CTA's epilogue adds to a tile: rows
+// [row0, row0 + 128) of the unit, columns [col0, col0 + kBN), one bulk prefetch per row
+// segment (at most 1 KiB).  Issued by the operand producer when the tile's first K block
+// is requested, a whole main loop before the epilogue reads them: in the Flash-RS order a
+// partial sum is written one ring step before it is added, long enough for it to have
+// left L2.  (A prefetch that comes before the partial sum is written only brings stale
+// lines into L2, where the later write updates them.)  Row pitches and column offsets are
+// multiples of 16 bytes: the reduce-scatter's N is a multiple of 4.
+__device__ __forceinline__ void prefetch_partial(const GemmUnit& u, int row0, int col0) {
+  if (u.acc_in == nullptr) return;
+  const int ncol = min(kBN, u.n_cols - col0);
+  if (ncol <= 0) return;
+  const uint32_t bytes = static_cast<uint32_t>(ncol) * 4u;
+  const int r1 = min(row0 + kBM, u.m_rows);
+  for (int r = row0; r < r1; ++r) prefetch_l2_bulk(u.acc_in + static_cast<int64_t>(r) * u.ld_acc + col0, bytes);
+}
+
 // ---------------------------------------------------------------------------
 // Partial-sum and fp32 epilogues through a per-warp staging buffer.
 //

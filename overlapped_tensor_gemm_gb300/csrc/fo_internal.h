@@ -109,7 +109,7 @@ enum CtrlWord : int {
 enum WaitSite : uint32_t {
   kSiteAgFlag = 1, kSiteFull = 2, kSiteEmpty = 3, kSiteTmemFull = 4,
   kSiteTmemEmpty = 5, kSiteAccInFlag = 6, kSiteDrain = 7, kSiteAttnFlag = 8,
-  kSiteAttnBar = 9
+  kSiteAttnBar = 9, kSiteVRange = 10
 };
 
 // host launchers (fo_gemm.cu: single-SM 128x256 tiles; fo_gemm2.cu: SM-pair 256x256 tiles)

@@ -60,6 +60,15 @@ __device__ __forceinline__ void raise_error(uint32_t* ctrl, uint32_t code, uint3
   atomicExch(ctrl + kCtrlAbort, 1u);
 }
 
+// Records an error that leaves the work running (an input value out of range): the
+// first error code wins, the abort word is not raised.
+__device__ __forceinline__ void note_error(uint32_t* ctrl, uint32_t code, uint32_t site, uint32_t detail) {
+  if (atomicCAS(ctrl + kCtrlError, 0u, code) == 0u) {
+    ctrl[kCtrlWhere] = site;
+    ctrl[kCtrlDetail] = detail;
+  }
+}
+
 __device__ __forceinline__ bool aborted(const uint32_t* ctrl) {
   return ld_relaxed_gpu(ctrl + kCtrlAbort) != 0u;
 }
@@ -171,6 +180,13 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, void* dst, u
       "[%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
       : "memory");
+}
+
+// Asks L2 to fetch [p, p + bytes) from global memory (no completion, no data returned to
+// the SM).  p 16-byte aligned, bytes a positive multiple of 16.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
 }
 
 __device__ __forceinline__ void tma_load_3d(const CUtensorMap* map, void* dst, uint64_t* bar, int32_t c0,

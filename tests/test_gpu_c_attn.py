@@ -90,3 +90,40 @@ def test_attention_constant_v_is_exact(ctx, m):
         got = to_bits(O[r])
         # one bf16 ulp allowed: the weights' sum and the P.V accumulation round differently
         assert np.abs(f64(got) - f64(want)).max() <= np.abs(f64(want)).max() * 2 ** -7
+
+
+def test_attention_v_beyond_fp16_range_reports_range_error(ctx):
+    """V enters the P.V product as fp16: a finite |v| above 65504 cannot be represented,
+    so the call must end with FO_ERR_RANGE from poll (no GPU fault, the context stays
+    usable); 65280, the largest bf16 value that fp16 holds, is accepted."""
+    import overlapped_tensor_gemm_gb300 as fo
+    P, m, H = 2, 128, 1
+    inp = wl.attn_inputs(P, P * m, H, 128, 52)
+    Q = [to_dev(x).reshape(m, H * 128) for x in inp["Q"]]
+    K = [to_dev(x).reshape(m, H * 128) for x in inp["K"]]
+    V = [to_dev(x).reshape(m, H * 128) for x in inp["V"]]
+    O = [torch.empty((m, H * 128), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    V[1][5, 17] = 65280.0                       # below 65504, exact in bf16 and fp16: accepted
+    ctx.qsplit_attn(Q, K, V, O, heads=H, head_dim=128)
+    torch.cuda.synchronize()
+    ctx.poll()
+    V[1][7, 3] = 65536.0                        # the next bf16 value, beyond fp16: reported
+    ctx.qsplit_attn(Q, K, V, O, heads=H, head_dim=128)
+    torch.cuda.synchronize()
+    with pytest.raises(fo.FoError) as e:
+        ctx.poll()
+    assert e.value.status == fo.FO_ERR_RANGE
+    V[1][7, 3] = 0.5                            # the context computes correctly afterwards
+    _, got = _attn_with(ctx, Q, K, V, P, m, H)
+    ref = ops.attention_definition(np.concatenate([f64(to_bits(q)) for q in Q]).reshape(P * m, H, 128),
+                                   np.concatenate([f64(to_bits(k)) for k in K]).reshape(P * m, H, 128),
+                                   np.concatenate([f64(to_bits(v)) for v in V]).reshape(P * m, H, 128))
+    assert_close(np.concatenate(got), ref, "attention after a range error")
+
+
+def _attn_with(ctx, Q, K, V, P, m, H):
+    O = [guarded((m, H * 128), torch.bfloat16) for _ in range(P)]
+    ctx.qsplit_attn(Q, K, V, O, heads=H, head_dim=128)
+    torch.cuda.synchronize()
+    ctx.poll()
+    return None, [f64(to_bits(o)).reshape(m, H, 128) for o in O]
