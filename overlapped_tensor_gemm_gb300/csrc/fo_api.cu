@@ -279,6 +279,7 @@ struct Launch {
   GemmParams p;
   MapSpec spec[kMaxMaps];
   int arrivals_per_tile = 4;  // epilogue warps that finish each tile (8 on SM pairs)
+  bool tn_pair = false;       // transposed reduce-scatter tiles on SM pairs (p.tn_S > 0)
   int num_units = 0;
   int num_groups = 0;
   int num_maps = 0;
@@ -380,14 +381,30 @@ GemmUnit blank_unit() {
   return u;
 }
 
+// Resident SM pairs for a launch (the persistent grid never exceeds them).
+int pair_grid(const fo_ctx* ctx, const fo_opts& o) {
+  int clusters = ctx->pair_clusters;
+  if (o.num_sms > 0 && o.num_sms / 2 < clusters) clusters = o.num_sms / 2 > 0 ? o.num_sms / 2 : 1;
+  return clusters;
+}
+
 fo_status launch_gemm(fo_ctx* ctx, Launch& L, const fo_opts& o, cudaStream_t stream) {
   if (L.p.total_tiles == 0) return FO_OK;
+  if (L.p.tn_S > 0) {  // transposed reduce-scatter tiles: the shape was chosen by the builder
+    if (L.tn_pair) {
+      int clusters = pair_grid(ctx, o);
+      if (L.p.total_tiles < clusters) clusters = L.p.total_tiles;
+      FO_CUDA(gemm_pair_launch(L.p, clusters, stream));
+    } else {
+      FO_CUDA(gemm_launch(L.p, grid_size(ctx, o, L.p.total_tiles), stream));
+    }
+    return FO_OK;
+  }
   if (o.sm_pairs == 0 && ctx->pair_clusters > 0 && L.pair_friendly()) {
     // 256x256 tiles on SM pairs; the persistent grid never exceeds the resident clusters
     FO_TRY(L.retile(2 * kBM));
     FO_TRY(L.pair_boxes());
-    int clusters = ctx->pair_clusters;
-    if (o.num_sms > 0 && o.num_sms / 2 < clusters) clusters = o.num_sms / 2 > 0 ? o.num_sms / 2 : 1;
+    int clusters = pair_grid(ctx, o);
     if (L.p.total_tiles < clusters) clusters = L.p.total_tiles;
     L.arrivals_per_tile = 8;
     FO_CUDA(gemm_pair_launch(L.p, clusters, stream));
@@ -746,28 +763,56 @@ float* rs_slot(const RsArgs& a, float* base, int r, int h) {
   return base + (static_cast<int64_t>(r) * a.P + h) * a.m * a.N;
 }
 
+// Transposed reduce-scatter tiles (GemmParams::tn_S) for a slice of m rows: 0 if they do
+// not apply, else the number of ring steps per tile, with *pair set when the tiles run on
+// SM pairs.  A tile waits on the tile of the previous rank in its pass group, which may
+// come later in the tile order (the ring closes from the last rank to the first), so every
+// rank's tile of a pass group must run at once: the grid must hold at least P tiles.
+int rs_tn_steps(const fo_ctx* ctx, const RsArgs& a, const fo_opts& o, bool* pair) {
+  const int P = a.P;
+  if (a.w_kn || a.m <= 0 || a.m > kBM || a.m % 32 != 0 || 256 % a.m != 0) return 0;
+  const int S = static_cast<int>(256 / a.m);
+  if (S > P || P % S != 0) return 0;
+  *pair = o.sm_pairs == 0 && ctx->pair_clusters > 0 && pair_grid(ctx, o) >= P;
+  if (*pair) return S;
+  return grid_size(ctx, o, 1 << 30) >= P ? S : 0;
+}
+
 fo_status rs_flash(fo_ctx* ctx, const RsArgs& a, const fo_opts& o, cudaStream_t stream, uint32_t* flags,
                    uint32_t epoch, DoneSignal* done = nullptr) {
   const int P = a.P;
   Launch L;
   fo_status st = FO_OK;
+  bool tn_pair = false;
+  const int S = rs_tn_steps(ctx, a, o, &tn_pair);
   int xmap[kMaxP], wmap[kMaxP];
   for (int r = 0; r < P; ++r) {
-    xmap[r] = L.add_map(&st, a.X[r].ptr, a.M, a.Kr, a.X[r].ld, kBM);
+    // transposed tiles: the tokens are the MMA's N side (one box of m rows per step) and
+    // the weight its M side (128-row boxes)
+    xmap[r] = L.add_map(&st, a.X[r].ptr, a.M, a.Kr, a.X[r].ld, S ? static_cast<int>(a.m) : kBM);
     if (st != FO_OK) return st;
-    wmap[r] = add_rs_weight(L, &st, a, r);
+    wmap[r] = S ? L.add_map(&st, a.W[r].ptr, a.N, a.Kr, a.W[r].ld, kBM) : add_rs_weight(L, &st, a, r);
     if (st != FO_OK) return st;
   }
   const int64_t tm = (a.m + kBM - 1) / kBM, tn = (a.N + kBN - 1) / kBN;
-  auto fbase = [&](int r, int h) { return kRsFlagBase + (static_cast<int64_t>(r) * P + h) * tm * tn * 4; };
+  // flags per (rank, hop): one per (tile, quadrant), or per (256-feature block, CTA half,
+  // quadrant) for transposed tiles
+  const int64_t per_hop = tm * tn * 4 > ((a.N + 255) / 256) * 8 ? tm * tn * 4 : ((a.N + 255) / 256) * 8;
+  auto fbase = [&](int r, int h) { return kRsFlagBase + (static_cast<int64_t>(r) * P + h) * per_hop; };
   if (fbase(P - 1, P) > (1 << 18)) return fail(FO_ERR_UNSUPPORTED, "too many reduce-scatter tiles for the flag area");
   auto add = [&](int r, int c) {
     const int h = mod(r - c - 1, P);  // position of rank r on chunk c's reduction chain
     GemmUnit& u = L.add_unit();
     u = blank_unit();
-    u.a_map = xmap[r];
-    u.a_row0 = static_cast<int32_t>(c * a.m);
-    u.b_map = wmap[r];
+    if (S) {  // A = the weight's features, B = the chunk's token rows
+      u.a_map = wmap[r];
+      u.b_map = xmap[r];
+      u.b_row0 = static_cast<int32_t>(c * a.m);
+    } else {
+      u.a_map = xmap[r];
+      u.a_row0 = static_cast<int32_t>(c * a.m);
+      u.b_map = wmap[r];
+    }
     u.m_rows = static_cast<int32_t>(a.m);
     u.n_cols = static_cast<int32_t>(a.N);
     u.k = static_cast<int32_t>(a.Kr);
@@ -789,16 +834,45 @@ fo_status rs_flash(fo_ctx* ctx, const RsArgs& a, const fo_opts& o, cudaStream_t 
       if (done) u.done_counter = static_cast<int32_t>(kDoneBase + r);
     }
   };
-  for (int t = 0; t < P; ++t) {
-    L.begin_group();
-    for (int i = 0; i < P; ++i) {
-      int r, c;
-      rs_unit(P, o.order, t, i, &r, &c);
-      add(r, c);
+  if (S) {
+    // units rank-major in step order: rank r computes at step t the chunk of rs_unit's order
+    for (int r = 0; r < P; ++r)
+      for (int t = 0; t < P; ++t) add(r, o.order == FO_ORDER_NAIVE ? t : mod(r - t - 1, P));
+    const int ncta = tn_pair ? 2 : 1;
+    GemmParams& q = L.p;
+    q.num_groups = 1;
+    q.group_unit_begin[0] = 0;
+    q.group_unit_begin[1] = L.num_units;
+    q.num_maps = L.num_maps;
+    q.tn_S = S;
+    q.tn_rows = static_cast<int32_t>(a.m);
+    q.tn_ranks = P;
+    q.tn_passes = P / S;
+    q.tn_fblocks = static_cast<int32_t>((a.N + ncta * kBM - 1) / (ncta * kBM));
+    q.tn_fb_group = 1;
+    q.total_tiles = q.tn_fblocks * q.tn_passes * P;
+    q.epoch = epoch;
+    q.timeout_ns = timeout_ns(o);
+    q.flags = flags;
+    q.ctrl = ctx->ctrl;
+    L.tn_pair = tn_pair;
+    L.arrivals_per_tile = 4 * ncta;
+    for (int i = 0; i < L.num_units; ++i) {  // per unit: one feature block of tiles
+      q.units[i].tiles_m = 1;
+      q.units[i].tiles_n = q.tn_fblocks;
     }
+  } else {
+    for (int t = 0; t < P; ++t) {
+      L.begin_group();
+      for (int i = 0; i < P; ++i) {
+        int r, c;
+        rs_unit(P, o.order, t, i, &r, &c);
+        add(r, c);
+      }
+    }
+    L.p.mn_major = a.w_kn ? 2 : 0;
+    FO_TRY(L.finish(epoch, timeout_ns(o), flags, ctx->ctrl, 0));
   }
-  L.p.mn_major = a.w_kn ? 2 : 0;
-  FO_TRY(L.finish(epoch, timeout_ns(o), flags, ctx->ctrl, 0));
   if (o.compute_only)  // every partial-sum flag published: no tile waits on another
     FO_CUDA(launch_fill_u32(flags + kRsFlagBase, fbase(P - 1, P) - kRsFlagBase, epoch, stream));
   FO_TRY(launch_gemm(ctx, L, o, stream));

@@ -68,8 +68,9 @@ __device__ void producer_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl)
   int waited_unit = -1;
   bool ok = true;
   const int mn = p.mn_major & 3;
+  const bool tn = p.tn_S > 0;
   for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
-    const TileCoord tc = decode_tile(p, tile);
+    const TileCoord tc = tile_coord(p, tile);
     const GemmUnit& u = p.units[tc.unit];
     if (u.wait_flag >= 0 && tc.unit != waited_unit) {
       ok = flag_wait(p.flags + u.wait_flag, p.epoch, p.ctrl, p.timeout_ns, kSiteAgFlag,
@@ -81,7 +82,6 @@ __device__ void producer_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl)
     }
     const int nk = (u.k + kBK - 1) / kBK;
     const int a_row = u.a_row0 + tc.mb * kBM;
-    prefetch_partial(u, tc.mb * kBM, tc.nb * kBN);
     const bool gated = u.gated != 0;
     const int b_row = u.b_row0 + tc.nb * (gated ? kBN / 2 : kBN);
     const int b_row_up = u.b_row1 + tc.nb * (kBN / 2);
@@ -114,7 +114,13 @@ __device__ void producer_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl)
       uint8_t* b = a + kABytes;
       uint64_t* bar = &ctl->full[stage];
       mbar_arrive_expect_tx(bar, kStageBytes);
-      if (mn & 1) {  // A stored [K][M]: x runs along M
+      if (tn) {  // A: 128 features of the weight; B: the token rows of the tile's tn_S steps
+        tma_load_2d(amap0, a, bar, kb * kBK, tc.nb * kBM);
+        for (int su = 0; su < p.tn_S; ++su) {
+          const GemmUnit& us = p.units[tc.unit + su];
+          tma_load_2d(&p.maps[us.b_map], b + su * p.tn_rows * 128, bar, kb * kBK, us.b_row0);
+        }
+      } else if (mn & 1) {  // A stored [K][M]: x runs along M
         tma_load_2d(amap, a, bar, arow, ax);
         tma_load_2d(amap, a + kMnBox, bar, arow + 64, ax);
       } else {
@@ -157,7 +163,7 @@ __device__ void mma_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl, uint
   bool ok = true;
   const uint32_t tiles_addr = smem_u32(tiles);
   for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
-    const TileCoord tc = decode_tile(p, tile);
+    const TileCoord tc = tile_coord(p, tile);
     const GemmUnit& u = p.units[tc.unit];
     if (!mbar_wait_fast(&ctl->tmem_empty[acc], acc_phase ^ 1u, p.ctrl, p.timeout_ns, kSiteTmemEmpty,
                    static_cast<uint32_t>(tile))) {
@@ -206,7 +212,20 @@ __device__ void epilogue_loop(const GemmParams& p, SmemCtl* ctl, uint32_t tmem_b
   int acc = 0;
   uint32_t acc_phase = 0;
   for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
-    const TileCoord tc = decode_tile(p, tile);
+    const TileCoord tc = tile_coord(p, tile);
+    if (p.tn_S > 0) {  // transposed reduce-scatter tile: its steps in order, one hop each
+      if (!warp_mbar_wait(&ctl->tmem_full[acc], acc_phase, p, kSiteTmemFull, static_cast<uint32_t>(tile), lane))
+        return;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
+      if (!epilogue_tn(p, tc, tb, 0, 1, q, lane)) return;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->tmem_empty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+      continue;
+    }
     const GemmUnit& u = p.units[tc.unit];
     const int tile_in_unit = tc.mb * u.tiles_n + tc.nb;
     const int row = tc.mb * kBM + q * 32 + lane;

@@ -51,8 +51,9 @@ __device__ void pair_producer(const GemmParams& p, uint8_t* tiles, PairCtl* ctl,
   int waited_unit = -1;
   bool ok = true;
   const int mn = p.mn_major & 3;
+  const bool tn = p.tn_S > 0;
   for (int tile = cluster; ok && tile < p.total_tiles; tile += nclusters) {
-    const TileCoord tc = decode_tile(p, tile);
+    const TileCoord tc = tile_coord(p, tile);
     const GemmUnit& u = p.units[tc.unit];
     if (u.wait_flag >= 0 && tc.unit != waited_unit) {
       ok = flag_wait(p.flags + u.wait_flag, p.epoch, p.ctrl, p.timeout_ns, kSiteAgFlag,
@@ -63,7 +64,6 @@ __device__ void pair_producer(const GemmParams& p, uint8_t* tiles, PairCtl* ctl,
     }
     const int nk = (u.k + kBK - 1) / kBK;
     const int a_row = u.a_row0 + tc.mb * 2 * kBM + static_cast<int>(cta) * kBM;
-    prefetch_partial(u, tc.mb * 2 * kBM + static_cast<int>(cta) * kBM, tc.nb * kBN);
     // B rows of this CTA: gated tiles put the gate rows in the leader and the up rows in the peer
     const int b_row = u.gated ? (cta == 0 ? u.b_row0 : u.b_row1) + tc.nb * (kBN / 2)
                               : u.b_row0 + tc.nb * kBN + static_cast<int>(cta) * (kBN / 2);
@@ -96,7 +96,16 @@ __device__ void pair_producer(const GemmParams& p, uint8_t* tiles, PairCtl* ctl,
       uint8_t* b = a + kPA;
       if (cta == 0) mbar_arrive_expect_tx(&ctl->full[stage], 2 * kPStage);
       const uint32_t bar = leader_full + stage * static_cast<uint32_t>(sizeof(uint64_t));
-      if (mn == 0) {
+      if (tn) {
+        // A: this CTA's 128 of the tile's 256 features; B: this CTA's half of the token
+        // rows, the tile's steps cta * tn_S/2 .. (cta + 1) * tn_S/2 - 1
+        tma_load_2d_pair(amap0, a, bar, kb * kBK, tc.nb * 2 * kBM + static_cast<int>(cta) * kBM);
+        const int half = p.tn_S / 2;
+        for (int su = 0; su < half; ++su) {
+          const GemmUnit& us = p.units[tc.unit + static_cast<int>(cta) * half + su];
+          tma_load_2d_pair(&p.maps[us.b_map], b + su * p.tn_rows * 128, bar, kb * kBK, us.b_row0);
+        }
+      } else if (mn == 0) {
         tma_load_2d_pair(amap, a, bar, ax, arow);
         tma_load_2d_pair(bmap, b, bar, bx, b_row);
       } else {
@@ -144,7 +153,7 @@ __device__ void pair_mma(const GemmParams& p, uint8_t* tiles, PairCtl* ctl, uint
   bool issued = false, ok = true;
   const uint32_t tiles_addr = smem_u32(tiles);
   for (int tile = cluster; ok && tile < p.total_tiles; tile += nclusters) {
-    const TileCoord tc = decode_tile(p, tile);
+    const TileCoord tc = tile_coord(p, tile);
     const GemmUnit& u = p.units[tc.unit];
     if (!mbar_wait_fast(&ctl->tmem_empty[acc], acc_phase ^ 1u, p.ctrl, p.timeout_ns, kSiteTmemEmpty,
                    static_cast<uint32_t>(tile))) {
@@ -193,7 +202,26 @@ __device__ void pair_epilogue(const GemmParams& p, PairCtl* ctl, uint32_t tmem_b
   int acc = 0;
   uint32_t acc_phase = 0;
   for (int tile = cluster; tile < p.total_tiles; tile += nclusters) {
-    const TileCoord tc = decode_tile(p, tile);
+    const TileCoord tc = tile_coord(p, tile);
+    if (p.tn_S > 0) {  // transposed reduce-scatter tile: its steps in order, one hop each
+      if (!warp_mbar_wait(&ctl->tmem_full[acc], acc_phase, p, kSiteTmemFull, static_cast<uint32_t>(tile), lane))
+        return;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
+      if (!epilogue_tn(p, tc, tb, static_cast<int>(cta), 2, q, lane)) return;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (cta == 0) {
+          mbar_arrive(&ctl->tmem_empty[acc]);
+        } else {
+          mbar_arrive_cluster(leader_tmem_empty + acc * static_cast<uint32_t>(sizeof(uint64_t)));
+        }
+      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+      continue;
+    }
     const GemmUnit& u = p.units[tc.unit];
     // flags per (tile, CTA half, lane quadrant): the same rows on both sides of a hop
     const int flag_slot = ((tc.mb * u.tiles_n + tc.nb) * 2 + static_cast<int>(cta)) * 4 + q;

@@ -80,23 +80,6 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int tile) 
   return c;
 }
 
-// L2 prefetch of the fp32 partial sums that this CTA's epilogue adds to a tile: rows
-// [row0, row0 + 128) of the unit, columns [col0, col0 + kBN), one bulk prefetch per row
-// segment (at most 1 KiB).  Issued by the operand producer when the tile's first K block
-// is requested, a whole main loop before the epilogue reads them: in the Flash-RS order a
-// partial sum is written one ring step before it is added, long enough for it to have
-// left L2.  (A prefetch that comes before the partial sum is written only brings stale
-// lines into L2, where the later write updates them.)  Row pitches and column offsets are
-// multiples of 16 bytes: the reduce-scatter's N is a multiple of 4.
-__device__ __forceinline__ void prefetch_partial(const GemmUnit& u, int row0, int col0) {
-  if (u.acc_in == nullptr) return;
-  const int ncol = min(kBN, u.n_cols - col0);
-  if (ncol <= 0) return;
-  const uint32_t bytes = static_cast<uint32_t>(ncol) * 4u;
-  const int r1 = min(row0 + kBM, u.m_rows);
-  for (int r = row0; r < r1; ++r) prefetch_l2_bulk(u.acc_in + static_cast<int64_t>(r) * u.ld_acc + col0, bytes);
-}
-
 // ---------------------------------------------------------------------------
 // Partial-sum and fp32 epilogues through a per-warp staging buffer.
 //
@@ -283,6 +266,96 @@ __device__ __forceinline__ bool warp_flag_wait(const uint32_t* flag, const GemmP
   ok = __shfl_sync(0xffffffffu, ok, 0);
   if (ok) (void)ld_acquire_gpu(flag);  // every lane orders its own partial-sum reads after the flag
   return ok != 0;
+}
+
+// ---------------------------------------------------------------------------
+// Transposed reduce-scatter tiles (GemmParams::tn_S > 0)
+// ---------------------------------------------------------------------------
+
+// Tile -> (first unit of the tile, feature block in nb).  Order: feature-block group,
+// pass, feature block inside the group, rank.
+__device__ __forceinline__ TileCoord decode_tile_tn(const GemmParams& p, int tile) {
+  const int per_pass = p.tn_fb_group * p.tn_ranks;
+  const int per_group = per_pass * p.tn_passes;
+  const int g = tile / per_group;
+  int rem = tile - g * per_group;
+  const int pass = rem / per_pass;
+  rem -= pass * per_pass;
+  const int fbi = rem / p.tn_ranks;
+  const int r = rem - fbi * p.tn_ranks;
+  TileCoord c;
+  c.unit = (r * p.tn_passes + pass) * p.tn_S;
+  c.mb = 0;
+  c.nb = g * p.tn_fb_group + fbi;
+  return c;
+}
+
+__device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int tile) {
+  return p.tn_S > 0 ? decode_tile_tn(p, tile) : decode_tile(p, tile);
+}
+
+// Epilogue of one unit of a transposed tile for one warp: its 32 accumulator lanes are the
+// features feat = f0 + lane, its columns [col0, col0 + tn_rows) the unit's token rows.
+// out[t][feat] = acc (+ acc_in[t][feat]); a warp instruction touches 32 consecutive features
+// of one token row (128 bytes of fp32, 64 of bf16).
+__device__ __forceinline__ void store_unit_tn(const GemmParams& p, const GemmUnit& u, uint32_t tbase, int col0,
+                                              int feat) {
+  const bool add = u.epi == kEpiAddF32 || u.epi == kEpiAddBF16;
+  const bool bf16_out = u.epi == kEpiBF16 || u.epi == kEpiAddBF16;
+  const bool fok = feat < u.n_cols;
+#pragma unroll 1
+  for (int c0 = 0; c0 < p.tn_rows; c0 += 16) {
+    uint32_t v[16];
+    float in[16];
+    tmem_ld16(tbase + col0 + c0, v);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int t = c0 + i;
+      in[i] = (add && fok && t < u.m_rows) ? __ldcg(u.acc_in + static_cast<int64_t>(t) * u.ld_acc + feat) : 0.0f;
+    }
+    tmem_wait_ld();
+    if (!fok) continue;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int t = c0 + i;
+      if (t >= u.m_rows) break;
+      const float x = __uint_as_float(v[i]) + in[i];
+      if (bf16_out) {
+        static_cast<uint16_t*>(u.c)[static_cast<int64_t>(t) * u.ldc + feat] =
+            __bfloat16_as_ushort(__float2bfloat16_rn(x));
+      } else {
+        static_cast<float*>(u.c)[static_cast<int64_t>(t) * u.ldc + feat] = x;
+      }
+    }
+  }
+}
+
+// The whole epilogue of a transposed tile for one warp (quadrant q of CTA `cta` of `ncta`):
+// the tile's units in step order, each after its incoming partial sum's flag, each
+// releasing its own flag for the next rank.  False if a wait gave up.
+__device__ __forceinline__ bool epilogue_tn(const GemmParams& p, const TileCoord& tc, uint32_t tbase, int cta,
+                                            int ncta, int q, int lane) {
+  const int f0 = (tc.nb * ncta + cta) * kBM + q * 32;
+  const int slot = (tc.nb * ncta + cta) * 4 + q;
+  for (int s = 0; s < p.tn_S; ++s) {
+    const GemmUnit& u = p.units[tc.unit + s];
+    if (u.in_flag_base >= 0) {
+      const int f = u.in_flag_base + slot;
+      if (!warp_flag_wait(p.flags + f, p, kSiteAccInFlag, static_cast<uint32_t>(f), lane)) return false;
+    }
+    store_unit_tn(p, u, tbase, s * p.tn_rows, f0 + lane);
+    if (u.out_flag_base >= 0) {
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) st_release_gpu(p.flags + u.out_flag_base + slot, p.epoch);
+    }
+    if (u.done_counter >= 0) {
+      __threadfence_system();
+      __syncwarp();
+      if (lane == 0) red_release_sys_add(p.flags + u.done_counter, 1u);
+    }
+  }
+  return true;
 }
 
 }  // namespace

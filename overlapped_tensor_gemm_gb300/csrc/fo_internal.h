@@ -86,6 +86,21 @@ struct GemmParams {
   // staged as 64 (M or N) x 64 (K) boxes, one per 64-wide block, and read by the MMA as
   // MN-major (no K chunks, no gating).  The kernels instantiate their MMA loop per value.
   int32_t mn_major;
+  // Transposed reduce-scatter tiles (tn_S > 0).  For slices of 32-128 token rows the MMA's
+  // M side is 128 output features (A = the rank's weight, K-major, one 128-row box) and its
+  // N side the token rows of tn_S consecutive ring steps of one rank (B = the activations,
+  // one box of tn_rows rows per step; tn_S * tn_rows = 256).  Units are laid out rank-major
+  // in step order (unit of rank r, step t at index r * tn_S * tn_passes + t); a tile is
+  // (rank r, pass, feature block fb) and covers the steps pass*tn_S .. +tn_S-1 of rank r.
+  // Tiles are ordered (fb group, pass, fb in group, rank), so the tn_passes tiles that read
+  // one weight block are close together (it is fetched from HBM about once), and the
+  // epilogue adds each step's partial sums in step order, one ring hop per step.
+  int32_t tn_S;
+  int32_t tn_rows;      // token rows per unit (256 / tn_S)
+  int32_t tn_ranks;
+  int32_t tn_passes;    // tiles per rank and feature block
+  int32_t tn_fblocks;   // feature blocks of 128 (single SM) or 256 (SM pair) features
+  int32_t tn_fb_group;  // feature blocks per ordering group (divides tn_fblocks)
   int32_t total_tiles;
   uint32_t epoch;
   uint64_t timeout_ns;

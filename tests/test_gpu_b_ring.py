@@ -150,3 +150,30 @@ def test_gated_fused_epilogue_matches_unfused(ctx):
     ctx.poll()
     for r in range(cfg.P):
         assert np.array_equal(to_bits(Z[r]), to_bits(Z2[r])), f"rank {r}: fused and unfused glue differ"
+
+
+# Slices of 32-128 rows run on transposed tiles (the weight's features on the MMA's M side,
+# the token rows of 256/m consecutive ring steps of one rank on its N side), on SM pairs by
+# default and on single SMs with single_sm; a grid smaller than P falls back to the
+# step-ordered tiles.  Ragged feature counts leave the last feature block partly empty.
+@pytest.mark.parametrize("P,m,Kr,N", [(8, 64, 256, 1024), (4, 64, 136, 516), (2, 128, 192, 260),
+                                      (8, 32, 128, 512), (8, 128, 64, 768)])
+@pytest.mark.parametrize("order", ["flash", "naive"])
+@pytest.mark.parametrize("single_sm", [False, True])
+def test_rs_transposed_tiles_integer_bit_exact(ctx, P, m, Kr, N, order, single_sm):
+    Y, ref = _rs(ctx, P, m, Kr, N, True, 400 + P + m, order=order, single_sm=single_sm)
+    for r in range(P):
+        assert_bits_equal(to_bits(Y[r]), ref[r], f"RS transposed {order} P={P} m={m} rank {r}")
+
+
+def test_rs_small_grid_falls_back_to_step_tiles(ctx):
+    P, m, Kr, N = 8, 64, 128, 512
+    Y, ref = _rs(ctx, P, m, Kr, N, True, 77, num_sms=4)
+    for r in range(P):
+        assert_bits_equal(to_bits(Y[r]), ref[r], f"RS small grid rank {r}")
+
+
+def test_rs_transposed_tiles_gaussian_tolerance(ctx):
+    Y, ref = _rs(ctx, 8, 64, 1024, 2048, False, 78)
+    for r in range(8):
+        assert_close(f64(to_bits(Y[r])), ref[r], f"RS transposed gaussian rank {r}")
