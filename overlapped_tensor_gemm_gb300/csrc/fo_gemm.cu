@@ -120,20 +120,22 @@ __device__ void producer_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl)
           const GemmUnit& us = p.units[tc.unit + su];
           tma_load_2d(&p.maps[us.b_map], b + su * p.tn_rows * 128, bar, kb * kBK, us.b_row0);
         }
-      } else if (mn & 1) {  // A stored [K][M]: x runs along M
-        tma_load_2d(amap, a, bar, arow, ax);
-        tma_load_2d(amap, a + kMnBox, bar, arow + 64, ax);
       } else {
-        tma_load_2d(amap, a, bar, ax, arow);
-      }
-      if (mn & 2) {  // B stored [K][N]
+        if (mn & 1) {  // A stored [K][M]: x runs along M
+          tma_load_2d(amap, a, bar, arow, ax);
+          tma_load_2d(amap, a + kMnBox, bar, arow + 64, ax);
+        } else {
+          tma_load_2d(amap, a, bar, ax, arow);
+        }
+        if (mn & 2) {  // B stored [K][N]
 #pragma unroll
-        for (int h = 0; h < kBN / 64; ++h) tma_load_2d(bmap, b + h * kMnBox, bar, b_row + h * 64, bx);
-      } else if (gated) {  // gate rows -> B rows [0,128), up rows -> B rows [128,256) (128-row boxes)
-        tma_load_2d(bmap, b, bar, bx, b_row);
-        tma_load_2d(bmap, b + kBBytes / 2, bar, bx, b_row_up);
-      } else {
-        tma_load_2d(bmap, b, bar, bx, b_row);
+          for (int h = 0; h < kBN / 64; ++h) tma_load_2d(bmap, b + h * kMnBox, bar, b_row + h * 64, bx);
+        } else if (gated) {  // gate rows -> B rows [0,128), up rows -> B rows [128,256) (128-row boxes)
+          tma_load_2d(bmap, b, bar, bx, b_row);
+          tma_load_2d(bmap, b + kBBytes / 2, bar, bx, b_row_up);
+        } else {
+          tma_load_2d(bmap, b, bar, bx, b_row);
+        }
       }
       armed |= 1u << stage;
       armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
