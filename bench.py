@@ -318,9 +318,44 @@ def run_ours(args, rank: int, world: int, device: int):
         ctx.poll()
         return a.elapsed_time(b) / iters
 
-    iters = max(args.steps, 5)
-    t_ag = timed(lambda: ctx.ag_gemm(X, Wc, H, order=args.ag_order, epilogue=epi), iters)
-    t_rs = timed(lambda: ctx.gemm_rs(H, Wr, Z), iters)
+    def timed_set(fns: dict, iters: int, rounds: int = 5) -> dict:
+        """Median ms per call of every function of `fns`, timed in `rounds` interleaved
+        rounds of `iters` back-to-back calls (CUDA events on the launching stream): at the
+        long sweep points the GPU runs into its power cap, and interleaving gives every
+        variant the same mix of clock states."""
+        for fn in fns.values():
+            fn()
+            fn()
+        torch.cuda.synchronize()
+        samples = {k: [] for k in fns}
+        for _ in range(rounds):
+            for k, fn in fns.items():
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for _ in range(iters):
+                    fn()
+                b.record(stream)
+                torch.cuda.synchronize()
+                samples[k].append(a.elapsed_time(b) / iters)
+        ctx.poll()
+        return {k: statistics.median(v) for k, v in samples.items()}
+
+    iters = max(2, min(args.steps, int(40.0 / max(ms_max, 1e-3))))  # ~40 ms of work per sample
+    # every variant, and the same variant with its transfers removed (compute_only: the
+    # same launches, every ring flag published before the launch, no copy enqueued)
+    ag = lambda o, c=False: (lambda: ctx.ag_gemm(X, Wc, H, order=o, epilogue=epi, compute_only=c))  # noqa: E731
+    rs = lambda o, c=False: (lambda: ctx.gemm_rs(H, Wr, Z, order=o, compute_only=c))  # noqa: E731
+    variants = [("ag", ag, ("flash", "serial", "slicing")), ("rs", rs, ("flash", "naive", "serial", "slicing"))]
+    if args.no_extras:
+        variants = [("ag", ag, ("flash",)), ("rs", rs, ("flash",))]
+    fns = {}
+    for op, fn, orders in variants:
+        for o in orders:
+            fns[(op, o, False)] = fn(o if not (op == "ag" and o == "flash") else args.ag_order)
+            if not args.no_extras:
+                fns[(op, o, True)] = fn(o, True)
+    tm = timed_set(fns, iters)
+    t_ag, t_rs = tm[("ag", "flash", False)], tm[("rs", "flash", False)]
     ag_tflops = flops["ag"] / (t_ag * 1e-3) / 1e12
     pair = cfg.m % 256 == 0  # 256-row tiles on SM pairs when every slice is a multiple of 256 rows
     kernel = "gemm_pair_kernel" if pair else "gemm_kernel"
@@ -339,18 +374,8 @@ def run_ours(args, rank: int, world: int, device: int):
             fn()
             torch.cuda.synchronize()
             return ctx.phase_ms()
-        # every variant, and the same variant with its transfers removed (compute_only: the
-        # same launches, every ring flag published before the launch, no copy enqueued)
-        ag = lambda o, c=False: (lambda: ctx.ag_gemm(X, Wc, H, order=o, epilogue=epi, compute_only=c))  # noqa: E731
-        rs = lambda o, c=False: (lambda: ctx.gemm_rs(H, Wr, Z, order=o, compute_only=c))  # noqa: E731
-        t = {("ag", "flash"): t_ag, ("rs", "flash"): t_rs}
-        tc = {}
-        for op, fn, orders in (("ag", ag, ("flash", "serial", "slicing")),
-                               ("rs", rs, ("flash", "naive", "serial", "slicing"))):
-            for o in orders:
-                if (op, o) not in t:
-                    t[(op, o)] = timed(fn(o), iters)
-                tc[(op, o)] = timed(fn(o, True), iters)
+        t = {(op, o): v for (op, o, c), v in tm.items() if not c}
+        tc = {(op, o): v for (op, o, c), v in tm.items() if c}
         ag_coll, ag_gemm = phase(ag("serial"))
         rs_coll, rs_gemm = phase(rs("serial"))
         exposed = {o: (t[("ag", "flash" if o == "naive" else o)] - tc[("ag", "flash" if o == "naive" else o)])
@@ -362,6 +387,7 @@ def run_ours(args, rank: int, world: int, device: int):
             "rs_naive_ms": round(t[("rs", "naive")], 4),
             "rs_serial_phases_ms": {"gemm": round(rs_gemm, 4), "ring_reduce": round(rs_coll, 4)},
             "compute_only_ms": {f"{op}_{o}": round(v, 4) for (op, o), v in tc.items()},
+            "timing": f"medians of 5 interleaved rounds of {iters} calls per variant",
         })
         ser = exposed["serial"]
         out["exposed_copy"] = {

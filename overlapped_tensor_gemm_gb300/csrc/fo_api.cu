@@ -763,6 +763,8 @@ float* rs_slot(const RsArgs& a, float* base, int r, int h) {
   return base + (static_cast<int64_t>(r) * a.P + h) * a.m * a.N;
 }
 
+constexpr int kTnFbGroup = 1;  // feature blocks per ordering group of the transposed tiles
+
 // Transposed reduce-scatter tiles (GemmParams::tn_S) for a slice of m rows: 0 if they do
 // not apply, else the number of ring steps per tile, with *pair set when the tiles run on
 // SM pairs.  A tile waits on the tile of the previous rank in its pass group, which may
@@ -849,7 +851,10 @@ fo_status rs_flash(fo_ctx* ctx, const RsArgs& a, const fo_opts& o, cudaStream_t 
     q.tn_ranks = P;
     q.tn_passes = P / S;
     q.tn_fblocks = static_cast<int32_t>((a.N + ncta * kBM - 1) / (ncta * kBM));
-    q.tn_fb_group = 1;
+    // passes of one feature block kTnFbGroup blocks apart (a divisor of the block count)
+    int fbg = kTnFbGroup < q.tn_fblocks ? kTnFbGroup : q.tn_fblocks;
+    while (q.tn_fblocks % fbg != 0) --fbg;
+    q.tn_fb_group = fbg;
     q.total_tiles = q.tn_fblocks * q.tn_passes * P;
     q.epoch = epoch;
     q.timeout_ns = timeout_ns(o);

@@ -294,25 +294,35 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int tile) {
   return p.tn_S > 0 ? decode_tile_tn(p, tile) : decode_tile(p, tile);
 }
 
+// Partial sums of 16 token rows (t0 .. t0+15) at this lane's feature; zero where absent.
+__device__ __forceinline__ void load_partial16(const GemmUnit& u, int t0, int feat, bool active, float (&in)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int t = t0 + i;
+    in[i] = (active && t < u.m_rows) ? __ldcg(u.acc_in + static_cast<int64_t>(t) * u.ld_acc + feat) : 0.0f;
+  }
+}
+
 // Epilogue of one unit of a transposed tile for one warp: its 32 accumulator lanes are the
 // features feat = f0 + lane, its columns [col0, col0 + tn_rows) the unit's token rows.
 // out[t][feat] = acc (+ acc_in[t][feat]); a warp instruction touches 32 consecutive features
-// of one token row (128 bytes of fp32, 64 of bf16).
+// of one token row (128 bytes of fp32, 64 of bf16).  The partial sums of the next 16 rows
+// are in flight while the current 16 are stored.
 __device__ __forceinline__ void store_unit_tn(const GemmParams& p, const GemmUnit& u, uint32_t tbase, int col0,
                                               int feat) {
   const bool add = u.epi == kEpiAddF32 || u.epi == kEpiAddBF16;
   const bool bf16_out = u.epi == kEpiBF16 || u.epi == kEpiAddBF16;
   const bool fok = feat < u.n_cols;
+  float nxt[16];
+  load_partial16(u, 0, feat, add && fok, nxt);
 #pragma unroll 1
   for (int c0 = 0; c0 < p.tn_rows; c0 += 16) {
-    uint32_t v[16];
     float in[16];
-    tmem_ld16(tbase + col0 + c0, v);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int t = c0 + i;
-      in[i] = (add && fok && t < u.m_rows) ? __ldcg(u.acc_in + static_cast<int64_t>(t) * u.ld_acc + feat) : 0.0f;
-    }
+    for (int i = 0; i < 16; ++i) in[i] = nxt[i];
+    uint32_t v[16];
+    tmem_ld16(tbase + col0 + c0, v);
+    if (c0 + 16 < p.tn_rows) load_partial16(u, c0 + 16, feat, add && fok, nxt);
     tmem_wait_ld();
     if (!fok) continue;
 #pragma unroll
