@@ -118,6 +118,11 @@ typedef struct {
                            the compute time of that order with the transfers removed.  The
                            receive buffers keep whatever an earlier call left in them: the
                            results are meaningless.  Not accepted with host buffers. */
+  int32_t split_layer;  /* fo_mlp_layer / fo_mlp_layer_host: 0 = one persistent launch for
+                           Flash-AG -> activation -> Flash-RS when the layer fits one launch
+                           (the reduce-scatter's tiles wait per 256-row block for the rows
+                           of the intermediate they read), 1 = two launches */
+  int32_t reserved;
 } fo_opts;
 
 /* Version of this ABI (major*100 + minor). */

@@ -46,7 +46,7 @@ class FoOpts(ctypes.Structure):
     _fields_ = [("order", ctypes.c_int32), ("link", ctypes.c_int32), ("n_slices", ctypes.c_int32),
                 ("timeout_us", ctypes.c_uint32), ("causal_prune", ctypes.c_int32), ("num_sms", ctypes.c_int32),
                 ("fault", ctypes.c_int32), ("epilogue", ctypes.c_int32), ("sm_pairs", ctypes.c_int32),
-                ("compute_only", ctypes.c_int32)]
+                ("compute_only", ctypes.c_int32), ("split_layer", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class FoError(RuntimeError):
@@ -134,9 +134,9 @@ def _mats(ts: Sequence) -> ctypes.Array:
 
 def opts(order: str = "flash", link: str = "default", n_slices: int = 0, timeout_us: int = 0,
          causal_prune: bool = False, num_sms: int = 0, fault: str = "none", epilogue: str = "plain",
-         single_sm: bool = False, compute_only: bool = False) -> FoOpts:
+         single_sm: bool = False, compute_only: bool = False, split_layer: bool = False) -> FoOpts:
     return FoOpts(ORDERS[order], LINKS[link], n_slices, timeout_us, int(causal_prune), num_sms, FAULTS[fault],
-                  EPILOGUES[epilogue], int(single_sm), int(compute_only))
+                  EPILOGUES[epilogue], int(single_sm), int(compute_only), int(split_layer), 0)
 
 
 def _stream(stream) -> ctypes.c_void_p:

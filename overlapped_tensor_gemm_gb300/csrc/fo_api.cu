@@ -121,6 +121,10 @@ enum BufId : int {
 constexpr int64_t kAgFlagBase = 0;
 constexpr int64_t kDoneBase = 64;
 constexpr int64_t kRsFlagBase = 256;
+// [kRowsBase, ...): one launch for a whole layer: per-(rank, slice, m-block) counts of the
+// stored rows of the intermediate activations (reset to zero before each such launch)
+constexpr int64_t kRowsBase = 1 << 18;
+constexpr size_t kFlagBytes = 2u << 20;
 
 constexpr int kMaxSlices = 16;
 
@@ -217,6 +221,7 @@ fo_status check_common(fo_ctx* ctx, int P, const fo_opts* opts) {
     if (opts->sm_pairs < 0 || opts->sm_pairs > 1) return fail(FO_ERR_INVALID_ARG, "sm_pairs must be 0 or 1");
     if (opts->compute_only < 0 || opts->compute_only > 1)
       return fail(FO_ERR_INVALID_ARG, "compute_only must be 0 or 1");
+    if (opts->split_layer < 0 || opts->split_layer > 1) return fail(FO_ERR_INVALID_ARG, "split_layer must be 0 or 1");
   }
   return FO_OK;
 }
@@ -378,6 +383,8 @@ GemmUnit blank_unit() {
   u.in_flag_base = -1;
   u.out_flag_base = -1;
   u.done_counter = -1;
+  u.rows_done_base = -1;
+  u.a_ready_base = -1;
   return u;
 }
 
@@ -563,8 +570,11 @@ fo_status enqueue_ag_ring(fo_ctx* ctx, const AgArgs& a, int64_t row0, int64_t ro
 // when flash.
 constexpr double kWeightMajorMaxBytes = 80.0 * (1 << 20);  // measured: 56 MiB better, 112 MiB equal
 
+// rows_base >= 0 (one launch for a whole layer): rank r's unit for slice s counts its stored
+// rows per m-block into counter rows_base + (r * P + s) * mblocks + mb.
 fo_status add_ag_units(Launch& L, const AgArgs& a, const int* xmap, const int* rmap, const int* wmap, int64_t row0,
-                       int64_t rows, bool flash, int64_t gated_f, bool weight_major = false) {
+                       int64_t rows, bool flash, int64_t gated_f, bool weight_major = false, int64_t rows_base = -1,
+                       int64_t mblocks = 0) {
   const int P = a.P;
   const int ngroups = weight_major ? 1 + (P > 1 ? P : 0) : P;
   for (int gi = 0; gi < ngroups; ++gi) {
@@ -605,6 +615,7 @@ fo_status add_ag_units(Launch& L, const AgArgs& a, const int* xmap, const int* r
       }
       u.c = bptr(a.Y[r], s * a.m + row0);
       u.ldc = a.Y[r].ld;
+      if (rows_base >= 0) u.rows_done_base = static_cast<int32_t>(rows_base + (static_cast<int64_t>(r) * P + s) * mblocks);
     }
   }
   return FO_OK;
@@ -632,7 +643,7 @@ fo_status ag_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_
   if (K == 0) return fail(FO_ERR_UNSUPPORTED, "K == 0");
   void* flags_v = nullptr;
   void* recv_v = nullptr;
-  FO_TRY(ensure_buf(ctx, kBufFlags, 1 << 20, &flags_v));
+  FO_TRY(ensure_buf(ctx, kBufFlags, kFlagBytes, &flags_v));
   FO_TRY(ensure_buf(ctx, kBufAgRecv, static_cast<size_t>(P) * M * K * 2, &recv_v));
   uint32_t* flags = static_cast<uint32_t*>(flags_v);
   AgArgs a{X, W, Y, P, m, K, N, static_cast<char*>(recv_v), w_kn, nullptr};
@@ -763,7 +774,7 @@ float* rs_slot(const RsArgs& a, float* base, int r, int h) {
   return base + (static_cast<int64_t>(r) * a.P + h) * a.m * a.N;
 }
 
-constexpr int kTnFbGroup = 1;  // feature blocks per ordering group of the transposed tiles
+constexpr int kTnFbGroup = 16;  // feature blocks per ordering group of the transposed tiles
 
 // Transposed reduce-scatter tiles (GemmParams::tn_S) for a slice of m rows: 0 if they do
 // not apply, else the number of ring steps per tile, with *pair set when the tiles run on
@@ -780,13 +791,18 @@ int rs_tn_steps(const fo_ctx* ctx, const RsArgs& a, const fo_opts& o, bool* pair
   return grid_size(ctx, o, 1 << 30) >= P ? S : 0;
 }
 
-fo_status rs_flash(fo_ctx* ctx, const RsArgs& a, const fo_opts& o, cudaStream_t stream, uint32_t* flags,
-                   uint32_t epoch, DoneSignal* done = nullptr) {
+// Appends the maps and units of a fused reduce-scatter (order FO_ORDER_FLASH or
+// FO_ORDER_NAIVE) to L.  S > 0: transposed tiles (rs_tn_steps), which take the whole launch;
+// otherwise one group per ring step.  `done`: the kept chunk's tiles count into the per-rank
+// completion counters.  ready_base >= 0 (one launch for a whole layer): rank r's unit for
+// chunk c waits, per m-block, until counter ready_base + (r * P + c) * mblocks + mb reaches
+// ready_count (the epilogue warps of the tiles that wrote those rows of X[r]).
+// *flag_end receives the end of the flag range the units use.
+fo_status build_rs_flash(fo_ctx* ctx, Launch& L, const RsArgs& a, const fo_opts& o, uint32_t* flags, uint32_t epoch,
+                         bool done, int S, bool tn_pair, int64_t* flag_end, int64_t ready_base = -1,
+                         int64_t mblocks = 0, int ready_count = 0) {
   const int P = a.P;
-  Launch L;
   fo_status st = FO_OK;
-  bool tn_pair = false;
-  const int S = rs_tn_steps(ctx, a, o, &tn_pair);
   int xmap[kMaxP], wmap[kMaxP];
   for (int r = 0; r < P; ++r) {
     // transposed tiles: the tokens are the MMA's N side (one box of m rows per step) and
@@ -802,6 +818,7 @@ fo_status rs_flash(fo_ctx* ctx, const RsArgs& a, const fo_opts& o, cudaStream_t 
   const int64_t per_hop = tm * tn * 4 > ((a.N + 255) / 256) * 8 ? tm * tn * 4 : ((a.N + 255) / 256) * 8;
   auto fbase = [&](int r, int h) { return kRsFlagBase + (static_cast<int64_t>(r) * P + h) * per_hop; };
   if (fbase(P - 1, P) > (1 << 18)) return fail(FO_ERR_UNSUPPORTED, "too many reduce-scatter tiles for the flag area");
+  *flag_end = fbase(P - 1, P);
   auto add = [&](int r, int c) {
     const int h = mod(r - c - 1, P);  // position of rank r on chunk c's reduction chain
     GemmUnit& u = L.add_unit();
@@ -818,6 +835,10 @@ fo_status rs_flash(fo_ctx* ctx, const RsArgs& a, const fo_opts& o, cudaStream_t 
     u.m_rows = static_cast<int32_t>(a.m);
     u.n_cols = static_cast<int32_t>(a.N);
     u.k = static_cast<int32_t>(a.Kr);
+    if (ready_base >= 0) {
+      u.a_ready_base = static_cast<int32_t>(ready_base + (static_cast<int64_t>(r) * P + c) * mblocks);
+      u.a_ready_count = ready_count;
+    }
     if (h > 0) {
       u.acc_in = rs_slot(a, a.recv, r, h);
       u.ld_acc = a.N;
@@ -876,23 +897,38 @@ fo_status rs_flash(fo_ctx* ctx, const RsArgs& a, const fo_opts& o, cudaStream_t 
       }
     }
     L.p.mn_major = a.w_kn ? 2 : 0;
-    FO_TRY(L.finish(epoch, timeout_ns(o), flags, ctx->ctrl, 0));
   }
+  return FO_OK;
+}
+
+// After the launch: the stream writes every kept-chunk completion counter's final value, so
+// copies that wait on them are released even if the kernel gave up early.
+fo_status publish_done(fo_ctx* ctx, const Launch& L, uint32_t* flags, cudaStream_t stream, DoneSignal* done) {
+  for (int i = 0; i < L.num_units; ++i) {
+    const GemmUnit& u = L.p.units[i];
+    if (u.done_counter < 0) continue;
+    const int r = static_cast<int>(u.done_counter - kDoneBase);
+    const uint32_t n = static_cast<uint32_t>(u.tiles_m * u.tiles_n * L.arrivals_per_tile);
+    ctx->done_total[r] += n;
+    done->target[r] = ctx->done_total[r];
+    FO_TRY(write_flag(stream, flags + kDoneBase + r, done->target[r]));
+  }
+  done->set = true;
+  return FO_OK;
+}
+
+fo_status rs_flash(fo_ctx* ctx, const RsArgs& a, const fo_opts& o, cudaStream_t stream, uint32_t* flags,
+                   uint32_t epoch, DoneSignal* done = nullptr) {
+  Launch L;
+  bool tn_pair = false;
+  const int S = rs_tn_steps(ctx, a, o, &tn_pair);
+  int64_t flag_end = 0;
+  FO_TRY(build_rs_flash(ctx, L, a, o, flags, epoch, done != nullptr, S, tn_pair, &flag_end));
+  if (!S) FO_TRY(L.finish(epoch, timeout_ns(o), flags, ctx->ctrl, 0));
   if (o.compute_only)  // every partial-sum flag published: no tile waits on another
-    FO_CUDA(launch_fill_u32(flags + kRsFlagBase, fbase(P - 1, P) - kRsFlagBase, epoch, stream));
+    FO_CUDA(launch_fill_u32(flags + kRsFlagBase, flag_end - kRsFlagBase, epoch, stream));
   FO_TRY(launch_gemm(ctx, L, o, stream));
-  if (done) {
-    for (int i = 0; i < L.num_units; ++i) {
-      const GemmUnit& u = L.p.units[i];
-      if (u.done_counter < 0) continue;
-      const int r = static_cast<int>(u.done_counter - kDoneBase);
-      const uint32_t n = static_cast<uint32_t>(u.tiles_m * u.tiles_n * L.arrivals_per_tile);
-      ctx->done_total[r] += n;
-      done->target[r] = ctx->done_total[r];
-      FO_TRY(write_flag(stream, flags + kDoneBase + r, done->target[r]));
-    }
-    done->set = true;
-  }
+  if (done) FO_TRY(publish_done(ctx, L, flags, stream, done));
   return FO_OK;
 }
 
@@ -985,7 +1021,7 @@ fo_status rs_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_
   if (m == 0 || N == 0) return FO_OK;
   if (Kr == 0) return fail(FO_ERR_UNSUPPORTED, "Kr == 0");
   void *flags_v = nullptr, *recv_v = nullptr;
-  FO_TRY(ensure_buf(ctx, kBufFlags, 1 << 20, &flags_v));
+  FO_TRY(ensure_buf(ctx, kBufFlags, kFlagBytes, &flags_v));
   FO_TRY(ensure_buf(ctx, kBufRsRecv, static_cast<size_t>(P) * P * m * N * 4, &recv_v));
   RsArgs a{X, W, Y, P, M, m, Kr, N, static_cast<float*>(recv_v), nullptr, w_kn};
   uint32_t* flags = static_cast<uint32_t*>(flags_v);
@@ -1060,7 +1096,7 @@ fo_status gemm_a2a_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, con
   if (m == 0 || Nb == 0) return FO_OK;
   if (K == 0) return fail(FO_ERR_UNSUPPORTED, "K == 0");
   void* flags_v = nullptr;
-  FO_TRY(ensure_buf(ctx, kBufFlags, 1 << 20, &flags_v));
+  FO_TRY(ensure_buf(ctx, kBufFlags, kFlagBytes, &flags_v));
   const uint32_t epoch = ++ctx->epoch;
   const bool serial = o.order == FO_ORDER_SERIAL;
   char* local = nullptr;
@@ -1147,7 +1183,7 @@ fo_status a2a_gemm_run(fo_ctx* ctx, const fo_mat* C, const fo_mat* W, int P, con
   if (m == 0 || N == 0) return FO_OK;
   if (Kc == 0) return fail(FO_ERR_UNSUPPORTED, "Kc == 0");
   void *flags_v = nullptr, *recv_v = nullptr;
-  FO_TRY(ensure_buf(ctx, kBufFlags, 1 << 20, &flags_v));
+  FO_TRY(ensure_buf(ctx, kBufFlags, kFlagBytes, &flags_v));
   FO_TRY(ensure_buf(ctx, kBufA2aRecv, static_cast<size_t>(P) * Mr * Kc * 2, &recv_v));
   uint32_t* flags = static_cast<uint32_t*>(flags_v);
   auto recv = [&](int d) { return static_cast<char*>(recv_v) + static_cast<int64_t>(d) * Mr * Kc * 2; };
@@ -1247,7 +1283,7 @@ fo_status gemm_batch(fo_ctx* ctx, int n, const fo_mat* A, bool a_mn, const fo_ma
     u.ldc = C[i].ld;
   }
   void* flags_v = nullptr;
-  FO_TRY(ensure_buf(ctx, kBufFlags, 1 << 20, &flags_v));
+  FO_TRY(ensure_buf(ctx, kBufFlags, kFlagBytes, &flags_v));
   L.p.mn_major = (a_mn ? 1 : 0) | (b_mn ? 2 : 0);
   FO_TRY(L.finish(++ctx->epoch, timeout_ns(o), static_cast<uint32_t*>(flags_v), ctx->ctrl, stream_a ? 1 : 0));
   return launch_gemm(ctx, L, o, stream);
@@ -1327,6 +1363,85 @@ fo_status row_backward_run(fo_ctx* ctx, const fo_mat* H, const fo_mat* W, const 
 // MLP layer
 // --------------------------------------------------------------------------
 
+// One persistent launch for a whole MLP layer (fused orders): the Flash-AG tiles (SiLU(gate)
+// * up epilogue when gated) come first in the tile order, then the Flash-RS tiles.  Each RS
+// tile's producer waits until every AG tile that writes its rows of H has stored them
+// (per-(rank, slice, m-block) counters of the storing epilogue warps), so the RS tiles of
+// the first ring steps -- which read slices the AG computed in its first steps -- fill the
+// AG's last wave instead of waiting for a second launch.  Every tile waits only on tiles of
+// smaller index.  *used = false (nothing enqueued) when the layer does not fit one launch.
+fo_status mlp_fused_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* Wc, const fo_mat* Wr, int P, bool gated,
+                        const fo_mat* Z, const fo_opts& o, cudaStream_t stream, const fo_mat* Xh, DoneSignal* done,
+                        bool* used) {
+  *used = false;
+  const int64_t m = X[0].rows, K = X[0].cols, Nc = Wc[0].rows, M = m * P;
+  const int64_t F = gated ? Nc / 2 : Nc;
+  if (o.split_layer || o.compute_only || (o.order != FO_ORDER_FLASH && o.order != FO_ORDER_NAIVE)) return FO_OK;
+  if (m == 0 || K == 0 || F == 0 || K % 8 != 0 || F % 8 != 0 || K % 4 != 0) return FO_OK;
+  if (5 * P > kMaxMaps || 2 * P * P > kMaxUnits) return FO_OK;
+  for (int r = 0; r < P; ++r) {
+    FO_TRY(check_mat(X[r], FO_BF16, "X_shards", r));
+    FO_TRY(check_mat(Wc[r], FO_BF16, "W_col", r));
+    FO_TRY(check_mat(Wr[r], FO_BF16, "W_row", r));
+    FO_TRY(check_mat(Z[r], FO_BF16, "Z", r));
+    if (X[r].rows != m || X[r].cols != K || Wc[r].rows != Nc || Wc[r].cols != K || Wr[r].rows != K ||
+        Wr[r].cols != F || Z[r].rows != m || Z[r].cols != K)
+      return fail(FO_ERR_SHAPE, "rank %d: need X [m, H], W_col [Nc, H], W_row [H, F], Z [m, H]", r);
+  }
+  fo_mat H[kMaxP];
+  void* h_v = nullptr;
+  FO_TRY(ensure_buf(ctx, gated ? kBufMlpH : kBufMlpY, static_cast<size_t>(P) * M * F * 2 + 16, &h_v));
+  for (int r = 0; r < P; ++r)
+    H[r] = fo_mat{static_cast<char*>(h_v) + static_cast<int64_t>(r) * M * F * 2, FO_BF16, 0, M, F, F};
+  RsArgs b{H, Wr, Z, P, M, m, F, K, nullptr, nullptr, false};
+  bool tn_pair = false;
+  if (rs_tn_steps(ctx, b, o, &tn_pair) != 0) return FO_OK;  // its own tile shape: two launches
+  const bool pairs = o.sm_pairs == 0 && ctx->pair_clusters > 0 && m % (2 * kBM) == 0;
+  const int64_t block_rows = pairs ? 2 * kBM : kBM, mblocks = (m + block_rows - 1) / block_rows;
+  if (kRowsBase + static_cast<int64_t>(P) * P * mblocks > static_cast<int64_t>(kFlagBytes / 4)) return FO_OK;
+
+  void *flags_v = nullptr, *recv_v = nullptr, *rs_recv_v = nullptr;
+  FO_TRY(ensure_buf(ctx, kBufFlags, kFlagBytes, &flags_v));
+  FO_TRY(ensure_buf(ctx, kBufAgRecv, static_cast<size_t>(P) * M * K * 2, &recv_v));
+  FO_TRY(ensure_buf(ctx, kBufRsRecv, static_cast<size_t>(P) * P * m * K * 4, &rs_recv_v));
+  uint32_t* flags = static_cast<uint32_t*>(flags_v);
+  b.recv = static_cast<float*>(rs_recv_v);
+  AgArgs a{X, Wc, H, P, m, K, Nc, static_cast<char*>(recv_v), false, Xh};
+  const uint32_t epoch = ++ctx->epoch;
+  Launch L;
+  fo_status st = FO_OK;
+  int xmap[kMaxP], rmap[kMaxP], wmap[kMaxP];
+  for (int r = 0; r < P; ++r) {
+    xmap[r] = L.add_map(&st, X[r].ptr, m, K, X[r].ld, kBM);
+    FO_TRY(st);
+    rmap[r] = L.add_map(&st, ag_slot(a, r, 0, 0), M, K, K, kBM);
+    FO_TRY(st);
+    wmap[r] = L.add_map(&st, Wc[r].ptr, Nc, K, Wc[r].ld, gated ? kBN / 2 : kBN);
+    FO_TRY(st);
+  }
+  const bool weight_major = static_cast<double>(P - 1) * m * K * 2 <= kWeightMajorMaxBytes;
+  FO_TRY(add_ag_units(L, a, xmap, rmap, wmap, 0, m, true, gated ? F : 0, weight_major, kRowsBase, mblocks));
+  // the RS tiles of rows [mb * block_rows, +block_rows) of chunk c wait for every AG tile
+  // (output columns per tile: 128 gated, 256 plain) of those rows of slice c to be stored
+  const int64_t ag_tiles_n = (F + (gated ? kBN / 2 : kBN) - 1) / (gated ? kBN / 2 : kBN);
+  const int ready = static_cast<int>(ag_tiles_n * (pairs ? 8 : 4));
+  int64_t flag_end = 0;
+  FO_TRY(build_rs_flash(ctx, L, b, o, flags, epoch, done != nullptr, 0, false, &flag_end, kRowsBase, mblocks, ready));
+  FO_TRY(L.finish(epoch, timeout_ns(o), flags, ctx->ctrl, 0));
+  if (pairs != (o.sm_pairs == 0 && ctx->pair_clusters > 0 && L.pair_friendly()))
+    return fail(FO_ERR_UNSUPPORTED, "layer launch: inconsistent tile shape");
+  *used = true;
+  FO_CUDA(cudaMemsetAsync(flags + kRowsBase, 0, static_cast<size_t>(P) * P * mblocks * 4, stream));
+  // ring copies first in host order (see ag_run), then the one launch
+  FO_TRY(fork_links(ctx, P, stream));
+  if (a.Xh) FO_TRY(enqueue_uploads(ctx, a, epoch, flags));
+  FO_TRY(enqueue_ag_ring(ctx, a, 0, m, true, epoch, o.fault, flags));
+  FO_TRY(launch_gemm(ctx, L, o, stream));
+  FO_TRY(join_links(ctx, P, stream));
+  if (done) FO_TRY(publish_done(ctx, L, flags, stream, done));
+  return FO_OK;
+}
+
 // Xh non-null: X are device buffers that the Flash-AG first fills from the host shards Xh.
 fo_status mlp_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* Wc, const fo_mat* Wr, int P, int gated,
                   const fo_mat* Z, const fo_opts& o, cudaStream_t stream, const fo_mat* Xh = nullptr,
@@ -1334,6 +1449,9 @@ fo_status mlp_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* Wc, const fo_mat* 
   const int64_t m = X[0].rows, M = m * P, Nc = Wc[0].rows;
   if (gated && Nc % 16 != 0) return fail(FO_ERR_UNSUPPORTED, "gated layer needs 2F with F % 8 == 0");
   const int64_t F = gated ? Nc / 2 : Nc;
+  bool fused = false;
+  FO_TRY(mlp_fused_run(ctx, X, Wc, Wr, P, gated != 0, Z, o, stream, Xh, done, &fused));
+  if (fused) return FO_OK;
   fo_mat Y[kMaxP], H[kMaxP];
   if (!gated) {
     void* y_v = nullptr;
@@ -1528,7 +1646,7 @@ fo_status fo_gemm(fo_ctx* ctx, const fo_mat* A, const fo_mat* B, const fo_mat* C
   u.ldc = C->ld;
   if (A->rows > (1 << 30)) return fail(FO_ERR_UNSUPPORTED, "M too large");
   void* flags_v = nullptr;
-  FO_TRY(ensure_buf(ctx, kBufFlags, 1 << 20, &flags_v));
+  FO_TRY(ensure_buf(ctx, kBufFlags, kFlagBytes, &flags_v));
   FO_TRY(L.finish(++ctx->epoch, timeout_ns(o), static_cast<uint32_t*>(flags_v), ctx->ctrl, 0));
   return launch_gemm(ctx, L, o, static_cast<cudaStream_t>(stream));
 }
@@ -1630,7 +1748,7 @@ fo_status fo_mlp_layer_host(fo_ctx* ctx, const fo_mat* X_shards, const fo_mat* W
     return FO_OK;
   }
   void* flags_v = nullptr;
-  FO_TRY(ensure_buf(ctx, kBufFlags, 1 << 20, &flags_v));
+  FO_TRY(ensure_buf(ctx, kBufFlags, kFlagBytes, &flags_v));
   uint32_t* flags = static_cast<uint32_t*>(flags_v);
   for (int r = 0; r < P; ++r) {
     cudaStream_t ls = ctx->link[r];
@@ -1729,7 +1847,7 @@ fo_status host_buffer(fo_ctx* ctx, int slot, size_t bytes, void** out) {
 }
 fo_status host_flags(fo_ctx* ctx, uint32_t** out) {
   void* v = nullptr;
-  FO_TRY(ensure_buf(ctx, kBufFlags, 1 << 20, &v));
+  FO_TRY(ensure_buf(ctx, kBufFlags, kFlagBytes, &v));
   *out = static_cast<uint32_t*>(v) + kAgFlagBase;
   return FO_OK;
 }

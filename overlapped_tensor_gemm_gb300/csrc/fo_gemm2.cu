@@ -62,6 +62,13 @@ __device__ void pair_producer(const GemmParams& p, uint8_t* tiles, PairCtl* ctl,
       fence_proxy_async_global();
       waited_unit = tc.unit;
     }
+    if (u.a_ready_base >= 0) {  // A rows written by an earlier tile of this launch
+      const int f = u.a_ready_base + tc.mb;
+      ok = count_wait(p.flags + f, static_cast<uint32_t>(u.a_ready_count), p.ctrl, p.timeout_ns, kSiteRowsReady,
+                      static_cast<uint32_t>(f));
+      if (!ok) break;
+      fence_proxy_async_global();
+    }
     const int nk = (u.k + kBK - 1) / kBK;
     const int a_row = u.a_row0 + tc.mb * 2 * kBM + static_cast<int>(cta) * kBM;
     // B rows of this CTA: gated tiles put the gate rows in the leader and the up rows in the peer
@@ -208,7 +215,7 @@ __device__ void pair_epilogue(const GemmParams& p, PairCtl* ctl, uint32_t tmem_b
         return;
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
-      if (!epilogue_tn(p, tc, tb, static_cast<int>(cta), 2, q, lane)) return;
+      if (!epilogue_tn(p, tc, tb, static_cast<int>(cta), 2, q, lane, stage)) return;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -271,6 +278,12 @@ __device__ void pair_epilogue(const GemmParams& p, PairCtl* ctl, uint32_t tmem_b
       __threadfence_system();
       __syncwarp();
       if (lane == 0) red_release_sys_add(p.flags + u.done_counter, 1u);
+    }
+    if (u.rows_done_base >= 0) {
+      // this warp's rows of the tile are stored: count them for the tiles that read them
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) red_release_gpu_add(p.flags + u.rows_done_base + tc.mb, 1u);
     }
     acc ^= 1;
     if (acc == 0) acc_phase ^= 1u;

@@ -181,9 +181,15 @@ __device__ __forceinline__ void store_bf16_row_chunk(const GemmUnit& u, int row,
 // With a partial-sum add, `pf` holds chunk 0's partials on entry (loaded before the
 // accumulator was complete) and the loads of chunk c+1 are in flight while chunk c is
 // staged and stored.
-__device__ __forceinline__ void store_rows(const GemmUnit& u, uint32_t tbase, int row0, int col0, int lane, bool add,
-                                           float4 (&pf)[8], float* stage) {
-  if (u.epi == kEpiBF16) {
+// tn_rows > 0: a unit of a transposed tile.  The warp's 32 TMEM lanes are then the output
+// columns [col0, col0 + 32) and TMEM columns tbase .. tbase + tn_rows the unit's rows
+// 0 .. tn_rows-1; each 32x32 chunk is staged transposed (row-major: every write
+// instruction fills one 128-byte row of the stage) and stored by the same row-contiguous
+// path.
+__device__ __noinline__ void store_rows(const GemmUnit& u, uint32_t tbase, int row0, int col0, int lane, bool add,
+                                           float4 (&pf)[8], float* stage, int tn_rows = 0) {
+  const bool tn = tn_rows > 0;
+  if (!tn && u.epi == kEpiBF16) {
     const int row = row0 + lane;
 #pragma unroll 1
     for (int c = 0; c < kBN / 32; ++c) {
@@ -196,22 +202,29 @@ __device__ __forceinline__ void store_rows(const GemmUnit& u, uint32_t tbase, in
     }
     return;
   }
+  const int nchunks = tn ? tn_rows / 32 : kBN / 32;
 #pragma unroll 1
-  for (int c = 0; c < kBN / 32; ++c) {
-    const int col = col0 + c * 32;
+  for (int c = 0; c < nchunks; ++c) {
+    const int r0 = tn ? c * 32 : row0;    // first row of the chunk
+    const int col = tn ? col0 : col0 + c * 32;
     if (col >= u.n_cols) break;
     uint32_t v[32];
     float4 next[8];
     tmem_ld32(tbase + c * 32, v);
-    if (add && c + 1 < kBN / 32) load_partial(u, row0, col + 32, lane, next);
+    if (add && c + 1 < nchunks) load_partial(u, tn ? r0 + 32 : row0, tn ? col0 : col + 32, lane, next);
     tmem_wait_ld();
+    if (tn) {
 #pragma unroll
-    for (int g = 0; g < 8; ++g)
-      *reinterpret_cast<float4*>(stage + stage_index(lane, g)) =
-          make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]), __uint_as_float(v[4 * g + 2]),
-                      __uint_as_float(v[4 * g + 3]));
+      for (int j = 0; j < 32; ++j) stage[stage_index(j, lane >> 2) + (lane & 3)] = __uint_as_float(v[j]);
+    } else {
+#pragma unroll
+      for (int g = 0; g < 8; ++g)
+        *reinterpret_cast<float4*>(stage + stage_index(lane, g)) =
+            make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]), __uint_as_float(v[4 * g + 2]),
+                        __uint_as_float(v[4 * g + 3]));
+    }
     __syncwarp();
-    store_staged(u, row0, col, lane, stage, add, pf);
+    store_staged(u, r0, col, lane, stage, add, pf);
     __syncwarp();  // the stage is rewritten by the next chunk
     if (add) {
 #pragma unroll
@@ -294,57 +307,11 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int tile) {
   return p.tn_S > 0 ? decode_tile_tn(p, tile) : decode_tile(p, tile);
 }
 
-// Partial sums of 16 token rows (t0 .. t0+15) at this lane's feature; zero where absent.
-__device__ __forceinline__ void load_partial16(const GemmUnit& u, int t0, int feat, bool active, float (&in)[16]) {
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int t = t0 + i;
-    in[i] = (active && t < u.m_rows) ? __ldcg(u.acc_in + static_cast<int64_t>(t) * u.ld_acc + feat) : 0.0f;
-  }
-}
-
-// Epilogue of one unit of a transposed tile for one warp: its 32 accumulator lanes are the
-// features feat = f0 + lane, its columns [col0, col0 + tn_rows) the unit's token rows.
-// out[t][feat] = acc (+ acc_in[t][feat]); a warp instruction touches 32 consecutive features
-// of one token row (128 bytes of fp32, 64 of bf16).  The partial sums of the next 16 rows
-// are in flight while the current 16 are stored.
-__device__ __forceinline__ void store_unit_tn(const GemmParams& p, const GemmUnit& u, uint32_t tbase, int col0,
-                                              int feat) {
-  const bool add = u.epi == kEpiAddF32 || u.epi == kEpiAddBF16;
-  const bool bf16_out = u.epi == kEpiBF16 || u.epi == kEpiAddBF16;
-  const bool fok = feat < u.n_cols;
-  float nxt[16];
-  load_partial16(u, 0, feat, add && fok, nxt);
-#pragma unroll 1
-  for (int c0 = 0; c0 < p.tn_rows; c0 += 16) {
-    float in[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) in[i] = nxt[i];
-    uint32_t v[16];
-    tmem_ld16(tbase + col0 + c0, v);
-    if (c0 + 16 < p.tn_rows) load_partial16(u, c0 + 16, feat, add && fok, nxt);
-    tmem_wait_ld();
-    if (!fok) continue;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int t = c0 + i;
-      if (t >= u.m_rows) break;
-      const float x = __uint_as_float(v[i]) + in[i];
-      if (bf16_out) {
-        static_cast<uint16_t*>(u.c)[static_cast<int64_t>(t) * u.ldc + feat] =
-            __bfloat16_as_ushort(__float2bfloat16_rn(x));
-      } else {
-        static_cast<float*>(u.c)[static_cast<int64_t>(t) * u.ldc + feat] = x;
-      }
-    }
-  }
-}
-
 // The whole epilogue of a transposed tile for one warp (quadrant q of CTA `cta` of `ncta`):
 // the tile's units in step order, each after its incoming partial sum's flag, each
 // releasing its own flag for the next rank.  False if a wait gave up.
 __device__ __forceinline__ bool epilogue_tn(const GemmParams& p, const TileCoord& tc, uint32_t tbase, int cta,
-                                            int ncta, int q, int lane) {
+                                            int ncta, int q, int lane, float* stage) {
   const int f0 = (tc.nb * ncta + cta) * kBM + q * 32;
   const int slot = (tc.nb * ncta + cta) * 4 + q;
   for (int s = 0; s < p.tn_S; ++s) {
@@ -353,7 +320,11 @@ __device__ __forceinline__ bool epilogue_tn(const GemmParams& p, const TileCoord
       const int f = u.in_flag_base + slot;
       if (!warp_flag_wait(p.flags + f, p, kSiteAccInFlag, static_cast<uint32_t>(f), lane)) return false;
     }
-    store_unit_tn(p, u, tbase, s * p.tn_rows, f0 + lane);
+    // the unit's token rows are TMEM columns [s * tn_rows, +tn_rows) of the accumulator
+    const bool add = u.epi == kEpiAddF32 || u.epi == kEpiAddBF16;
+    float4 pf[8];
+    if (add) load_partial(u, 0, f0, lane, pf);
+    store_rows(u, tbase + s * p.tn_rows, 0, f0, lane, add, pf, stage, p.tn_rows);
     if (u.out_flag_base >= 0) {
       __threadfence();
       __syncwarp();

@@ -33,9 +33,9 @@ constexpr int kBN = 256;            // UMMA N
 constexpr int kBK = 64;             // one 128-byte swizzle atom of bf16
 constexpr int kStages = 4;
 constexpr int kGemmThreads = 192;   // warp 0: TMA, warp 1: MMA, warps 2-5: epilogue
-constexpr int kMaxMaps = 24;
-constexpr int kMaxUnits = 64;
-constexpr int kMaxGroups = 16;
+constexpr int kMaxMaps = 40;    // one launch of a whole MLP layer: 3P maps for Flash-AG + 2P for Flash-RS
+constexpr int kMaxUnits = 128;  // P*P units per decomposed collective, two collectives per layer
+constexpr int kMaxGroups = 24;
 
 enum EpiMode : int32_t {
   kEpiBF16 = 0,        // C (bf16) = acc
@@ -66,6 +66,13 @@ struct GemmUnit {
   int32_t a_map2, a2_row_stride, chunk_flag_base;
   int32_t done_counter;        // >= 0: every epilogue warp adds 1 to flags[done_counter] after its
                                // part of a tile is stored (system-scope release)
+  // One launch for a whole layer: a producing unit counts, per m-block of its tiles, the
+  // epilogue warps that have stored their rows (flags[rows_done_base + m-block], gpu-scope
+  // release); a consuming unit's producer waits before loading A rows of m-block mb until
+  // flags[a_ready_base + mb] >= a_ready_count (the counters start at zero every launch).
+  int32_t rows_done_base;      // -1: none
+  int32_t a_ready_base;        // -1: none
+  int32_t a_ready_count;
   void* c;                     // output
   const float* acc_in;         // fp32 partial sum to add (kEpiAdd*)
   int64_t ldc, ld_acc;         // leading dimensions in elements
@@ -107,6 +114,8 @@ struct GemmParams {
   uint32_t* flags;             // ring flags (epoch-valued)
   uint32_t* ctrl;              // device control block (error word, abort flag)
 };
+static_assert(sizeof(GemmParams) <= 32764, "GemmParams must fit the kernel parameter space");
+
 // A tile's position: unit index, m-block and n-block inside the unit.
 struct TileCoord {
   int unit, mb, nb;
@@ -124,7 +133,7 @@ enum CtrlWord : int {
 enum WaitSite : uint32_t {
   kSiteAgFlag = 1, kSiteFull = 2, kSiteEmpty = 3, kSiteTmemFull = 4,
   kSiteTmemEmpty = 5, kSiteAccInFlag = 6, kSiteDrain = 7, kSiteAttnFlag = 8,
-  kSiteAttnBar = 9, kSiteVRange = 10
+  kSiteAttnBar = 9, kSiteVRange = 10, kSiteRowsReady = 11
 };
 
 // host launchers (fo_gemm.cu: single-SM 128x256 tiles; fo_gemm2.cu: SM-pair 256x256 tiles)

@@ -91,6 +91,29 @@ static __device__ __noinline__ bool flag_wait(const uint32_t* flag, uint32_t epo
   }
 }
 
+// Spin (acquire) until the counter *p reaches `target` (a count that starts at zero for
+// the launch).  False on timeout or abort.
+static __device__ __noinline__ bool count_wait(const uint32_t* p, uint32_t target, uint32_t* ctrl,
+                                               uint64_t timeout_ns, uint32_t site, uint32_t detail) {
+  if (ld_acquire_gpu(p) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(p) >= target) return true;
+    if ((it & 63u) == 0u) {
+      if (aborted(ctrl)) return false;
+      if (global_timer_ns() - t0 > timeout_ns) {
+        raise_error(ctrl, FO_ERR_TIMEOUT, site, detail);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------

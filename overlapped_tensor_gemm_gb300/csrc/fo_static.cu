@@ -157,6 +157,8 @@ extern "C" FO_API fo_status fo_gemm_rs_noalloc(const fo_mat* X, const fo_mat* W_
       u.in_flag_base = -1;
       u.out_flag_base = -1;
       u.done_counter = -1;
+      u.rows_done_base = -1;
+      u.a_ready_base = -1;
       if (h > 0) {
         u.acc_in = slot(r, h);
         u.ld_acc = N;
