@@ -8,6 +8,11 @@ from oracle import bf16
 # max-abs relative to the largest reference magnitude).
 REL_L2 = 2e-3
 MAX_ABS_FRAC = 1e-2
+# A block that chains three operations with bf16-rounded outputs (the attention block: QKV
+# projection, attention, output projection) rounds at three points; at each the two sides'
+# pre-rounding values may fall on either side of a bf16 boundary.  Independent rounding
+# stages add in quadrature: the per-operation bound times sqrt(3).
+REL_L2_THREE_STAGES = REL_L2 * 3 ** 0.5
 
 
 def to_dev(bits: np.ndarray, device="cuda") -> torch.Tensor:
@@ -32,7 +37,7 @@ def assert_bits_equal(got_bits: np.ndarray, ref_f64: np.ndarray, what: str = "")
                              f"got {bf16.to_f64(got_bits[i])} want {ref_f64[i]}")
 
 
-def assert_close(got: np.ndarray, ref: np.ndarray, what: str = "", round_ref: bool = True):
+def assert_close(got: np.ndarray, ref: np.ndarray, what: str = "", round_ref: bool = True, rel_l2: float = REL_L2):
     """Tolerance check of a bf16 result; the reference is rounded to bf16 (the
     operation's output type) unless round_ref is False."""
     got = np.asarray(got, np.float64)
@@ -46,7 +51,7 @@ def assert_close(got: np.ndarray, ref: np.ndarray, what: str = "", round_ref: bo
     rel = num / den
     mx = np.abs(got - ref).max() if got.size else 0.0
     lim = MAX_ABS_FRAC * (np.abs(ref).max() if ref.size else 0.0)
-    assert rel <= REL_L2, f"{what}: rel-L2 {rel:.3e} > {REL_L2}"
+    assert rel <= rel_l2, f"{what}: rel-L2 {rel:.3e} > {rel_l2}"
     assert mx <= lim, f"{what}: max-abs {mx:.3e} > {lim:.3e}"
 
 

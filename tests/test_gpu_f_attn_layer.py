@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import fo_workloads as wl
-from helpers import assert_close, f64, to_bits, to_dev, guarded
+from helpers import REL_L2_THREE_STAGES, assert_close, f64, to_bits, to_dev, guarded
 from oracle import ops
 
 pytestmark = pytest.mark.gpu
@@ -33,7 +33,7 @@ def _run(ctx, P, tokens, hidden, heads, seed, causal=True, **kw):
     _, _, ref = ops.attn_layer([f64(x) for x in inp["X_shards"]], [f64(w) for w in inp["W_qkv"]],
                                [f64(w) for w in inp["W_o"]], heads, causal=causal)
     for d in range(P):
-        assert_close(f64(to_bits(Z[d])), ref[d], f"attention block rank {d}")
+        assert_close(f64(to_bits(Z[d])), ref[d], f"attention block rank {d}", rel_l2=REL_L2_THREE_STAGES)
 
 
 # P=2, 128-row slices: single-SM GEMM tiles, 2 attention query blocks per head;
@@ -96,4 +96,4 @@ def test_attention_block_bench_shape_sampled_rows(ctx):
     ref = ops.gemm_rs_definition(chunks, [f64(w) for w in inp["W_o"]])
     for d in range(P):
         got = f64(to_bits(Z[d][torch.as_tensor(rows[d], device="cuda")]))
-        assert_close(got, ref[d], f"attention block (bench shape) rank {d}")
+        assert_close(got, ref[d], f"attention block (bench shape) rank {d}", rel_l2=REL_L2_THREE_STAGES)
