@@ -59,7 +59,8 @@ typedef enum {
   FO_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed                */
   FO_ERR_TIMEOUT = 5,       /* a device wait ran past opts.timeout_us           */
   FO_ERR_OOM = 6,           /* workspace growth failed                          */
-  FO_ERR_RANGE = 7          /* an input value outside what a kernel represents  */
+  FO_ERR_RANGE = 7,         /* an input value outside what a kernel represents  */
+  FO_ERR_INTERNAL = 8       /* an index check of the debug build failed (a bug)  */
 } fo_status;
 
 typedef enum { FO_BF16 = 0, FO_F32 = 1 } fo_dtype;

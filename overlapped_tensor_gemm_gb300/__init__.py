@@ -20,9 +20,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfo.so")
 
 (FO_OK, FO_ERR_INVALID_ARG, FO_ERR_SHAPE, FO_ERR_UNSUPPORTED, FO_ERR_CUDA, FO_ERR_TIMEOUT, FO_ERR_OOM,
- FO_ERR_RANGE) = range(8)
+ FO_ERR_RANGE, FO_ERR_INTERNAL) = range(9)
 STATUS_NAMES = ["FO_OK", "FO_ERR_INVALID_ARG", "FO_ERR_SHAPE", "FO_ERR_UNSUPPORTED", "FO_ERR_CUDA",
-                "FO_ERR_TIMEOUT", "FO_ERR_OOM", "FO_ERR_RANGE"]
+                "FO_ERR_TIMEOUT", "FO_ERR_OOM", "FO_ERR_RANGE", "FO_ERR_INTERNAL"]
 FO_BF16, FO_F32 = 0, 1
 ORDERS = {"flash": 0, "naive": 1, "slicing": 2, "serial": 3}
 LINKS = {"default": 0, "ce": 1, "push": 2}

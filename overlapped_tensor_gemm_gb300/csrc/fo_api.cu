@@ -371,6 +371,7 @@ struct Launch {
     p.epoch = epoch;
     p.timeout_ns = tmo;
     p.flags = flags;
+    p.flag_words = static_cast<int32_t>(kFlagBytes / 4);
     p.ctrl = ctrl;
     return FO_OK;
   }
@@ -880,6 +881,7 @@ fo_status build_rs_flash(fo_ctx* ctx, Launch& L, const RsArgs& a, const fo_opts&
     q.epoch = epoch;
     q.timeout_ns = timeout_ns(o);
     q.flags = flags;
+    q.flag_words = static_cast<int32_t>(kFlagBytes / 4);
     q.ctrl = ctx->ctrl;
     L.tn_pair = tn_pair;
     L.arrivals_per_tile = 4 * ncta;

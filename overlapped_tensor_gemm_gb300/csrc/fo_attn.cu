@@ -86,6 +86,7 @@ struct AttnParams {
   float scale_log2;             // log2(e) / sqrt(head_dim)
   uint64_t timeout_ns;
   uint32_t* flags;              // arrival flags, index rank*P + slice
+  int32_t flag_words;           // words at `flags` (checked by the debug build)
   uint32_t* ctrl;
   int32_t wait_flags;           // 0: every slice is already in place (serial order)
   int32_t ring;                 // 1: query split (K/V ring); 0: P independent problems (own slice only)
@@ -194,6 +195,14 @@ __device__ void attn_producer(const AttnParams& p, uint8_t* smem, AttnCtl* ctl) 
     const Item& it = kit.it;
     const int s = slice_of(p, it.r, kit.t);
     const int fidx = it.r * p.P + s;
+#ifdef FO_DEBUG_BOUNDS
+    // debug build: the item, its key block and its flag word lie inside the launch
+    if (!(it.r >= 0 && it.r < p.P && it.qb >= 0 && it.qb < p.nkb && it.h >= 0 && it.h < p.heads && kit.kb >= 0 &&
+          kit.kb < p.nkb && fidx >= 0 && fidx < p.flag_words && fidx < 64)) {
+      raise_error(p.ctrl, FO_ERR_INTERNAL, kSiteBounds, static_cast<uint32_t>(kit.i));
+      return false;
+    }
+#endif
     if (kit.t > 0 && p.wait_flags && !((seen >> fidx) & 1ull)) {
       if (!flag_wait(p.flags + fidx, p.epoch, p.ctrl, p.timeout_ns, kSiteAttnFlag, fidx)) return false;
       fence_proxy_async_global();
@@ -799,6 +808,7 @@ fo_status attn_run(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K, const fo_mat* 
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kHd)));
   p.timeout_ns = host_timeout_ns(o);
   p.flags = flags;
+  p.flag_words = static_cast<int32_t>((2u << 20) / 4);  // the context's flag buffer (2 MiB)
   p.ctrl = host_ctrl(ctx);
   p.ring = ring ? 1 : 0;
 

@@ -71,6 +71,10 @@ __device__ void producer_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl)
   const bool tn = p.tn_S > 0;
   for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
     const TileCoord tc = tile_coord(p, tile);
+    if (!tile_ok(p, tc, tile, 1)) {
+      ok = false;
+      break;
+    }
     const GemmUnit& u = p.units[tc.unit];
     if (u.wait_flag >= 0 && tc.unit != waited_unit) {
       ok = flag_wait(p.flags + u.wait_flag, p.epoch, p.ctrl, p.timeout_ns, kSiteAgFlag,
@@ -173,6 +177,10 @@ __device__ void mma_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl, uint
   const uint32_t tiles_addr = smem_u32(tiles);
   for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
     const TileCoord tc = tile_coord(p, tile);
+    if (!tile_ok(p, tc, tile, 1)) {
+      ok = false;
+      break;
+    }
     const GemmUnit& u = p.units[tc.unit];
     if (!mbar_wait_fast(&ctl->tmem_empty[acc], acc_phase ^ 1u, p.ctrl, p.timeout_ns, kSiteTmemEmpty,
                    static_cast<uint32_t>(tile))) {
@@ -222,75 +230,17 @@ __device__ void epilogue_loop(const GemmParams& p, SmemCtl* ctl, uint32_t tmem_b
   uint32_t acc_phase = 0;
   for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
     const TileCoord tc = tile_coord(p, tile);
-    if (p.tn_S > 0) {  // transposed reduce-scatter tile: its steps in order, one hop each
-      if (!warp_mbar_wait(&ctl->tmem_full[acc], acc_phase, p, kSiteTmemFull, static_cast<uint32_t>(tile), lane))
-        return;
-      tc_fence_after();
-      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
-      if (!epilogue_tn(p, tc, tb, 0, 1, q, lane, stage)) return;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->tmem_empty[acc]);
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
-      continue;
-    }
-    const GemmUnit& u = p.units[tc.unit];
-    const int tile_in_unit = tc.mb * u.tiles_n + tc.nb;
-    const int row = tc.mb * kBM + q * 32 + lane;
-    const bool row_ok = row < u.m_rows;
-    // the partial sum's flag and first chunk are taken while the accumulator is computed
-    const bool add = u.epi == kEpiAddF32 || u.epi == kEpiAddBF16;
-    if (u.in_flag_base >= 0) {
-      const int f = u.in_flag_base + tile_in_unit * 4 + q;
-      if (!warp_flag_wait(p.flags + f, p, kSiteAccInFlag, static_cast<uint32_t>(f), lane)) return;
-    }
-    float4 part[8];
-    if (add) load_partial(u, row - lane, tc.nb * kBN, lane, part);
-    if (!warp_mbar_wait(&ctl->tmem_full[acc], acc_phase, p, kSiteTmemFull, static_cast<uint32_t>(tile), lane))
-      return;
-    tc_fence_after();
+    if (!tile_ok(p, tc, tile, 1)) return;
     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
-    if (u.epi == kEpiSiluMul) {
-#pragma unroll 1
-      for (int c = 0; c < kBN / 64; ++c) {
-        uint32_t g[32], v[32];
-        tmem_ld32(tbase + c * 32, g);
-        tmem_ld32(tbase + kBN / 2 + c * 32, v);
-        tmem_wait_ld();
-        const int col = tc.nb * (kBN / 2) + c * 32;
-        if (row_ok && col < u.n_cols) store_silu_chunk(u, row, col, g, v);
-      }
-    } else {
-      store_rows(u, tbase, row - lane, tc.nb * kBN, lane, add, part, stage);
-    }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&ctl->tmem_empty[acc]);
-    if (u.out_flag_base >= 0) {
-      // rows of this quadrant are stored: publish them to the next rank
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) st_release_gpu(p.flags + u.out_flag_base + tile_in_unit * 4 + q, p.epoch);
-    }
-    if (u.done_counter >= 0) {
-      // this warp's rows of the tile are final: count them for a copy engine that waits
-      __threadfence_system();
-      __syncwarp();
-      if (lane == 0) red_release_sys_add(p.flags + u.done_counter, 1u);
-    }
-    if (u.rows_done_base >= 0) {
-      // this warp's rows of the tile are stored: count them for the tiles that read them
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) red_release_gpu_add(p.flags + u.rows_done_base + tc.mb, 1u);
-    }
+    if (!epilogue_tile(p, tc, tile, &ctl->tmem_full[acc], acc_phase, tbase, 0, 1, q, lane, stage,
+                       [&] { mbar_arrive(&ctl->tmem_empty[acc]); }))
+      return;
     acc ^= 1;
     if (acc == 0) acc_phase ^= 1u;
   }
 }
 
-__global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __maxnreg__(192) gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = smem_u32(smem_raw);
   uint8_t* tiles = smem_raw + ((1024u - (base & 1023u)) & 1023u);

@@ -54,6 +54,10 @@ __device__ void pair_producer(const GemmParams& p, uint8_t* tiles, PairCtl* ctl,
   const bool tn = p.tn_S > 0;
   for (int tile = cluster; ok && tile < p.total_tiles; tile += nclusters) {
     const TileCoord tc = tile_coord(p, tile);
+    if (!tile_ok(p, tc, tile, 2)) {
+      ok = false;
+      break;
+    }
     const GemmUnit& u = p.units[tc.unit];
     if (u.wait_flag >= 0 && tc.unit != waited_unit) {
       ok = flag_wait(p.flags + u.wait_flag, p.epoch, p.ctrl, p.timeout_ns, kSiteAgFlag,
@@ -161,6 +165,10 @@ __device__ void pair_mma(const GemmParams& p, uint8_t* tiles, PairCtl* ctl, uint
   const uint32_t tiles_addr = smem_u32(tiles);
   for (int tile = cluster; ok && tile < p.total_tiles; tile += nclusters) {
     const TileCoord tc = tile_coord(p, tile);
+    if (!tile_ok(p, tc, tile, 2)) {
+      ok = false;
+      break;
+    }
     const GemmUnit& u = p.units[tc.unit];
     if (!mbar_wait_fast(&ctl->tmem_empty[acc], acc_phase ^ 1u, p.ctrl, p.timeout_ns, kSiteTmemEmpty,
                    static_cast<uint32_t>(tile))) {
@@ -210,87 +218,24 @@ __device__ void pair_epilogue(const GemmParams& p, PairCtl* ctl, uint32_t tmem_b
   uint32_t acc_phase = 0;
   for (int tile = cluster; tile < p.total_tiles; tile += nclusters) {
     const TileCoord tc = tile_coord(p, tile);
-    if (p.tn_S > 0) {  // transposed reduce-scatter tile: its steps in order, one hop each
-      if (!warp_mbar_wait(&ctl->tmem_full[acc], acc_phase, p, kSiteTmemFull, static_cast<uint32_t>(tile), lane))
-        return;
-      tc_fence_after();
-      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
-      if (!epilogue_tn(p, tc, tb, static_cast<int>(cta), 2, q, lane, stage)) return;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (cta == 0) {
-          mbar_arrive(&ctl->tmem_empty[acc]);
-        } else {
-          mbar_arrive_cluster(leader_tmem_empty + acc * static_cast<uint32_t>(sizeof(uint64_t)));
-        }
-      }
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
-      continue;
-    }
-    const GemmUnit& u = p.units[tc.unit];
-    // flags per (tile, CTA half, lane quadrant): the same rows on both sides of a hop
-    const int flag_slot = ((tc.mb * u.tiles_n + tc.nb) * 2 + static_cast<int>(cta)) * 4 + q;
-    const int row = tc.mb * 2 * kBM + static_cast<int>(cta) * kBM + q * 32 + lane;
-    const bool row_ok = row < u.m_rows;
-    // the partial sum's flag and first chunk are taken while the accumulator is computed
-    const bool add = u.epi == kEpiAddF32 || u.epi == kEpiAddBF16;
-    if (u.in_flag_base >= 0) {
-      const int f = u.in_flag_base + flag_slot;
-      if (!warp_flag_wait(p.flags + f, p, kSiteAccInFlag, static_cast<uint32_t>(f), lane)) return;
-    }
-    float4 part[8];
-    if (add) load_partial(u, row - lane, tc.nb * kBN, lane, part);
-    if (!warp_mbar_wait(&ctl->tmem_full[acc], acc_phase, p, kSiteTmemFull, static_cast<uint32_t>(tile), lane))
-      return;
-    tc_fence_after();
+    if (!tile_ok(p, tc, tile, 2)) return;
     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
-    if (u.epi == kEpiSiluMul) {
-#pragma unroll 1
-      for (int c = 0; c < kBN / 64; ++c) {
-        uint32_t g[32], v[32];
-        tmem_ld32(tbase + c * 32, g);
-        tmem_ld32(tbase + kBN / 2 + c * 32, v);
-        tmem_wait_ld();
-        const int col = tc.nb * (kBN / 2) + c * 32;
-        if (row_ok && col < u.n_cols) store_silu_chunk(u, row, col, g, v);
-      }
-    } else {
-      store_rows(u, tbase, row - lane, tc.nb * kBN, lane, add, part, stage);
-    }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) {
+    auto arrive_empty = [&] {
       if (cta == 0) {
         mbar_arrive(&ctl->tmem_empty[acc]);
       } else {
         mbar_arrive_cluster(leader_tmem_empty + acc * static_cast<uint32_t>(sizeof(uint64_t)));
       }
-    }
-    if (u.out_flag_base >= 0) {
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) st_release_gpu(p.flags + u.out_flag_base + flag_slot, p.epoch);
-    }
-    if (u.done_counter >= 0) {
-      // this warp's rows of the tile are final: count them for a copy engine that waits
-      __threadfence_system();
-      __syncwarp();
-      if (lane == 0) red_release_sys_add(p.flags + u.done_counter, 1u);
-    }
-    if (u.rows_done_base >= 0) {
-      // this warp's rows of the tile are stored: count them for the tiles that read them
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) red_release_gpu_add(p.flags + u.rows_done_base + tc.mb, 1u);
-    }
+    };
+    if (!epilogue_tile(p, tc, tile, &ctl->tmem_full[acc], acc_phase, tbase, static_cast<int>(cta), 2, q, lane, stage,
+                       arrive_empty))
+      return;
     acc ^= 1;
     if (acc == 0) acc_phase ^= 1u;
   }
 }
 
-__global__ void __launch_bounds__(kGemmThreads, 1) gemm_pair_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __maxnreg__(192) gemm_pair_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = smem_u32(smem_raw);
   uint8_t* tiles = smem_raw + ((1024u - (base & 1023u)) & 1023u);

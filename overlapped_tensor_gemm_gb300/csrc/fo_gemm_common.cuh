@@ -186,7 +186,7 @@ __device__ __forceinline__ void store_bf16_row_chunk(const GemmUnit& u, int row,
 // 0 .. tn_rows-1; each 32x32 chunk is staged transposed (row-major: every write
 // instruction fills one 128-byte row of the stage) and stored by the same row-contiguous
 // path.
-__device__ __noinline__ void store_rows(const GemmUnit& u, uint32_t tbase, int row0, int col0, int lane, bool add,
+__device__ __forceinline__ void store_rows(const GemmUnit& u, uint32_t tbase, int row0, int col0, int lane, bool add,
                                            float4 (&pf)[8], float* stage, int tn_rows = 0) {
   const bool tn = tn_rows > 0;
   if (!tn && u.epi == kEpiBF16) {
@@ -307,36 +307,130 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int tile) {
   return p.tn_S > 0 ? decode_tile_tn(p, tile) : decode_tile(p, tile);
 }
 
-// The whole epilogue of a transposed tile for one warp (quadrant q of CTA `cta` of `ncta`):
-// the tile's units in step order, each after its incoming partial sum's flag, each
-// releasing its own flag for the next rank.  False if a wait gave up.
-__device__ __forceinline__ bool epilogue_tn(const GemmParams& p, const TileCoord& tc, uint32_t tbase, int cta,
-                                            int ncta, int q, int lane, float* stage) {
-  const int f0 = (tc.nb * ncta + cta) * kBM + q * 32;
-  const int slot = (tc.nb * ncta + cta) * 4 + q;
-  for (int s = 0; s < p.tn_S; ++s) {
-    const GemmUnit& u = p.units[tc.unit + s];
-    if (u.in_flag_base >= 0) {
-      const int f = u.in_flag_base + slot;
+// Flag release and completion counters after a unit's rows of a tile are stored.
+__device__ __forceinline__ void publish_unit(const GemmParams& p, const GemmUnit& u, int slot, int mb, int lane) {
+  if (u.out_flag_base >= 0) {
+    // rows of this quadrant are stored: publish them to the next rank
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) st_release_gpu(p.flags + u.out_flag_base + slot, p.epoch);
+  }
+  if (u.done_counter >= 0) {
+    // this warp's rows of the tile are final: count them for a copy engine that waits
+    __threadfence_system();
+    __syncwarp();
+    if (lane == 0) red_release_sys_add(p.flags + u.done_counter, 1u);
+  }
+  if (u.rows_done_base >= 0) {
+    // this warp's rows of the tile are stored: count them for the tiles that read them
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) red_release_gpu_add(p.flags + u.rows_done_base + mb, 1u);
+  }
+}
+
+// One tile's epilogue for one epilogue warp (TMEM lane quadrant q of CTA `cta` of `ncta`).
+// A step-ordered tile has one unit: its partial sum's flag and first chunk are taken while
+// the accumulator is still computed, and its flag is released after the accumulator is
+// freed.  A transposed tile has tn_S units (ring steps of one rank), handled in step order:
+// each after its incoming partial sum's flag, each released before the next.  This is the
+// only call site of store_rows, so a kernel inlines one copy of it.  `arrive_empty()`
+// frees the accumulator.  False if a wait gave up.
+template <class ArriveEmpty>
+__device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const TileCoord& tc, int tile, uint64_t* tmem_full,
+                                              uint32_t acc_phase, uint32_t tbase, int cta, int ncta, int q, int lane,
+                                              float* stage, ArriveEmpty arrive_empty) {
+  const bool tn = p.tn_S > 0;
+  const GemmUnit& u0 = p.units[tc.unit];
+  const int blk = tn ? tc.nb : tc.mb * u0.tiles_n + tc.nb;
+  const int slot = (blk * ncta + cta) * 4 + q;           // flags per (tile, CTA half, quadrant)
+  const int row0 = tn ? 0 : (tc.mb * ncta + cta) * kBM + q * 32;  // the warp's first row
+  const int col0 = tn ? (tc.nb * ncta + cta) * kBM + q * 32 : tc.nb * kBN;
+  float4 pf[8];
+  if (!tn) {
+    if (u0.in_flag_base >= 0) {
+      const int f = u0.in_flag_base + slot;
       if (!warp_flag_wait(p.flags + f, p, kSiteAccInFlag, static_cast<uint32_t>(f), lane)) return false;
     }
-    // the unit's token rows are TMEM columns [s * tn_rows, +tn_rows) of the accumulator
-    const bool add = u.epi == kEpiAddF32 || u.epi == kEpiAddBF16;
-    float4 pf[8];
-    if (add) load_partial(u, 0, f0, lane, pf);
-    store_rows(u, tbase + s * p.tn_rows, 0, f0, lane, add, pf, stage, p.tn_rows);
-    if (u.out_flag_base >= 0) {
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) st_release_gpu(p.flags + u.out_flag_base + slot, p.epoch);
-    }
-    if (u.done_counter >= 0) {
-      __threadfence_system();
-      __syncwarp();
-      if (lane == 0) red_release_sys_add(p.flags + u.done_counter, 1u);
-    }
+    if (u0.epi == kEpiAddF32 || u0.epi == kEpiAddBF16) load_partial(u0, row0, col0, lane, pf);
   }
+  if (!warp_mbar_wait(tmem_full, acc_phase, p, kSiteTmemFull, static_cast<uint32_t>(tile), lane)) return false;
+  tc_fence_after();
+  const int nparts = tn ? p.tn_S : 1;
+  for (int s = 0; s < nparts; ++s) {
+    const GemmUnit& u = p.units[tc.unit + s];
+    const bool add = u.epi == kEpiAddF32 || u.epi == kEpiAddBF16;
+    if (tn) {
+      if (u.in_flag_base >= 0) {
+        const int f = u.in_flag_base + slot;
+        if (!warp_flag_wait(p.flags + f, p, kSiteAccInFlag, static_cast<uint32_t>(f), lane)) return false;
+      }
+      if (add) load_partial(u, 0, col0, lane, pf);
+    }
+    if (u.epi == kEpiSiluMul) {
+      const int row = row0 + lane;
+#pragma unroll 1
+      for (int c = 0; c < kBN / 64; ++c) {
+        uint32_t g[32], v[32];
+        tmem_ld32(tbase + c * 32, g);
+        tmem_ld32(tbase + kBN / 2 + c * 32, v);
+        tmem_wait_ld();
+        const int col = tc.nb * (kBN / 2) + c * 32;
+        if (row < u.m_rows && col < u.n_cols) store_silu_chunk(u, row, col, g, v);
+      }
+    } else {
+      // transposed: the unit's token rows are TMEM columns [s * tn_rows, +tn_rows)
+      store_rows(u, tbase + (tn ? s * p.tn_rows : 0), row0, col0, lane, add, pf, stage, tn ? p.tn_rows : 0);
+    }
+    if (tn) publish_unit(p, u, slot, tc.mb, lane);
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) arrive_empty();
+  if (!tn) publish_unit(p, u0, slot, tc.mb, lane);
   return true;
+}
+
+// ---------------------------------------------------------------------------
+// Debug build (FO_DEBUG_BOUNDS): index checks
+// ---------------------------------------------------------------------------
+// The tile's decoded coordinates, the operand maps of its units and every flag word the
+// tile reads or writes are checked against the launch's extents.  A failure records
+// FO_ERR_INTERNAL (site kSiteBounds, detail: the tile) and raises the abort word, and the
+// role leaves its loop as after a wait that ran out.  The release build compiles the
+// checks away.
+__device__ __forceinline__ bool tile_ok(const GemmParams& p, const TileCoord& tc, int tile, int ncta) {
+#ifdef FO_DEBUG_BOUNDS
+  auto flag_ok = [&](int64_t i) { return i >= 0 && i < p.flag_words; };
+  const int nunits = p.group_unit_begin[p.num_groups];
+  const int nsub = p.tn_S > 0 ? p.tn_S : 1;
+  bool ok = tc.unit >= 0 && tc.unit + nsub <= nunits && nunits <= kMaxUnits && tc.nb >= 0 && tc.mb >= 0;
+  if (ok) ok = p.tn_S > 0 ? tc.nb < p.tn_fblocks
+                          : tc.mb < p.units[tc.unit].tiles_m && tc.nb < p.units[tc.unit].tiles_n;
+  for (int s = 0; ok && s < nsub; ++s) {
+    const GemmUnit& u = p.units[tc.unit + s];
+    // the largest flag slot of the tile: per (tile or feature block, CTA half, quadrant)
+    const int64_t blk = p.tn_S > 0 ? tc.nb : static_cast<int64_t>(tc.mb) * u.tiles_n + tc.nb;
+    const int64_t slot_max = (blk * ncta + ncta - 1) * 4 + 3;
+    if (u.wait_flag >= 0) ok = ok && flag_ok(u.wait_flag);
+    if (u.in_flag_base >= 0) ok = ok && flag_ok(u.in_flag_base + slot_max);
+    if (u.out_flag_base >= 0) ok = ok && flag_ok(u.out_flag_base + slot_max);
+    if (u.done_counter >= 0) ok = ok && flag_ok(u.done_counter);
+    if (u.rows_done_base >= 0) ok = ok && flag_ok(static_cast<int64_t>(u.rows_done_base) + tc.mb);
+    if (u.a_ready_base >= 0) ok = ok && flag_ok(static_cast<int64_t>(u.a_ready_base) + tc.mb);
+    if (u.kchunk > 0 && u.chunk_flag_base >= 0) ok = ok && flag_ok(u.chunk_flag_base + u.chunk_nsrc - 1);
+    ok = ok && u.a_map >= 0 && u.a_map < p.num_maps && u.b_map >= 0 && u.b_map < p.num_maps;
+    if (u.kchunk > 0) ok = ok && u.a_map2 >= 0 && u.a_map2 < p.num_maps;
+  }
+  if (!ok) raise_error(p.ctrl, FO_ERR_INTERNAL, kSiteBounds, static_cast<uint32_t>(tile));
+  return ok;
+#else
+  (void)p;
+  (void)tc;
+  (void)tile;
+  (void)ncta;
+  return true;
+#endif
 }
 
 }  // namespace

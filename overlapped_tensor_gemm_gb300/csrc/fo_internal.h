@@ -112,6 +112,7 @@ struct GemmParams {
   uint32_t epoch;
   uint64_t timeout_ns;
   uint32_t* flags;             // ring flags (epoch-valued)
+  int32_t flag_words;          // words at `flags` (the debug build checks every flag index)
   uint32_t* ctrl;              // device control block (error word, abort flag)
 };
 static_assert(sizeof(GemmParams) <= 32764, "GemmParams must fit the kernel parameter space");
@@ -133,7 +134,7 @@ enum CtrlWord : int {
 enum WaitSite : uint32_t {
   kSiteAgFlag = 1, kSiteFull = 2, kSiteEmpty = 3, kSiteTmemFull = 4,
   kSiteTmemEmpty = 5, kSiteAccInFlag = 6, kSiteDrain = 7, kSiteAttnFlag = 8,
-  kSiteAttnBar = 9, kSiteVRange = 10, kSiteRowsReady = 11
+  kSiteAttnBar = 9, kSiteVRange = 10, kSiteRowsReady = 11, kSiteBounds = 12
 };
 
 // host launchers (fo_gemm.cu: single-SM 128x256 tiles; fo_gemm2.cu: SM-pair 256x256 tiles)

@@ -100,3 +100,20 @@ def test_library_all_to_all_order_follows_the_oracle_schedule(lib, P):
         assert cons[0][r] == (r, r)
         assert sorted(d for t in range(P) for rr, d in prod[t] if rr == r) == list(range(P))
         assert sorted(s for t in range(P) for rr, s in cons[t] if rr == r) == list(range(P))
+
+
+def test_debug_bounds_build_compiles_and_exports(repo_root, tmp_path):
+    """The debug build (index checks in the kernels, failures recorded as FO_ERR_INTERNAL)
+    compiles for sm_103a and exports the same entry points."""
+    from overlapped_tensor_gemm_gb300 import _build
+    out = _build.build(debug_bounds=True, out=str(tmp_path / "libfo_debug.so"))
+    dbg = ctypes.CDLL(out)
+    for name in _declared(repo_root):
+        assert hasattr(dbg, name), name
+
+
+def test_struct_layouts_match_the_header():
+    """fo_opts and fo_mat in the binding have the header's size (twelve 4-byte fields,
+    and a pointer, two 4-byte and three 8-byte fields)."""
+    assert ctypes.sizeof(fo.FoOpts) == 12 * 4
+    assert ctypes.sizeof(fo.FoMat) == 8 + 4 + 4 + 3 * 8
