@@ -60,6 +60,7 @@ static_assert(kSmemBytes <= 232448 - 16 * 1024, "the persistent GEMM must leave 
 // warp roles
 // ---------------------------------------------------------------------------
 
+template <bool TN>
 __device__ void producer_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl) {
   int stage = 0;
   uint32_t phase = 0;
@@ -68,9 +69,9 @@ __device__ void producer_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl)
   int waited_unit = -1;
   bool ok = true;
   const int mn = p.mn_major & 3;
-  const bool tn = p.tn_S > 0;
+  constexpr bool tn = TN;
   for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
-    const TileCoord tc = tile_coord(p, tile);
+    const TileCoord tc = tile_coord<TN>(p, tile);
     if (!tile_ok(p, tc, tile, 1)) {
       ok = false;
       break;
@@ -165,7 +166,7 @@ __device__ void producer_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl)
 
 // The operand orientation is a template argument: the instruction descriptor stays a
 // compile-time constant and the K loop carries no per-block dispatch.
-template <bool AMN, bool BMN>
+template <bool AMN, bool BMN, bool TN>
 __device__ void mma_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl, uint32_t tmem_base) {
   constexpr uint32_t idesc = kIdesc | (AMN ? kIdescAMn : 0u) | (BMN ? kIdescBMn : 0u);
   int stage = 0;
@@ -176,7 +177,7 @@ __device__ void mma_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl, uint
   bool ok = true;
   const uint32_t tiles_addr = smem_u32(tiles);
   for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
-    const TileCoord tc = tile_coord(p, tile);
+    const TileCoord tc = tile_coord<TN>(p, tile);
     if (!tile_ok(p, tc, tile, 1)) {
       ok = false;
       break;
@@ -223,16 +224,17 @@ __device__ void mma_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl, uint
   }
 }
 
+template <bool TN>
 __device__ void epilogue_loop(const GemmParams& p, SmemCtl* ctl, uint32_t tmem_base, int warp, int lane,
                               float* stage) {
   const int q = warp & 3;  // TMEM lanes [32q, 32q+32) are the only ones this warp may access
   int acc = 0;
   uint32_t acc_phase = 0;
   for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
-    const TileCoord tc = tile_coord(p, tile);
+    const TileCoord tc = tile_coord<TN>(p, tile);
     if (!tile_ok(p, tc, tile, 1)) return;
     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
-    if (!epilogue_tile(p, tc, tile, &ctl->tmem_full[acc], acc_phase, tbase, 0, 1, q, lane, stage,
+    if (!epilogue_tile<TN>(p, tc, tile, &ctl->tmem_full[acc], acc_phase, tbase, 0, 1, q, lane, stage,
                        [&] { mbar_arrive(&ctl->tmem_empty[acc]); }))
       return;
     acc ^= 1;
@@ -240,7 +242,8 @@ __device__ void epilogue_loop(const GemmParams& p, SmemCtl* ctl, uint32_t tmem_b
   }
 }
 
-__global__ void __maxnreg__(192) gemm_kernel(const __grid_constant__ GemmParams p) {
+template <bool TN>
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = smem_u32(smem_raw);
   uint8_t* tiles = smem_raw + ((1024u - (base & 1023u)) & 1023u);
@@ -275,19 +278,23 @@ __global__ void __maxnreg__(192) gemm_kernel(const __grid_constant__ GemmParams 
   const uint32_t tmem_base = ctl->tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) producer_loop(p, tiles, ctl);
+    if (lane == 0) producer_loop<TN>(p, tiles, ctl);
   } else if (warp == 1) {
     if (lane == 0) {
-      switch (p.mn_major & 3) {
-        case 0: mma_loop<false, false>(p, tiles, ctl, tmem_base); break;
-        case 2: mma_loop<false, true>(p, tiles, ctl, tmem_base); break;
-        case 3: mma_loop<true, true>(p, tiles, ctl, tmem_base); break;
-        default: mma_loop<true, false>(p, tiles, ctl, tmem_base); break;
+      if (TN) {  // transposed tiles: K-major operands only
+        mma_loop<false, false, true>(p, tiles, ctl, tmem_base);
+      } else {
+        switch (p.mn_major & 3) {
+          case 0: mma_loop<false, false, false>(p, tiles, ctl, tmem_base); break;
+          case 2: mma_loop<false, true, false>(p, tiles, ctl, tmem_base); break;
+          case 3: mma_loop<true, true, false>(p, tiles, ctl, tmem_base); break;
+          default: mma_loop<true, false, false>(p, tiles, ctl, tmem_base); break;
+        }
       }
     }
     __syncwarp();
   } else {
-    epilogue_loop(p, ctl, tmem_base, warp, lane, epi_stage + (warp - 2) * (kEpiStageBytes / 4));
+    epilogue_loop<TN>(p, ctl, tmem_base, warp, lane, epi_stage + (warp - 2) * (kEpiStageBytes / 4));
   }
 
   tc_fence_before();
@@ -305,12 +312,18 @@ int gemm_smem_bytes() { return kSmemBytes; }
 // Called once at context creation, before any persistent kernel runs: also loads the
 // helper kernels (see preload_helper_kernels).
 cudaError_t gemm_configure() {
-  const cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   return e != cudaSuccess ? e : preload_helper_kernels();
 }
 
 cudaError_t gemm_launch(const GemmParams& p, int grid, cudaStream_t s) {
-  gemm_kernel<<<grid, kGemmThreads, kSmemBytes, s>>>(p);
+  if (p.tn_S > 0) {
+    gemm_kernel<true><<<grid, kGemmThreads, kSmemBytes, s>>>(p);
+  } else {
+    gemm_kernel<false><<<grid, kGemmThreads, kSmemBytes, s>>>(p);
+  }
   return cudaGetLastError();
 }
 

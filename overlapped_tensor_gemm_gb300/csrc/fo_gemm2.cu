@@ -43,6 +43,7 @@ constexpr int kPairSmem = kPairStages * kPStage + 4 * kEpiStageBytes + 1024 + st
 // persistent grid: leave shared memory free on every SM.
 static_assert(kPairSmem <= 232448 - 16 * 1024, "the persistent GEMM must leave 16 KiB of shared memory free");
 
+template <bool TN>
 __device__ void pair_producer(const GemmParams& p, uint8_t* tiles, PairCtl* ctl, uint32_t cta) {
   const uint32_t leader_full = map_to_cta(smem_u32(&ctl->full[0]), 0);
   const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
@@ -51,9 +52,9 @@ __device__ void pair_producer(const GemmParams& p, uint8_t* tiles, PairCtl* ctl,
   int waited_unit = -1;
   bool ok = true;
   const int mn = p.mn_major & 3;
-  const bool tn = p.tn_S > 0;
+  constexpr bool tn = TN;
   for (int tile = cluster; ok && tile < p.total_tiles; tile += nclusters) {
-    const TileCoord tc = tile_coord(p, tile);
+    const TileCoord tc = tile_coord<TN>(p, tile);
     if (!tile_ok(p, tc, tile, 2)) {
       ok = false;
       break;
@@ -155,7 +156,7 @@ __device__ void pair_producer(const GemmParams& p, uint8_t* tiles, PairCtl* ctl,
 
 // The operand orientation is a template argument: the instruction descriptor stays a
 // compile-time constant and the K loop carries no per-block dispatch.
-template <bool AMN, bool BMN>
+template <bool AMN, bool BMN, bool TN>
 __device__ void pair_mma(const GemmParams& p, uint8_t* tiles, PairCtl* ctl, uint32_t tmem_base) {
   constexpr uint32_t idesc = kPIdesc | (AMN ? kIdescAMn : 0u) | (BMN ? kIdescBMn : 0u);
   const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
@@ -164,7 +165,7 @@ __device__ void pair_mma(const GemmParams& p, uint8_t* tiles, PairCtl* ctl, uint
   bool issued = false, ok = true;
   const uint32_t tiles_addr = smem_u32(tiles);
   for (int tile = cluster; ok && tile < p.total_tiles; tile += nclusters) {
-    const TileCoord tc = tile_coord(p, tile);
+    const TileCoord tc = tile_coord<TN>(p, tile);
     if (!tile_ok(p, tc, tile, 2)) {
       ok = false;
       break;
@@ -209,6 +210,7 @@ __device__ void pair_mma(const GemmParams& p, uint8_t* tiles, PairCtl* ctl, uint
   }
 }
 
+template <bool TN>
 __device__ void pair_epilogue(const GemmParams& p, PairCtl* ctl, uint32_t tmem_base, uint32_t cta, int warp,
                               int lane, float* stage) {
   const int q = warp & 3;
@@ -217,7 +219,7 @@ __device__ void pair_epilogue(const GemmParams& p, PairCtl* ctl, uint32_t tmem_b
   int acc = 0;
   uint32_t acc_phase = 0;
   for (int tile = cluster; tile < p.total_tiles; tile += nclusters) {
-    const TileCoord tc = tile_coord(p, tile);
+    const TileCoord tc = tile_coord<TN>(p, tile);
     if (!tile_ok(p, tc, tile, 2)) return;
     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
     auto arrive_empty = [&] {
@@ -227,7 +229,7 @@ __device__ void pair_epilogue(const GemmParams& p, PairCtl* ctl, uint32_t tmem_b
         mbar_arrive_cluster(leader_tmem_empty + acc * static_cast<uint32_t>(sizeof(uint64_t)));
       }
     };
-    if (!epilogue_tile(p, tc, tile, &ctl->tmem_full[acc], acc_phase, tbase, static_cast<int>(cta), 2, q, lane, stage,
+    if (!epilogue_tile<TN>(p, tc, tile, &ctl->tmem_full[acc], acc_phase, tbase, static_cast<int>(cta), 2, q, lane, stage,
                        arrive_empty))
       return;
     acc ^= 1;
@@ -235,7 +237,8 @@ __device__ void pair_epilogue(const GemmParams& p, PairCtl* ctl, uint32_t tmem_b
   }
 }
 
-__global__ void __maxnreg__(192) gemm_pair_kernel(const __grid_constant__ GemmParams p) {
+template <bool TN>
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_pair_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = smem_u32(smem_raw);
   uint8_t* tiles = smem_raw + ((1024u - (base & 1023u)) & 1023u);
@@ -271,19 +274,23 @@ __global__ void __maxnreg__(192) gemm_pair_kernel(const __grid_constant__ GemmPa
   const uint32_t tmem_base = ctl->tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) pair_producer(p, tiles, ctl, cta);
+    if (lane == 0) pair_producer<TN>(p, tiles, ctl, cta);
   } else if (warp == 1) {
     if (lane == 0 && cta == 0) {
-      switch (p.mn_major & 3) {
-        case 0: pair_mma<false, false>(p, tiles, ctl, tmem_base); break;
-        case 2: pair_mma<false, true>(p, tiles, ctl, tmem_base); break;
-        case 3: pair_mma<true, true>(p, tiles, ctl, tmem_base); break;
-        default: pair_mma<true, false>(p, tiles, ctl, tmem_base); break;
+      if (TN) {  // transposed tiles: K-major operands only
+        pair_mma<false, false, true>(p, tiles, ctl, tmem_base);
+      } else {
+        switch (p.mn_major & 3) {
+          case 0: pair_mma<false, false, false>(p, tiles, ctl, tmem_base); break;
+          case 2: pair_mma<false, true, false>(p, tiles, ctl, tmem_base); break;
+          case 3: pair_mma<true, true, false>(p, tiles, ctl, tmem_base); break;
+          default: pair_mma<true, false, false>(p, tiles, ctl, tmem_base); break;
+        }
       }
     }
     __syncwarp();
   } else {
-    pair_epilogue(p, ctl, tmem_base, cta, warp, lane, epi_stage + (warp - 2) * (kEpiStageBytes / 4));
+    pair_epilogue<TN>(p, ctl, tmem_base, cta, warp, lane, epi_stage + (warp - 2) * (kEpiStageBytes / 4));
   }
 
   tc_fence_before();
@@ -297,7 +304,11 @@ __global__ void __maxnreg__(192) gemm_pair_kernel(const __grid_constant__ GemmPa
 }  // namespace
 
 cudaError_t gemm_pair_configure() {
-  return cudaFuncSetAttribute(gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
+  const cudaError_t e =
+      cudaFuncSetAttribute(gemm_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
+  return e != cudaSuccess
+             ? e
+             : cudaFuncSetAttribute(gemm_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
 }
 
 // Number of SM pairs that can be resident at once (the persistent grid must not exceed it).
@@ -314,7 +325,7 @@ int gemm_pair_max_clusters() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<false>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -334,7 +345,8 @@ cudaError_t gemm_pair_launch(const GemmParams& p, int clusters, cudaStream_t s) 
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel, p);
+  return p.tn_S > 0 ? cudaLaunchKernelEx(&cfg, gemm_pair_kernel<true>, p)
+                    : cudaLaunchKernelEx(&cfg, gemm_pair_kernel<false>, p);
 }
 
 }  // namespace fo

@@ -303,8 +303,11 @@ __device__ __forceinline__ TileCoord decode_tile_tn(const GemmParams& p, int til
   return c;
 }
 
+// TN: the launch runs transposed reduce-scatter tiles (the kernels are instantiated per
+// tile kind, so the step-ordered instantiation carries none of the transposed code).
+template <bool TN>
 __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int tile) {
-  return p.tn_S > 0 ? decode_tile_tn(p, tile) : decode_tile(p, tile);
+  return TN ? decode_tile_tn(p, tile) : decode_tile(p, tile);
 }
 
 // Flag release and completion counters after a unit's rows of a tile are stored.
@@ -336,11 +339,11 @@ __device__ __forceinline__ void publish_unit(const GemmParams& p, const GemmUnit
 // each after its incoming partial sum's flag, each released before the next.  This is the
 // only call site of store_rows, so a kernel inlines one copy of it.  `arrive_empty()`
 // frees the accumulator.  False if a wait gave up.
-template <class ArriveEmpty>
+template <bool TN, class ArriveEmpty>
 __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const TileCoord& tc, int tile, uint64_t* tmem_full,
                                               uint32_t acc_phase, uint32_t tbase, int cta, int ncta, int q, int lane,
                                               float* stage, ArriveEmpty arrive_empty) {
-  const bool tn = p.tn_S > 0;
+  constexpr bool tn = TN;
   const GemmUnit& u0 = p.units[tc.unit];
   const int blk = tn ? tc.nb : tc.mb * u0.tiles_n + tc.nb;
   const int slot = (blk * ncta + cta) * 4 + q;           // flags per (tile, CTA half, quadrant)
