@@ -373,6 +373,7 @@ struct Launch {
     p.flags = flags;
     p.flag_words = static_cast<int32_t>(kFlagBytes / 4);
     p.ctrl = ctrl;
+    p.rows_all_index = -1;
     return FO_OK;
   }
 };
@@ -883,6 +884,7 @@ fo_status build_rs_flash(fo_ctx* ctx, Launch& L, const RsArgs& a, const fo_opts&
     q.flags = flags;
     q.flag_words = static_cast<int32_t>(kFlagBytes / 4);
     q.ctrl = ctx->ctrl;
+    q.rows_all_index = -1;
     L.tn_pair = tn_pair;
     L.arrivals_per_tile = 4 * ncta;
     for (int i = 0; i < L.num_units; ++i) {  // per unit: one feature block of tiles
@@ -1400,7 +1402,7 @@ fo_status mlp_fused_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* Wc, const fo
   if (rs_tn_steps(ctx, b, o, &tn_pair) != 0) return FO_OK;  // its own tile shape: two launches
   const bool pairs = o.sm_pairs == 0 && ctx->pair_clusters > 0 && m % (2 * kBM) == 0;
   const int64_t block_rows = pairs ? 2 * kBM : kBM, mblocks = (m + block_rows - 1) / block_rows;
-  if (kRowsBase + static_cast<int64_t>(P) * P * mblocks > static_cast<int64_t>(kFlagBytes / 4)) return FO_OK;
+  if (kRowsBase + static_cast<int64_t>(P) * P * mblocks + 1 > static_cast<int64_t>(kFlagBytes / 4)) return FO_OK;
 
   void *flags_v = nullptr, *recv_v = nullptr, *rs_recv_v = nullptr;
   FO_TRY(ensure_buf(ctx, kBufFlags, kFlagBytes, &flags_v));
@@ -1432,8 +1434,15 @@ fo_status mlp_fused_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* Wc, const fo
   FO_TRY(L.finish(epoch, timeout_ns(o), flags, ctx->ctrl, 0));
   if (pairs != (o.sm_pairs == 0 && ctx->pair_clusters > 0 && L.pair_friendly()))
     return fail(FO_ERR_UNSUPPORTED, "layer launch: inconsistent tile shape");
+  // the word after the per-block counters counts every AG epilogue warp of the launch
+  int64_t ag_arrivals = 0;
+  for (int i = 0; i < L.num_units; ++i)
+    if (L.p.units[i].rows_done_base >= 0)
+      ag_arrivals += static_cast<int64_t>((m + block_rows - 1) / block_rows) * ag_tiles_n * (pairs ? 8 : 4);
+  L.p.rows_all_index = static_cast<int32_t>(kRowsBase + static_cast<int64_t>(P) * P * mblocks);
+  L.p.rows_all_count = static_cast<int32_t>(ag_arrivals);
   *used = true;
-  FO_CUDA(cudaMemsetAsync(flags + kRowsBase, 0, static_cast<size_t>(P) * P * mblocks * 4, stream));
+  FO_CUDA(cudaMemsetAsync(flags + kRowsBase, 0, (static_cast<size_t>(P) * P * mblocks + 1) * 4, stream));
   // ring copies first in host order (see ag_run), then the one launch
   FO_TRY(fork_links(ctx, P, stream));
   if (a.Xh) FO_TRY(enqueue_uploads(ctx, a, epoch, flags));

@@ -51,6 +51,7 @@ __device__ void pair_producer(const GemmParams& p, uint8_t* tiles, PairCtl* ctl,
   uint32_t phase = 0, armed = 0, armed_phase = 0;
   int waited_unit = -1;
   bool ok = true;
+  bool rows_all_done = false;
   const int mn = p.mn_major & 3;
   constexpr bool tn = TN;
   for (int tile = cluster; ok && tile < p.total_tiles; tile += nclusters) {
@@ -67,12 +68,9 @@ __device__ void pair_producer(const GemmParams& p, uint8_t* tiles, PairCtl* ctl,
       fence_proxy_async_global();
       waited_unit = tc.unit;
     }
-    if (u.a_ready_base >= 0) {  // A rows written by an earlier tile of this launch
-      const int f = u.a_ready_base + tc.mb;
-      ok = count_wait(p.flags + f, static_cast<uint32_t>(u.a_ready_count), p.ctrl, p.timeout_ns, kSiteRowsReady,
-                      static_cast<uint32_t>(f));
-      if (!ok) break;
-      fence_proxy_async_global();
+    if (!wait_rows_ready(p, u, tc.mb, &rows_all_done)) {  // A rows written by an earlier tile
+      ok = false;
+      break;
     }
     const int nk = (u.k + kBK - 1) / kBK;
     const int a_row = u.a_row0 + tc.mb * 2 * kBM + static_cast<int>(cta) * kBM;

@@ -328,8 +328,28 @@ __device__ __forceinline__ void publish_unit(const GemmParams& p, const GemmUnit
     // this warp's rows of the tile are stored: count them for the tiles that read them
     __threadfence();
     __syncwarp();
-    if (lane == 0) red_release_gpu_add(p.flags + u.rows_done_base + mb, 1u);
+    if (lane == 0) {
+      red_release_gpu_add(p.flags + u.rows_done_base + mb, 1u);
+      if (p.rows_all_index >= 0) red_release_gpu_add(p.flags + p.rows_all_index, 1u);
+    }
   }
+}
+
+// Producer side of the row counters: before loading A rows of m-block mb that earlier tiles
+// of this launch write, wait for their count -- unless every producing tile of the launch
+// is known to be done (*all_done), after which nothing is checked or fenced again.
+__device__ __forceinline__ bool wait_rows_ready(const GemmParams& p, const GemmUnit& u, int mb, bool* all_done) {
+  if (u.a_ready_base < 0 || *all_done) return true;
+  if (p.rows_all_index >= 0 && ld_acquire_gpu(p.flags + p.rows_all_index) >= static_cast<uint32_t>(p.rows_all_count)) {
+    *all_done = true;
+  } else {
+    const int f = u.a_ready_base + mb;
+    if (!count_wait(p.flags + f, static_cast<uint32_t>(u.a_ready_count), p.ctrl, p.timeout_ns, kSiteRowsReady,
+                    static_cast<uint32_t>(f)))
+      return false;
+  }
+  fence_proxy_async_global();  // the rows were written through the generic proxy; TMA reads them
+  return true;
 }
 
 // One tile's epilogue for one epilogue warp (TMEM lane quadrant q of CTA `cta` of `ncta`).
@@ -410,6 +430,7 @@ __device__ __forceinline__ bool tile_ok(const GemmParams& p, const TileCoord& tc
   bool ok = tc.unit >= 0 && tc.unit + nsub <= nunits && nunits <= kMaxUnits && tc.nb >= 0 && tc.mb >= 0;
   if (ok) ok = p.tn_S > 0 ? tc.nb < p.tn_fblocks
                           : tc.mb < p.units[tc.unit].tiles_m && tc.nb < p.units[tc.unit].tiles_n;
+  if (p.rows_all_index >= 0) ok = ok && flag_ok(p.rows_all_index);
   for (int s = 0; ok && s < nsub; ++s) {
     const GemmUnit& u = p.units[tc.unit + s];
     // the largest flag slot of the tile: per (tile or feature block, CTA half, quadrant)

@@ -108,6 +108,12 @@ struct GemmParams {
   int32_t tn_passes;    // tiles per rank and feature block
   int32_t tn_fblocks;   // feature blocks of 128 (single SM) or 256 (SM pair) features
   int32_t tn_fb_group;  // feature blocks per ordering group (divides tn_fblocks)
+  // One launch for a whole layer: every epilogue warp that counts rows into a
+  // rows_done_base counter also adds 1 to flags[rows_all_index]; once that word reaches
+  // rows_all_count every producing tile has stored its rows, and a producer stops checking
+  // per-block counters (-1: no such word).
+  int32_t rows_all_index;
+  int32_t rows_all_count;
   int32_t total_tiles;
   uint32_t epoch;
   uint64_t timeout_ns;

@@ -187,6 +187,7 @@ extern "C" FO_API fo_status fo_gemm_rs_noalloc(const fo_mat* X, const fo_mat* W_
   p.timeout_ns = (timeout_us ? static_cast<uint64_t>(timeout_us) : 1000000ull) * 1000ull;
   p.flags = flags;
   p.flag_words = static_cast<int32_t>(kFlagBytes / 4);
+  p.rows_all_index = -1;
   p.ctrl = ctrl;
   // Tiles wait on tiles of smaller index owned by other CTAs, so every CTA of this grid must
   // be resident at once: the call needs the whole GPU while it runs.
