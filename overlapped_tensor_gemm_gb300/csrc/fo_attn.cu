@@ -820,11 +820,9 @@ fo_status attn_run(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K, const fo_mat* 
                                                        host_ctrl(ctx));
     if (cudaGetLastError() != cudaSuccess) return host_fail(FO_ERR_CUDA, "transpose launch failed");
   }
-  // 2) the K/V ring on the link streams, then 3) the attention kernel, concurrently
-  //    (serial baseline: the whole ring first, then the kernel without flag waits);
-  //    independent problems: the kernel alone.  The ring is enqueued first: an executor
-  //    that serialises the work (a profiler) then runs the copies before the kernel that
-  //    waits on them.
+  // 2) the attention kernel and 3) the K/V ring on the link streams, concurrently (host
+  //    order: host_copies_first) (serial baseline: the whole ring first, then the kernel
+  //    without flag waits); independent problems: the kernel alone.
   if (!ring) {
     p.wait_flags = 0;
     attn_kernel<<<host_grid(ctx, o, p.total_items), kAttnThreads, kAttnSmem, stream>>>(p);
@@ -845,6 +843,12 @@ fo_status attn_run(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K, const fo_mat* 
   }
   if (serial) host_phase_record(ctx, 0, stream);
   if ((st = host_fork(ctx, P, stream)) != FO_OK) return st;
+  const bool kernel_first = !serial && !host_copies_first();
+  if (kernel_first) {
+    attn_kernel<<<grid, kAttnThreads, kAttnSmem, stream>>>(p);
+    const cudaError_t le = cudaGetLastError();
+    if (le != cudaSuccess) return host_fail(FO_ERR_CUDA, cudaGetErrorString(le));
+  }
   const bool prune = o.causal_prune && causal;
   for (int t = 1; t < P; ++t) {
     for (int r = 0; r < P; ++r) {
@@ -864,7 +868,7 @@ fo_status attn_run(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K, const fo_mat* 
       if (cudaEventRecord(host_ev_hop(ctx, r, t), ls) != cudaSuccess) return host_fail(FO_ERR_CUDA, "event failed");
     }
   }
-  if (!serial) {
+  if (!serial && !kernel_first) {
     attn_kernel<<<grid, kAttnThreads, kAttnSmem, stream>>>(p);
     const cudaError_t le = cudaGetLastError();
     if (le != cudaSuccess) return host_fail(FO_ERR_CUDA, cudaGetErrorString(le));

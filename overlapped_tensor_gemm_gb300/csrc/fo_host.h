@@ -20,6 +20,7 @@ fo_status host_encode_map(CUtensorMap* map, const void* ptr, int64_t rows, int64
                           CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 fo_status host_check_mat(const fo_mat& a, int32_t dtype, const char* what, int r);
 fo_status host_fail(fo_status st, const char* msg);
+bool host_copies_first();  // host order of a ring's copies and the kernel that waits on them
 uint64_t host_timeout_ns(const fo_opts& o);
 int host_grid(fo_ctx* ctx, const fo_opts& o, int work);
 void host_phase_record(fo_ctx* ctx, int i, cudaStream_t s);     // serial baselines' phase events
