@@ -492,15 +492,21 @@ fo_status write_flag(cudaStream_t s, uint32_t* flag, uint32_t value) {
 // every SM before the copies start; measured on GB300, enqueuing the 16K MLP layer's
 // all-gather copies first made its launch 4% slower (no change at 4K tokens).  A tool that
 // serialises the work it intercepts (a kernel profiler) would then run the kernel alone,
-// waiting for copies queued behind it until its waits give up, so under such a tool --
-// recognised by the injection library it loads (CUDA_INJECTION64_PATH), or when
-// FO_COPIES_FIRST=1 -- the copies are enqueued first.
+// waiting for copies queued behind it until its waits give up, so under such a tool the
+// copies are enqueued first.  Such a tool is recognised by the environment it gives the
+// process it runs: Nsight Compute's injection settings (NV_NSIGHT_INJECTION_TRANSPORT_TYPE,
+// NV_COMPUTE_PROFILER_PERFWORKS_DIR) or an injection library (CUDA_INJECTION64_PATH).
+// FO_COPIES_FIRST=1 / 0 forces the order.
 bool copies_first() {
   static const bool v = [] {
-    const char* inj = std::getenv("CUDA_INJECTION64_PATH");
     const char* force = std::getenv("FO_COPIES_FIRST");
     if (force && force[0]) return force[0] == '1';
-    return inj != nullptr && inj[0] != '\0';
+    for (const char* name : {"NV_NSIGHT_INJECTION_TRANSPORT_TYPE", "NV_COMPUTE_PROFILER_PERFWORKS_DIR",
+                             "CUDA_INJECTION64_PATH"}) {
+      const char* v = std::getenv(name);
+      if (v && v[0]) return true;
+    }
+    return false;
   }();
   return v;
 }
