@@ -802,7 +802,7 @@ float* rs_slot(const RsArgs& a, float* base, int r, int h) {
   return base + (static_cast<int64_t>(r) * a.P + h) * a.m * a.N;
 }
 
-constexpr int kTnFbGroup = 16;  // feature blocks per ordering group of the transposed tiles
+constexpr int kTnFbGroup = 32;  // feature blocks per ordering group of the transposed tiles (measured: 2..32)
 
 // Transposed reduce-scatter tiles (GemmParams::tn_S) for a slice of m rows: 0 if they do
 // not apply, else the number of ring steps per tile, with *pair set when the tiles run on
