@@ -383,6 +383,7 @@ GemmUnit blank_unit() {
   GemmUnit u;
   std::memset(&u, 0, sizeof(u));
   u.wait_flag = -1;
+  u.wait_flag2 = -1;
   u.in_flag_base = -1;
   u.out_flag_base = -1;
   u.done_counter = -1;
@@ -542,8 +543,14 @@ struct AgArgs {
                      // the upload's flag)
 };
 
+// Rank r's receive buffer holds the slices in ring-step order: slice s at position
+// (r - s) mod P, the position of the step that computes it (position 0, the rank's own
+// slice, is filled only for step-pair units), so two consecutive steps are 2m contiguous
+// rows.
+int ag_position(const AgArgs& a, int r, int s) { return ((r - s) % a.P + a.P) % a.P; }
+char* ag_rank_buffer(const AgArgs& a, int r) { return a.recv + static_cast<int64_t>(r) * a.P * a.m * a.K * 2; }
 char* ag_slot(const AgArgs& a, int r, int s, int64_t row_in_slice) {
-  return a.recv + ((static_cast<int64_t>(r) * a.P + s) * a.m + row_in_slice) * a.K * 2;
+  return a.recv + ((static_cast<int64_t>(r) * a.P + ag_position(a, r, s)) * a.m + row_in_slice) * a.K * 2;
 }
 
 // The ring all-gather of rows [row0, row0 + rows) of every slice, on the link
@@ -553,13 +560,18 @@ char* ag_slot(const AgArgs& a, int r, int s, int64_t row_in_slice) {
 // link streams, each publishing the (rank r, slice r) flag, which no ring hop uses, so the
 // GEMM of rank 0's own slice starts after one slice has crossed the host link instead of
 // all of them; each rank's first ring hop follows its upload on the same stream.
-fo_status enqueue_uploads(fo_ctx* ctx, const AgArgs& a, uint32_t epoch, uint32_t* flag_base) {
+// With step pairs, each rank's own slice is also copied to position 0 of its receive buffer
+// (after the upload, if any), and the (r, r) flag is published after that copy.
+fo_status enqueue_uploads(fo_ctx* ctx, const AgArgs& a, uint32_t epoch, uint32_t* flag_base, bool step_pairs) {
   for (int r = 0; r < a.P; ++r) {
     cudaStream_t ls = ctx->link[r];
-    if (r > 0) FO_CUDA(cudaStreamWaitEvent(ls, ctx->ev_hop[r - 1][0], 0));
-    FO_CUDA(cudaMemcpy2DAsync(a.X[r].ptr, a.X[r].ld * 2, a.Xh[r].ptr, a.Xh[r].ld * 2, a.K * 2, a.m,
-                              cudaMemcpyHostToDevice, ls));
-    FO_CUDA(cudaEventRecord(ctx->ev_hop[r][0], ls));
+    if (a.Xh) {
+      if (r > 0) FO_CUDA(cudaStreamWaitEvent(ls, ctx->ev_hop[r - 1][0], 0));
+      FO_CUDA(cudaMemcpy2DAsync(a.X[r].ptr, a.X[r].ld * 2, a.Xh[r].ptr, a.Xh[r].ld * 2, a.K * 2, a.m,
+                                cudaMemcpyHostToDevice, ls));
+      FO_CUDA(cudaEventRecord(ctx->ev_hop[r][0], ls));
+    }
+    if (step_pairs) FO_TRY(copy_rows(ag_slot(a, r, r, 0), a.K, a.X[r].ptr, a.X[r].ld, a.m, a.K, 2, ls));
     FO_TRY(write_flag(ls, flag_base + kAgFlagBase + r * a.P + r, epoch));
   }
   return FO_OK;
@@ -600,6 +612,55 @@ constexpr double kWeightMajorMaxBytes = 80.0 * (1 << 20);  // measured: 56 MiB b
 
 // rows_base >= 0 (one launch for a whole layer): rank r's unit for slice s counts its stored
 // rows per m-block into counter rows_base + (r * P + s) * mblocks + mb.
+// step_pairs (whole-slice flash launches with 128-row slices, P even): one unit per two
+// consecutive steps (t, t+1) of a rank, 256 rows of its step-ordered receive buffer, so the
+// launch runs 256-row tiles on SM pairs: the first 128 rows (slice of step t) wait on that
+// slice's flag and are stored at its output rows, the next 128 likewise for step t+1.
+fo_status add_ag_step_pairs(Launch& L, const AgArgs& a, const int* rmap, const int* wmap, int64_t gated_f,
+                            bool weight_major) {
+  const int P = a.P, npairs = P / 2;
+  auto add = [&](int r, int j) {
+    int r0, s0, r1, s1;
+    ag_unit(P, 2 * j, r, &r0, &s0);
+    ag_unit(P, 2 * j + 1, r, &r1, &s1);
+    GemmUnit& u = L.add_unit();
+    u = blank_unit();
+    u.a_map = rmap[r];
+    u.a_row0 = static_cast<int32_t>(2 * j * a.m);  // positions 2j and 2j+1
+    u.wait_flag = static_cast<int32_t>(kAgFlagBase + r * P + s0);
+    u.wait_flag2 = static_cast<int32_t>(kAgFlagBase + r * P + s1);
+    u.b_map = wmap[r];
+    u.m_rows = static_cast<int32_t>(2 * a.m);
+    u.k = static_cast<int32_t>(a.K);
+    if (gated_f > 0) {
+      u.gated = 1;
+      u.b_row1 = static_cast<int32_t>(gated_f);
+      u.n_cols = static_cast<int32_t>(gated_f);
+      u.epi = kEpiSiluMul;
+    } else {
+      u.n_cols = static_cast<int32_t>(a.N);
+      u.epi = kEpiBF16;
+    }
+    u.c = bptr(a.Y[r], s0 * a.m);
+    u.c2 = bptr(a.Y[r], s1 * a.m);
+    u.ldc = a.Y[r].ld;
+  };
+  if (weight_major) {  // steps (0, 1) of every rank, then rank by rank its other pairs, weight-major
+    L.begin_group();
+    for (int r = 0; r < P; ++r) add(r, 0);
+    for (int r = 0; r < P && npairs > 1; ++r) {
+      L.begin_group(true);
+      for (int j = 1; j < npairs; ++j) add(r, j);
+    }
+  } else {
+    for (int j = 0; j < npairs; ++j) {
+      L.begin_group();
+      for (int r = 0; r < P; ++r) add(r, j);
+    }
+  }
+  return FO_OK;
+}
+
 fo_status add_ag_units(Launch& L, const AgArgs& a, const int* xmap, const int* rmap, const int* wmap, int64_t row0,
                        int64_t rows, bool flash, int64_t gated_f, bool weight_major = false, int64_t rows_base = -1,
                        int64_t mblocks = 0) {
@@ -626,7 +687,7 @@ fo_status add_ag_units(Launch& L, const AgArgs& a, const int* xmap, const int* r
         if (flash && a.Xh) u.wait_flag = static_cast<int32_t>(kAgFlagBase + r * P + r);  // uploaded slice
       } else {
         u.a_map = rmap[r];
-        u.a_row0 = static_cast<int32_t>(s * a.m + row0);
+        u.a_row0 = static_cast<int32_t>(ag_position(a, r, s) * a.m + row0);
         if (flash) u.wait_flag = static_cast<int32_t>(kAgFlagBase + r * P + s);
       }
       u.b_map = wmap[r];
@@ -689,18 +750,25 @@ fo_status ag_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_
   const uint64_t tmo = timeout_ns(o);
 
   fo_status st = FO_OK;
+  // 128-row slices in a whole-slice fused launch: two steps per 256-row tile on SM pairs
+  const bool step_pairs = (o.order == FO_ORDER_FLASH || o.order == FO_ORDER_NAIVE) && !o.compute_only &&
+                          m == kBM && P % 2 == 0 && o.sm_pairs == 0 && ctx->pair_clusters > 0;
   auto build = [&](Launch& L, int64_t row0, int64_t rows, bool flash, int* xmap, int* rmap, int* wmap,
                    bool weight_major) -> fo_status {
     for (int r = 0; r < P; ++r) {
       xmap[r] = L.add_map(&st, X[r].ptr, m, K, X[r].ld, kBM);
       if (st != FO_OK) return st;
-      rmap[r] = L.add_map(&st, ag_slot(a, r, 0, 0), M, K, K, kBM);
+      rmap[r] = L.add_map(&st, ag_rank_buffer(a, r), M, K, K, kBM);
       if (st != FO_OK) return st;
       wmap[r] = w_kn ? L.add_map_mn(&st, W[r].ptr, K, N, W[r].ld)
                      : L.add_map(&st, W[r].ptr, N, K, W[r].ld, gated ? kBN / 2 : kBN);
       if (st != FO_OK) return st;
     }
-    FO_TRY(add_ag_units(L, a, xmap, rmap, wmap, row0, rows, flash, gated_f, weight_major));
+    if (flash && step_pairs && row0 == 0 && rows == m) {
+      FO_TRY(add_ag_step_pairs(L, a, rmap, wmap, gated_f, weight_major));
+    } else {
+      FO_TRY(add_ag_units(L, a, xmap, rmap, wmap, row0, rows, flash, gated_f, weight_major));
+    }
     L.p.mn_major = w_kn ? 2 : 0;
     return L.finish(epoch, tmo, flags, ctx->ctrl, 0);
   };
@@ -723,7 +791,7 @@ fo_status ag_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_
     // order: copies_first)
     FO_TRY(fork_links(ctx, P, stream));
     if (!copies_first()) FO_TRY(launch_gemm(ctx, L, o, stream));
-    if (a.Xh) FO_TRY(enqueue_uploads(ctx, a, epoch, flags));
+    if (a.Xh || step_pairs) FO_TRY(enqueue_uploads(ctx, a, epoch, flags, step_pairs));
     FO_TRY(enqueue_ag_ring(ctx, a, 0, m, true, epoch, o.fault, flags));
     if (copies_first()) FO_TRY(launch_gemm(ctx, L, o, stream));
     return join_links(ctx, P, stream);
@@ -1444,7 +1512,7 @@ fo_status mlp_fused_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* Wc, const fo
   for (int r = 0; r < P; ++r) {
     xmap[r] = L.add_map(&st, X[r].ptr, m, K, X[r].ld, kBM);
     FO_TRY(st);
-    rmap[r] = L.add_map(&st, ag_slot(a, r, 0, 0), M, K, K, kBM);
+    rmap[r] = L.add_map(&st, ag_rank_buffer(a, r), M, K, K, kBM);
     FO_TRY(st);
     wmap[r] = L.add_map(&st, Wc[r].ptr, Nc, K, Wc[r].ld, gated ? kBN / 2 : kBN);
     FO_TRY(st);
@@ -1472,7 +1540,7 @@ fo_status mlp_fused_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* Wc, const fo
   // the ring's copies run concurrently with the launch (host order: copies_first)
   FO_TRY(fork_links(ctx, P, stream));
   if (!copies_first()) FO_TRY(launch_gemm(ctx, L, o, stream));
-  if (a.Xh) FO_TRY(enqueue_uploads(ctx, a, epoch, flags));
+  if (a.Xh) FO_TRY(enqueue_uploads(ctx, a, epoch, flags, false));
   FO_TRY(enqueue_ag_ring(ctx, a, 0, m, true, epoch, o.fault, flags));
   if (copies_first()) FO_TRY(launch_gemm(ctx, L, o, stream));
   FO_TRY(join_links(ctx, P, stream));

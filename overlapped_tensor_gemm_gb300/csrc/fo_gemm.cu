@@ -66,7 +66,7 @@ __device__ void producer_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl)
   uint32_t phase = 0;
   uint32_t armed = 0;        // bit s: stage s has been armed at least once
   uint32_t armed_phase = 0;  // bit s: phase parity of the last arming of stage s
-  int waited_unit = -1;
+  int waited_flag = -1;  // the last flag this thread has waited for
   bool ok = true;
   bool rows_all_done = false;
   const int mn = p.mn_major & 3;
@@ -78,13 +78,14 @@ __device__ void producer_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl)
       break;
     }
     const GemmUnit& u = p.units[tc.unit];
-    if (u.wait_flag >= 0 && tc.unit != waited_unit) {
-      ok = flag_wait(p.flags + u.wait_flag, p.epoch, p.ctrl, p.timeout_ns, kSiteAgFlag,
-                     static_cast<uint32_t>(u.wait_flag));
+    // a step-pair unit's second 128-row block is the second step's slice
+    const int wf = (tc.mb > 0 && u.wait_flag2 >= 0) ? u.wait_flag2 : u.wait_flag;
+    if (wf >= 0 && wf != waited_flag) {
+      ok = flag_wait(p.flags + wf, p.epoch, p.ctrl, p.timeout_ns, kSiteAgFlag, static_cast<uint32_t>(wf));
       if (!ok) break;
       // the slice was written by a ring copy; order the TMA reads after the acquire
       fence_proxy_async_global();
-      waited_unit = tc.unit;
+      waited_flag = wf;
     }
     if (!wait_rows_ready(p, u, tc.mb, &rows_all_done)) {  // A rows written by an earlier tile
       ok = false;

@@ -49,7 +49,7 @@ __device__ void pair_producer(const GemmParams& p, uint8_t* tiles, PairCtl* ctl,
   const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
   int stage = 0;
   uint32_t phase = 0, armed = 0, armed_phase = 0;
-  int waited_unit = -1;
+  int waited_flag = -1;  // the last flag this thread has waited for
   bool ok = true;
   bool rows_all_done = false;
   const int mn = p.mn_major & 3;
@@ -61,12 +61,13 @@ __device__ void pair_producer(const GemmParams& p, uint8_t* tiles, PairCtl* ctl,
       break;
     }
     const GemmUnit& u = p.units[tc.unit];
-    if (u.wait_flag >= 0 && tc.unit != waited_unit) {
-      ok = flag_wait(p.flags + u.wait_flag, p.epoch, p.ctrl, p.timeout_ns, kSiteAgFlag,
-                     static_cast<uint32_t>(u.wait_flag));
+    // a step-pair unit's second 128 rows (this CTA's, when cta == 1) are the second step's slice
+    const int wf = (cta == 1 && u.wait_flag2 >= 0) ? u.wait_flag2 : u.wait_flag;
+    if (wf >= 0 && wf != waited_flag) {
+      ok = flag_wait(p.flags + wf, p.epoch, p.ctrl, p.timeout_ns, kSiteAgFlag, static_cast<uint32_t>(wf));
       if (!ok) break;
       fence_proxy_async_global();
-      waited_unit = tc.unit;
+      waited_flag = wf;
     }
     if (!wait_rows_ready(p, u, tc.mb, &rows_all_done)) {  // A rows written by an earlier tile
       ok = false;

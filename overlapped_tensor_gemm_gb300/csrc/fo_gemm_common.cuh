@@ -117,8 +117,8 @@ __device__ __forceinline__ void load_partial(const GemmUnit& u, int row0, int co
 }
 
 // Stores one staged chunk (+ the partial sums when `add`) in the coalesced layout.
-__device__ __forceinline__ void store_staged(const GemmUnit& u, int row0, int col, int lane, const float* stage,
-                                             bool add, const float4 (&pf)[8]) {
+__device__ __forceinline__ void store_staged(const GemmUnit& u, void* out, int row0, int col, int lane,
+                                             const float* stage, bool add, const float4 (&pf)[8]) {
   const int c = col + 4 * (lane & 7);
   const bool bf16_out = u.epi == kEpiBF16 || u.epi == kEpiAddBF16;
 #pragma unroll
@@ -135,7 +135,7 @@ __device__ __forceinline__ void store_staged(const GemmUnit& u, int row0, int co
     if (r >= u.m_rows || c >= u.n_cols) continue;
     const int ncol = u.n_cols - c;
     if (bf16_out) {
-      uint16_t* dst = static_cast<uint16_t*>(u.c) + static_cast<int64_t>(r) * u.ldc + c;
+      uint16_t* dst = static_cast<uint16_t*>(out) + static_cast<int64_t>(r) * u.ldc + c;
       if (ncol >= 4) {
         *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w));
       } else {
@@ -144,7 +144,7 @@ __device__ __forceinline__ void store_staged(const GemmUnit& u, int row0, int co
         if (ncol > 2) dst[2] = __bfloat16_as_ushort(__float2bfloat16_rn(x.z));
       }
     } else {
-      float* dst = static_cast<float*>(u.c) + static_cast<int64_t>(r) * u.ldc + c;
+      float* dst = static_cast<float*>(out) + static_cast<int64_t>(r) * u.ldc + c;
       if (ncol >= 4) {
         st_v4_u32(dst, __float_as_uint(x.x), __float_as_uint(x.y), __float_as_uint(x.z), __float_as_uint(x.w));
       } else {
@@ -158,8 +158,9 @@ __device__ __forceinline__ void store_staged(const GemmUnit& u, int row0, int co
 
 // A plain bf16 chunk of one row (lane = row), stored straight from registers: without
 // partial sums to load this was measured faster than the staged path.
-__device__ __forceinline__ void store_bf16_row_chunk(const GemmUnit& u, int row, int col, const uint32_t (&v)[32]) {
-  uint16_t* dst = static_cast<uint16_t*>(u.c) + static_cast<int64_t>(row) * u.ldc + col;
+__device__ __forceinline__ void store_bf16_row_chunk(const GemmUnit& u, void* out, int row, int col,
+                                                     const uint32_t (&v)[32]) {
+  uint16_t* dst = static_cast<uint16_t*>(out) + static_cast<int64_t>(row) * u.ldc + col;
   if (col + 32 <= u.n_cols) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -186,8 +187,8 @@ __device__ __forceinline__ void store_bf16_row_chunk(const GemmUnit& u, int row,
 // 0 .. tn_rows-1; each 32x32 chunk is staged transposed (row-major: every write
 // instruction fills one 128-byte row of the stage) and stored by the same row-contiguous
 // path.
-__device__ __forceinline__ void store_rows(const GemmUnit& u, uint32_t tbase, int row0, int col0, int lane, bool add,
-                                           float4 (&pf)[8], float* stage, int tn_rows = 0) {
+__device__ __forceinline__ void store_rows(const GemmUnit& u, void* out, uint32_t tbase, int row0, int col0, int lane,
+                                           bool add, float4 (&pf)[8], float* stage, int tn_rows = 0) {
   const bool tn = tn_rows > 0;
   if (!tn && u.epi == kEpiBF16) {
     const int row = row0 + lane;
@@ -198,7 +199,7 @@ __device__ __forceinline__ void store_rows(const GemmUnit& u, uint32_t tbase, in
       uint32_t v[32];
       tmem_ld32(tbase + c * 32, v);
       tmem_wait_ld();
-      if (row < u.m_rows) store_bf16_row_chunk(u, row, col, v);
+      if (row < u.m_rows) store_bf16_row_chunk(u, out, row, col, v);
     }
     return;
   }
@@ -224,7 +225,7 @@ __device__ __forceinline__ void store_rows(const GemmUnit& u, uint32_t tbase, in
                         __uint_as_float(v[4 * g + 3]));
     }
     __syncwarp();
-    store_staged(u, r0, col, lane, stage, add, pf);
+    store_staged(u, out, r0, col, lane, stage, add, pf);
     __syncwarp();  // the stage is rewritten by the next chunk
     if (add) {
 #pragma unroll
@@ -240,8 +241,8 @@ __device__ __forceinline__ float round_bf16(float x) {
 // MLP glue fused into the gate/up epilogue: the gate and up accumulators are
 // rounded to bf16 first (as the unfused layer stores them), then
 // SiLU(g) * u = g / (1 + exp(-g)) * u in fp32, rounded once to bf16.
-__device__ __forceinline__ void store_silu_chunk(const GemmUnit& u, int row, int col, const uint32_t (&g)[32],
-                                                 const uint32_t (&v)[32]) {
+__device__ __forceinline__ void store_silu_chunk(const GemmUnit& u, void* out, int row, int col,
+                                                 const uint32_t (&g)[32], const uint32_t (&v)[32]) {
   float h[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
@@ -249,7 +250,7 @@ __device__ __forceinline__ void store_silu_chunk(const GemmUnit& u, int row, int
     const float ui = round_bf16(__uint_as_float(v[i]));
     h[i] = gi / (1.0f + expf(-gi)) * ui;
   }
-  uint16_t* dst = static_cast<uint16_t*>(u.c) + static_cast<int64_t>(row) * u.ldc + col;
+  uint16_t* dst = static_cast<uint16_t*>(out) + static_cast<int64_t>(row) * u.ldc + col;
   if (col + 32 <= u.n_cols) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -367,8 +368,13 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const TileCoo
   const GemmUnit& u0 = p.units[tc.unit];
   const int blk = tn ? tc.nb : tc.mb * u0.tiles_n + tc.nb;
   const int slot = (blk * ncta + cta) * 4 + q;           // flags per (tile, CTA half, quadrant)
-  const int row0 = tn ? 0 : (tc.mb * ncta + cta) * kBM + q * 32;  // the warp's first row
+  int row0 = tn ? 0 : (tc.mb * ncta + cta) * kBM + q * 32;  // the warp's first row
   const int col0 = tn ? (tc.nb * ncta + cta) * kBM + q * 32 : tc.nb * kBN;
+  void* out = u0.c;
+  if (!tn && u0.c2 != nullptr && row0 >= kBM) {  // a step-pair unit: rows [kBM, 2 kBM) are the second step's
+    out = u0.c2;
+    row0 -= kBM;
+  }
   float4 pf[8];
   if (!tn) {
     if (u0.in_flag_base >= 0) {
@@ -399,11 +405,12 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const TileCoo
         tmem_ld32(tbase + kBN / 2 + c * 32, v);
         tmem_wait_ld();
         const int col = tc.nb * (kBN / 2) + c * 32;
-        if (row < u.m_rows && col < u.n_cols) store_silu_chunk(u, row, col, g, v);
+        if (row < u.m_rows && col < u.n_cols) store_silu_chunk(u, out, row, col, g, v);
       }
     } else {
       // transposed: the unit's token rows are TMEM columns [s * tn_rows, +tn_rows)
-      store_rows(u, tbase + (tn ? s * p.tn_rows : 0), row0, col0, lane, add, pf, stage, tn ? p.tn_rows : 0);
+      store_rows(u, tn ? u.c : out, tbase + (tn ? s * p.tn_rows : 0), row0, col0, lane, add, pf, stage,
+                 tn ? p.tn_rows : 0);
     }
     if (tn) publish_unit(p, u, slot, tc.mb, lane);
   }
@@ -437,6 +444,7 @@ __device__ __forceinline__ bool tile_ok(const GemmParams& p, const TileCoord& tc
     const int64_t blk = p.tn_S > 0 ? tc.nb : static_cast<int64_t>(tc.mb) * u.tiles_n + tc.nb;
     const int64_t slot_max = (blk * ncta + ncta - 1) * 4 + 3;
     if (u.wait_flag >= 0) ok = ok && flag_ok(u.wait_flag);
+    if (u.wait_flag2 >= 0) ok = ok && flag_ok(u.wait_flag2) && u.m_rows == 2 * kBM;
     if (u.in_flag_base >= 0) ok = ok && flag_ok(u.in_flag_base + slot_max);
     if (u.out_flag_base >= 0) ok = ok && flag_ok(u.out_flag_base + slot_max);
     if (u.done_counter >= 0) ok = ok && flag_ok(u.done_counter);

@@ -51,6 +51,11 @@ struct GemmUnit {
   int32_t m_rows, n_cols, k;   // valid extent of this unit
   int32_t tiles_m, tiles_n;
   int32_t wait_flag;           // AG: flag index that must reach `epoch` before A is read (-1: none)
+  // A step-pair unit (AG with 128-row slices): its 256 rows are two ring steps' slices,
+  // stored next to each other in step order; rows [128, 256) wait on wait_flag2 (not
+  // wait_flag) and are stored at c2 (not c) from its row 0.  wait_flag2 = -1, c2 = null:
+  // an ordinary unit.
+  int32_t wait_flag2;
   int32_t in_flag_base;        // RS: per-tile flags guarding acc_in (-1: none)
   int32_t out_flag_base;       // RS: per-tile flags released after C is written (-1: none)
   int32_t epi;                 // EpiMode
@@ -74,6 +79,7 @@ struct GemmUnit {
   int32_t a_ready_base;        // -1: none
   int32_t a_ready_count;
   void* c;                     // output
+  void* c2;                    // step-pair unit: output of rows [128, 256)
   const float* acc_in;         // fp32 partial sum to add (kEpiAdd*)
   int64_t ldc, ld_acc;         // leading dimensions in elements
 };

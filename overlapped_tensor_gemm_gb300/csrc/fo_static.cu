@@ -154,6 +154,7 @@ extern "C" FO_API fo_status fo_gemm_rs_noalloc(const fo_mat* X, const fo_mat* W_
       u.tiles_m = static_cast<int32_t>(tm);
       u.tiles_n = static_cast<int32_t>(tn);
       u.wait_flag = -1;
+      u.wait_flag2 = -1;
       u.in_flag_base = -1;
       u.out_flag_base = -1;
       u.done_counter = -1;
