@@ -369,7 +369,9 @@ def run_ours(args, rank: int, world: int, device: int):
     t_ag, t_rs = tm[("ag", "flash", False)], tm[("rs", "flash", False)]
     t_one, t_two = tm[("layer", "one", False)], tm[("layer", "two", False)]
     ag_tflops = flops["ag"] / (t_ag * 1e-3) / 1e12
-    pair = cfg.m % 256 == 0  # 256-row tiles on SM pairs when every slice is a multiple of 256 rows
+    # 256-row tiles on SM pairs when every slice is a multiple of 256 rows, or (all-gather) when
+    # 128-row slices pair up two ring steps per tile (P even)
+    pair = cfg.m % 256 == 0 or (cfg.m == 128 and cfg.P % 2 == 0 and not one_launch)
     kernel = "gemm_pair_kernel" if pair else "gemm_kernel"
     if one_launch:  # the step is one launch: the whole layer's FLOP over its duration
         dom = {"kernel": f"{kernel} (whole MLP layer in one launch: Flash-AG with the {epi} epilogue, "

@@ -751,8 +751,8 @@ fo_status ag_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_
 
   fo_status st = FO_OK;
   // 128-row slices in a whole-slice fused launch: two steps per 256-row tile on SM pairs
-  const bool step_pairs = (o.order == FO_ORDER_FLASH || o.order == FO_ORDER_NAIVE) && !o.compute_only &&
-                          m == kBM && P % 2 == 0 && o.sm_pairs == 0 && ctx->pair_clusters > 0;
+  const bool step_pairs = (o.order == FO_ORDER_FLASH || o.order == FO_ORDER_NAIVE) && m == kBM && P % 2 == 0 &&
+                          o.sm_pairs == 0 && ctx->pair_clusters > 0;
   auto build = [&](Launch& L, int64_t row0, int64_t rows, bool flash, int* xmap, int* rmap, int* wmap,
                    bool weight_major) -> fo_status {
     for (int r = 0; r < P; ++r) {
