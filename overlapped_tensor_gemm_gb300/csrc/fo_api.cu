@@ -870,6 +870,7 @@ float* rs_slot(const RsArgs& a, float* base, int r, int h) {
   return base + (static_cast<int64_t>(r) * a.P + h) * a.m * a.N;
 }
 
+constexpr double kStreamPartialsBytes = 96.0 * (1 << 20);  // L2 is 126 MB
 constexpr int kTnFbGroup = 32;  // feature blocks per ordering group of the transposed tiles (measured: 2..32)
 
 // Transposed reduce-scatter tiles (GemmParams::tn_S) for a slice of m rows: 0 if they do
@@ -908,6 +909,8 @@ fo_status build_rs_flash(fo_ctx* ctx, Launch& L, const RsArgs& a, const fo_opts&
     wmap[r] = S ? L.add_map(&st, a.W[r].ptr, a.N, a.Kr, a.W[r].ld, kBM) : add_rs_weight(L, &st, a, r);
     if (st != FO_OK) return st;
   }
+  // one ring step's partial sums beyond kStreamPartialsBytes: stream them past L2
+  L.p.stream_partials = static_cast<double>(P) * a.m * a.N * 4 > kStreamPartialsBytes ? 1 : 0;
   const int64_t tm = (a.m + kBM - 1) / kBM, tn = (a.N + kBN - 1) / kBN;
   // flags per (rank, hop): one per (tile, quadrant), or per (256-feature block, CTA half,
   // quadrant) for transposed tiles

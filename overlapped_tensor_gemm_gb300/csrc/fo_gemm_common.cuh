@@ -96,7 +96,8 @@ __device__ __forceinline__ int stage_index(int row, int g) { return row * 32 + (
 
 // Partial sums of one chunk in the coalesced layout: pf[i] = row 4i + lane/8 of the warp's
 // rows (first row `row0`), columns col + 4*(lane%8) .. +3; zero outside the unit.
-__device__ __forceinline__ void load_partial(const GemmUnit& u, int row0, int col, int lane, float4 (&pf)[8]) {
+__device__ __forceinline__ void load_partial(const GemmUnit& u, int row0, int col, int lane, float4 (&pf)[8],
+                                             bool stream = false) {
   const int c = col + 4 * (lane & 7);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -105,7 +106,7 @@ __device__ __forceinline__ void load_partial(const GemmUnit& u, int row0, int co
     if (r < u.m_rows && c < u.n_cols) {
       const float* src = u.acc_in + static_cast<int64_t>(r) * u.ld_acc + c;
       if (c + 4 <= u.n_cols) {
-        x = ld_cg_f4(src);
+        x = stream ? ld_cs_f4(src) : ld_cg_f4(src);
       } else {
         x.x = __ldcg(src);
         if (c + 1 < u.n_cols) x.y = __ldcg(src + 1);
@@ -118,7 +119,8 @@ __device__ __forceinline__ void load_partial(const GemmUnit& u, int row0, int co
 
 // Stores one staged chunk (+ the partial sums when `add`) in the coalesced layout.
 __device__ __forceinline__ void store_staged(const GemmUnit& u, void* out, int row0, int col, int lane,
-                                             const float* stage, bool add, const float4 (&pf)[8]) {
+                                             const float* stage, bool add, const float4 (&pf)[8],
+                                             bool stream = false) {
   const int c = col + 4 * (lane & 7);
   const bool bf16_out = u.epi == kEpiBF16 || u.epi == kEpiAddBF16;
 #pragma unroll
@@ -146,7 +148,11 @@ __device__ __forceinline__ void store_staged(const GemmUnit& u, void* out, int r
     } else {
       float* dst = static_cast<float*>(out) + static_cast<int64_t>(r) * u.ldc + c;
       if (ncol >= 4) {
-        st_v4_u32(dst, __float_as_uint(x.x), __float_as_uint(x.y), __float_as_uint(x.z), __float_as_uint(x.w));
+        if (stream) {
+          st_cs_v4_u32(dst, __float_as_uint(x.x), __float_as_uint(x.y), __float_as_uint(x.z), __float_as_uint(x.w));
+        } else {
+          st_v4_u32(dst, __float_as_uint(x.x), __float_as_uint(x.y), __float_as_uint(x.z), __float_as_uint(x.w));
+        }
       } else {
         dst[0] = x.x;
         if (ncol > 1) dst[1] = x.y;
@@ -188,7 +194,8 @@ __device__ __forceinline__ void store_bf16_row_chunk(const GemmUnit& u, void* ou
 // instruction fills one 128-byte row of the stage) and stored by the same row-contiguous
 // path.
 __device__ __forceinline__ void store_rows(const GemmUnit& u, void* out, uint32_t tbase, int row0, int col0, int lane,
-                                           bool add, float4 (&pf)[8], float* stage, int tn_rows = 0) {
+                                           bool add, float4 (&pf)[8], float* stage, int tn_rows = 0,
+                                           bool stream = false) {
   const bool tn = tn_rows > 0;
   if (!tn && u.epi == kEpiBF16) {
     const int row = row0 + lane;
@@ -212,7 +219,7 @@ __device__ __forceinline__ void store_rows(const GemmUnit& u, void* out, uint32_
     uint32_t v[32];
     float4 next[8];
     tmem_ld32(tbase + c * 32, v);
-    if (add && c + 1 < nchunks) load_partial(u, tn ? r0 + 32 : row0, tn ? col0 : col + 32, lane, next);
+    if (add && c + 1 < nchunks) load_partial(u, tn ? r0 + 32 : row0, tn ? col0 : col + 32, lane, next, stream);
     tmem_wait_ld();
     if (tn) {
 #pragma unroll
@@ -225,7 +232,7 @@ __device__ __forceinline__ void store_rows(const GemmUnit& u, void* out, uint32_
                         __uint_as_float(v[4 * g + 3]));
     }
     __syncwarp();
-    store_staged(u, out, r0, col, lane, stage, add, pf);
+    store_staged(u, out, r0, col, lane, stage, add, pf, stream);
     __syncwarp();  // the stage is rewritten by the next chunk
     if (add) {
 #pragma unroll
@@ -381,7 +388,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const TileCoo
       const int f = u0.in_flag_base + slot;
       if (!warp_flag_wait(p.flags + f, p, kSiteAccInFlag, static_cast<uint32_t>(f), lane)) return false;
     }
-    if (u0.epi == kEpiAddF32 || u0.epi == kEpiAddBF16) load_partial(u0, row0, col0, lane, pf);
+    if (u0.epi == kEpiAddF32 || u0.epi == kEpiAddBF16) load_partial(u0, row0, col0, lane, pf, p.stream_partials != 0);
   }
   if (!warp_mbar_wait(tmem_full, acc_phase, p, kSiteTmemFull, static_cast<uint32_t>(tile), lane)) return false;
   tc_fence_after();
@@ -394,7 +401,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const TileCoo
         const int f = u.in_flag_base + slot;
         if (!warp_flag_wait(p.flags + f, p, kSiteAccInFlag, static_cast<uint32_t>(f), lane)) return false;
       }
-      if (add) load_partial(u, 0, col0, lane, pf);
+      if (add) load_partial(u, 0, col0, lane, pf, p.stream_partials != 0);
     }
     if (u.epi == kEpiSiluMul) {
       const int row = row0 + lane;
@@ -410,7 +417,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const TileCoo
     } else {
       // transposed: the unit's token rows are TMEM columns [s * tn_rows, +tn_rows)
       store_rows(u, tn ? u.c : out, tbase + (tn ? s * p.tn_rows : 0), row0, col0, lane, add, pf, stage,
-                 tn ? p.tn_rows : 0);
+                 tn ? p.tn_rows : 0, p.stream_partials != 0);
     }
     if (tn) publish_unit(p, u, slot, tc.mb, lane);
   }

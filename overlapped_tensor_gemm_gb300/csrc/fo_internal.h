@@ -120,6 +120,10 @@ struct GemmParams {
   // per-block counters (-1: no such word).
   int32_t rows_all_index;
   int32_t rows_all_count;
+  // 1: the fp32 partial sums are loaded and stored as streaming (evict-first) data: one ring
+  // step's partial sums are larger than L2, so they come back from DRAM anyway, and should
+  // not evict the operands the GEMM reuses.
+  int32_t stream_partials;
   int32_t total_tiles;
   uint32_t epoch;
   uint64_t timeout_ns;

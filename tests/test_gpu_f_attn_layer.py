@@ -36,7 +36,8 @@ def _run(ctx, P, tokens, hidden, heads, seed, causal=True, **kw):
         assert_close(f64(to_bits(Z[d])), ref[d], f"attention block rank {d}", rel_l2=REL_L2_THREE_STAGES)
 
 
-# P=2, 128-row slices: single-SM GEMM tiles, 2 attention query blocks per head;
+# P=2, 128-row slices: two ring steps per SM-pair tile in the QKV all-gather, transposed tiles
+# in the output projection's reduce-scatter, 2 attention query blocks per head;
 # P=4, 256-row slices: SM-pair GEMM tiles, 8 query blocks per head, 2 heads per rank.
 @pytest.mark.parametrize("P,tokens,hidden,heads", [(2, 256, 256, 1), (4, 1024, 1024, 2)])
 def test_attention_block_matches_oracle(ctx, P, tokens, hidden, heads):

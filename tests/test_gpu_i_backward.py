@@ -61,7 +61,8 @@ def _row(ctx, P, m, Fr, N, seed, integer, **kw):
     _cmp(dW, rdw, integer, "dW")
 
 
-# 128-row slices: single-SM tiles; 256-row slices: SM pairs; ragged K / N / F
+# 128-row slices (P even): two ring steps per SM-pair tile in the all-gather, transposed tiles
+# in the reduce-scatter; 256-row slices: SM pairs; P = 3 and ragged K / N / F: single-SM tiles
 @pytest.mark.parametrize("P,m,K,Nr", [(2, 128, 256, 256), (4, 256, 384, 512), (3, 128, 200, 136)])
 @pytest.mark.parametrize("order", ["flash", "naive", "serial"])
 def test_column_parallel_backward_integer_exact(ctx, P, m, K, Nr, order):
