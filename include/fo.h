@@ -112,7 +112,10 @@ typedef struct {
   int32_t fault;        /* fo_fault                                                   */
   int32_t epilogue;     /* fo_epilogue (fo_ag_gemm only)                              */
   int32_t sm_pairs;     /* GEMM tiles: 0 = automatic (256x256 tiles on SM pairs when every
-                           unit's rows are a multiple of 256), 1 = single-SM 128x256 tiles */
+                           unit's rows are a multiple of 256; the transposed reduce-scatter
+                           tiles of 32-128-row slices on single SMs, measured faster there),
+                           1 = single-SM 128x256 tiles everywhere, 2 = SM pairs wherever a
+                           tile kind has that form (transposed tiles included) */
   int32_t compute_only; /* timing diagnostic (fo_ag_gemm, fo_gemm_rs, fo_qsplit_attn): every
                            kernel of the chosen order runs, every ring flag is published
                            before the launch and no ring copy is enqueued, so the call takes

@@ -134,9 +134,11 @@ def _mats(ts: Sequence) -> ctypes.Array:
 
 def opts(order: str = "flash", link: str = "default", n_slices: int = 0, timeout_us: int = 0,
          causal_prune: bool = False, num_sms: int = 0, fault: str = "none", epilogue: str = "plain",
-         single_sm: bool = False, compute_only: bool = False, split_layer: bool = False) -> FoOpts:
+         single_sm: bool = False, compute_only: bool = False, split_layer: bool = False,
+         pairs: bool = False) -> FoOpts:
+    tiles = 2 if pairs else int(single_sm)  # fo_opts.sm_pairs
     return FoOpts(ORDERS[order], LINKS[link], n_slices, timeout_us, int(causal_prune), num_sms, FAULTS[fault],
-                  EPILOGUES[epilogue], int(single_sm), int(compute_only), int(split_layer), 0)
+                  EPILOGUES[epilogue], tiles, int(compute_only), int(split_layer), 0)
 
 
 def _stream(stream) -> ctypes.c_void_p:

@@ -219,7 +219,7 @@ fo_status check_common(fo_ctx* ctx, int P, const fo_opts* opts) {
     if (opts->num_sms < 0) return fail(FO_ERR_INVALID_ARG, "num_sms < 0");
     if (opts->epilogue < FO_EPI_PLAIN || opts->epilogue > FO_EPI_SILU_GATE)
       return fail(FO_ERR_INVALID_ARG, "unknown epilogue %d", opts->epilogue);
-    if (opts->sm_pairs < 0 || opts->sm_pairs > 1) return fail(FO_ERR_INVALID_ARG, "sm_pairs must be 0 or 1");
+    if (opts->sm_pairs < 0 || opts->sm_pairs > 2) return fail(FO_ERR_INVALID_ARG, "sm_pairs must be 0, 1 or 2");
     if (opts->compute_only < 0 || opts->compute_only > 1)
       return fail(FO_ERR_INVALID_ARG, "compute_only must be 0 or 1");
     if (opts->split_layer < 0 || opts->split_layer > 1) return fail(FO_ERR_INVALID_ARG, "split_layer must be 0 or 1");
@@ -411,7 +411,7 @@ fo_status launch_gemm(fo_ctx* ctx, Launch& L, const fo_opts& o, cudaStream_t str
     }
     return FO_OK;
   }
-  if (o.sm_pairs == 0 && ctx->pair_clusters > 0 && L.pair_friendly()) {
+  if (o.sm_pairs != 1 && ctx->pair_clusters > 0 && L.pair_friendly()) {
     // 256x256 tiles on SM pairs; the persistent grid never exceeds the resident clusters
     FO_TRY(L.retile(2 * kBM));
     FO_TRY(L.pair_boxes());
@@ -752,7 +752,7 @@ fo_status ag_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_
   fo_status st = FO_OK;
   // 128-row slices in a whole-slice fused launch: two steps per 256-row tile on SM pairs
   const bool step_pairs = (o.order == FO_ORDER_FLASH || o.order == FO_ORDER_NAIVE) && m == kBM && P % 2 == 0 &&
-                          o.sm_pairs == 0 && ctx->pair_clusters > 0;
+                          o.sm_pairs != 1 && ctx->pair_clusters > 0;
   auto build = [&](Launch& L, int64_t row0, int64_t rows, bool flash, int* xmap, int* rmap, int* wmap,
                    bool weight_major) -> fo_status {
     for (int r = 0; r < P; ++r) {
@@ -875,7 +875,9 @@ constexpr int kTnFbGroup = 32;  // feature blocks per ordering group of the tran
 
 // Transposed reduce-scatter tiles (GemmParams::tn_S) for a slice of m rows: 0 if they do
 // not apply, else the number of ring steps per tile, with *pair set when the tiles run on
-// SM pairs.  A tile waits on the tile of the previous rank in its pass group, which may
+// SM pairs (only on request, fo_opts.sm_pairs == 2: the single-SM form was measured faster,
+// tail GEMM-RS 0.263-0.269 vs 0.274-0.281 ms, 1K sweep point 0.446-0.449 vs 0.455-0.457
+// ms).  A tile waits on the tile of the previous rank in its pass group, which may
 // come later in the tile order (the ring closes from the last rank to the first), so every
 // rank's tile of a pass group must run at once: the grid must hold at least P tiles.
 int rs_tn_steps(const fo_ctx* ctx, const RsArgs& a, const fo_opts& o, bool* pair) {
@@ -883,7 +885,7 @@ int rs_tn_steps(const fo_ctx* ctx, const RsArgs& a, const fo_opts& o, bool* pair
   if (a.w_kn || a.m <= 0 || a.m > kBM || a.m % 32 != 0 || 256 % a.m != 0) return 0;
   const int S = static_cast<int>(256 / a.m);
   if (S > P || P % S != 0) return 0;
-  *pair = o.sm_pairs == 0 && ctx->pair_clusters > 0 && pair_grid(ctx, o) >= P;
+  *pair = o.sm_pairs == 2 && ctx->pair_clusters > 0 && pair_grid(ctx, o) >= P;
   if (*pair) return S;
   return grid_size(ctx, o, 1 << 30) >= P ? S : 0;
 }
@@ -1497,7 +1499,7 @@ fo_status mlp_fused_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* Wc, const fo
   RsArgs b{H, Wr, Z, P, M, m, F, K, nullptr, nullptr, false};
   bool tn_pair = false;
   if (rs_tn_steps(ctx, b, o, &tn_pair) != 0) return FO_OK;  // its own tile shape: two launches
-  const bool pairs = o.sm_pairs == 0 && ctx->pair_clusters > 0 && m % (2 * kBM) == 0;
+  const bool pairs = o.sm_pairs != 1 && ctx->pair_clusters > 0 && m % (2 * kBM) == 0;
   const int64_t block_rows = pairs ? 2 * kBM : kBM, mblocks = (m + block_rows - 1) / block_rows;
   if (kRowsBase + static_cast<int64_t>(P) * P * mblocks + 1 > static_cast<int64_t>(kFlagBytes / 4)) return FO_OK;
 
@@ -1529,7 +1531,7 @@ fo_status mlp_fused_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* Wc, const fo
   int64_t flag_end = 0;
   FO_TRY(build_rs_flash(ctx, L, b, o, flags, epoch, done != nullptr, 0, false, &flag_end, kRowsBase, mblocks, ready));
   FO_TRY(L.finish(epoch, timeout_ns(o), flags, ctx->ctrl, 0));
-  if (pairs != (o.sm_pairs == 0 && ctx->pair_clusters > 0 && L.pair_friendly()))
+  if (pairs != (o.sm_pairs != 1 && ctx->pair_clusters > 0 && L.pair_friendly()))
     return fail(FO_ERR_UNSUPPORTED, "layer launch: inconsistent tile shape");
   // the word after the per-block counters counts every AG epilogue warp of the launch
   int64_t ag_arrivals = 0;

@@ -153,15 +153,15 @@ def test_gated_fused_epilogue_matches_unfused(ctx):
 
 
 # Slices of 32-128 rows run on transposed tiles (the weight's features on the MMA's M side,
-# the token rows of 256/m consecutive ring steps of one rank on its N side), on SM pairs by
-# default and on single SMs with single_sm; a grid smaller than P falls back to the
+# the token rows of 256/m consecutive ring steps of one rank on its N side), on single SMs by
+# default and on SM pairs on request (pairs=True); a grid smaller than P falls back to the
 # step-ordered tiles.  Ragged feature counts leave the last feature block partly empty.
 @pytest.mark.parametrize("P,m,Kr,N", [(8, 64, 256, 1024), (4, 64, 136, 516), (2, 128, 192, 260),
                                       (8, 32, 128, 512), (8, 128, 64, 768)])
 @pytest.mark.parametrize("order", ["flash", "naive"])
-@pytest.mark.parametrize("single_sm", [False, True])
-def test_rs_transposed_tiles_integer_bit_exact(ctx, P, m, Kr, N, order, single_sm):
-    Y, ref = _rs(ctx, P, m, Kr, N, True, 400 + P + m, order=order, single_sm=single_sm)
+@pytest.mark.parametrize("pairs", [False, True])
+def test_rs_transposed_tiles_integer_bit_exact(ctx, P, m, Kr, N, order, pairs):
+    Y, ref = _rs(ctx, P, m, Kr, N, True, 400 + P + m, order=order, pairs=pairs)
     for r in range(P):
         assert_bits_equal(to_bits(Y[r]), ref[r], f"RS transposed {order} P={P} m={m} rank {r}")
 
