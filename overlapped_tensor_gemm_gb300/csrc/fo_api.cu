@@ -379,19 +379,6 @@ struct Launch {
   }
 };
 
-GemmUnit blank_unit() {
-  GemmUnit u;
-  std::memset(&u, 0, sizeof(u));
-  u.wait_flag = -1;
-  u.wait_flag2 = -1;
-  u.in_flag_base = -1;
-  u.out_flag_base = -1;
-  u.done_counter = -1;
-  u.rows_done_base = -1;
-  u.a_ready_base = -1;
-  return u;
-}
-
 // Resident SM pairs for a launch (the persistent grid never exceeds them).
 int pair_grid(const fo_ctx* ctx, const fo_opts& o) {
   int clusters = ctx->pair_clusters;
@@ -545,8 +532,8 @@ struct AgArgs {
 
 // Rank r's receive buffer holds the slices in ring-step order: slice s at position
 // (r - s) mod P, the position of the step that computes it (position 0, the rank's own
-// slice, is filled only for step-pair units), so two consecutive steps are 2m contiguous
-// rows.
+// slice, stays empty: step-pair units read that slice in place), so two consecutive
+// received steps are 2m contiguous rows.
 int ag_position(const AgArgs& a, int r, int s) { return ((r - s) % a.P + a.P) % a.P; }
 char* ag_rank_buffer(const AgArgs& a, int r) { return a.recv + static_cast<int64_t>(r) * a.P * a.m * a.K * 2; }
 char* ag_slot(const AgArgs& a, int r, int s, int64_t row_in_slice) {
@@ -560,9 +547,8 @@ char* ag_slot(const AgArgs& a, int r, int s, int64_t row_in_slice) {
 // link streams, each publishing the (rank r, slice r) flag, which no ring hop uses, so the
 // GEMM of rank 0's own slice starts after one slice has crossed the host link instead of
 // all of them; each rank's first ring hop follows its upload on the same stream.
-// With step pairs, each rank's own slice is also copied to position 0 of its receive buffer
-// (after the upload, if any), and the (r, r) flag is published after that copy.
-fo_status enqueue_uploads(fo_ctx* ctx, const AgArgs& a, uint32_t epoch, uint32_t* flag_base, bool step_pairs) {
+// Step pairs wait on the (r, r) flag too (a stream write, or the upload's completion).
+fo_status enqueue_uploads(fo_ctx* ctx, const AgArgs& a, uint32_t epoch, uint32_t* flag_base) {
   for (int r = 0; r < a.P; ++r) {
     cudaStream_t ls = ctx->link[r];
     if (a.Xh) {
@@ -571,7 +557,6 @@ fo_status enqueue_uploads(fo_ctx* ctx, const AgArgs& a, uint32_t epoch, uint32_t
                                 cudaMemcpyHostToDevice, ls));
       FO_CUDA(cudaEventRecord(ctx->ev_hop[r][0], ls));
     }
-    if (step_pairs) FO_TRY(copy_rows(ag_slot(a, r, r, 0), a.K, a.X[r].ptr, a.X[r].ld, a.m, a.K, 2, ls));
     FO_TRY(write_flag(ls, flag_base + kAgFlagBase + r * a.P + r, epoch));
   }
   return FO_OK;
@@ -616,8 +601,8 @@ constexpr double kWeightMajorMaxBytes = 80.0 * (1 << 20);  // measured: 56 MiB b
 // consecutive steps (t, t+1) of a rank, 256 rows of its step-ordered receive buffer, so the
 // launch runs 256-row tiles on SM pairs: the first 128 rows (slice of step t) wait on that
 // slice's flag and are stored at its output rows, the next 128 likewise for step t+1.
-fo_status add_ag_step_pairs(Launch& L, const AgArgs& a, const int* rmap, const int* wmap, int64_t gated_f,
-                            bool weight_major) {
+fo_status add_ag_step_pairs(Launch& L, const AgArgs& a, const int* xmap, const int* rmap, const int* wmap,
+                            int64_t gated_f, bool weight_major) {
   const int P = a.P, npairs = P / 2;
   auto add = [&](int r, int j) {
     int r0, s0, r1, s1;
@@ -627,6 +612,10 @@ fo_status add_ag_step_pairs(Launch& L, const AgArgs& a, const int* rmap, const i
     u = blank_unit();
     u.a_map = rmap[r];
     u.a_row0 = static_cast<int32_t>(2 * j * a.m);  // positions 2j and 2j+1
+    if (j == 0) {  // step 0 is the rank's own slice: read in place, no copy into position 0
+      u.a_map_lo = xmap[r];
+      u.a_row_lo = 0;
+    }
     u.wait_flag = static_cast<int32_t>(kAgFlagBase + r * P + s0);
     u.wait_flag2 = static_cast<int32_t>(kAgFlagBase + r * P + s1);
     u.b_map = wmap[r];
@@ -765,7 +754,7 @@ fo_status ag_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_
       if (st != FO_OK) return st;
     }
     if (flash && step_pairs && row0 == 0 && rows == m) {
-      FO_TRY(add_ag_step_pairs(L, a, rmap, wmap, gated_f, weight_major));
+      FO_TRY(add_ag_step_pairs(L, a, xmap, rmap, wmap, gated_f, weight_major));
     } else {
       FO_TRY(add_ag_units(L, a, xmap, rmap, wmap, row0, rows, flash, gated_f, weight_major));
     }
@@ -791,7 +780,7 @@ fo_status ag_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* W, int P, const fo_
     // order: copies_first)
     FO_TRY(fork_links(ctx, P, stream));
     if (!copies_first()) FO_TRY(launch_gemm(ctx, L, o, stream));
-    if (a.Xh || step_pairs) FO_TRY(enqueue_uploads(ctx, a, epoch, flags, step_pairs));
+    if (a.Xh || step_pairs) FO_TRY(enqueue_uploads(ctx, a, epoch, flags));
     FO_TRY(enqueue_ag_ring(ctx, a, 0, m, true, epoch, o.fault, flags));
     if (copies_first()) FO_TRY(launch_gemm(ctx, L, o, stream));
     return join_links(ctx, P, stream);
@@ -1545,7 +1534,7 @@ fo_status mlp_fused_run(fo_ctx* ctx, const fo_mat* X, const fo_mat* Wc, const fo
   // the ring's copies run concurrently with the launch (host order: copies_first)
   FO_TRY(fork_links(ctx, P, stream));
   if (!copies_first()) FO_TRY(launch_gemm(ctx, L, o, stream));
-  if (a.Xh) FO_TRY(enqueue_uploads(ctx, a, epoch, flags, false));
+  if (a.Xh) FO_TRY(enqueue_uploads(ctx, a, epoch, flags));
   FO_TRY(enqueue_ag_ring(ctx, a, 0, m, true, epoch, o.fault, flags));
   if (copies_first()) FO_TRY(launch_gemm(ctx, L, o, stream));
   FO_TRY(join_links(ctx, P, stream));

@@ -92,13 +92,14 @@ __device__ void producer_loop(const GemmParams& p, uint8_t* tiles, SmemCtl* ctl)
       break;
     }
     const int nk = (u.k + kBK - 1) / kBK;
-    const int a_row = u.a_row0 + tc.mb * kBM;
+    const bool lo = tc.mb == 0 && u.a_map_lo >= 0;  // a step-pair unit's first 128 rows, read in place
+    const int a_row = lo ? u.a_row_lo : u.a_row0 + tc.mb * kBM;
     const bool gated = u.gated != 0;
     const int b_row = u.b_row0 + tc.nb * (gated ? kBN / 2 : kBN);
     const int b_row_up = u.b_row1 + tc.nb * (kBN / 2);
     // per-tile values in registers: the k loop below re-reads nothing from the parameters
     const bool chunked = u.kchunk > 0;
-    const CUtensorMap* amap0 = &p.maps[u.a_map];
+    const CUtensorMap* amap0 = &p.maps[lo ? u.a_map_lo : u.a_map];
     const CUtensorMap* bmap = &p.maps[u.b_map];
     for (int kb = 0; kb < nk; ++kb) {
       if (!mbar_wait_fast(&ctl->empty[stage], phase ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty,

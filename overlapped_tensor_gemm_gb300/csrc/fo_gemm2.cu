@@ -74,13 +74,15 @@ __device__ void pair_producer(const GemmParams& p, uint8_t* tiles, PairCtl* ctl,
       break;
     }
     const int nk = (u.k + kBK - 1) / kBK;
-    const int a_row = u.a_row0 + tc.mb * 2 * kBM + static_cast<int>(cta) * kBM;
+    // a step-pair unit may read its first 128 rows (this CTA's, when cta == 0) in place
+    const bool lo = cta == 0 && u.a_map_lo >= 0;
+    const int a_row = lo ? u.a_row_lo + tc.mb * 2 * kBM : u.a_row0 + tc.mb * 2 * kBM + static_cast<int>(cta) * kBM;
     // B rows of this CTA: gated tiles put the gate rows in the leader and the up rows in the peer
     const int b_row = u.gated ? (cta == 0 ? u.b_row0 : u.b_row1) + tc.nb * (kBN / 2)
                               : u.b_row0 + tc.nb * kBN + static_cast<int>(cta) * (kBN / 2);
     // per-tile values in registers: the k loop below re-reads nothing from the parameters
     const bool chunked = u.kchunk > 0;
-    const CUtensorMap* amap0 = &p.maps[u.a_map];
+    const CUtensorMap* amap0 = &p.maps[lo ? u.a_map_lo : u.a_map];
     const CUtensorMap* bmap = &p.maps[u.b_map];
     for (int kb = 0; kb < nk; ++kb) {
       if (!mbar_wait_fast(&ctl->empty[stage], phase ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty,

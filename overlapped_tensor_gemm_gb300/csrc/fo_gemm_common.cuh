@@ -452,6 +452,7 @@ __device__ __forceinline__ bool tile_ok(const GemmParams& p, const TileCoord& tc
     const int64_t slot_max = (blk * ncta + ncta - 1) * 4 + 3;
     if (u.wait_flag >= 0) ok = ok && flag_ok(u.wait_flag);
     if (u.wait_flag2 >= 0) ok = ok && flag_ok(u.wait_flag2) && u.m_rows == 2 * kBM;
+    if (u.a_map_lo >= 0) ok = ok && u.a_map_lo < p.num_maps && u.wait_flag2 >= 0;
     if (u.in_flag_base >= 0) ok = ok && flag_ok(u.in_flag_base + slot_max);
     if (u.out_flag_base >= 0) ok = ok && flag_ok(u.out_flag_base + slot_max);
     if (u.done_counter >= 0) ok = ok && flag_ok(u.done_counter);

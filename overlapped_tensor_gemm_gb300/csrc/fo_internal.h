@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cstring>
+
 #include "../../include/fo.h"
 
 namespace fo {
@@ -54,8 +56,10 @@ struct GemmUnit {
   // A step-pair unit (AG with 128-row slices): its 256 rows are two ring steps' slices,
   // stored next to each other in step order; rows [128, 256) wait on wait_flag2 (not
   // wait_flag) and are stored at c2 (not c) from its row 0.  wait_flag2 = -1, c2 = null:
-  // an ordinary unit.
+  // an ordinary unit.  a_map_lo >= 0: rows [0, 128) are read from that map at row a_row_lo
+  // instead (the rank's own slice, read in place).
   int32_t wait_flag2;
+  int32_t a_map_lo, a_row_lo;
   int32_t in_flag_base;        // RS: per-tile flags guarding acc_in (-1: none)
   int32_t out_flag_base;       // RS: per-tile flags released after C is written (-1: none)
   int32_t epi;                 // EpiMode
@@ -132,6 +136,22 @@ struct GemmParams {
   uint32_t* ctrl;              // device control block (error word, abort flag)
 };
 static_assert(sizeof(GemmParams) <= 32764, "GemmParams must fit the kernel parameter space");
+
+// A unit with every optional feature off (-1 indices, null pointers, zero counts): every
+// builder starts from this, so a field added later has its neutral value everywhere.
+inline GemmUnit blank_unit() {
+  GemmUnit u;
+  std::memset(&u, 0, sizeof(u));
+  u.wait_flag = -1;
+  u.wait_flag2 = -1;
+  u.a_map_lo = -1;
+  u.in_flag_base = -1;
+  u.out_flag_base = -1;
+  u.done_counter = -1;
+  u.rows_done_base = -1;
+  u.a_ready_base = -1;
+  return u;
+}
 
 // A tile's position: unit index, m-block and n-block inside the unit.
 struct TileCoord {

@@ -145,6 +145,7 @@ extern "C" FO_API fo_status fo_gemm_rs_noalloc(const fo_mat* X, const fo_mat* W_
       const int c = ((r - t - 1) % P + P) % P;  // rank-adaptive: the kept chunk r comes at t = P-1
       const int h = t;
       GemmUnit& u = p.units[nu++];
+      u = blank_unit();
       u.a_map = r;
       u.b_map = P + r;
       u.a_row0 = static_cast<int32_t>(c * m);
@@ -153,13 +154,6 @@ extern "C" FO_API fo_status fo_gemm_rs_noalloc(const fo_mat* X, const fo_mat* W_
       u.k = static_cast<int32_t>(Kr);
       u.tiles_m = static_cast<int32_t>(tm);
       u.tiles_n = static_cast<int32_t>(tn);
-      u.wait_flag = -1;
-      u.wait_flag2 = -1;
-      u.in_flag_base = -1;
-      u.out_flag_base = -1;
-      u.done_counter = -1;
-      u.rows_done_base = -1;
-      u.a_ready_base = -1;
       if (h > 0) {
         u.acc_in = slot(r, h);
         u.ld_acc = N;
