@@ -320,8 +320,8 @@ FO_API fo_status fo_attn_layer(fo_ctx* ctx, const fo_mat* X_shards, const fo_mat
  *                   the call's work has completed on `stream` (NULL: none).
  * Shapes whose receive slots (P*(P-1)*m*N*4 bytes) or flags exceed the static
  * area are rejected with FO_ERR_UNSUPPORTED.  The first call on a device does a
- * one-time set-up (it configures the kernel with that device current); make that
- * first call before any stream capture.  Every call asks for the array's device
+ * one-time set-up (it configures the kernel with that device current).  Every
+ * call asks for the array's device
  * address with the caller's device current (in host code the array's name is
  * only a stand-in).  Every call shares the array, which keeps the previous
  * call's contents: each call first clears, on `stream`, the control words and
