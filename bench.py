@@ -462,38 +462,47 @@ def attention_bench(ctx, pk, iters: int, order: str = "flash", baselines: bool =
     O = [torch.empty(shape, dtype=torch.bfloat16, device="cuda") for _ in range(c.P)]
     stream = torch.cuda.current_stream()
 
-    def timed(o, compute_only=False, prune=True):
+    def call(o, compute_only=False, prune=True):
         # causal-pruned forwarding (a K/V slice goes only to the ranks that use it; the same
         # output as the full ring) unless prune is False
         kw = dict(heads=c.heads, head_dim=c.head_dim, order=o, compute_only=compute_only, causal_prune=prune)
-        for _ in range(2):
-            ctx.qsplit_attn(Q, K, V, O, **kw)
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(iters):
-            ctx.qsplit_attn(Q, K, V, O, **kw)
-        b.record(stream)
-        torch.cuda.synchronize()
-        ctx.poll()
-        return a.elapsed_time(b) / iters
+        return lambda: ctx.qsplit_attn(Q, K, V, O, **kw)
 
-    ms = timed(order)
+    fns = {"main": call(order)}
+    if baselines:
+        # the same launches with every arrival flag published and no copy: T_compute of each order
+        fns.update({"full": call(order, prune=False), "serial": call("serial"),
+                    "main_c": call(order, compute_only=True), "serial_c": call("serial", compute_only=True)})
+    for fn in fns.values():
+        fn()
+        fn()
+    torch.cuda.synchronize()
+    # medians of interleaved rounds, so that a slow moment of the GPU hits every variant alike
+    samples = {k: [] for k in fns}
+    for _ in range(5):
+        for k, fn in fns.items():
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(iters):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            samples[k].append(a.elapsed_time(b) / iters)
+    ctx.poll()
+    t = {k: statistics.median(v) for k, v in samples.items()}
+    ms = t["main"]
     tf = c.flops() / (ms * 1e-3) / 1e12
-    full_ms = timed(order, prune=False) if baselines else None
     out = {"workload": f"query-split causal attention, P={c.P}, seq {c.seq}, {c.heads} heads, head_dim "
                        f"{c.head_dim}", "order": f"{order}, causal-pruned K/V forwarding", "ms": round(ms, 4),
            "tflops": round(tf, 2),
            "frac_of_bf16_peak": round(tf / pk["bf16_burst"], 4), "flop": c.flops(),
-           "flop_counting": "causal triangle only (QK^T and PV)"}
+           "flop_counting": "causal triangle only (QK^T and PV)",
+           "timing": f"medians of 5 interleaved rounds of {iters} calls per variant"}
     if baselines:
-        t_serial = timed("serial")
         ctx.qsplit_attn(Q, K, V, O, heads=c.heads, head_dim=c.head_dim, order="serial", causal_prune=True)
         torch.cuda.synchronize()
         ring_ms, kernel_ms = ctx.phase_ms()
-        # the same launches with every arrival flag published and no copy: T_compute of each order
-        t_c = timed(order, compute_only=True)
-        t_serial_c = timed("serial", compute_only=True)
+        full_ms, t_serial, t_c, t_serial_c = t["full"], t["serial"], t["main_c"], t["serial_c"]
         out.update({"full_ring_ms": round(full_ms, 4),
                     "serial_ms": round(t_serial, 4), "serial_phases_ms": {"ring": round(ring_ms, 4),
                                                                            "kernel": round(kernel_ms, 4)},
