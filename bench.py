@@ -213,9 +213,16 @@ def cpu_cores() -> int:
 
 
 def calibrate_rows(cfg, inp_f64, target_s: float) -> int:
-    dt, _ = oracle_mlp_sample(cfg, inp_f64, 2, 0)
-    per_row = max(dt / 2, 1e-4)
-    return int(max(2, min(cfg.m, target_s / per_row)))
+    """Token rows per slice for an oracle sample of about target_s seconds.  A small sample's
+    time is mostly the fixed cost of streaming the fp64 weights, so the sample is grown until
+    one run takes at least half the target and then scaled in proportion (which, with a fixed
+    part in the cost, can only fall short of the target, never overshoot it)."""
+    r = 2
+    dt, _ = oracle_mlp_sample(cfg, inp_f64, r, 0)
+    while dt < 0.5 * target_s and r < cfg.m:
+        r = int(min(cfg.m, max(2 * r, r * 0.6 * target_s / max(dt, 1e-3))))
+        dt, _ = oracle_mlp_sample(cfg, inp_f64, r, 0)
+    return int(max(2, min(cfg.m, r * target_s / max(dt, 1e-3))))
 
 
 # --------------------------------------------------------------------------
