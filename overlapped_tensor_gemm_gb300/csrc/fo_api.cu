@@ -598,9 +598,10 @@ constexpr double kWeightMajorMaxBytes = 80.0 * (1 << 20);  // measured: 56 MiB b
 // rows_base >= 0 (one launch for a whole layer): rank r's unit for slice s counts its stored
 // rows per m-block into counter rows_base + (r * P + s) * mblocks + mb.
 // step_pairs (whole-slice flash launches with 128-row slices, P even): one unit per two
-// consecutive steps (t, t+1) of a rank, 256 rows of its step-ordered receive buffer, so the
-// launch runs 256-row tiles on SM pairs: the first 128 rows (slice of step t) wait on that
-// slice's flag and are stored at its output rows, the next 128 likewise for step t+1.
+// consecutive steps (t, t+1) of a rank, 256 rows of its step-ordered receive buffer (for
+// steps 0 and 1 the first 128 rows are the rank's own shard, read in place), so the launch
+// runs 256-row tiles on SM pairs: the first 128 rows (slice of step t) wait on that slice's
+// flag and are stored at its output rows, the next 128 likewise for step t+1.
 fo_status add_ag_step_pairs(Launch& L, const AgArgs& a, const int* xmap, const int* rmap, const int* wmap,
                             int64_t gated_f, bool weight_major) {
   const int P = a.P, npairs = P / 2;
