@@ -419,7 +419,9 @@ int mod(int a, int P) { return ((a % P) + P) % P; }
 //   Flash-AG: unit i of step t is rank i, computing slice (i - t) mod P (its own at t = 0).
 //   Flash-RS: unit i of step t is rank (t + i) mod P, computing chunk (r - t - 1) mod P,
 //             so the kept chunk r comes at t = P-1; the rotation places every unit at the
-//             position of the unit of step t-1 whose partial sum it consumes.
+//             position of the unit of step t-1 whose partial sum it consumes.  (The fused
+//             step-ordered launch computes the same units, grouped two steps at a time in
+//             its tile order: build_rs_flash.)
 //   naive RS: step c is chunk c on every rank, units in chain order r = c+1, c+2, ..., c.
 void ag_unit(int P, int t, int i, int* rank, int* slice) {
   *rank = i;
@@ -862,6 +864,9 @@ float* rs_slot(const RsArgs& a, float* base, int r, int h) {
 
 constexpr double kStreamPartialsBytes = 96.0 * (1 << 20);  // L2 is 126 MB
 constexpr int kTnFbGroup = 32;  // feature blocks per ordering group of the transposed tiles (measured: 2..32)
+// Ring steps per tile-order group of the step-ordered Flash-RS (measured 1, 2, 4, 8: every
+// grouping beat one step per group; 2: 16K layer 2.2-2.4% and 4K layer ~3% faster than 1)
+constexpr int kRsStepGroup = 2;
 
 // Transposed reduce-scatter tiles (GemmParams::tn_S) for a slice of m rows: 0 if they do
 // not apply, else the number of ring steps per tile, with *pair set when the tiles run on
@@ -882,7 +887,8 @@ int rs_tn_steps(const fo_ctx* ctx, const RsArgs& a, const fo_opts& o, bool* pair
 
 // Appends the maps and units of a fused reduce-scatter (order FO_ORDER_FLASH or
 // FO_ORDER_NAIVE) to L.  S > 0: transposed tiles (rs_tn_steps), which take the whole launch;
-// otherwise one group per ring step.  `done`: the kept chunk's tiles count into the per-rank
+// otherwise step-ordered tiles, in groups of kRsStepGroup ring steps (Flash order) or one
+// group per ring step (naive order).  `done`: the kept chunk's tiles count into the per-rank
 // completion counters.  ready_base >= 0 (one launch for a whole layer): rank r's unit for
 // chunk c waits, per m-block, until counter ready_base + (r * P + c) * mblocks + mb reaches
 // ready_count (the epilogue warps of the tiles that wrote those rows of X[r]).
@@ -981,12 +987,35 @@ fo_status build_rs_flash(fo_ctx* ctx, Launch& L, const RsArgs& a, const fo_opts&
       q.units[i].tiles_n = q.tn_fblocks;
     }
   } else {
-    for (int t = 0; t < P; ++t) {
-      L.begin_group();
-      for (int i = 0; i < P; ++i) {
-        int r, c;
-        rs_unit(P, o.order, t, i, &r, &c);
-        add(r, c);
+    if (o.order == FO_ORDER_FLASH) {
+      // Groups of kRsStepGroup ring steps.  Inside a group each rank's units follow one
+      // another (the weight it streams is read for the group's steps in close succession,
+      // and a step's partial sums are read about one unit after they are written instead
+      // of a whole step later); a unit whose producer (rank r-1, previous step) is not yet
+      // placed is preceded by that producer's chain, so every unit waits only on units
+      // earlier in the tile order.  The ranks' computations and the order of additions on
+      // each chunk are those of the step schedule (rs_unit): only the tile order changes.
+      for (int t0 = 0; t0 < P; t0 += kRsStepGroup) {
+        const int gs = kRsStepGroup < P - t0 ? kRsStepGroup : P - t0;
+        L.begin_group();
+        bool placed[kMaxP][kRsStepGroup] = {};
+        auto emit = [&](auto&& self, int r, int k) -> void {
+          if (placed[r][k]) return;
+          if (k > 0) self(self, mod(r - 1, P), k - 1);
+          add(r, mod(r - (t0 + k) - 1, P));  // rank r at step t0 + k: chunk (r - t - 1) mod P
+          placed[r][k] = true;
+        };
+        for (int r = 0; r < P; ++r)
+          for (int k = 0; k < gs; ++k) emit(emit, r, k);
+      }
+    } else {
+      for (int t = 0; t < P; ++t) {
+        L.begin_group();
+        for (int i = 0; i < P; ++i) {
+          int r, c;
+          rs_unit(P, o.order, t, i, &r, &c);
+          add(r, c);
+        }
       }
     }
     L.p.mn_major = a.w_kn ? 2 : 0;
