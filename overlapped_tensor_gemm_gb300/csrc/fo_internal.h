@@ -128,6 +128,9 @@ struct GemmParams {
   // step's partial sums are larger than L2, so they come back from DRAM anyway, and should
   // not evict the operands the GEMM reuses.
   int32_t stream_partials;
+  // SM-pair kernel: 1: pairs claim tiles in order from a launch-wide counter; 0: pair c runs
+  // tiles c, c + pairs, c + 2 * pairs, ...
+  int32_t claim_tiles;
   int32_t total_tiles;
   uint32_t epoch;
   uint64_t timeout_ns;
@@ -164,13 +167,16 @@ enum CtrlWord : int {
   kCtrlAbort = 1,     // non-zero: every CTA leaves its loops
   kCtrlWhere = 2,     // where the first timeout happened (see WaitSite)
   kCtrlDetail = 3,    // flag index / tile index of the first timeout
+  kCtrlTiles = 4,     // SM-pair GEMM: the next unclaimed tile of the running launch (zero
+                      // between launches: the launch's last claim resets it)
   kCtrlWords = 8
 };
 
 enum WaitSite : uint32_t {
   kSiteAgFlag = 1, kSiteFull = 2, kSiteEmpty = 3, kSiteTmemFull = 4,
   kSiteTmemEmpty = 5, kSiteAccInFlag = 6, kSiteDrain = 7, kSiteAttnFlag = 8,
-  kSiteAttnBar = 9, kSiteVRange = 10, kSiteRowsReady = 11, kSiteBounds = 12
+  kSiteAttnBar = 9, kSiteVRange = 10, kSiteRowsReady = 11, kSiteBounds = 12,
+  kSiteSched = 13
 };
 
 // host launchers (fo_gemm.cu: single-SM 128x256 tiles; fo_gemm2.cu: SM-pair 256x256 tiles)

@@ -363,6 +363,42 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// 32-bit store into another CTA's shared memory (shared::cluster address)
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+// try_wait with acquire at cluster scope: the phase was completed by an arrive.release.cluster
+// of another CTA, and the waiter reads what that CTA wrote into this CTA's shared memory
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait of the same kind.  False on timeout or abort.
+static __device__ __noinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t* ctrl,
+                                                      uint64_t timeout_ns, uint32_t site, uint32_t detail) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 63u) == 0u) {
+      if (aborted(ctrl)) return false;
+      if (global_timer_ns() - t0 > timeout_ns) {
+        raise_error(ctrl, FO_ERR_TIMEOUT, site, detail);
+        return false;
+      }
+    }
+  }
+}
+
 // TMA load into this CTA's shared memory whose completion is signalled on an
 // mbarrier that may live in the peer CTA of the pair (the MMA-issuing CTA).
 __device__ __forceinline__ void tma_load_2d_pair(const CUtensorMap* map, void* dst, uint32_t bar_cluster_addr,
