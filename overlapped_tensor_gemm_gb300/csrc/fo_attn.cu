@@ -12,21 +12,21 @@
 // in TMEM.
 //
 // CTA layout (320 threads, one CTA per SM):
-//   warp 0      TMA: K and V^T blocks in two stage rings of three stages, K
-//               two blocks ahead of V; waits for the slice's arrival flag
-//               before reading it.
-//   warp 1      tcgen05.mma: S = Q K^T into one of two TMEM score buffers
-//               (the next block's scores overlap this block's softmax), then
-//               O += P V into the TMEM accumulator; Q and P are read from TMEM,
-//               so shared memory holds only the K and V^T rings.
+//   warp 0      TMA: the item's Q block into shared memory, K and V^T blocks in
+//               stage rings of three and two stages, K two blocks ahead of V;
+//               waits for the slice's arrival flag before reading it.
+//   warp 1      tcgen05.mma: S = Q K^T into one of two TMEM score buffers, then
+//               O += P V into the TMEM accumulator, P read from its own TMEM
+//               buffer.  A score buffer is free again as soon as the softmax
+//               warps have read it, so the scores of block j + 2 can be computed
+//               while block j's softmax still runs.
 //   warps 2-9   softmax: two warps per query row (one per 64-key half); they
-//               write the item's Q rows into TMEM, load their half of the score
-//               row, mask the diagonal block, exchange the row maximum, update
-//               max/sum, rescale their half of the O row only when the max grew
+//               load their half of the score row, mask the diagonal block,
+//               exchange the row maximum, update max/sum, release the score
+//               buffer, rescale their half of the O row only when the max grew
 //               by more than 2^8 (the final division by the sum uses the same
-//               reference max, so this is exact), and write P as fp16 over the
-//               scores they have read, so a block's softmax does not wait for
-//               the previous block's P.V.
+//               reference max, so this is exact), and write P as fp16 into the
+//               P buffer once the previous block's P.V has read it.
 // V is transposed once per rank (V^T [heads*128, tokens]) before the ring so
 // that both MMAs read K-major operands.  The P.V product runs in fp16: the
 // transpose converts V's bf16 values to fp16 (exact for |v| within fp16's
@@ -61,22 +61,19 @@ constexpr int kVStages = 2;
 constexpr int kVRows = kHd + 16;
 constexpr uint32_t kVHalfBytes = kVRows * 128;           // [144 rows x 64 keys] swizzled
 constexpr uint32_t kVStageBytes = 2 * kVHalfBytes;
-// TMEM: S0 [0,128), S1 [128,256), O [256,400) (column 384 = row sum), Q [448,512).
-// P of a block is written over the first 32 columns of each warp's 64 score columns
-// of its S buffer.
+// TMEM: S0 [0,128), S1 [128,256), O [256,400) (column 384 = row sum), P [400,464):
+// keys 64h + 2c, 64h + 2c + 1 of a block as one fp16 pair in column 400 + 32h + c.
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 256;
 constexpr uint32_t kSumCol = kOCol + kHd;
-constexpr uint32_t kQCol = 448;          // Q as packed bf16 pairs: 128 head dims in 64 columns
+constexpr uint32_t kPCol = 400;
 constexpr uint32_t kIdescS = umma_idesc_bf16(128, 128);   // S = Q K^T, bf16 operands
 constexpr uint32_t kIdescO = umma_idesc_f16(128, kVRows); // [O | sums] += P [V | 1 0..0], fp16
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct AttnParams {
-  CUtensorMap maps[3 * kMaxP];  // per rank r: K local = r, K received = P+r, V^T = 2P+r
-  const uint16_t* q[kMaxP];     // Q shards (read by the softmax warps into TMEM)
-  int64_t ld_q[kMaxP];
+  CUtensorMap maps[4 * kMaxP];  // per rank r: K local = r, K received = P+r, V^T = 2P+r, Q = 3P+r
   uint16_t* out[kMaxP];
   int64_t ld_out[kMaxP];
   int32_t P, heads, nkb, causal;
@@ -93,31 +90,35 @@ struct AttnParams {
 };
 
 struct alignas(8) AttnCtl {
-  uint64_t q_full;                  // the item's Q is in TMEM (the softmax warps wrote it)
+  uint64_t q_full;                  // the item's Q block has landed in shared memory
+  uint64_t q_empty;                 // the item's last score MMA has completed
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
   uint64_t s_full[2];               // per S buffer: scores computed
-  uint64_t p_full[2];               // per S buffer: P written over the scores
-  uint64_t pv_done[2];              // per S buffer: the P.V that read its P completed
+  uint64_t s_free[2];               // per S buffer: every softmax warp has read the scores
+  uint64_t p_full;                  // one phase per block: P written
+  uint64_t pv_done;                 // one phase per block: its P.V completed
   uint64_t drain;
   uint64_t xchg[4][2];   // per lane quadrant, two slots: the column halves' partial max / sum exchange
   uint32_t tmem_base;
   uint32_t pad;
 };
 
-// Shared memory: K stages | V^T stages | exchange | control  (Q, S, P and O live in TMEM)
+// Shared memory: K stages | V^T stages | Q | exchange | control  (S, P and O live in TMEM)
 constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
-constexpr uint32_t kOffXch = kOffV + kVStages * kVStageBytes;  // float [2 slots][2 halves][128 rows]
+constexpr uint32_t kOffQ = kOffV + kVStages * kVStageBytes;    // [128 queries x 128 dims], two 64-dim halves
+constexpr uint32_t kOffXch = kOffQ + kTileBytes;               // float [2 slots][2 halves][128 rows]
 constexpr uint32_t kOffCtl = kOffXch + 2 * 2 * 128 * 4;
 constexpr int kAttnSmem = static_cast<int>(kOffCtl + sizeof(AttnCtl) + 1024);
+static_assert(kOffQ % 1024 == 0, "the Q block must sit on a 1024-byte boundary (128-byte swizzle)");
 // Every persistent kernel of this library leaves shared memory and registers of
 // its SM free: the ring's device-to-device copies may run as a small copy kernel
 // that must be able to start while the persistent grid occupies every SM.  The
 // register share of one SM sub-partition (16K) holds up to three of this
 // kernel's ten warps; the kernel is therefore kept at <= 136 registers per thread
 // (3 warps x 32 x 136 = 13056, leaving 3328), checked at context set-up.
-static_assert(kAttnSmem <= 232448 - 24 * 1024, "attention kernel must leave 24 KiB of shared memory free");
+static_assert(kAttnSmem <= 232448 - 16 * 1024, "attention kernel must leave 16 KiB of shared memory free");
 
 struct Item {
   int r, qb, h;
@@ -185,6 +186,8 @@ struct BlockIter {
 __device__ void attn_producer(const AttnParams& p, uint8_t* smem, AttnCtl* ctl) {
   int kst = 0, vst = 0;
   uint32_t kph = 0, vph = 0;
+  uint32_t q_uses = 0;
+  bool q_armed = false;
   uint64_t seen = 0;  // bit r*P+s: arrival of slice s at rank r already observed
   uint32_t karmed = 0, karmed_ph = 0, varmed = 0, varmed_ph = 0;
   BlockIter kit, vit;
@@ -207,6 +210,21 @@ __device__ void attn_producer(const AttnParams& p, uint8_t* smem, AttnCtl* ctl) 
       if (!flag_wait(p.flags + fidx, p.epoch, p.ctrl, p.timeout_ns, kSiteAttnFlag, fidx)) return false;
       fence_proxy_async_global();
       seen |= 1ull << fidx;
+    }
+    if (kit.t == 0 && kit.kb == 0) {
+      // the item's Q block, once the previous item's last score MMA has read the old one
+      if (!mbar_wait_fast(&ctl->q_empty, (q_uses & 1u) ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty, kit.i)) return false;
+      mbar_arrive_expect_tx(&ctl->q_full, kTileBytes);
+      for (int c = 0; c < 2; ++c)
+        tma_load_2d(&p.maps[3 * p.P + it.r], smem + kOffQ + c * kHalfBytes, &ctl->q_full, it.h * kHd + c * 64,
+                    it.qb * kQB);
+      q_armed = true;
+      ++q_uses;
+      const int inext = kit.i + static_cast<int>(gridDim.x);
+      if (inext < p.total_items) {  // the next item's Q block into L2
+        const Item nx = decode_item(p, inext);
+        for (int c = 0; c < 2; ++c) tma_prefetch_l2_2d(&p.maps[3 * p.P + nx.r], nx.h * kHd + c * 64, nx.qb * kQB);
+      }
     }
     if (!mbar_wait_fast(&ctl->k_empty[kst], kph ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty, kit.i)) return false;
     const CUtensorMap* kmap = kit.t == 0 ? &p.maps[it.r] : &p.maps[p.P + it.r];
@@ -251,6 +269,7 @@ __device__ void attn_producer(const AttnParams& p, uint8_t* smem, AttnCtl* ctl) 
     if (!issue_v()) ok = false;
   }
   if (!ok) {
+    if (q_armed) mbar_wait_drain(&ctl->q_full, (q_uses - 1) & 1u, kDrainNs);
     for (int s = 0; s < kKStages; ++s)
       if ((karmed >> s) & 1u) mbar_wait_drain(&ctl->k_full[s], (karmed_ph >> s) & 1u, kDrainNs);
     for (int s = 0; s < kVStages; ++s)
@@ -271,25 +290,24 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       : "memory");
 }
 
-// S = Q K^T for one 128-key block: Q from TMEM (column c holds head dims 2c, 2c+1),
-// K from the two 64-dim swizzle halves of the stage (16 head dims per MMA).
-__device__ __forceinline__ void issue_s(uint32_t tmem_s, uint32_t tmem_q, uint32_t k_addr) {
+// S = Q K^T for one 128-key block: Q and K from the two 64-dim swizzle halves of their
+// shared-memory blocks (16 head dims per MMA).
+__device__ __forceinline__ void issue_s(uint32_t tmem_s, uint32_t q_addr, uint32_t k_addr) {
 #pragma unroll
   for (int k = 0; k < kHd / 16; ++k) {
     const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
-    umma_ts(tmem_s, tmem_q + k * 8, umma_sdesc_sw128(k_addr + off), kIdescS, k > 0 ? 1u : 0u);
+    umma_bf16_ss(tmem_s, umma_sdesc_sw128(q_addr + off), umma_sdesc_sw128(k_addr + off), kIdescS, k > 0 ? 1u : 0u);
   }
 }
 
-// [O | sums] += P [V | 1 0..0] for one 128-key block: P from the S buffer (keys 64h + 2c,
-// 64h + 2c + 1 in column 64h + c, c < 32), V^T (and the ones row) from the two 64-key
-// swizzle halves of the stage.
+// [O | sums] += P [V | 1 0..0] for one 128-key block: P from its TMEM buffer (keys 64h + 2c,
+// 64h + 2c + 1 in column 32h + c), V^T (and the ones row) from the two 64-key swizzle
+// halves of the stage.
 __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr, bool first) {
 #pragma unroll
   for (int k = 0; k < kKB / 16; ++k) {
     const uint32_t off = (k >> 2) * kVHalfBytes + (k & 3) * 32;
-    umma_ts(tmem_o, tmem_p + (k >> 2) * 64 + (k & 3) * 8, umma_sdesc_sw128(v_addr + off), kIdescO,
-            (first && k == 0) ? 0u : 1u);
+    umma_ts(tmem_o, tmem_p + k * 8, umma_sdesc_sw128(v_addr + off), kIdescO, (first && k == 0) ? 0u : 1u);
   }
 }
 
@@ -318,75 +336,86 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// S buffer b of block gs may be overwritten once the P.V of block gs - 2 (whose P
-// lives there) has completed.
+// S buffer b of block gs may be overwritten once the softmax warps have read the scores
+// of block gs - 2 from it.
 __device__ __forceinline__ uint32_t s_free_parity(uint32_t gs) { return ((gs >> 1) & 1u) ^ 1u; }
 
+// This CTA's key blocks in schedule order, for one kind of MMA: item i (stride
+// gridDim.x), block j of its n blocks.
+struct MmaWalk {
+  int i, j, n;
+  __device__ void start(const AttnParams& p) {
+    i = blockIdx.x;
+    j = 0;
+    n = i < p.total_items ? item_blocks(p, decode_item(p, i)) : 0;
+  }
+  __device__ void next(const AttnParams& p) {
+    if (++j < n) return;
+    j = 0;
+    i += gridDim.x;
+    n = i < p.total_items ? item_blocks(p, decode_item(p, i)) : 0;
+  }
+};
+
+// Two independent walks over the CTA's key blocks: the score MMAs (block gs: its K stage
+// loaded, its S buffer released by the softmax of block gs - 2, the item's Q loaded) and
+// the P.V MMAs (block gp: its P written, its V stage loaded).  Each issues as soon as its
+// operands are ready, scores first when both are, so the scores of block j + 2 are
+// computed while the softmax of block j still runs.
 __device__ void attn_mma(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, uint32_t tmem_base) {
   const uint32_t sbase = smem_u32(smem);
-  uint32_t q_uses = 0;
-  uint32_t g = 0;  // global key-block counter of this CTA
-  bool issued = false, ok = true;
-  for (int i = blockIdx.x; ok && i < p.total_items; i += gridDim.x) {
-    const Item it = decode_item(p, i);
-    const int n = item_blocks(p, it);
-    if (!mbar_wait_fast(&ctl->q_full, q_uses & 1u, p.ctrl, p.timeout_ns, kSiteFull, i)) break;
-    ++q_uses;
-    tc_fence_after();
-    {  // scores of the item's first block
-      const uint32_t st = g % kKStages, sb = g & 1u;
-      if (!mbar_wait_fast(&ctl->k_full[st], (g / kKStages) & 1u, p.ctrl, p.timeout_ns, kSiteFull, i) ||
-          !mbar_wait_fast(&ctl->pv_done[sb], s_free_parity(g), p.ctrl, p.timeout_ns, kSiteTmemEmpty, i)) {
-        ok = false;
-        break;
+  uint32_t q_uses = 0, gs = 0, gp = 0;  // items whose Q was waited for; score / P.V blocks issued
+  bool q_ready = false, issued = false, ok = true;
+  MmaWalk ws, wp;
+  ws.start(p);
+  wp.start(p);
+  uint64_t t0 = global_timer_ns();
+  for (uint32_t spin = 1; ok && wp.i < p.total_items; ++spin) {
+    bool progressed = false;
+    if (ws.i < p.total_items) {
+      if (ws.j == 0 && !q_ready && mbar_test(&ctl->q_full, q_uses & 1u)) {
+        q_ready = true;
+        ++q_uses;
       }
+      const uint32_t st = gs % kKStages, sb = gs & 1u;
+      if ((ws.j > 0 || q_ready) && mbar_test(&ctl->k_full[st], (gs / kKStages) & 1u) &&
+          mbar_test(&ctl->s_free[sb], s_free_parity(gs))) {
+        tc_fence_after();
+        issue_s(tmem_base + sb * 128, sbase + kOffQ, sbase + kOffK + st * kTileBytes);
+        issued = true;
+        umma_commit(&ctl->k_empty[st]);  // the K stage is free once these scores are computed
+        umma_commit(&ctl->s_full[sb]);
+        if (ws.j + 1 == ws.n) {  // the item's last scores: its Q block may be replaced
+          umma_commit(&ctl->q_empty);
+          q_ready = false;
+        }
+        ++gs;
+        ws.next(p);
+        progressed = true;
+      }
+    }
+    const uint32_t vs = gp % kVStages;
+    if (gp < gs && mbar_test(&ctl->p_full, gp & 1u) && mbar_test(&ctl->v_full[vs], (gp / kVStages) & 1u)) {
       tc_fence_after();
-      issue_s(tmem_base + sb * 128, tmem_base + kQCol, sbase + kOffK + st * kTileBytes);
-      issued = true;
-      umma_commit(&ctl->k_empty[st]);  // the K stage is free once these scores are computed
-      umma_commit(&ctl->s_full[sb]);
+      issue_pv(tmem_base + kOCol, tmem_base + kPCol, sbase + kOffV + vs * kVStageBytes, wp.j == 0);
+      umma_commit(&ctl->v_empty[vs]);
+      umma_commit(&ctl->pv_done);
+      ++gp;
+      wp.next(p);
+      progressed = true;
     }
-    // Block j's step: the scores of block j + 1 and the P.V of block j, the two
-    // independent, issued in whichever order their operands become ready (scores
-    // first when both are), so a late K block does not hold back a ready P.V.
-    for (int j = 0; ok && j < n; ++j) {
-      const uint32_t gj = g + j;
-      const uint32_t gs = gj + 1, st = gs % kKStages, sb = gs & 1u;
-      const uint32_t pb = gj & 1u, vs = gj % kVStages;  // S buffer (holding P) and V stage of block gj
-      bool need_s = j + 1 < n, need_pv = true;
-      const uint64_t t0 = global_timer_ns();
-      for (uint32_t spin = 1; need_s || need_pv; ++spin) {
-        bool progressed = false;
-        if (need_s && mbar_test(&ctl->k_full[st], (gs / kKStages) & 1u) &&
-            mbar_test(&ctl->pv_done[sb], s_free_parity(gs))) {
-          tc_fence_after();
-          issue_s(tmem_base + sb * 128, tmem_base + kQCol, sbase + kOffK + st * kTileBytes);
-          umma_commit(&ctl->k_empty[st]);
-          umma_commit(&ctl->s_full[sb]);
-          need_s = false;
-          progressed = true;
-        }
-        if (need_pv && mbar_test(&ctl->p_full[pb], (gj >> 1) & 1u) &&
-            mbar_test(&ctl->v_full[vs], (gj / kVStages) & 1u)) {
-          tc_fence_after();
-          issue_pv(tmem_base + kOCol, tmem_base + pb * 128, sbase + kOffV + vs * kVStageBytes, j == 0);
-          umma_commit(&ctl->v_empty[vs]);
-          umma_commit(&ctl->pv_done[pb]);
-          need_pv = false;
-          progressed = true;
-        }
-        if (!progressed && (spin & 63u) == 0u) {
-          if (aborted(p.ctrl)) {
-            ok = false;
-          } else if (global_timer_ns() - t0 > p.timeout_ns) {
-            raise_error(p.ctrl, FO_ERR_TIMEOUT, need_pv ? kSiteFull : kSiteTmemEmpty, static_cast<uint32_t>(i));
-            ok = false;
-          }
-          if (!ok) break;
-        }
+    if (progressed) {
+      t0 = 0;
+    } else if ((spin & 63u) == 0u) {
+      const uint64_t now = global_timer_ns();
+      if (t0 == 0) t0 = now;
+      if (aborted(p.ctrl)) {
+        ok = false;
+      } else if (now - t0 > p.timeout_ns) {
+        raise_error(p.ctrl, FO_ERR_TIMEOUT, gp < gs ? kSiteFull : kSiteTmemEmpty, static_cast<uint32_t>(wp.i));
+        ok = false;
       }
     }
-    g += n;
   }
   if (!ok && issued) {
     umma_commit(&ctl->drain);
@@ -414,11 +443,6 @@ __device__ __forceinline__ void unpack2(uint64_t x, float& lo, float& hi) {
 __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t r;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -454,33 +478,6 @@ __device__ __forceinline__ bool xch_collect(AttnCtl* ctl, const float* xch, uint
   return true;
 }
 
-// This thread's query row of item `it` (its warp's 64 head dims) into the TMEM Q
-// region, then the warp's arrival on q_full.  The caller guarantees that no score
-// MMA still reads the region.
-__device__ __forceinline__ void write_q(const AttnParams& p, AttnCtl* ctl, const Item& it, uint32_t lane_base,
-                                        int row, int hf, int lane) {
-  const uint16_t* src = p.q[it.r] + static_cast<int64_t>(it.qb * kQB + row) * p.ld_q[it.r] + it.h * kHd + hf * 64;
-  uint32_t v[32];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const uint4 x = *reinterpret_cast<const uint4*>(src + 8 * k);
-    v[4 * k] = x.x;
-    v[4 * k + 1] = x.y;
-    v[4 * k + 2] = x.z;
-    v[4 * k + 3] = x.w;
-  }
-  tmem_st32(lane_base + kQCol + hf * 32, v);
-  tmem_wait_st();
-  tc_fence_before();
-  __syncwarp();
-  if (lane == 0) mbar_arrive(&ctl->q_full);
-}
-
-__device__ __forceinline__ void prefetch_row_l2(const AttnParams& p, const Item& it, int row, int hf) {
-  const uint16_t* src = p.q[it.r] + static_cast<int64_t>(it.qb * kQB + row) * p.ld_q[it.r] + it.h * kHd + hf * 64;
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
-}
-
 __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, uint32_t tmem_base, int warp,
                              int lane) {
   const int q = warp & 3;
@@ -491,16 +488,8 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
   float* xch = reinterpret_cast<float*>(smem + kOffXch);
   uint32_t g = 0, xuses = 0;
   const uint64_t c2 = pack2(p.scale_log2, p.scale_log2);
-  if (blockIdx.x < p.total_items) write_q(p, ctl, decode_item(p, blockIdx.x), lane_base, row, hf, lane);
   for (int i = blockIdx.x; i < p.total_items; i += gridDim.x) {
     const Item it = decode_item(p, i);
-    const int inext = i + static_cast<int>(gridDim.x);
-    const bool has_next = inext < p.total_items;
-    Item nx = it;
-    if (has_next) {
-      nx = decode_item(p, inext);
-      prefetch_row_l2(p, nx, row, hf);
-    }
     float m_ref = -INFINITY;
     int j = 0;
     const int nsteps = steps_of(p, it.r);
@@ -510,7 +499,7 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
       const bool diag_step = p.causal && t == 0;
       for (int kb = 0; kb < nb; ++kb, ++j) {
         const uint32_t gj = g + j;
-        const uint32_t sb = gj & 1u;  // S buffer of this block (P is written over it)
+        const uint32_t sb = gj & 1u;  // S buffer of this block
         const bool diag = diag_step && kb == it.qb;
         if (!warp_wait(&ctl->s_full[sb], (gj >> 1) & 1u, p, kSiteTmemFull, i, lane)) return;
         tc_fence_after();
@@ -573,18 +562,19 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
             rescale = true;
           }
           if (__any_sync(0xffffffffu, rescale)) {
-            load_scores(s);  // the scores are still in TMEM (P not yet written)
+            load_scores(s);  // the scores are still in TMEM (the buffer is not released yet)
             weights(s, m_ref, packed);
           }
         }
-        // The item's last scores are read: every score MMA of the item has completed, so
-        // the next item's Q can take the TMEM Q region now, ahead of this item's end.
-        if (j + 1 == n && has_next) write_q(p, ctl, nx, lane_base, row, hf, lane);
-        if (__any_sync(0xffffffffu, rescale)) {
-          // O must hold every earlier block (P.V of block gj - 1 complete) before it is rescaled
-          const uint32_t pb = (gj - 1) & 1u;
-          if (!warp_wait(&ctl->pv_done[pb], ((gj - 1) >> 1) & 1u, p, kSiteDrain, i, lane)) return;
-          tc_fence_after();
+        // the scores are read: the buffer may take the scores of block gj + 2
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->s_free[sb]);
+        // the previous block's P.V has read the P buffer and added into O (every block of
+        // this CTA goes through the one buffer; the first has no predecessor)
+        if (gj > 0 && !warp_wait(&ctl->pv_done, (gj - 1) & 1u, p, kSiteDrain, i, lane)) return;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, rescale)) {  // O holds every earlier block: rescale it
 #pragma unroll 1
           for (int c = 0; c < 2; ++c) {
             uint32_t v[32];
@@ -599,17 +589,17 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
             tmem_st1(lane_base + kSumCol, __float_as_uint(__uint_as_float(v) * alpha));
           }
         }
-        // P over the first half of this warp's (already read) score columns
-        tmem_st32(lane_base + sb * 128 + col0, packed);
+        // P: this warp's 64 keys as 32 fp16 pairs
+        tmem_st32(lane_base + kPCol + hf * 32, packed);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->p_full[sb]);
+        if (lane == 0) mbar_arrive(&ctl->p_full);
       }
     }
     // epilogue: O row / row sum -> bf16 (this warp's 64 columns)
     const uint32_t glast = g + j - 1;
-    if (!warp_wait(&ctl->pv_done[glast & 1u], (glast >> 1) & 1u, p, kSiteDrain, i, lane)) return;
+    if (!warp_wait(&ctl->pv_done, glast & 1u, p, kSiteDrain, i, lane)) return;
     tc_fence_after();
     const float inv = 1.f / __uint_as_float(tmem_ld1(lane_base + kSumCol));
     uint16_t* orow = p.out[it.r] + static_cast<int64_t>(it.qb * kQB + row) * p.ld_out[it.r] + it.h * kHd + col0;
@@ -639,7 +629,8 @@ __global__ void __maxnreg__(136) attn_kernel(const __grid_constant__ AttnParams 
   AttnCtl* ctl = reinterpret_cast<AttnCtl*>(smem + kOffCtl);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(&ctl->q_full, 8);
+    mbar_init(&ctl->q_full, 1);
+    mbar_init(&ctl->q_empty, 1);
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&ctl->k_full[s], 1);
       mbar_init(&ctl->k_empty[s], 1);
@@ -650,9 +641,10 @@ __global__ void __maxnreg__(136) attn_kernel(const __grid_constant__ AttnParams 
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&ctl->s_full[b], 1);
-      mbar_init(&ctl->p_full[b], 8);
-      mbar_init(&ctl->pv_done[b], 1);
+      mbar_init(&ctl->s_free[b], 8);
     }
+    mbar_init(&ctl->p_full, 8);
+    mbar_init(&ctl->pv_done, 1);
     for (int q = 0; q < 4; ++q)
       for (int b = 0; b < 2; ++b) mbar_init(&ctl->xchg[q][b], 2);
     mbar_init(&ctl->drain, 1);
@@ -660,7 +652,7 @@ __global__ void __maxnreg__(136) attn_kernel(const __grid_constant__ AttnParams 
     fence_proxy_async_shared();
   }
   if (warp == 0 && lane == 0)
-    for (int i = 0; i < 3 * p.P; ++i) tma_prefetch_desc(&p.maps[i]);
+    for (int i = 0; i < 4 * p.P; ++i) tma_prefetch_desc(&p.maps[i]);
   // the row-sum rows below every V^T stage half: row kHd all ones (fp16), the rest zero
   // (a row of equal 16-byte chunks is invariant under the 128-byte swizzle)
   for (int i = threadIdx.x; i < kVStages * 2 * 16 * 8; i += blockDim.x) {
@@ -795,8 +787,7 @@ fo_status attn_run(fo_ctx* ctx, const fo_mat* Q, const fo_mat* K, const fo_mat* 
     if ((st = host_encode_map(&p.maps[2 * P + r], vt_slot(r, 0), static_cast<int64_t>(P) * HD, m, m, kHd,
                               CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != FO_OK)
       return st;
-    p.q[r] = static_cast<const uint16_t*>(Q[r].ptr);
-    p.ld_q[r] = Q[r].ld;
+    if ((st = host_encode_map(&p.maps[3 * P + r], Q[r].ptr, m, HD, Q[r].ld, kQB)) != FO_OK) return st;
     p.out[r] = static_cast<uint16_t*>(O[r].ptr);
     p.ld_out[r] = O[r].ld;
   }

@@ -205,6 +205,13 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, void* dst, u
       : "memory");
 }
 
+// Pulls a tile of a tensor map into L2 (no shared memory, no completion signal).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t c0, int32_t c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(const CUtensorMap* map, void* dst, uint64_t* bar, int32_t c0,
                                             int32_t c1, int32_t c2) {
   asm volatile(
