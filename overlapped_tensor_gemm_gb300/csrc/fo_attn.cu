@@ -11,15 +11,18 @@
 // online-softmax state: row max and sum in registers, the output accumulator
 // in TMEM.
 //
-// CTA layout (320 threads, one CTA per SM):
-//   warp 0      TMA: the item's Q block into shared memory, K and V^T blocks in
-//               stage rings of three and two stages, K two blocks ahead of V;
-//               waits for the slice's arrival flag before reading it.
-//   warp 1      tcgen05.mma: S = Q K^T into one of two TMEM score buffers, then
-//               O += P V into the TMEM accumulator, P read from its own TMEM
-//               buffer.  A score buffer is free again as soon as the softmax
-//               warps have read it, so the scores of block j + 2 can be computed
-//               while block j's softmax still runs.
+// CTA layout (384 threads, one CTA per SM):
+//   warp 0      TMA: the item's Q block into shared memory and the K blocks
+//               into a ring of three stages; waits for the slice's arrival flag
+//               before reading it.
+//   warp 10     TMA: the V^T blocks into a ring of two stages, independently
+//               of the K walk (so neither load waits behind the other).
+//   warp 1      tcgen05.mma: S = Q K^T into one of two TMEM score buffers.  A
+//               score buffer is free again as soon as the softmax warps have
+//               read it, so the scores of block j + 2 can be computed while
+//               block j's softmax still runs.
+//   warp 11     tcgen05.mma: O += P V into the TMEM accumulator, P read from its
+//               own TMEM buffer.
 //   warps 2-9   softmax: two warps per query row (one per 64-key half); they
 //               load their half of the score row, mask the diagonal block,
 //               exchange the row maximum, update max/sum, release the score
@@ -49,10 +52,11 @@ namespace {
 constexpr int kHd = 128;                 // head_dim
 constexpr int kQB = 128;                 // queries per block
 constexpr int kKB = 128;                 // keys per block
-constexpr int kAttnThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 softmax
+// warp 0 TMA (Q, K), warp 1 score MMAs, warps 2-9 softmax, warp 10 TMA (V^T), warp 11 P.V MMAs
+constexpr int kAttnThreads = 384;
 constexpr uint32_t kTileBytes = 128 * 128 * 2;   // one 128x128 16-bit operand (two 64-column swizzle halves)
 constexpr uint32_t kHalfBytes = kTileBytes / 2;
-constexpr int kKStages = 3;              // K runs kKStages - 1 blocks ahead of V
+constexpr int kKStages = 3;
 constexpr int kVStages = 2;
 // The P.V MMA also produces the softmax row sums: every V^T stage carries 16 extra
 // rows below its 128 head dims, the first all ones and the rest zero (written once at
@@ -98,7 +102,7 @@ struct alignas(8) AttnCtl {
   uint64_t s_free[2];               // per S buffer: every softmax warp has read the scores
   uint64_t p_full;                  // one phase per block: P written
   uint64_t pv_done;                 // one phase per block: its P.V completed
-  uint64_t drain;
+  uint64_t drain, drain_pv;         // failure paths: the score / P.V issuer's MMAs have completed
   uint64_t xchg[4][2];   // per lane quadrant, two slots: the column halves' partial max / sum exchange
   uint32_t tmem_base;
   uint32_t pad;
@@ -116,7 +120,7 @@ static_assert(kOffQ % 1024 == 0, "the Q block must sit on a 1024-byte boundary (
 // its SM free: the ring's device-to-device copies may run as a small copy kernel
 // that must be able to start while the persistent grid occupies every SM.  The
 // register share of one SM sub-partition (16K) holds up to three of this
-// kernel's ten warps; the kernel is therefore kept at <= 136 registers per thread
+// kernel's twelve warps; the kernel is therefore kept at <= 136 registers per thread
 // (3 warps x 32 x 136 = 13056, leaving 3328), checked at context set-up.
 static_assert(kAttnSmem <= 232448 - 16 * 1024, "attention kernel must leave 16 KiB of shared memory free");
 
@@ -181,99 +185,88 @@ struct BlockIter {
   }
 };
 
-// K runs kKStages - 1 blocks ahead of V: a K stage is refilled as soon as the score MMA
-// that read it completes, a V stage once the P.V MMA that read it completes.
-__device__ void attn_producer(const AttnParams& p, uint8_t* smem, AttnCtl* ctl) {
-  int kst = 0, vst = 0;
-  uint32_t kph = 0, vph = 0;
-  uint32_t q_uses = 0;
-  bool q_armed = false;
+// The loads of one operand kind, each in its own thread so that neither waits behind the
+// other: the item's Q block and the K blocks (values = false), or the V^T blocks (values =
+// true).  A stage is refilled as soon as the MMA that read it completes; a slice is read
+// once its arrival flag is seen.
+__device__ void attn_producer(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, bool values) {
+  const int nst = values ? kVStages : kKStages;
+  uint64_t* const full = values ? ctl->v_full : ctl->k_full;
+  uint64_t* const empty = values ? ctl->v_empty : ctl->k_empty;
+  int st = 0;
+  uint32_t ph = 0, q_uses = 0, armed = 0, armed_ph = 0;
+  bool q_armed = false, ok = true;
   uint64_t seen = 0;  // bit r*P+s: arrival of slice s at rank r already observed
-  uint32_t karmed = 0, karmed_ph = 0, varmed = 0, varmed_ph = 0;
-  BlockIter kit, vit;
-  kit.start(p);
-  vit.start(p);
-  bool ok = true;
-  auto issue_k = [&]() -> bool {
-    const Item& it = kit.it;
-    const int s = slice_of(p, it.r, kit.t);
+  BlockIter bi;
+  bi.start(p);
+  while (ok && bi.valid(p)) {
+    const Item& it = bi.it;
+    const int s = slice_of(p, it.r, bi.t);
     const int fidx = it.r * p.P + s;
 #ifdef FO_DEBUG_BOUNDS
     // debug build: the item, its key block and its flag word lie inside the launch
-    if (!(it.r >= 0 && it.r < p.P && it.qb >= 0 && it.qb < p.nkb && it.h >= 0 && it.h < p.heads && kit.kb >= 0 &&
-          kit.kb < p.nkb && fidx >= 0 && fidx < p.flag_words && fidx < 64)) {
-      raise_error(p.ctrl, FO_ERR_INTERNAL, kSiteBounds, static_cast<uint32_t>(kit.i));
-      return false;
+    if (!(it.r >= 0 && it.r < p.P && it.qb >= 0 && it.qb < p.nkb && it.h >= 0 && it.h < p.heads && bi.kb >= 0 &&
+          bi.kb < p.nkb && fidx >= 0 && fidx < p.flag_words && fidx < 64)) {
+      raise_error(p.ctrl, FO_ERR_INTERNAL, kSiteBounds, static_cast<uint32_t>(bi.i));
+      ok = false;
+      break;
     }
 #endif
-    if (kit.t > 0 && p.wait_flags && !((seen >> fidx) & 1ull)) {
-      if (!flag_wait(p.flags + fidx, p.epoch, p.ctrl, p.timeout_ns, kSiteAttnFlag, fidx)) return false;
+    if (bi.t > 0 && p.wait_flags && !((seen >> fidx) & 1ull)) {
+      if (!flag_wait(p.flags + fidx, p.epoch, p.ctrl, p.timeout_ns, kSiteAttnFlag, fidx)) {
+        ok = false;
+        break;
+      }
       fence_proxy_async_global();
       seen |= 1ull << fidx;
     }
-    if (kit.t == 0 && kit.kb == 0) {
+    if (!values && bi.t == 0 && bi.kb == 0) {
       // the item's Q block, once the previous item's last score MMA has read the old one
-      if (!mbar_wait_fast(&ctl->q_empty, (q_uses & 1u) ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty, kit.i)) return false;
+      if (!mbar_wait_fast(&ctl->q_empty, (q_uses & 1u) ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty, bi.i)) {
+        ok = false;
+        break;
+      }
       mbar_arrive_expect_tx(&ctl->q_full, kTileBytes);
       for (int c = 0; c < 2; ++c)
         tma_load_2d(&p.maps[3 * p.P + it.r], smem + kOffQ + c * kHalfBytes, &ctl->q_full, it.h * kHd + c * 64,
                     it.qb * kQB);
       q_armed = true;
       ++q_uses;
-      const int inext = kit.i + static_cast<int>(gridDim.x);
+      const int inext = bi.i + static_cast<int>(gridDim.x);
       if (inext < p.total_items) {  // the next item's Q block into L2
         const Item nx = decode_item(p, inext);
         for (int c = 0; c < 2; ++c) tma_prefetch_l2_2d(&p.maps[3 * p.P + nx.r], nx.h * kHd + c * 64, nx.qb * kQB);
       }
     }
-    if (!mbar_wait_fast(&ctl->k_empty[kst], kph ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty, kit.i)) return false;
-    const CUtensorMap* kmap = kit.t == 0 ? &p.maps[it.r] : &p.maps[p.P + it.r];
-    const int krow0 = kit.t == 0 ? 0 : s * p.m;
-    uint8_t* kt = smem + kOffK + kst * kTileBytes;
-    mbar_arrive_expect_tx(&ctl->k_full[kst], kTileBytes);
-    for (int c = 0; c < 2; ++c)
-      tma_load_2d(kmap, kt + c * kHalfBytes, &ctl->k_full[kst], it.h * kHd + c * 64, krow0 + kit.kb * kKB);
-    karmed |= 1u << kst;
-    karmed_ph = (karmed_ph & ~(1u << kst)) | (kph << kst);
-    if (++kst == kKStages) {
-      kst = 0;
-      kph ^= 1u;
-    }
-    kit.next(p);
-    return true;
-  };
-  auto issue_v = [&]() -> bool {
-    const Item& it = vit.it;
-    const int s = slice_of(p, it.r, vit.t);  // arrival already observed by the K walk
-    if (!mbar_wait_fast(&ctl->v_empty[vst], vph ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty, vit.i)) return false;
-    uint8_t* vt = smem + kOffV + vst * kVStageBytes;
-    mbar_arrive_expect_tx(&ctl->v_full[vst], kTileBytes);  // the 128 head-dim rows of both key halves
-    for (int c = 0; c < 2; ++c)
-      tma_load_2d(&p.maps[2 * p.P + it.r], vt + c * kVHalfBytes, &ctl->v_full[vst], vit.kb * kKB + c * 64,
-                  (s * p.heads + it.h) * kHd);
-    varmed |= 1u << vst;
-    varmed_ph = (varmed_ph & ~(1u << vst)) | (vph << vst);
-    if (++vst == kVStages) {
-      vst = 0;
-      vph ^= 1u;
-    }
-    vit.next(p);
-    return true;
-  };
-  for (int a = 0; ok && a < kKStages - 1 && kit.valid(p); ++a) ok = issue_k();
-  while (ok && vit.valid(p)) {
-    if (kit.valid(p) && !issue_k()) {
+    if (!mbar_wait_fast(&empty[st], ph ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty, bi.i)) {
       ok = false;
       break;
     }
-    if (!issue_v()) ok = false;
+    mbar_arrive_expect_tx(&full[st], kTileBytes);  // V^T: the 128 head-dim rows of both key halves
+    if (values) {
+      uint8_t* vt = smem + kOffV + st * kVStageBytes;
+      for (int c = 0; c < 2; ++c)
+        tma_load_2d(&p.maps[2 * p.P + it.r], vt + c * kVHalfBytes, &full[st], bi.kb * kKB + c * 64,
+                    (s * p.heads + it.h) * kHd);
+    } else {
+      const CUtensorMap* kmap = bi.t == 0 ? &p.maps[it.r] : &p.maps[p.P + it.r];
+      const int krow0 = bi.t == 0 ? 0 : s * p.m;
+      uint8_t* kt = smem + kOffK + st * kTileBytes;
+      for (int c = 0; c < 2; ++c)
+        tma_load_2d(kmap, kt + c * kHalfBytes, &full[st], it.h * kHd + c * 64, krow0 + bi.kb * kKB);
+    }
+    armed |= 1u << st;
+    armed_ph = (armed_ph & ~(1u << st)) | (ph << st);
+    if (++st == nst) {
+      st = 0;
+      ph ^= 1u;
+    }
+    bi.next(p);
   }
   if (!ok) {
     if (q_armed) mbar_wait_drain(&ctl->q_full, (q_uses - 1) & 1u, kDrainNs);
-    for (int s = 0; s < kKStages; ++s)
-      if ((karmed >> s) & 1u) mbar_wait_drain(&ctl->k_full[s], (karmed_ph >> s) & 1u, kDrainNs);
-    for (int s = 0; s < kVStages; ++s)
-      if ((varmed >> s) & 1u) mbar_wait_drain(&ctl->v_full[s], (varmed_ph >> s) & 1u, kDrainNs);
+    for (int i = 0; i < nst; ++i)
+      if ((armed >> i) & 1u) mbar_wait_drain(&full[i], (armed_ph >> i) & 1u, kDrainNs);
   }
 }
 
@@ -323,19 +316,6 @@ __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
   tmem_wait_st();
 }
 
-// Non-blocking test of the phase of parity `parity`.
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // S buffer b of block gs may be overwritten once the softmax warps have read the scores
 // of block gs - 2 from it.
 __device__ __forceinline__ uint32_t s_free_parity(uint32_t gs) { return ((gs >> 1) & 1u) ^ 1u; }
@@ -357,69 +337,65 @@ struct MmaWalk {
   }
 };
 
-// Two independent walks over the CTA's key blocks: the score MMAs (block gs: its K stage
-// loaded, its S buffer released by the softmax of block gs - 2, the item's Q loaded) and
-// the P.V MMAs (block gp: its P written, its V stage loaded).  Each issues as soon as its
-// operands are ready, scores first when both are, so the scores of block j + 2 are
-// computed while the softmax of block j still runs.
-__device__ void attn_mma(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, uint32_t tmem_base) {
+// The score MMAs and the P.V MMAs are issued by two threads (warps 1 and 11).  An MMA
+// issue returns only about as fast as the tensor pipe accepts the instructions, so one
+// thread issuing both kinds would hold a ready P.V back behind the score MMAs it is still
+// issuing (measured: ~1,000 cycles per block).  Each thread's commits track its own MMAs.
+//
+// Scores: block gs once its K stage is loaded, its S buffer is released by the softmax of
+// block gs - 2 and (first block of an item) the item's Q block is loaded.
+__device__ void attn_mma_s(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, uint32_t tmem_base) {
   const uint32_t sbase = smem_u32(smem);
-  uint32_t q_uses = 0, gs = 0, gp = 0;  // items whose Q was waited for; score / P.V blocks issued
-  bool q_ready = false, issued = false, ok = true;
-  MmaWalk ws, wp;
-  ws.start(p);
-  wp.start(p);
-  uint64_t t0 = global_timer_ns();
-  for (uint32_t spin = 1; ok && wp.i < p.total_items; ++spin) {
-    bool progressed = false;
-    if (ws.i < p.total_items) {
-      if (ws.j == 0 && !q_ready && mbar_test(&ctl->q_full, q_uses & 1u)) {
-        q_ready = true;
-        ++q_uses;
-      }
-      const uint32_t st = gs % kKStages, sb = gs & 1u;
-      if ((ws.j > 0 || q_ready) && mbar_test(&ctl->k_full[st], (gs / kKStages) & 1u) &&
-          mbar_test(&ctl->s_free[sb], s_free_parity(gs))) {
-        tc_fence_after();
-        issue_s(tmem_base + sb * 128, sbase + kOffQ, sbase + kOffK + st * kTileBytes);
-        issued = true;
-        umma_commit(&ctl->k_empty[st]);  // the K stage is free once these scores are computed
-        umma_commit(&ctl->s_full[sb]);
-        if (ws.j + 1 == ws.n) {  // the item's last scores: its Q block may be replaced
-          umma_commit(&ctl->q_empty);
-          q_ready = false;
-        }
-        ++gs;
-        ws.next(p);
-        progressed = true;
-      }
+  uint32_t q_uses = 0, gs = 0;
+  bool issued = false, ok = true;
+  MmaWalk ws;
+  for (ws.start(p); ok && ws.i < p.total_items; ws.next(p), ++gs) {
+    const uint32_t st = gs % kKStages, sb = gs & 1u;
+    if (ws.j == 0) {
+      if (!mbar_wait_fast(&ctl->q_full, q_uses & 1u, p.ctrl, p.timeout_ns, kSiteFull, ws.i)) break;
+      ++q_uses;
     }
-    const uint32_t vs = gp % kVStages;
-    if (gp < gs && mbar_test(&ctl->p_full, gp & 1u) && mbar_test(&ctl->v_full[vs], (gp / kVStages) & 1u)) {
-      tc_fence_after();
-      issue_pv(tmem_base + kOCol, tmem_base + kPCol, sbase + kOffV + vs * kVStageBytes, wp.j == 0);
-      umma_commit(&ctl->v_empty[vs]);
-      umma_commit(&ctl->pv_done);
-      ++gp;
-      wp.next(p);
-      progressed = true;
+    if (!mbar_wait_fast(&ctl->k_full[st], (gs / kKStages) & 1u, p.ctrl, p.timeout_ns, kSiteFull, ws.i) ||
+        !mbar_wait_fast(&ctl->s_free[sb], s_free_parity(gs), p.ctrl, p.timeout_ns, kSiteTmemEmpty, ws.i)) {
+      ok = false;
+      break;
     }
-    if (progressed) {
-      t0 = 0;
-    } else if ((spin & 63u) == 0u) {
-      const uint64_t now = global_timer_ns();
-      if (t0 == 0) t0 = now;
-      if (aborted(p.ctrl)) {
-        ok = false;
-      } else if (now - t0 > p.timeout_ns) {
-        raise_error(p.ctrl, FO_ERR_TIMEOUT, gp < gs ? kSiteFull : kSiteTmemEmpty, static_cast<uint32_t>(wp.i));
-        ok = false;
-      }
-    }
+    tc_fence_after();
+    issue_s(tmem_base + sb * 128, sbase + kOffQ, sbase + kOffK + st * kTileBytes);
+    issued = true;
+    umma_commit(&ctl->k_empty[st]);  // the K stage is free once these scores are computed
+    umma_commit(&ctl->s_full[sb]);
+    if (ws.j + 1 == ws.n) umma_commit(&ctl->q_empty);  // the item's last scores: Q may be replaced
   }
+  if (ws.i < p.total_items) ok = false;
   if (!ok && issued) {
     umma_commit(&ctl->drain);
     mbar_wait_drain(&ctl->drain, 0, kDrainNs);
+  }
+}
+
+// P.V: block gp once its P is written and its V^T stage is loaded.
+__device__ void attn_mma_pv(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, uint32_t tmem_base) {
+  const uint32_t sbase = smem_u32(smem);
+  uint32_t gp = 0;
+  bool issued = false, ok = true;
+  MmaWalk wp;
+  for (wp.start(p); ok && wp.i < p.total_items; wp.next(p), ++gp) {
+    const uint32_t vs = gp % kVStages;
+    if (!mbar_wait_fast(&ctl->p_full, gp & 1u, p.ctrl, p.timeout_ns, kSiteFull, wp.i) ||
+        !mbar_wait_fast(&ctl->v_full[vs], (gp / kVStages) & 1u, p.ctrl, p.timeout_ns, kSiteFull, wp.i)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    issue_pv(tmem_base + kOCol, tmem_base + kPCol, sbase + kOffV + vs * kVStageBytes, wp.j == 0);
+    issued = true;
+    umma_commit(&ctl->v_empty[vs]);
+    umma_commit(&ctl->pv_done);
+  }
+  if (!ok && issued) {
+    umma_commit(&ctl->drain_pv);
+    mbar_wait_drain(&ctl->drain_pv, 0, kDrainNs);
   }
 }
 
@@ -648,6 +624,7 @@ __global__ void __maxnreg__(136) attn_kernel(const __grid_constant__ AttnParams 
     for (int q = 0; q < 4; ++q)
       for (int b = 0; b < 2; ++b) mbar_init(&ctl->xchg[q][b], 2);
     mbar_init(&ctl->drain, 1);
+    mbar_init(&ctl->drain_pv, 1);
     fence_barrier_init();
     fence_proxy_async_shared();
   }
@@ -670,10 +647,16 @@ __global__ void __maxnreg__(136) attn_kernel(const __grid_constant__ AttnParams 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
-  if (warp == 0) {
-    if (lane == 0) attn_producer(p, smem, ctl);
-  } else if (warp == 1) {
-    if (lane == 0) attn_mma(p, smem, ctl, tmem_base);
+  if (warp == 0 || warp == 10) {
+    if (lane == 0) attn_producer(p, smem, ctl, warp == 10);
+  } else if (warp == 1 || warp == 11) {
+    if (lane == 0) {
+      if (warp == 1) {
+        attn_mma_s(p, smem, ctl, tmem_base);
+      } else {
+        attn_mma_pv(p, smem, ctl, tmem_base);
+      }
+    }
     __syncwarp();
   } else {
     attn_softmax(p, smem, ctl, tmem_base, warp, lane);
