@@ -128,16 +128,19 @@ struct Item {
   int r, qb, h;
 };
 
-// Items in decreasing cost order: ranks with more visible slices first, then
-// groups of kHeadGroup heads, then later query blocks (longer causal rows), then
-// the heads of the group.  Grouping heads keeps the CTAs that run at the same time
-// on fewer heads' K/V blocks, which then stay in L2 for all their query blocks.
+// Item order: rank by rank from rank 0 (whose items need no received slice; with the
+// causal mask rank r's items need r hops, so while the lower ranks' items run the ring
+// delivers the slices the higher ranks need: measured 2.5% faster with the pruned ring,
+// 6.5% with the full ring, than starting with the most expensive rank), then groups of
+// kHeadGroup heads, then later query blocks (longer causal rows) first, then the heads
+// of the group.  Grouping heads keeps the CTAs that run at the same time on fewer heads'
+// K/V blocks, which then stay in L2 for all their query blocks.
 constexpr int kHeadGroup = 8;
 __device__ __forceinline__ Item decode_item(const AttnParams& p, int i) {
   const int per_rank = p.nkb * p.heads;
   const int grp = p.heads % kHeadGroup == 0 ? kHeadGroup : p.heads;
   Item it;
-  it.r = p.P - 1 - i / per_rank;
+  it.r = i / per_rank;
   const int rem = i % per_rank;
   const int in_grp = rem % (p.nkb * grp);
   it.qb = p.nkb - 1 - in_grp / grp;
