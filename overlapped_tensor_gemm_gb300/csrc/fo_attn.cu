@@ -75,6 +75,10 @@ constexpr uint32_t kIdescS = umma_idesc_bf16(128, 128);   // S = Q K^T, bf16 ope
 constexpr uint32_t kIdescO = umma_idesc_f16(128, kVRows); // [O | sums] += P [V | 1 0..0], fp16
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// Items are claimed in order from a launch-wide counter by the Q/K loading thread, which
+// hands each index to the other roles through a ring of kItemSlots in shared memory.
+constexpr int kItemSlots = 8;
+constexpr uint32_t kItemReaders = 1 + 1 + 1 + 8;  // V^T loader, score and P.V issuers, softmax warps
 
 struct AttnParams {
   CUtensorMap maps[4 * kMaxP];  // per rank r: K local = r, K received = P+r, V^T = 2P+r, Q = 3P+r
@@ -103,6 +107,9 @@ struct alignas(8) AttnCtl {
   uint64_t p_full;                  // one phase per block: P written
   uint64_t pv_done;                 // one phase per block: its P.V completed
   uint64_t drain, drain_pv;         // failure paths: the score / P.V issuer's MMAs have completed
+  uint64_t item_full[kItemSlots];   // the slot holds the CTA's next claimed item
+  uint64_t item_empty[kItemSlots];  // every reader has taken the slot's item
+  int32_t item[kItemSlots];
   uint64_t xchg[4][2];   // per lane quadrant, two slots: the column halves' partial max / sum exchange
   uint32_t tmem_base;
   uint32_t pad;
@@ -128,23 +135,42 @@ struct Item {
   int r, qb, h;
 };
 
-// Item order: rank by rank from rank 0 (whose items need no received slice; with the
-// causal mask rank r's items need r hops, so while the lower ranks' items run the ring
-// delivers the slices the higher ranks need: measured 2.5% faster with the pruned ring,
-// 6.5% with the full ring, than starting with the most expensive rank), then groups of
-// kHeadGroup heads, then later query blocks (longer causal rows) first, then the heads
-// of the group.  Grouping heads keeps the CTAs that run at the same time on fewer heads'
-// K/V blocks, which then stay in L2 for all their query blocks.
+// Item order (a position in the launch's claim order -> rank, query block, head).  Rank
+// r's items need the slices of r hops (causal mask), so the order starts with items that
+// need none: rank 0's query blocks of the upper half; then ranks 1 .. P-1 (while the lower
+// ranks' items run, the ring delivers the slices the higher ranks need: measured 2.5%
+// faster with the pruned ring, 6.5% with the full ring, than the most expensive rank
+// first); and ends with rank 0's short items, which fill the pairs' finishing times.
+// Within a segment: groups of kHeadGroup heads, later query blocks (longer causal rows)
+// first, then the heads of the group.  Grouping heads keeps the CTAs that run at the same
+// time on fewer heads' K/V blocks, which then stay in L2 for all their query blocks.
 constexpr int kHeadGroup = 8;
 __device__ __forceinline__ Item decode_item(const AttnParams& p, int i) {
-  const int per_rank = p.nkb * p.heads;
   const int grp = p.heads % kHeadGroup == 0 ? kHeadGroup : p.heads;
+  const int half = p.nkb / 2;  // rank 0's query blocks below this one come last
+  const int n_first = (p.nkb - half) * p.heads, n_mid = (p.P - 1) * p.nkb * p.heads;
   Item it;
-  it.r = i / per_rank;
-  const int rem = i % per_rank;
-  const int in_grp = rem % (p.nkb * grp);
-  it.qb = p.nkb - 1 - in_grp / grp;
-  it.h = rem / (p.nkb * grp) * grp + in_grp % grp;
+  int local, nq, qb0;
+  if (i < n_first) {
+    it.r = 0;
+    local = i;
+    nq = p.nkb - half;
+    qb0 = half;
+  } else if (i < n_first + n_mid) {
+    const int j = i - n_first;
+    it.r = 1 + j / (p.nkb * p.heads);
+    local = j % (p.nkb * p.heads);
+    nq = p.nkb;
+    qb0 = 0;
+  } else {
+    it.r = 0;
+    local = i - n_first - n_mid;
+    nq = half;
+    qb0 = 0;
+  }
+  const int in_grp = local % (nq * grp);
+  it.qb = qb0 + nq - 1 - in_grp / grp;
+  it.h = local / (nq * grp) * grp + in_grp % grp;
   return it;
 }
 
@@ -159,32 +185,60 @@ __device__ __forceinline__ int item_blocks(const AttnParams& p, const Item& it) 
 
 // ---------------------------------------------------------------------------
 
-// Walks this CTA's key blocks in schedule order: items (stride gridDim.x), ring
-// steps (local slice first), 128-key blocks.
+// The CTA's k-th claimed item (total_items or more: none left), or -1 when the wait gave
+// up.  Called by one thread, or (kWarp) by a whole warp whose lane 0 waits, reads and
+// frees the slot and passes the index to the other lanes.
+template <bool kWarp>
+__device__ __forceinline__ int item_take(const AttnParams& p, AttnCtl* ctl, int k, int lane) {
+  int item = -1;
+  if (!kWarp || lane == 0) {
+    const int slot = k & (kItemSlots - 1);
+    if (mbar_wait_fast(&ctl->item_full[slot], static_cast<uint32_t>(k / kItemSlots) & 1u, p.ctrl, p.timeout_ns,
+                       kSiteSched, static_cast<uint32_t>(k))) {
+      item = *static_cast<volatile int32_t*>(&ctl->item[slot]);
+      mbar_arrive(&ctl->item_empty[slot]);
+    }
+  }
+  if (kWarp) item = __shfl_sync(0xffffffffu, item, 0);
+  return item;
+}
+
+// The Q/K loading thread's side: publishes the CTA's k-th item once every reader has taken
+// the slot's previous one.  False when the wait gave up.
+__device__ __forceinline__ bool item_put(const AttnParams& p, AttnCtl* ctl, int k, int item) {
+  const int slot = k & (kItemSlots - 1);
+  if (!mbar_wait_fast(&ctl->item_empty[slot], (static_cast<uint32_t>(k / kItemSlots) & 1u) ^ 1u, p.ctrl,
+                      p.timeout_ns, kSiteSched, static_cast<uint32_t>(k)))
+    return false;
+  ctl->item[slot] = item;
+  mbar_arrive(&ctl->item_full[slot]);
+  return true;
+}
+
+// Walks one role's key blocks in schedule order: the CTA's items in claim order, ring steps
+// (local slice first), 128-key blocks.  begin() takes the next item index; step() returns
+// true once the item's last block has been passed.
 struct BlockIter {
   int i, t, kb, nsteps, nb;
   Item it;
-  __device__ void start(const AttnParams& p) {
-    i = blockIdx.x;
+  __device__ void begin(const AttnParams& p, int item) {
+    i = item;
     t = kb = 0;
-    if (i < p.total_items) load(p);
+    if (valid(p)) {
+      it = decode_item(p, i);
+      nsteps = steps_of(p, it.r);
+      nb = blocks_of(p, it, 0);
+    }
   }
-  __device__ void load(const AttnParams& p) {
-    it = decode_item(p, i);
-    nsteps = steps_of(p, it.r);
-    nb = blocks_of(p, it, 0);
-  }
-  __device__ bool valid(const AttnParams& p) const { return i < p.total_items; }
-  __device__ void next(const AttnParams& p) {
-    if (++kb < nb) return;
+  __device__ bool valid(const AttnParams& p) const { return i >= 0 && i < p.total_items; }
+  __device__ bool step(const AttnParams& p) {
+    if (++kb < nb) return false;
     kb = 0;
     if (++t < nsteps) {
       nb = blocks_of(p, it, t);
-      return;
+      return false;
     }
-    t = 0;
-    i += gridDim.x;
-    if (i < p.total_items) load(p);
+    return true;
   }
 };
 
@@ -200,8 +254,23 @@ __device__ void attn_producer(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, 
   uint32_t ph = 0, q_uses = 0, armed = 0, armed_ph = 0;
   bool q_armed = false, ok = true;
   uint64_t seen = 0;  // bit r*P+s: arrival of slice s at rank r already observed
+  uint32_t* const counter = p.ctrl + kCtrlItems;
+  int k = 0, next = 0;  // the item sequence number; (Q/K thread) the claim for the next item
+  // Q/K thread: claims an item and publishes it; the launch's last claim (every CTA claims
+  // exactly one index past the end) resets the counter for the next launch on the stream
+  auto claim = [&](int kk, int item) -> int {
+    if (!item_put(p, ctl, kk, item)) return -1;
+    if (item == p.total_items + static_cast<int>(gridDim.x) - 1) atomicExch(counter, 0u);
+    if (item < p.total_items) next = static_cast<int>(atomicAdd(counter, 1u));
+    return item;
+  };
   BlockIter bi;
-  bi.start(p);
+  if (values) {
+    bi.begin(p, item_take<false>(p, ctl, 0, 0));
+  } else {
+    bi.begin(p, claim(0, static_cast<int>(atomicAdd(counter, 1u))));
+  }
+  if (bi.i < 0) ok = false;
   while (ok && bi.valid(p)) {
     const Item& it = bi.it;
     const int s = slice_of(p, it.r, bi.t);
@@ -235,11 +304,6 @@ __device__ void attn_producer(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, 
                     it.qb * kQB);
       q_armed = true;
       ++q_uses;
-      const int inext = bi.i + static_cast<int>(gridDim.x);
-      if (inext < p.total_items) {  // the next item's Q block into L2
-        const Item nx = decode_item(p, inext);
-        for (int c = 0; c < 2; ++c) tma_prefetch_l2_2d(&p.maps[3 * p.P + nx.r], nx.h * kHd + c * 64, nx.qb * kQB);
-      }
     }
     if (!mbar_wait_fast(&empty[st], ph ^ 1u, p.ctrl, p.timeout_ns, kSiteEmpty, bi.i)) {
       ok = false;
@@ -258,13 +322,22 @@ __device__ void attn_producer(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, 
       for (int c = 0; c < 2; ++c)
         tma_load_2d(kmap, kt + c * kHalfBytes, &full[st], it.h * kHd + c * 64, krow0 + bi.kb * kKB);
     }
+    if (!values && bi.t == 0 && bi.kb == (bi.nb > 1 ? 1 : 0) && next < p.total_items) {
+      // the next item's Q block into L2 (after the item's second load: its claim has returned by then)
+      const Item nx = decode_item(p, next);
+      for (int c = 0; c < 2; ++c) tma_prefetch_l2_2d(&p.maps[3 * p.P + nx.r], nx.h * kHd + c * 64, nx.qb * kQB);
+    }
     armed |= 1u << st;
     armed_ph = (armed_ph & ~(1u << st)) | (ph << st);
     if (++st == nst) {
       st = 0;
       ph ^= 1u;
     }
-    bi.next(p);
+    if (bi.step(p)) {
+      ++k;
+      bi.begin(p, values ? item_take<false>(p, ctl, k, 0) : claim(k, next));
+      if (bi.i < 0) ok = false;
+    }
   }
   if (!ok) {
     if (q_armed) mbar_wait_drain(&ctl->q_full, (q_uses - 1) & 1u, kDrainNs);
@@ -323,21 +396,25 @@ __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
 // of block gs - 2 from it.
 __device__ __forceinline__ uint32_t s_free_parity(uint32_t gs) { return ((gs >> 1) & 1u) ^ 1u; }
 
-// This CTA's key blocks in schedule order, for one kind of MMA: item i (stride
-// gridDim.x), block j of its n blocks.
+// This CTA's key blocks in schedule order, for one kind of MMA: its k-th claimed item i
+// (-1: the wait for it gave up), block j of its n blocks.
 struct MmaWalk {
-  int i, j, n;
-  __device__ void start(const AttnParams& p) {
-    i = blockIdx.x;
+  int i, j, n, k;
+  __device__ void take(const AttnParams& p, AttnCtl* ctl) {
+    i = item_take<false>(p, ctl, k, 0);
     j = 0;
-    n = i < p.total_items ? item_blocks(p, decode_item(p, i)) : 0;
+    n = i >= 0 && i < p.total_items ? item_blocks(p, decode_item(p, i)) : 0;
   }
-  __device__ void next(const AttnParams& p) {
+  __device__ void start(const AttnParams& p, AttnCtl* ctl) {
+    k = 0;
+    take(p, ctl);
+  }
+  __device__ void next(const AttnParams& p, AttnCtl* ctl) {
     if (++j < n) return;
-    j = 0;
-    i += gridDim.x;
-    n = i < p.total_items ? item_blocks(p, decode_item(p, i)) : 0;
+    ++k;
+    take(p, ctl);
   }
+  __device__ bool valid(const AttnParams& p) const { return i >= 0 && i < p.total_items; }
 };
 
 // The score MMAs and the P.V MMAs are issued by two threads (warps 1 and 11).  An MMA
@@ -352,7 +429,7 @@ __device__ void attn_mma_s(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, uin
   uint32_t q_uses = 0, gs = 0;
   bool issued = false, ok = true;
   MmaWalk ws;
-  for (ws.start(p); ok && ws.i < p.total_items; ws.next(p), ++gs) {
+  for (ws.start(p, ctl); ok && ws.valid(p); ws.next(p, ctl), ++gs) {
     const uint32_t st = gs % kKStages, sb = gs & 1u;
     if (ws.j == 0) {
       if (!mbar_wait_fast(&ctl->q_full, q_uses & 1u, p.ctrl, p.timeout_ns, kSiteFull, ws.i)) break;
@@ -370,7 +447,7 @@ __device__ void attn_mma_s(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, uin
     umma_commit(&ctl->s_full[sb]);
     if (ws.j + 1 == ws.n) umma_commit(&ctl->q_empty);  // the item's last scores: Q may be replaced
   }
-  if (ws.i < p.total_items) ok = false;
+  if (ws.i < 0 || ws.valid(p)) ok = false;
   if (!ok && issued) {
     umma_commit(&ctl->drain);
     mbar_wait_drain(&ctl->drain, 0, kDrainNs);
@@ -383,7 +460,7 @@ __device__ void attn_mma_pv(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, ui
   uint32_t gp = 0;
   bool issued = false, ok = true;
   MmaWalk wp;
-  for (wp.start(p); ok && wp.i < p.total_items; wp.next(p), ++gp) {
+  for (wp.start(p, ctl); ok && wp.valid(p); wp.next(p, ctl), ++gp) {
     const uint32_t vs = gp % kVStages;
     if (!mbar_wait_fast(&ctl->p_full, gp & 1u, p.ctrl, p.timeout_ns, kSiteFull, wp.i) ||
         !mbar_wait_fast(&ctl->v_full[vs], (gp / kVStages) & 1u, p.ctrl, p.timeout_ns, kSiteFull, wp.i)) {
@@ -396,6 +473,7 @@ __device__ void attn_mma_pv(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, ui
     umma_commit(&ctl->v_empty[vs]);
     umma_commit(&ctl->pv_done);
   }
+  if (wp.i < 0) ok = false;
   if (!ok && issued) {
     umma_commit(&ctl->drain_pv);
     mbar_wait_drain(&ctl->drain_pv, 0, kDrainNs);
@@ -467,7 +545,9 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
   float* xch = reinterpret_cast<float*>(smem + kOffXch);
   uint32_t g = 0, xuses = 0;
   const uint64_t c2 = pack2(p.scale_log2, p.scale_log2);
-  for (int i = blockIdx.x; i < p.total_items; i += gridDim.x) {
+  for (int k = 0;; ++k) {
+    const int i = item_take<true>(p, ctl, k, lane);
+    if (i < 0 || i >= p.total_items) break;
     const Item it = decode_item(p, i);
     float m_ref = -INFINITY;
     int j = 0;
@@ -628,6 +708,10 @@ __global__ void __maxnreg__(136) attn_kernel(const __grid_constant__ AttnParams 
       for (int b = 0; b < 2; ++b) mbar_init(&ctl->xchg[q][b], 2);
     mbar_init(&ctl->drain, 1);
     mbar_init(&ctl->drain_pv, 1);
+    for (int s = 0; s < kItemSlots; ++s) {
+      mbar_init(&ctl->item_full[s], 1);
+      mbar_init(&ctl->item_empty[s], kItemReaders);
+    }
     fence_barrier_init();
     fence_proxy_async_shared();
   }

@@ -169,6 +169,7 @@ enum CtrlWord : int {
   kCtrlDetail = 3,    // flag index / tile index of the first timeout
   kCtrlTiles = 4,     // SM-pair GEMM: the next unclaimed tile of the running launch (zero
                       // between launches: the launch's last claim resets it)
+  kCtrlItems = 5,     // attention: the next unclaimed item of the running launch (likewise)
   kCtrlWords = 8
 };
 
