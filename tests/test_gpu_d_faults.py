@@ -57,6 +57,14 @@ def test_skipped_kv_hop_times_out_in_attention(m):
         ctx.qsplit_attn(Q, K, V, O, heads=H, head_dim=128)
         torch.cuda.synchronize()
         ctx.poll()
+    # the recovered context computes what a fresh one does (every item of the launch ran)
+    O2 = [torch.zeros((m, 128), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    with fo.Context(0) as ctx2:
+        ctx2.qsplit_attn(Q, K, V, O2, heads=H, head_dim=128)
+        torch.cuda.synchronize()
+        ctx2.poll()
+    for r in range(P):
+        assert torch.equal(O[r].view(torch.int16), O2[r].view(torch.int16)), f"attention after recovery, rank {r}"
 
 
 def test_skipped_all_to_all_hop_times_out_and_context_recovers():
