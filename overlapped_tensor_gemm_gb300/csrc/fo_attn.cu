@@ -21,15 +21,17 @@
 //               score buffer is free again as soon as the softmax warps have
 //               read it, so the scores of block j + 2 can be computed while
 //               block j's softmax still runs.
-//   warp 11     tcgen05.mma: O += P V into the TMEM accumulator, P read from its
-//               own TMEM buffer.
+//   warp 11     tcgen05.mma: O += P V into the TMEM accumulator, P read from one
+//               of two TMEM P buffers.
 //   warps 2-9   softmax: two warps per query row (one per 64-key half); they
 //               load their half of the score row, mask the diagonal block,
-//               exchange the row maximum, update max/sum, release the score
-//               buffer, rescale their half of the O row only when the max grew
-//               by more than 2^8 (the final division by the sum uses the same
-//               reference max, so this is exact), and write P as fp16 into the
-//               P buffer once the previous block's P.V has read it.
+//               exchange the row maximum, release the score buffer, keep their
+//               half of the row sum in registers, rescale their half of the O row
+//               only when the max grew by more than 2^8 (the final division by the
+//               sum uses the same reference max, so this is exact), and write P
+//               as fp16 into the block's P buffer once the P.V of two blocks
+//               earlier has read it; at the item's end the two halves of the row
+//               sum are added.
 // V is transposed once per rank (V^T [heads*128, tokens]) before the ring so
 // that both MMAs read K-major operands.  The P.V product runs in fp16: the
 // transpose converts V's bf16 values to fp16 (exact for |v| within fp16's
@@ -58,21 +60,17 @@ constexpr uint32_t kTileBytes = 128 * 128 * 2;   // one 128x128 16-bit operand (
 constexpr uint32_t kHalfBytes = kTileBytes / 2;
 constexpr int kKStages = 3;
 constexpr int kVStages = 2;
-// The P.V MMA also produces the softmax row sums: every V^T stage carries 16 extra
-// rows below its 128 head dims, the first all ones and the rest zero (written once at
-// start, never overwritten by the loads), so O gains 16 columns whose first is
-// sum_j P_ij, accumulated and rescaled exactly like the output itself.
-constexpr int kVRows = kHd + 16;
-constexpr uint32_t kVHalfBytes = kVRows * 128;           // [144 rows x 64 keys] swizzled
+constexpr uint32_t kVHalfBytes = kHd * 128;             // [128 head dims x 64 keys] swizzled
 constexpr uint32_t kVStageBytes = 2 * kVHalfBytes;
-// TMEM: S0 [0,128), S1 [128,256), O [256,400) (column 384 = row sum), P [400,464):
-// keys 64h + 2c, 64h + 2c + 1 of a block as one fp16 pair in column 400 + 32h + c.
+// TMEM: S0 [0,128), S1 [128,256), O [256,384), P0 [384,448), P1 [448,512).  Block j writes
+// its P into buffer j & 1: keys 64h + 2c, 64h + 2c + 1 as one fp16 pair in column
+// 384 + 64 (j & 1) + 32h + c.  Two P buffers let block j + 1's softmax write its P while
+// block j's P.V still reads the other one.
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 256;
-constexpr uint32_t kSumCol = kOCol + kHd;
-constexpr uint32_t kPCol = 400;
+constexpr uint32_t kPCol = 384;
 constexpr uint32_t kIdescS = umma_idesc_bf16(128, 128);   // S = Q K^T, bf16 operands
-constexpr uint32_t kIdescO = umma_idesc_f16(128, kVRows); // [O | sums] += P [V | 1 0..0], fp16
+constexpr uint32_t kIdescO = umma_idesc_f16(128, kHd);    // O += P V, fp16
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // Items are claimed in order from a launch-wide counter by the Q/K loading thread, which
@@ -104,8 +102,8 @@ struct alignas(8) AttnCtl {
   uint64_t v_full[kVStages], v_empty[kVStages];
   uint64_t s_full[2];               // per S buffer: scores computed
   uint64_t s_free[2];               // per S buffer: every softmax warp has read the scores
-  uint64_t p_full;                  // one phase per block: P written
-  uint64_t pv_done;                 // one phase per block: its P.V completed
+  uint64_t p_full[2];               // per P buffer: P written
+  uint64_t pv_done[2];              // per P buffer: the P.V that read it completed
   uint64_t drain, drain_pv;         // failure paths: the score / P.V issuer's MMAs have completed
   uint64_t item_full[kItemSlots];   // the slot holds the CTA's next claimed item
   uint64_t item_empty[kItemSlots];  // every reader has taken the slot's item
@@ -369,27 +367,14 @@ __device__ __forceinline__ void issue_s(uint32_t tmem_s, uint32_t q_addr, uint32
   }
 }
 
-// [O | sums] += P [V | 1 0..0] for one 128-key block: P from its TMEM buffer (keys 64h + 2c,
-// 64h + 2c + 1 in column 32h + c), V^T (and the ones row) from the two 64-key swizzle
-// halves of the stage.
+// O += P V for one 128-key block: P from its TMEM buffer (keys 64h + 2c, 64h + 2c + 1 in
+// column 32h + c), V^T from the two 64-key swizzle halves of the stage.
 __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr, bool first) {
 #pragma unroll
   for (int k = 0; k < kKB / 16; ++k) {
     const uint32_t off = (k >> 2) * kVHalfBytes + (k & 3) * 32;
     umma_ts(tmem_o, tmem_p + k * 8, umma_sdesc_sw128(v_addr + off), kIdescO, (first && k == 0) ? 0u : 1u);
   }
-}
-
-// One 32-bit TMEM column of this warp's 32 lanes (load waits for completion; store does too).
-__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
-  uint32_t v;
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v) : "r"(taddr) : "memory");
-  tmem_wait_ld();
-  return v;
-}
-__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
-  tmem_wait_st();
 }
 
 // S buffer b of block gs may be overwritten once the softmax warps have read the scores
@@ -462,16 +447,16 @@ __device__ void attn_mma_pv(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, ui
   MmaWalk wp;
   for (wp.start(p, ctl); ok && wp.valid(p); wp.next(p, ctl), ++gp) {
     const uint32_t vs = gp % kVStages;
-    if (!mbar_wait_fast(&ctl->p_full, gp & 1u, p.ctrl, p.timeout_ns, kSiteFull, wp.i) ||
+    if (!mbar_wait_fast(&ctl->p_full[gp & 1u], (gp >> 1) & 1u, p.ctrl, p.timeout_ns, kSiteFull, wp.i) ||
         !mbar_wait_fast(&ctl->v_full[vs], (gp / kVStages) & 1u, p.ctrl, p.timeout_ns, kSiteFull, wp.i)) {
       ok = false;
       break;
     }
     tc_fence_after();
-    issue_pv(tmem_base + kOCol, tmem_base + kPCol, sbase + kOffV + vs * kVStageBytes, wp.j == 0);
+    issue_pv(tmem_base + kOCol, tmem_base + kPCol + (gp & 1u) * 64, sbase + kOffV + vs * kVStageBytes, wp.j == 0);
     issued = true;
     umma_commit(&ctl->v_empty[vs]);
-    umma_commit(&ctl->pv_done);
+    umma_commit(&ctl->pv_done[gp & 1u]);
   }
   if (wp.i < 0) ok = false;
   if (!ok && issued) {
@@ -500,6 +485,11 @@ __device__ __forceinline__ void unpack2(uint64_t x, float& lo, float& hi) {
 __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t r;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -550,6 +540,7 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
     if (i < 0 || i >= p.total_items) break;
     const Item it = decode_item(p, i);
     float m_ref = -INFINITY;
+    uint64_t lsum = pack2(0.f, 0.f);  // this warp's part of the row sum, in two lanes of a pair
     int j = 0;
     const int nsteps = steps_of(p, it.r);
     const int n = item_blocks(p, it);
@@ -579,15 +570,18 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
               if (static_cast<int>(col0) + k > row) s[k] = -INFINITY;
           }
         };
-        // p = 2^(s * scale - m): one packed FMA per pair, ex2 per weight (the row sums
-        // come out of the P.V MMA)
-        auto weights = [&](const float (&s)[64], float m, uint32_t (&packed)[32]) {
+        // p = 2^(s * scale - m): one packed FMA per pair, ex2 per weight; the block's sum of
+        // this warp's weights in packed pairs
+        auto weights = [&](const float (&s)[64], float m, uint32_t (&packed)[32], uint64_t& bsum) {
           const uint64_t nm2 = pack2(-m, -m);
+          bsum = pack2(0.f, 0.f);
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
             float x0, x1;
             unpack2(ffma2(pack2(s[2 * k], s[2 * k + 1]), c2, nm2), x0, x1);
-            packed[k] = pack_f16x2(fast_exp2(x0), fast_exp2(x1));
+            const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+            packed[k] = pack_f16x2(e0, e1);
+            bsum = fadd2(bsum, pack2(e0, e1));
           }
         };
         float s[64];
@@ -605,14 +599,15 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
         xch_publish(ctl, xch, xuses, q, hf, row, mx, lane);
         float other;
         uint32_t packed[32];
+        uint64_t bsum;
         bool rescale = false;
         float alpha = 1.f;
         if (j == 0) {
           if (!xch_collect(ctl, xch, xuses, q, hf, row, &other, p, lane, i)) return;
           m_ref = fmaxf(mx, other) * p.scale_log2;  // block 0 holds key 0 <= every query: finite
-          weights(s, m_ref, packed);
+          weights(s, m_ref, packed, bsum);
         } else {
-          weights(s, m_ref, packed);
+          weights(s, m_ref, packed, bsum);
           if (!xch_collect(ctl, xch, xuses, q, hf, row, &other, p, lane, i)) return;
           const float bm = fmaxf(mx, other) * p.scale_log2;
           if (bm > m_ref + kRescaleThreshold) {
@@ -622,18 +617,20 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
           }
           if (__any_sync(0xffffffffu, rescale)) {
             load_scores(s);  // the scores are still in TMEM (the buffer is not released yet)
-            weights(s, m_ref, packed);
+            weights(s, m_ref, packed, bsum);
           }
         }
+        // this warp's part of the row sum: earlier blocks rescaled like O, plus this block
+        lsum = fadd2(ffma2(lsum, pack2(alpha, alpha), pack2(0.f, 0.f)), bsum);
         // the scores are read: the buffer may take the scores of block gj + 2
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->s_free[sb]);
-        // the previous block's P.V has read the P buffer and added into O (every block of
-        // this CTA goes through the one buffer; the first has no predecessor)
-        if (gj > 0 && !warp_wait(&ctl->pv_done, (gj - 1) & 1u, p, kSiteDrain, i, lane)) return;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, rescale)) {  // O holds every earlier block: rescale it
+        const uint32_t pb = gj & 1u;  // P buffer of this block
+        if (__any_sync(0xffffffffu, rescale)) {
+          // O must hold every earlier block (P.V of block gj - 1 complete) before it is rescaled
+          if (gj > 0 && !warp_wait(&ctl->pv_done[pb ^ 1u], ((gj - 1) >> 1) & 1u, p, kSiteDrain, i, lane)) return;
+          tc_fence_after();
 #pragma unroll 1
           for (int c = 0; c < 2; ++c) {
             uint32_t v[32];
@@ -643,24 +640,28 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
             for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
             tmem_st32(lane_base + kOCol + col0 + c * 32, v);
           }
-          if (hf == 1) {  // and the row-sum column
-            const uint32_t v = tmem_ld1(lane_base + kSumCol);
-            tmem_st1(lane_base + kSumCol, __float_as_uint(__uint_as_float(v) * alpha));
-          }
         }
+        // the P buffer's previous block (gj - 2) has been read by its P.V
+        if (!warp_wait(&ctl->pv_done[pb], s_free_parity(gj), p, kSiteDrain, i, lane)) return;
+        tc_fence_after();
         // P: this warp's 64 keys as 32 fp16 pairs
-        tmem_st32(lane_base + kPCol + hf * 32, packed);
+        tmem_st32(lane_base + kPCol + pb * 64 + hf * 32, packed);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->p_full);
+        if (lane == 0) mbar_arrive(&ctl->p_full[pb]);
       }
     }
-    // epilogue: O row / row sum -> bf16 (this warp's 64 columns)
+    // epilogue: O row / row sum -> bf16 (this warp's 64 columns); the row sum is this
+    // warp's part plus the partner warp's
+    float lo, hi, other_sum;
+    unpack2(lsum, lo, hi);
+    xch_publish(ctl, xch, xuses, q, hf, row, lo + hi, lane);
+    if (!xch_collect(ctl, xch, xuses, q, hf, row, &other_sum, p, lane, i)) return;
     const uint32_t glast = g + j - 1;
-    if (!warp_wait(&ctl->pv_done, glast & 1u, p, kSiteDrain, i, lane)) return;
+    if (!warp_wait(&ctl->pv_done[glast & 1u], (glast >> 1) & 1u, p, kSiteDrain, i, lane)) return;
     tc_fence_after();
-    const float inv = 1.f / __uint_as_float(tmem_ld1(lane_base + kSumCol));
+    const float inv = 1.f / (hf == 0 ? (lo + hi) + other_sum : other_sum + (lo + hi));
     uint16_t* orow = p.out[it.r] + static_cast<int64_t>(it.qb * kQB + row) * p.ld_out[it.r] + it.h * kHd + col0;
 #pragma unroll 1
     for (int c = 0; c < 2; ++c) {
@@ -702,8 +703,10 @@ __global__ void __maxnreg__(136) attn_kernel(const __grid_constant__ AttnParams 
       mbar_init(&ctl->s_full[b], 1);
       mbar_init(&ctl->s_free[b], 8);
     }
-    mbar_init(&ctl->p_full, 8);
-    mbar_init(&ctl->pv_done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&ctl->p_full[b], 8);
+      mbar_init(&ctl->pv_done[b], 1);
+    }
     for (int q = 0; q < 4; ++q)
       for (int b = 0; b < 2; ++b) mbar_init(&ctl->xchg[q][b], 2);
     mbar_init(&ctl->drain, 1);
@@ -717,14 +720,6 @@ __global__ void __maxnreg__(136) attn_kernel(const __grid_constant__ AttnParams 
   }
   if (warp == 0 && lane == 0)
     for (int i = 0; i < 4 * p.P; ++i) tma_prefetch_desc(&p.maps[i]);
-  // the row-sum rows below every V^T stage half: row kHd all ones (fp16), the rest zero
-  // (a row of equal 16-byte chunks is invariant under the 128-byte swizzle)
-  for (int i = threadIdx.x; i < kVStages * 2 * 16 * 8; i += blockDim.x) {
-    const int chunk = i & 7, rrow = (i >> 3) & 15, half = i >> 7;
-    const uint32_t v = rrow == 0 ? 0x3C003C00u : 0u;
-    *reinterpret_cast<uint4*>(smem + kOffV + half * kVHalfBytes + (kHd + rrow) * 128 + chunk * 16) =
-        make_uint4(v, v, v, v);
-  }
   fence_proxy_async_shared();
   if (warp == 1) {
     tmem_alloc(&ctl->tmem_base, kTmemCols);
