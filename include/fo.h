@@ -147,7 +147,11 @@ FO_API fo_status fo_ctx_destroy(fo_ctx* ctx);
 /* Reads the device error word after the caller has synchronised the stream of
  * the previous calls, and clears it.  FO_OK; FO_ERR_TIMEOUT when a device wait
  * gave up (the work of that call is then incomplete); FO_ERR_RANGE when an input
- * held a value the kernels cannot represent (see fo_qsplit_attn). */
+ * held a value the kernels cannot represent (see fo_qsplit_attn).  After a
+ * FO_ERR_TIMEOUT, call this before the next call on the context: until then the
+ * device keeps the failure's abort word set (later kernels leave their loops at
+ * once) and the launch-wide work counters of the failed launch uncleared; this
+ * call clears the whole control block. */
 FO_API fo_status fo_ctx_poll(fo_ctx* ctx);
 
 /* Device milliseconds of the two phases of the last FO_ORDER_SERIAL call on
