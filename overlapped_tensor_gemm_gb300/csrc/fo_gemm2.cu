@@ -293,7 +293,7 @@ __device__ void pair_mma(const GemmParams& p, uint8_t* tiles, PairCtl* ctl, uint
   }
 }
 
-template <bool TN>
+template <bool TN, bool kRows>
 __device__ void pair_epilogue(const GemmParams& p, PairCtl* ctl, uint32_t tmem_base, uint32_t cta, int warp,
                               int lane, float* stage) {
   const int q = warp & 3;
@@ -314,7 +314,7 @@ __device__ void pair_epilogue(const GemmParams& p, PairCtl* ctl, uint32_t tmem_b
         mbar_arrive_cluster(leader_tmem_empty + acc * static_cast<uint32_t>(sizeof(uint64_t)));
       }
     };
-    if (!epilogue_tile<TN>(p, tc, tile, &ctl->tmem_full[acc], acc_phase, tbase, static_cast<int>(cta), 2, q, lane, stage,
+    if (!epilogue_tile<TN, kRows>(p, tc, tile, &ctl->tmem_full[acc], acc_phase, tbase, static_cast<int>(cta), 2, q, lane, stage,
                        arrive_empty))
       return;
     acc ^= 1;
@@ -322,7 +322,10 @@ __device__ void pair_epilogue(const GemmParams& p, PairCtl* ctl, uint32_t tmem_b
   }
 }
 
-template <bool TN>
+// TN: transposed reduce-scatter tiles; kRows: the lane-per-row partial-sum epilogue
+// (GemmParams::row_epilogue, step-ordered tiles only).  Each combination is its own
+// instantiation, with its own register count.
+template <bool TN, bool kRows>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_pair_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = smem_u32(smem_raw);
@@ -379,7 +382,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_pair_kernel(const __grid
     }
     __syncwarp();
   } else {
-    pair_epilogue<TN>(p, ctl, tmem_base, cta, warp, lane, epi_stage + (warp - 2) * (kEpiStageBytes / 4));
+    pair_epilogue<TN, kRows>(p, ctl, tmem_base, cta, warp, lane, epi_stage + (warp - 2) * (kEpiStageBytes / 4));
   }
 
   tc_fence_before();
@@ -393,11 +396,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_pair_kernel(const __grid
 }  // namespace
 
 cudaError_t gemm_pair_configure() {
-  const cudaError_t e =
-      cudaFuncSetAttribute(gemm_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
-  return e != cudaSuccess
-             ? e
-             : cudaFuncSetAttribute(gemm_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
+  cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kPairSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_pair_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_pair_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
+  return e;
 }
 
 // Number of SM pairs that can be resident at once (the persistent grid must not exceed it).
@@ -414,7 +419,7 @@ int gemm_pair_max_clusters() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<false>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<false, false>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -434,8 +439,9 @@ cudaError_t gemm_pair_launch(const GemmParams& p, int clusters, cudaStream_t s) 
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return p.tn_S > 0 ? cudaLaunchKernelEx(&cfg, gemm_pair_kernel<true>, p)
-                    : cudaLaunchKernelEx(&cfg, gemm_pair_kernel<false>, p);
+  if (p.tn_S > 0) return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<true, false>, p);
+  return p.row_epilogue ? cudaLaunchKernelEx(&cfg, gemm_pair_kernel<false, true>, p)
+                        : cudaLaunchKernelEx(&cfg, gemm_pair_kernel<false, false>, p);
 }
 
 }  // namespace fo
