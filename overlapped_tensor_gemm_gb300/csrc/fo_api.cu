@@ -385,10 +385,9 @@ struct Launch {
 constexpr int kClaimTilesPerPair = 128;
 // SM-pair launches with at least this many partial-sum tiles (reduce-scatter steps) per pair
 // store partial sums lane per row from registers instead of through the shared-memory stage
-// (see store_rows), except one-launch layers long enough to claim their tiles.  Measured:
-// Flash-RS launches with 54-215 such tiles per pair 7-11% faster lane per row, with 27 or
-// fewer faster staged; the 4K one-launch layer 2-4% faster lane per row, the 8K and 16K
-// layers 1.3-2.5% slower.
+// (see store_rows).  Measured: Flash-RS launches with 54-215 such tiles per pair 7-12% faster
+// lane per row, with 27 or fewer faster staged; one-launch layers at 4K-16K 1.3-3% faster
+// (steady-state benchmark runs).
 constexpr int kRowEpilogueTilesPerPair = 40;
 
 // Resident SM pairs for a launch (the persistent grid never exceeds them).
@@ -420,14 +419,11 @@ fo_status launch_gemm(fo_ctx* ctx, Launch& L, const fo_opts& o, cudaStream_t str
     L.arrivals_per_tile = 8;
     L.p.claim_tiles = L.p.total_tiles >= kClaimTilesPerPair * clusters;
     int64_t add_tiles = 0;  // tiles whose epilogue adds an incoming partial sum
-    bool has_ag = false;    // all-gather tiles too (a one-launch layer)
     for (int i = 0; i < L.num_units; ++i) {
       const GemmUnit& u = L.p.units[i];
       if (u.epi == kEpiAddF32 || u.epi == kEpiAddBF16) add_tiles += static_cast<int64_t>(u.tiles_m) * u.tiles_n;
-      if (u.epi == kEpiBF16 || u.epi == kEpiSiluMul) has_ag = true;
     }
-    L.p.row_epilogue = add_tiles >= static_cast<int64_t>(kRowEpilogueTilesPerPair) * clusters &&
-                       !(has_ag && L.p.claim_tiles);
+    L.p.row_epilogue = add_tiles >= static_cast<int64_t>(kRowEpilogueTilesPerPair) * clusters;
     FO_CUDA(gemm_pair_launch(L.p, clusters, stream));
     return FO_OK;
   }
