@@ -243,7 +243,7 @@ __device__ void epilogue_loop(const GemmParams& p, SmemCtl* ctl, uint32_t tmem_b
 }
 
 template <bool TN>
-__global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __maxnreg__(kGemmMaxRegs) gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = smem_u32(smem_raw);
   uint8_t* tiles = smem_raw + ((1024u - (base & 1023u)) & 1023u);

@@ -326,7 +326,7 @@ __device__ void pair_epilogue(const GemmParams& p, PairCtl* ctl, uint32_t tmem_b
 // (GemmParams::row_epilogue, step-ordered tiles only).  Each combination is its own
 // instantiation, with its own register count.
 template <bool TN, bool kRows>
-__global__ void __launch_bounds__(kGemmThreads, 1) gemm_pair_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __maxnreg__(kGemmMaxRegs) gemm_pair_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = smem_u32(smem_raw);
   uint8_t* tiles = smem_raw + ((1024u - (base & 1023u)) & 1023u);

@@ -96,48 +96,61 @@ __device__ __forceinline__ int stage_index(int row, int g) { return row * 32 + (
 
 // Partial sums of one chunk in the coalesced layout: pf[i] = row 4i + lane/8 of the warp's
 // rows (first row `row0`), columns col + 4*(lane%8) .. +3; zero outside the unit.
+// The staged path's helpers copy the unit fields they use into locals first: read through
+// the reference into the kernel's parameter space, they were read again after every global
+// store (the stores' inline assembly may write memory), which measured 5-12% slower
+// reduce-scatter launches at K = 1024-3584 per rank.
 __device__ __forceinline__ void load_partial(const GemmUnit& u, int row0, int col, int lane, float4 (&pf)[8],
                                              bool stream = false) {
   const int c = col + 4 * (lane & 7);
+  const int m_rows = u.m_rows, n_cols = u.n_cols;
+  const float* acc_in = u.acc_in;
+  const int64_t ld_acc = u.ld_acc;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int r = row0 + 4 * i + (lane >> 3);
     float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    if (r < u.m_rows && c < u.n_cols) {
-      const float* src = u.acc_in + static_cast<int64_t>(r) * u.ld_acc + c;
-      if (c + 4 <= u.n_cols) {
+    if (r < m_rows && c < n_cols) {
+      const float* src = acc_in + static_cast<int64_t>(r) * ld_acc + c;
+      if (c + 4 <= n_cols) {
         x = stream ? ld_cs_f4(src) : ld_cg_f4(src);
       } else {
         x.x = __ldcg(src);
-        if (c + 1 < u.n_cols) x.y = __ldcg(src + 1);
-        if (c + 2 < u.n_cols) x.z = __ldcg(src + 2);
+        if (c + 1 < n_cols) x.y = __ldcg(src + 1);
+        if (c + 2 < n_cols) x.z = __ldcg(src + 2);
       }
     }
     pf[i] = x;
   }
 }
 
-// Stores one staged chunk (+ the partial sums when `add`) in the coalesced layout.
+// Stores one staged chunk (+ the partial sums when `add`) in the coalesced layout.  The
+// chunk's eight stage reads are issued before its stores, which would otherwise order each
+// read after the previous store (measured: short-K reduce-scatter launches 5-15% faster).
 __device__ __forceinline__ void store_staged(const GemmUnit& u, void* out, int row0, int col, int lane,
                                              const float* stage, bool add, const float4 (&pf)[8],
                                              bool stream = false) {
   const int c = col + 4 * (lane & 7);
   const bool bf16_out = u.epi == kEpiBF16 || u.epi == kEpiAddBF16;
+  const int m_rows = u.m_rows;
+  const int ncol = u.n_cols - c;
+  const int64_t ldc = u.ldc;
+  float4 xs[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) xs[i] = *reinterpret_cast<const float4*>(stage + stage_index(4 * i + (lane >> 3), lane & 7));
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int rl = 4 * i + (lane >> 3);
-    const int r = row0 + rl;
-    float4 x = *reinterpret_cast<const float4*>(stage + stage_index(rl, lane & 7));
+    const int r = row0 + 4 * i + (lane >> 3);
+    float4 x = xs[i];
     if (add) {
       x.x += pf[i].x;
       x.y += pf[i].y;
       x.z += pf[i].z;
       x.w += pf[i].w;
     }
-    if (r >= u.m_rows || c >= u.n_cols) continue;
-    const int ncol = u.n_cols - c;
+    if (r >= m_rows || ncol <= 0) continue;
     if (bf16_out) {
-      uint16_t* dst = static_cast<uint16_t*>(out) + static_cast<int64_t>(r) * u.ldc + c;
+      uint16_t* dst = static_cast<uint16_t*>(out) + static_cast<int64_t>(r) * ldc + c;
       if (ncol >= 4) {
         *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w));
       } else {
@@ -146,7 +159,7 @@ __device__ __forceinline__ void store_staged(const GemmUnit& u, void* out, int r
         if (ncol > 2) dst[2] = __bfloat16_as_ushort(__float2bfloat16_rn(x.z));
       }
     } else {
-      float* dst = static_cast<float*>(out) + static_cast<int64_t>(r) * u.ldc + c;
+      float* dst = static_cast<float*>(out) + static_cast<int64_t>(r) * ldc + c;
       if (ncol >= 4) {
         if (stream) {
           st_cs_v4_u32(dst, __float_as_uint(x.x), __float_as_uint(x.y), __float_as_uint(x.z), __float_as_uint(x.w));

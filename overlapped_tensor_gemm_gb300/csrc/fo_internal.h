@@ -35,6 +35,10 @@ constexpr int kBN = 256;            // UMMA N
 constexpr int kBK = 64;             // one 128-byte swizzle atom of bf16
 constexpr int kStages = 4;
 constexpr int kGemmThreads = 192;   // warp 0: TMA, warp 1: MMA, warps 2-5: epilogue
+// Registers per thread of the GEMM kernels.  Two of the six warps share an SM sub-partition
+// (16K registers): at 200 they hold 12,800 of them, which leaves room for the ring's
+// device-to-device copies when those run as a small copy kernel beside the persistent grid.
+constexpr int kGemmMaxRegs = 200;
 constexpr int kMaxMaps = 40;    // one launch of a whole MLP layer: 3P maps for Flash-AG + 2P for Flash-RS
 constexpr int kMaxUnits = 128;  // P*P units per decomposed collective, two collectives per layer
 constexpr int kMaxGroups = 24;
