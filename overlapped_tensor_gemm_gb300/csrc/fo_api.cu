@@ -383,12 +383,6 @@ struct Launch {
 // (measured: 8K and 16K layers, 200-400 tiles per pair, 7-8% faster; the 4K layer, ~100,
 // equal; the 2K and Llama-3-8B layers, 37-50, 1-2% slower than striding)
 constexpr int kClaimTilesPerPair = 128;
-// SM-pair launches with at least this many partial-sum tiles (reduce-scatter steps) per pair
-// store partial sums lane per row from registers instead of through the shared-memory stage
-// (see store_rows).  Measured: Flash-RS launches with 54-215 such tiles per pair 7-12% faster
-// lane per row, with 27 or fewer faster staged; one-launch layers at 4K-16K 1.3-3% faster
-// (steady-state benchmark runs).
-constexpr int kRowEpilogueTilesPerPair = 40;
 
 // Resident SM pairs for a launch (the persistent grid never exceeds them).
 int pair_grid(const fo_ctx* ctx, const fo_opts& o) {
@@ -418,12 +412,6 @@ fo_status launch_gemm(fo_ctx* ctx, Launch& L, const fo_opts& o, cudaStream_t str
     if (L.p.total_tiles < clusters) clusters = L.p.total_tiles;
     L.arrivals_per_tile = 8;
     L.p.claim_tiles = L.p.total_tiles >= kClaimTilesPerPair * clusters;
-    int64_t add_tiles = 0;  // tiles whose epilogue adds an incoming partial sum
-    for (int i = 0; i < L.num_units; ++i) {
-      const GemmUnit& u = L.p.units[i];
-      if (u.epi == kEpiAddF32 || u.epi == kEpiAddBF16) add_tiles += static_cast<int64_t>(u.tiles_m) * u.tiles_n;
-    }
-    L.p.row_epilogue = add_tiles >= static_cast<int64_t>(kRowEpilogueTilesPerPair) * clusters;
     FO_CUDA(gemm_pair_launch(L.p, clusters, stream));
     return FO_OK;
   }

@@ -234,7 +234,7 @@ __device__ void epilogue_loop(const GemmParams& p, SmemCtl* ctl, uint32_t tmem_b
     const TileCoord tc = tile_coord<TN>(p, tile);
     if (!tile_ok(p, tc, tile, 1)) return;
     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
-    if (!epilogue_tile<TN, false>(p, tc, tile, &ctl->tmem_full[acc], acc_phase, tbase, 0, 1, q, lane, stage,
+    if (!epilogue_tile<TN>(p, tc, tile, &ctl->tmem_full[acc], acc_phase, tbase, 0, 1, q, lane, stage,
                        [&] { mbar_arrive(&ctl->tmem_empty[acc]); }))
       return;
     acc ^= 1;

@@ -293,7 +293,7 @@ __device__ void pair_mma(const GemmParams& p, uint8_t* tiles, PairCtl* ctl, uint
   }
 }
 
-template <bool TN, bool kRows>
+template <bool TN>
 __device__ void pair_epilogue(const GemmParams& p, PairCtl* ctl, uint32_t tmem_base, uint32_t cta, int warp,
                               int lane, float* stage) {
   const int q = warp & 3;
@@ -314,7 +314,7 @@ __device__ void pair_epilogue(const GemmParams& p, PairCtl* ctl, uint32_t tmem_b
         mbar_arrive_cluster(leader_tmem_empty + acc * static_cast<uint32_t>(sizeof(uint64_t)));
       }
     };
-    if (!epilogue_tile<TN, kRows>(p, tc, tile, &ctl->tmem_full[acc], acc_phase, tbase, static_cast<int>(cta), 2, q, lane, stage,
+    if (!epilogue_tile<TN>(p, tc, tile, &ctl->tmem_full[acc], acc_phase, tbase, static_cast<int>(cta), 2, q, lane, stage,
                        arrive_empty))
       return;
     acc ^= 1;
@@ -322,10 +322,9 @@ __device__ void pair_epilogue(const GemmParams& p, PairCtl* ctl, uint32_t tmem_b
   }
 }
 
-// TN: transposed reduce-scatter tiles; kRows: the lane-per-row partial-sum epilogue
-// (GemmParams::row_epilogue, step-ordered tiles only).  Each combination is its own
-// instantiation, with its own register count.
-template <bool TN, bool kRows>
+// TN: transposed reduce-scatter tiles (each tile kind is its own instantiation, with its
+// own register count).
+template <bool TN>
 __global__ void __maxnreg__(kGemmMaxRegs) gemm_pair_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = smem_u32(smem_raw);
@@ -382,7 +381,7 @@ __global__ void __maxnreg__(kGemmMaxRegs) gemm_pair_kernel(const __grid_constant
     }
     __syncwarp();
   } else {
-    pair_epilogue<TN, kRows>(p, ctl, tmem_base, cta, warp, lane, epi_stage + (warp - 2) * (kEpiStageBytes / 4));
+    pair_epilogue<TN>(p, ctl, tmem_base, cta, warp, lane, epi_stage + (warp - 2) * (kEpiStageBytes / 4));
   }
 
   tc_fence_before();
@@ -396,12 +395,9 @@ __global__ void __maxnreg__(kGemmMaxRegs) gemm_pair_kernel(const __grid_constant
 }  // namespace
 
 cudaError_t gemm_pair_configure() {
-  cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kPairSmem);
+  cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gemm_pair_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gemm_pair_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
+    e = cudaFuncSetAttribute(gemm_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
   return e;
 }
 
@@ -419,7 +415,7 @@ int gemm_pair_max_clusters() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<false, false>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<false>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -439,9 +435,8 @@ cudaError_t gemm_pair_launch(const GemmParams& p, int clusters, cudaStream_t s) 
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (p.tn_S > 0) return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<true, false>, p);
-  return p.row_epilogue ? cudaLaunchKernelEx(&cfg, gemm_pair_kernel<false, true>, p)
-                        : cudaLaunchKernelEx(&cfg, gemm_pair_kernel<false, false>, p);
+  if (p.tn_S > 0) return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<true>, p);
+  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<false>, p);
 }
 
 }  // namespace fo

@@ -175,74 +175,6 @@ __device__ __forceinline__ void store_staged(const GemmUnit& u, void* out, int r
   }
 }
 
-// The lane-per-row epilogue: the partial sums of one row's 32 columns [col, col + 32)
-// (zero outside the unit).
-__device__ __forceinline__ void load_row_partial(const GemmUnit& u, int row, int col, float4 (&pr)[8], bool stream) {
-  const float* src = u.acc_in + static_cast<int64_t>(row) * u.ld_acc + col;
-  const bool full = row < u.m_rows && col + 32 <= u.n_cols;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    if (full) {
-      x = stream ? ld_cs_f4(src + 4 * i) : ld_cg_f4(src + 4 * i);
-    } else if (row < u.m_rows) {
-      const int c = col + 4 * i;
-      if (c < u.n_cols) x.x = __ldcg(src + 4 * i);
-      if (c + 1 < u.n_cols) x.y = __ldcg(src + 4 * i + 1);
-      if (c + 2 < u.n_cols) x.z = __ldcg(src + 4 * i + 2);
-      if (c + 3 < u.n_cols) x.w = __ldcg(src + 4 * i + 3);
-    }
-    pr[i] = x;
-  }
-}
-
-// The lane-per-row epilogue: one row's 32 accumulator columns (+ the partial sums when
-// `add`), stored as fp32 or bf16.
-__device__ __forceinline__ void store_row_chunk(const GemmUnit& u, void* out, int row, int col, const uint32_t (&v)[32],
-                                                bool add, const float4 (&pr)[8], bool stream) {
-  if (row >= u.m_rows) return;
-  float x[32];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    x[4 * i + 0] = __uint_as_float(v[4 * i + 0]) + (add ? pr[i].x : 0.0f);
-    x[4 * i + 1] = __uint_as_float(v[4 * i + 1]) + (add ? pr[i].y : 0.0f);
-    x[4 * i + 2] = __uint_as_float(v[4 * i + 2]) + (add ? pr[i].z : 0.0f);
-    x[4 * i + 3] = __uint_as_float(v[4 * i + 3]) + (add ? pr[i].w : 0.0f);
-  }
-  const int ncol = u.n_cols - col;
-  if (u.epi == kEpiBF16 || u.epi == kEpiAddBF16) {
-    uint16_t* dst = static_cast<uint16_t*>(out) + static_cast<int64_t>(row) * u.ldc + col;
-    if (ncol >= 32) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        st_v4_u32(dst + 8 * i, pack_bf16x2(x[8 * i + 0], x[8 * i + 1]), pack_bf16x2(x[8 * i + 2], x[8 * i + 3]),
-                  pack_bf16x2(x[8 * i + 4], x[8 * i + 5]), pack_bf16x2(x[8 * i + 6], x[8 * i + 7]));
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i < ncol) dst[i] = __bfloat16_as_ushort(__float2bfloat16_rn(x[i]));
-    }
-  } else {
-    float* dst = static_cast<float*>(out) + static_cast<int64_t>(row) * u.ldc + col;
-    if (ncol >= 32) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (stream) {
-          st_cs_v4_u32(dst + 4 * i, __float_as_uint(x[4 * i]), __float_as_uint(x[4 * i + 1]),
-                       __float_as_uint(x[4 * i + 2]), __float_as_uint(x[4 * i + 3]));
-        } else {
-          st_v4_u32(dst + 4 * i, __float_as_uint(x[4 * i]), __float_as_uint(x[4 * i + 1]), __float_as_uint(x[4 * i + 2]),
-                    __float_as_uint(x[4 * i + 3]));
-        }
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i < ncol) dst[i] = x[i];
-    }
-  }
-}
-
 // A plain bf16 chunk of one row (lane = row), stored straight from registers: without
 // partial sums to load this was measured faster than the staged path.
 __device__ __forceinline__ void store_bf16_row_chunk(const GemmUnit& u, void* out, int row, int col,
@@ -268,18 +200,15 @@ __device__ __forceinline__ void store_bf16_row_chunk(const GemmUnit& u, void* ou
 // The kBN columns of the warp's 32 accumulator rows (first row `row0`), chunk by chunk.
 // With a partial-sum add, `pf` holds chunk 0's partials on entry (loaded before the
 // accumulator was complete) and the loads of chunk c+1 are in flight while chunk c is
-// stored.  Step-ordered tiles store either lane per row straight from registers
-// (kRows, `pf` then in that layout) or through the warp's shared-memory stage in
-// row-contiguous 128-byte segments.  The stage costs shared-memory bandwidth that the
-// operand ring of a running main loop also needs; the lane-per-row accesses are less
-// coalesced (measured: lane per row 9-10% faster for Flash-RS launches of 54 or more
-// tiles per SM pair, the stage 6-11% faster for launches of 27 or fewer).
+// stored, through the warp's shared-memory stage in row-contiguous 128-byte segments
+// (measured faster than storing lane per row straight from registers, which touches 32
+// rows per instruction: Flash-RS launches 3-12% faster at 13-400 tiles per SM pair).
 // tn_rows > 0: a unit of a transposed tile.  The warp's 32 TMEM lanes are then the output
 // columns [col0, col0 + 32) and TMEM columns tbase .. tbase + tn_rows the unit's rows
 // 0 .. tn_rows-1; each 32x32 chunk is staged transposed (row-major: every write
 // instruction fills one 128-byte row of the stage) and stored by the same row-contiguous
 // path.
-template <bool kTn, bool kRows>
+template <bool kTn>
 __device__ __forceinline__ void store_rows(const GemmUnit& u, void* out, uint32_t tbase, int row0, int col0, int lane,
                                            bool add, float4 (&pf)[8], float* stage, int tn_rows, bool stream) {
   constexpr bool tn = kTn;
@@ -293,25 +222,6 @@ __device__ __forceinline__ void store_rows(const GemmUnit& u, void* out, uint32_
       tmem_ld32(tbase + c * 32, v);
       tmem_wait_ld();
       if (row < u.m_rows) store_bf16_row_chunk(u, out, row, col, v);
-    }
-    return;
-  }
-  if (!tn && kRows) {
-    const int row = row0 + lane;
-#pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
-      const int col = col0 + c * 32;
-      if (col >= u.n_cols) break;
-      uint32_t v[32];
-      float4 next[8];
-      tmem_ld32(tbase + c * 32, v);
-      if (add && c + 1 < kBN / 32) load_row_partial(u, row, col + 32, next, stream);
-      tmem_wait_ld();
-      store_row_chunk(u, out, row, col, v, add, pf, stream);
-      if (add) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) pf[i] = next[i];
-      }
     }
     return;
   }
@@ -472,7 +382,7 @@ __device__ __forceinline__ bool wait_rows_ready(const GemmParams& p, const GemmU
 // each after its incoming partial sum's flag, each released before the next.  This is the
 // only call site of store_rows, so a kernel inlines one copy of it.  `arrive_empty()`
 // frees the accumulator.  False if a wait gave up.
-template <bool TN, bool kRows, class ArriveEmpty>
+template <bool TN, class ArriveEmpty>
 __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const TileCoord& tc, int tile, uint64_t* tmem_full,
                                               uint32_t acc_phase, uint32_t tbase, int cta, int ncta, int q, int lane,
                                               float* stage, ArriveEmpty arrive_empty) {
@@ -494,11 +404,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const TileCoo
       if (!warp_flag_wait(p.flags + f, p, kSiteAccInFlag, static_cast<uint32_t>(f), lane)) return false;
     }
     if (u0.epi == kEpiAddF32 || u0.epi == kEpiAddBF16) {
-      if (kRows) {
-        load_row_partial(u0, row0 + lane, col0, pf, p.stream_partials != 0);
-      } else {
-        load_partial(u0, row0, col0, lane, pf, p.stream_partials != 0);
-      }
+      load_partial(u0, row0, col0, lane, pf, p.stream_partials != 0);
     }
   }
   if (!warp_mbar_wait(tmem_full, acc_phase, p, kSiteTmemFull, static_cast<uint32_t>(tile), lane)) return false;
@@ -527,7 +433,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const TileCoo
       }
     } else {
       // transposed: the unit's token rows are TMEM columns [s * tn_rows, +tn_rows)
-      store_rows<TN, kRows>(u, tn ? u.c : out, tbase + (tn ? s * p.tn_rows : 0), row0, col0, lane, add, pf, stage,
+      store_rows<TN>(u, tn ? u.c : out, tbase + (tn ? s * p.tn_rows : 0), row0, col0, lane, add, pf, stage,
                             tn ? p.tn_rows : 0, p.stream_partials != 0);
     }
     if (tn) publish_unit(p, u, slot, tc.mb, lane);

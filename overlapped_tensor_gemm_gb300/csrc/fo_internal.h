@@ -135,9 +135,6 @@ struct GemmParams {
   // SM-pair kernel: 1: pairs claim tiles in order from a launch-wide counter; 0: pair c runs
   // tiles c, c + pairs, c + 2 * pairs, ...
   int32_t claim_tiles;
-  // 1: the step-ordered tiles' partial-sum epilogue works lane per row straight from
-  // registers; 0: through the per-warp shared-memory stage (coalesced 128-byte rows)
-  int32_t row_epilogue;
   int32_t total_tiles;
   uint32_t epoch;
   uint64_t timeout_ns;
