@@ -226,15 +226,19 @@ __device__ __forceinline__ void store_rows(const GemmUnit& u, void* out, uint32_
     return;
   }
   const int nchunks = tn ? tn_rows / 32 : kBN / 32;
-#pragma unroll 1
-  for (int c = 0; c < nchunks; ++c) {
+  // Chunk c: its accumulator columns through the stage plus the partial sums `cur` (loaded
+  // while the previous chunk was stored), while the next chunk's partial sums load into
+  // `nxt`.  Two chunks per iteration, the buffers swapping roles: a copy of the loaded
+  // registers at the end of a chunk would wait for its loads there (measured: the K = 1024
+  // reduce-scatter launch 12% faster without that copy).
+  float4 alt[8];
+  auto chunk = [&](int c, float4 (&cur)[8], float4 (&nxt)[8]) -> bool {
     const int r0 = tn ? c * 32 : row0;    // first row of the chunk
     const int col = tn ? col0 : col0 + c * 32;
-    if (col >= u.n_cols) break;
+    if (col >= u.n_cols) return false;
     uint32_t v[32];
-    float4 next[8];
     tmem_ld32(tbase + c * 32, v);
-    if (add && c + 1 < nchunks) load_partial(u, tn ? r0 + 32 : row0, tn ? col0 : col + 32, lane, next, stream);
+    if (add && c + 1 < nchunks) load_partial(u, tn ? r0 + 32 : row0, tn ? col0 : col + 32, lane, nxt, stream);
     tmem_wait_ld();
     if (tn) {
 #pragma unroll
@@ -247,12 +251,14 @@ __device__ __forceinline__ void store_rows(const GemmUnit& u, void* out, uint32_
                         __uint_as_float(v[4 * g + 3]));
     }
     __syncwarp();
-    store_staged(u, out, r0, col, lane, stage, add, pf, stream);
+    store_staged(u, out, r0, col, lane, stage, add, cur, stream);
     __syncwarp();  // the stage is rewritten by the next chunk
-    if (add) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) pf[i] = next[i];
-    }
+    return true;
+  };
+#pragma unroll 1
+  for (int c = 0; c < nchunks; c += 2) {
+    if (!chunk(c, pf, alt)) break;
+    if (c + 1 < nchunks && !chunk(c + 1, alt, pf)) break;
   }
 }
 
