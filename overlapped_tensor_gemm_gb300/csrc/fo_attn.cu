@@ -17,21 +17,20 @@
 //               before reading it.
 //   warp 10     TMA: the V^T blocks into a ring of two stages, independently
 //               of the K walk (so neither load waits behind the other).
-//   warp 1      tcgen05.mma: S = Q K^T into one of two TMEM score buffers.  A
-//               score buffer is free again as soon as the softmax warps have
-//               read it, so the scores of block j + 2 can be computed while
-//               block j's softmax still runs.
-//   warp 11     tcgen05.mma: O += P V into the TMEM accumulator, P read from one
-//               of two TMEM P buffers.
+//   warp 1      tcgen05.mma: S = Q K^T into one of three TMEM score buffers; a
+//               buffer is free again once the P.V that read its block's P has
+//               completed, so the scores of block j + 2 are computed while block
+//               j's softmax runs, without waiting for it.
+//   warp 11     tcgen05.mma: O += P V into the TMEM accumulator, P read from the
+//               block's score buffer.
 //   warps 2-9   softmax: two warps per query row (one per 64-key half); they
 //               load their half of the score row, mask the diagonal block,
-//               exchange the row maximum, release the score buffer, keep their
-//               half of the row sum in registers, rescale their half of the O row
-//               only when the max grew by more than 2^8 (the final division by the
-//               sum uses the same reference max, so this is exact), and write P
-//               as fp16 into the block's P buffer once the P.V of two blocks
-//               earlier has read it; at the item's end the two halves of the row
-//               sum are added.
+//               exchange the row maximum, keep their half of the row sum in
+//               registers, rescale their half of the O row only when the max grew
+//               by more than 2^8 (the final division by the sum uses the same
+//               reference max, so this is exact), and write P as fp16 over the
+//               first half of their own score columns; at the item's end the two
+//               halves of the row sum are added.
 // V is transposed once per rank (V^T [heads*128, tokens]) before the ring so
 // that both MMAs read K-major operands.  The P.V product runs in fp16: the
 // transpose converts V's bf16 values to fp16 (exact for |v| within fp16's
@@ -62,13 +61,15 @@ constexpr int kKStages = 3;
 constexpr int kVStages = 2;
 constexpr uint32_t kVHalfBytes = kHd * 128;             // [128 head dims x 64 keys] swizzled
 constexpr uint32_t kVStageBytes = 2 * kVHalfBytes;
-// TMEM: S0 [0,128), S1 [128,256), O [256,384), P0 [384,448), P1 [448,512).  Block j writes
-// its P into buffer j & 1: keys 64h + 2c, 64h + 2c + 1 as one fp16 pair in column
-// 384 + 64 (j & 1) + 32h + c.  Two P buffers let block j + 1's softmax write its P while
-// block j's P.V still reads the other one.
+// TMEM: S0 [0,128), S1 [128,256), S2 [256,384), O [384,512).  Block j uses score buffer
+// j % 3; its softmax warp for keys 64h..64h+63 (score columns 128 (j % 3) + 64h + [0, 64))
+// writes P over the first half of those columns: keys 64h + 2c, 64h + 2c + 1 as one fp16
+// pair in column 128 (j % 3) + 64h + c, after its last read of them.  (P in buffers of its
+// own would leave room for two score buffers only; their release then waited for the
+// softmax's row-maximum exchange, and the score MMAs of block j + 2 with it.)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kOCol = 256;
-constexpr uint32_t kPCol = 384;
+constexpr int kSBufs = 3;
+constexpr uint32_t kOCol = 384;
 constexpr uint32_t kIdescS = umma_idesc_bf16(128, 128);   // S = Q K^T, bf16 operands
 constexpr uint32_t kIdescO = umma_idesc_f16(128, kHd);    // O += P V, fp16
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
@@ -100,10 +101,9 @@ struct alignas(8) AttnCtl {
   uint64_t q_empty;                 // the item's last score MMA has completed
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
-  uint64_t s_full[2];               // per S buffer: scores computed
-  uint64_t s_free[2];               // per S buffer: every softmax warp has read the scores
-  uint64_t p_full[2];               // per P buffer: P written
-  uint64_t pv_done[2];              // per P buffer: the P.V that read it completed
+  uint64_t s_full[kSBufs];          // per score buffer: scores computed
+  uint64_t p_full[kSBufs];          // per score buffer: every softmax warp has written its P
+  uint64_t s_free[kSBufs];          // per score buffer: the P.V that read its P has completed
   uint64_t drain, drain_pv;         // failure paths: the score / P.V issuer's MMAs have completed
   uint64_t item_full[kItemSlots];   // the slot holds the CTA's next claimed item
   uint64_t item_empty[kItemSlots];  // every reader has taken the slot's item
@@ -367,19 +367,21 @@ __device__ __forceinline__ void issue_s(uint32_t tmem_s, uint32_t q_addr, uint32
   }
 }
 
-// O += P V for one 128-key block: P from its TMEM buffer (keys 64h + 2c, 64h + 2c + 1 in
-// column 32h + c), V^T from the two 64-key swizzle halves of the stage.
+// O += P V for one 128-key block: P from its score buffer (keys 64h + 2c, 64h + 2c + 1 in
+// column 64h + c), V^T from the two 64-key swizzle halves of the stage.
 __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr, bool first) {
 #pragma unroll
   for (int k = 0; k < kKB / 16; ++k) {
     const uint32_t off = (k >> 2) * kVHalfBytes + (k & 3) * 32;
-    umma_ts(tmem_o, tmem_p + k * 8, umma_sdesc_sw128(v_addr + off), kIdescO, (first && k == 0) ? 0u : 1u);
+    umma_ts(tmem_o, tmem_p + (k >> 2) * 64 + (k & 3) * 8, umma_sdesc_sw128(v_addr + off), kIdescO,
+            (first && k == 0) ? 0u : 1u);
   }
 }
 
-// S buffer b of block gs may be overwritten once the softmax warps have read the scores
-// of block gs - 2 from it.
-__device__ __forceinline__ uint32_t s_free_parity(uint32_t gs) { return ((gs >> 1) & 1u) ^ 1u; }
+// Block g's score buffer and the parity of its phases: phase n of a buffer's barriers
+// belongs to block 3n + buffer.
+__device__ __forceinline__ uint32_t sbuf_of(uint32_t g) { return g % kSBufs; }
+__device__ __forceinline__ uint32_t sbuf_parity(uint32_t g) { return (g / kSBufs) & 1u; }
 
 // This CTA's key blocks in schedule order, for one kind of MMA: its k-th claimed item i
 // (-1: the wait for it gave up), block j of its n blocks.
@@ -415,13 +417,13 @@ __device__ void attn_mma_s(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, uin
   bool issued = false, ok = true;
   MmaWalk ws;
   for (ws.start(p, ctl); ok && ws.valid(p); ws.next(p, ctl), ++gs) {
-    const uint32_t st = gs % kKStages, sb = gs & 1u;
+    const uint32_t st = gs % kKStages, sb = sbuf_of(gs);
     if (ws.j == 0) {
       if (!mbar_wait_fast(&ctl->q_full, q_uses & 1u, p.ctrl, p.timeout_ns, kSiteFull, ws.i)) break;
       ++q_uses;
     }
     if (!mbar_wait_fast(&ctl->k_full[st], (gs / kKStages) & 1u, p.ctrl, p.timeout_ns, kSiteFull, ws.i) ||
-        !mbar_wait_fast(&ctl->s_free[sb], s_free_parity(gs), p.ctrl, p.timeout_ns, kSiteTmemEmpty, ws.i)) {
+        !mbar_wait_fast(&ctl->s_free[sb], sbuf_parity(gs) ^ 1u, p.ctrl, p.timeout_ns, kSiteTmemEmpty, ws.i)) {
       ok = false;
       break;
     }
@@ -447,16 +449,16 @@ __device__ void attn_mma_pv(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, ui
   MmaWalk wp;
   for (wp.start(p, ctl); ok && wp.valid(p); wp.next(p, ctl), ++gp) {
     const uint32_t vs = gp % kVStages;
-    if (!mbar_wait_fast(&ctl->p_full[gp & 1u], (gp >> 1) & 1u, p.ctrl, p.timeout_ns, kSiteFull, wp.i) ||
+    if (!mbar_wait_fast(&ctl->p_full[sbuf_of(gp)], sbuf_parity(gp), p.ctrl, p.timeout_ns, kSiteFull, wp.i) ||
         !mbar_wait_fast(&ctl->v_full[vs], (gp / kVStages) & 1u, p.ctrl, p.timeout_ns, kSiteFull, wp.i)) {
       ok = false;
       break;
     }
     tc_fence_after();
-    issue_pv(tmem_base + kOCol, tmem_base + kPCol + (gp & 1u) * 64, sbase + kOffV + vs * kVStageBytes, wp.j == 0);
+    issue_pv(tmem_base + kOCol, tmem_base + sbuf_of(gp) * 128, sbase + kOffV + vs * kVStageBytes, wp.j == 0);
     issued = true;
     umma_commit(&ctl->v_empty[vs]);
-    umma_commit(&ctl->pv_done[gp & 1u]);
+    umma_commit(&ctl->s_free[sbuf_of(gp)]);  // P read and O updated: the buffer may take new scores
   }
   if (wp.i < 0) ok = false;
   if (!ok && issued) {
@@ -549,9 +551,9 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
       const bool diag_step = p.causal && t == 0;
       for (int kb = 0; kb < nb; ++kb, ++j) {
         const uint32_t gj = g + j;
-        const uint32_t sb = gj & 1u;  // S buffer of this block
+        const uint32_t sb = sbuf_of(gj);  // score buffer of this block (P goes there too)
         const bool diag = diag_step && kb == it.qb;
-        if (!warp_wait(&ctl->s_full[sb], (gj >> 1) & 1u, p, kSiteTmemFull, i, lane)) return;
+        if (!warp_wait(&ctl->s_full[sb], sbuf_parity(gj), p, kSiteTmemFull, i, lane)) return;
         tc_fence_after();
         // raw scores of this warp's 64 keys (scale applied in the exponent); on the
         // diagonal block key > query is masked
@@ -616,20 +618,17 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
             rescale = true;
           }
           if (__any_sync(0xffffffffu, rescale)) {
-            load_scores(s);  // the scores are still in TMEM (the buffer is not released yet)
+            load_scores(s);  // the scores are still in TMEM (P has not been written over them)
             weights(s, m_ref, packed, bsum);
           }
         }
         // this warp's part of the row sum: earlier blocks rescaled like O, plus this block
         lsum = fadd2(ffma2(lsum, pack2(alpha, alpha), pack2(0.f, 0.f)), bsum);
-        // the scores are read: the buffer may take the scores of block gj + 2
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->s_free[sb]);
-        const uint32_t pb = gj & 1u;  // P buffer of this block
         if (__any_sync(0xffffffffu, rescale)) {
           // O must hold every earlier block (P.V of block gj - 1 complete) before it is rescaled
-          if (gj > 0 && !warp_wait(&ctl->pv_done[pb ^ 1u], ((gj - 1) >> 1) & 1u, p, kSiteDrain, i, lane)) return;
+          if (gj > 0 &&
+              !warp_wait(&ctl->s_free[sbuf_of(gj - 1)], sbuf_parity(gj - 1), p, kSiteDrain, i, lane))
+            return;
           tc_fence_after();
 #pragma unroll 1
           for (int c = 0; c < 2; ++c) {
@@ -641,15 +640,13 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
             tmem_st32(lane_base + kOCol + col0 + c * 32, v);
           }
         }
-        // the P buffer's previous block (gj - 2) has been read by its P.V
-        if (!warp_wait(&ctl->pv_done[pb], s_free_parity(gj), p, kSiteDrain, i, lane)) return;
-        tc_fence_after();
-        // P: this warp's 64 keys as 32 fp16 pairs
-        tmem_st32(lane_base + kPCol + pb * 64 + hf * 32, packed);
+        // P: this warp's 64 keys as 32 fp16 pairs, over the first half of its own score
+        // columns (every read of them is done)
+        tmem_st32(lane_base + sb * 128 + col0, packed);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->p_full[pb]);
+        if (lane == 0) mbar_arrive(&ctl->p_full[sb]);
       }
     }
     // epilogue: O row / row sum -> bf16 (this warp's 64 columns); the row sum is this
@@ -659,7 +656,7 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
     xch_publish(ctl, xch, xuses, q, hf, row, lo + hi, lane);
     if (!xch_collect(ctl, xch, xuses, q, hf, row, &other_sum, p, lane, i)) return;
     const uint32_t glast = g + j - 1;
-    if (!warp_wait(&ctl->pv_done[glast & 1u], (glast >> 1) & 1u, p, kSiteDrain, i, lane)) return;
+    if (!warp_wait(&ctl->s_free[sbuf_of(glast)], sbuf_parity(glast), p, kSiteDrain, i, lane)) return;
     tc_fence_after();
     const float inv = 1.f / (hf == 0 ? (lo + hi) + other_sum : other_sum + (lo + hi));
     uint16_t* orow = p.out[it.r] + static_cast<int64_t>(it.qb * kQB + row) * p.ld_out[it.r] + it.h * kHd + col0;
@@ -699,13 +696,10 @@ __global__ void __maxnreg__(136) attn_kernel(const __grid_constant__ AttnParams 
       mbar_init(&ctl->v_full[s], 1);
       mbar_init(&ctl->v_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kSBufs; ++b) {
       mbar_init(&ctl->s_full[b], 1);
-      mbar_init(&ctl->s_free[b], 8);
-    }
-    for (int b = 0; b < 2; ++b) {
       mbar_init(&ctl->p_full[b], 8);
-      mbar_init(&ctl->pv_done[b], 1);
+      mbar_init(&ctl->s_free[b], 1);
     }
     for (int q = 0; q < 4; ++q)
       for (int b = 0; b < 2; ++b) mbar_init(&ctl->xchg[q][b], 2);
