@@ -545,7 +545,6 @@ __device__ void attn_softmax(const AttnParams& p, uint8_t* smem, AttnCtl* ctl, u
     uint64_t lsum = pack2(0.f, 0.f);  // this warp's part of the row sum, in two lanes of a pair
     int j = 0;
     const int nsteps = steps_of(p, it.r);
-    const int n = item_blocks(p, it);
     for (int t = 0; t < nsteps; ++t) {
       const int nb = blocks_of(p, it, t);
       const bool diag_step = p.causal && t == 0;
